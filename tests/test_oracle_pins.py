@@ -1,0 +1,462 @@
+"""Pins of the double-precision oracle against facts the pages and the
+mathematics fix, independent of the oracle's own code: closed forms,
+library special cases, invariants, finite differences, brute force and
+hand-worked fixtures.  CPU only."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_worked.json")
+
+
+def _uniform_bounds(B, spp):
+    return np.arange(0, B + 1, spp, dtype=np.int64)
+
+
+# ----------------------------------------------------------------------------
+# group advantages
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("n", [2, 3, 4, 8, 16])
+def test_adv_bernoulli_closed_form(n):
+    # k successes out of n: mean k/n, population std sqrt(k(n-k))/n, hence
+    # A_success = sqrt((n-k)/k) and A_failure = -sqrt(k/(n-k)).
+    for k in range(1, n):
+        r = np.zeros(n, np.float32)
+        r[:k] = 1.0
+        A = oracle.group_advantages(r, [0, n])
+        assert np.allclose(A[:k], math.sqrt((n - k) / k), rtol=1e-14, atol=0)
+        assert np.allclose(A[k:], -math.sqrt(k / (n - k)), rtol=1e-14, atol=0)
+    # one of eight: +sqrt(7) and -1/sqrt(7)
+    r = np.zeros(8, np.float32)
+    r[3] = 1
+    A = oracle.group_advantages(r, [0, 8])
+    assert A[3] == pytest.approx(2.6457513110645907, rel=1e-15)
+    assert A[0] == pytest.approx(-0.3779644730092272, rel=1e-15)
+
+
+def test_adv_pair_is_plus_minus_one():
+    # two distinct rewards a<b: (b - mean) / popstd = ((b-a)/2) / ((b-a)/2) = 1
+    rng = np.random.default_rng(3)
+    r = rng.normal(size=64).astype(np.float32)
+    A = oracle.group_advantages(r, _uniform_bounds(64, 2))
+    hi = np.maximum(r[0::2], r[1::2])
+    assert np.allclose(np.abs(A), 1.0, rtol=1e-12)
+    assert np.all((A[0::2] > 0) == (r[0::2] == hi))
+
+
+def test_adv_invariants_random_groups():
+    rng = np.random.default_rng(0)
+    bounds = np.array([0, 3, 10, 11, 27, 40], np.int64)  # includes a singleton group
+    r = rng.normal(size=40).astype(np.float32)
+    A = oracle.group_advantages(r, bounds)
+    for g in range(len(bounds) - 1):
+        a = A[bounds[g]:bounds[g + 1]]
+        if len(a) == 1:
+            assert a[0] == 0.0  # singleton group is degenerate
+            continue
+        assert abs(a.sum()) < 1e-12
+        assert np.sqrt(np.mean((a - a.mean()) ** 2)) == pytest.approx(1.0, rel=1e-12)
+        # order is preserved
+        rr = r[bounds[g]:bounds[g + 1]]
+        assert np.all(np.argsort(a, kind="stable") == np.argsort(rr, kind="stable"))
+
+
+@pytest.mark.parametrize("value", [0.0, 1.0, -3.5, 7.25])
+def test_adv_degenerate_group_is_exactly_zero(value):
+    r = np.full(8, value, np.float32)
+    r2 = np.concatenate([r, np.array([0, 1, 0, 1, 1, 0, 0, 0], np.float32)])
+    A = oracle.group_advantages(r2, [0, 8, 16])
+    assert np.all(A[:8] == 0.0)
+    assert np.any(A[8:] != 0.0)
+
+
+def test_adv_eps_floor_and_add():
+    # two rewards 2*delta apart: population std = delta < eps
+    a = np.float32(0.0)
+    b = np.float32(1e-7)
+    delta = (float(b) - float(a)) / 2
+    A = oracle.group_advantages(np.array([a, b]), [0, 2], adv_eps=1e-6)
+    assert A[1] == pytest.approx(delta / 1e-6, rel=1e-12)
+    assert A[0] == pytest.approx(-delta / 1e-6, rel=1e-12)
+    A2 = oracle.group_advantages(np.array([a, b]), [0, 2], adv_eps=1e-6, eps_add=True)
+    assert A2[1] == pytest.approx(delta / (delta + 1e-6), rel=1e-12)
+    # far above eps the two conventions differ by the factor sd/(sd+eps)
+    A3 = oracle.group_advantages(np.array([0, 1], np.float32), [0, 2], adv_eps=1e-6, eps_add=True)
+    assert A3[1] == pytest.approx(0.5 / (0.5 + 1e-6), rel=1e-14)
+
+
+def test_adv_csr_example_matches_uniform_groups():
+    g = json.load(open(GOLDEN))["group_boundaries_example"]
+    rng = np.random.default_rng(1)
+    r = (rng.random(24) < 0.5).astype(np.float32)
+    A_csr = oracle.group_advantages(r, g["boundaries"])
+    A_uni = oracle.group_advantages(r, _uniform_bounds(24, g["samples_per_prompt"]))
+    assert np.array_equal(A_csr, A_uni)
+
+
+def test_adv_rejects_bad_input():
+    r = np.zeros(8, np.float32)
+    with pytest.raises(ValueError):
+        oracle.group_advantages(r, [0, 4, 4, 8])  # empty group
+    with pytest.raises(ValueError):
+        oracle.group_advantages(r, [0, 4, 7])  # does not end at B
+    with pytest.raises(ValueError):
+        oracle.group_advantages(np.array([0, np.nan], np.float32), [0, 2])
+
+
+# ----------------------------------------------------------------------------
+# log-softmax rows
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("V", [1, 2, 64, 4097, 151936])
+def test_logsoftmax_constant_row(V):
+    rows = np.full((2, V), 3.25, np.float32)
+    lse, lp = oracle.log_softmax_rows(rows, "f32", np.array([0, V - 1]))
+    assert np.allclose(lp, -math.log(V), rtol=0, atol=1e-12 * max(1, math.log(V)))
+
+
+def test_logsoftmax_matches_torch_float64():
+    rng = np.random.default_rng(5)
+    rows = rng.normal(scale=3.0, size=(16, 1000))
+    acts = rng.integers(0, 1000, 16)
+    lse, lp = oracle.log_softmax_rows(rows, "f64", acts)
+    ref = torch.log_softmax(torch.from_numpy(rows), dim=-1).numpy()
+    assert np.allclose(lp, ref[np.arange(16), acts], rtol=0, atol=1e-12)
+    assert np.allclose(lse, torch.logsumexp(torch.from_numpy(rows), -1).numpy(), atol=1e-12)
+
+
+def test_logsoftmax_shift_invariance_and_widening():
+    rng = np.random.default_rng(6)
+    x = rng.normal(size=(4, 333)).astype(np.float32)
+    acts = np.array([0, 5, 100, 332])
+    _, a = oracle.log_softmax_rows(x, "f32", acts)
+    _, b = oracle.log_softmax_rows(x.astype(np.float64) + 1000.0, "f64", acts)
+    assert np.allclose(a, b, atol=1e-11)
+    # bf16 bits widen exactly: the same values stored as f32 give the same result
+    bf = torch.from_numpy(x).to(torch.bfloat16)
+    _, c = oracle.log_softmax_rows(bf.view(torch.uint16).numpy(), "bf16", acts)
+    _, d = oracle.log_softmax_rows(bf.float().numpy(), "f32", acts)
+    assert np.array_equal(c, d)
+    # f16 likewise, including subnormals
+    h = torch.from_numpy(x * 1e-5).to(torch.float16)
+    _, e = oracle.log_softmax_rows(h.view(torch.uint16).numpy(), "f16", acts)
+    _, f = oracle.log_softmax_rows(h.float().numpy(), "f32", acts)
+    assert np.array_equal(e, f)
+
+
+# ----------------------------------------------------------------------------
+# storage rounding (used for rounded expectations)
+# ----------------------------------------------------------------------------
+def test_round_to_matches_torch_casts():
+    rng = np.random.default_rng(7)
+    x = np.concatenate([rng.normal(size=5000) * 10.0 ** rng.integers(-12, 4, 5000),
+                        [0.0, -0.0, 1e-40, 6e-8, 3e-5, 65504.0, 70000.0]])
+    for dt, tdt in (("bf16", torch.bfloat16), ("f16", torch.float16)):
+        got = oracle.round_to(x, dt)
+        # torch rounds double -> bf16/f16 directly, nearest-even
+        want = torch.from_numpy(x).to(tdt).view(torch.uint16).numpy()
+        assert np.array_equal(got, want), dt
+    assert np.array_equal(oracle.round_to(x, "f32"), x.astype(np.float32))
+
+
+# ----------------------------------------------------------------------------
+# the fused path: helpers
+# ----------------------------------------------------------------------------
+def _case(B=4, T=5, V=11, spp=2, seed=0, scale=1.0, dtype="f64"):
+    rng = np.random.default_rng(seed)
+    X = rng.normal(scale=scale, size=(B, T, V))
+    Y = X + rng.normal(scale=0.3, size=(B, T, V))
+    acts = rng.integers(0, V, (B, T))
+    mask = (rng.random((B, T)) < 0.8).astype(np.uint8)
+    mask[:, 0] = 1
+    rewards = rng.normal(size=B).astype(np.float32)
+    bounds = _uniform_bounds(B, spp)
+    lp = torch.log_softmax(torch.from_numpy(X), -1).numpy()
+    exact = np.take_along_axis(lp, acts[..., None], -1)[..., 0]
+    old = exact + rng.normal(scale=0.1, size=(B, T))
+    return dict(policy=X, ref=Y, dtype=dtype, actions=acts, old=old, mask=mask,
+                rewards=rewards, bounds=bounds)
+
+
+def _run(c, **kw):
+    args = dict(eps_lo=0.2, eps_hi=0.2, beta=0.04)
+    args.update(kw)
+    return oracle.fused(c["policy"], c["ref"], c["dtype"], c["actions"], c["old"], c["mask"],
+                        c["rewards"], c["bounds"], **args)
+
+
+# ----------------------------------------------------------------------------
+# special case -> library routine: cross-entropy gradient
+# ----------------------------------------------------------------------------
+def test_special_case_is_cross_entropy_gradient():
+    # A = +1 (pair of rewards), one active token (c = 1), r = 1, beta = 0:
+    # dL/dx = -(onehot - softmax) = the gradient of cross-entropy.
+    rng = np.random.default_rng(11)
+    V = 37
+    x = rng.normal(size=(2, 1, V))
+    a = np.array([[5], [0]])
+    lp = torch.log_softmax(torch.from_numpy(x[0, 0]), -1)[5].item()
+    c = dict(policy=x, ref=x, dtype="f64", actions=a, old=np.array([[lp], [0.0]]),
+             mask=np.array([[1], [0]], np.uint8), rewards=np.array([1, 0], np.float32),
+             bounds=np.array([0, 2]))
+    res = _run(c, beta=0.0)
+    xt = torch.from_numpy(x[0, 0]).clone().requires_grad_(True)
+    torch.nn.functional.cross_entropy(xt[None], torch.tensor([5]), reduction="sum").backward()
+    assert np.allclose(res["grad_f64"][0, 0], xt.grad.numpy(), rtol=0, atol=1e-14)
+    assert np.all(res["grad_f64"][1] == 0)
+    assert res["loss"] == pytest.approx(-1.0, abs=1e-14)
+
+
+# ----------------------------------------------------------------------------
+# identity: ref == policy and old == logp -> r == 1, KL == 0 exactly
+# ----------------------------------------------------------------------------
+def test_identity_ratio_one_kl_zero():
+    c = _case(seed=2)
+    c["ref"] = c["policy"]
+    first = _run(c)
+    c["old"] = first["logp"]
+    res = _run(c)
+    m = c["mask"].astype(bool)
+    assert np.all(res["ratio"][m] == 1.0)
+    assert res["kl"] == 0.0 and np.all(res["per_seq_kl"] == 0.0)
+    A = res["A"]
+    N = m.sum()
+    assert res["loss"] == pytest.approx(-(A[:, None] * m).sum() / N, rel=1e-14)
+    for eps in (0.01, 0.2, 0.5):
+        assert _run(c, eps_lo=eps, eps_hi=eps)["loss"] == res["loss"]
+
+
+# ----------------------------------------------------------------------------
+# clipping: zero policy gradient exactly where the clip branch is active
+# ----------------------------------------------------------------------------
+def test_clipped_tokens_have_zero_gradient():
+    V = 9
+    rng = np.random.default_rng(4)
+    x = rng.normal(size=(4, 1, V))
+    acts = np.array([[1], [2], [3], [4]])
+    lp = np.take_along_axis(torch.log_softmax(torch.from_numpy(x), -1).numpy(),
+                            acts[..., None], -1)[..., 0]
+    # groups {0,1} and {2,3}, rewards make A = (+1,-1,+1,-1)
+    rewards = np.array([1, 0, 1, 0], np.float32)
+    # ratios: 1.5 (A>0 clipped), 0.5 (A<0 clipped), 0.5 (A>0 unclipped), 1.5 (A<0 unclipped)
+    old = lp - np.log(np.array([[1.5], [0.5], [0.5], [1.5]]))
+    c = dict(policy=x, ref=x, dtype="f64", actions=acts, old=old, mask=np.ones((4, 1), np.uint8),
+             rewards=rewards, bounds=np.array([0, 2, 4]))
+    res = _run(c, beta=0.0)
+    g = res["grad_f64"]
+    assert np.all(g[0] == 0) and np.all(g[1] == 0)
+    assert np.all(g[2] != 0) and np.all(g[3] != 0)
+    sm = torch.softmax(torch.from_numpy(x), -1).numpy()
+    onehot = np.eye(V)[acts[:, 0]][:, None]
+    # unclipped rows: w = c * (-A r), c = 1/4
+    assert np.allclose(g[2], 0.25 * (-1 * 0.5) * (onehot[2] - sm[2]), atol=1e-15)
+    assert np.allclose(g[3], 0.25 * (+1 * 1.5) * (onehot[3] - sm[3]), atol=1e-15)
+    # with beta > 0 the KL term still moves the clipped rows (ref != policy)
+    c["ref"] = x + 0.5
+    c["ref"][:, :, 0] += 1.0
+    res2 = _run(c, beta=0.3)
+    assert np.any(res2["grad_f64"][0] != 0)
+
+
+def test_degenerate_group_gradient():
+    c = _case(B=4, T=3, V=7, spp=2, seed=9)
+    c["rewards"] = np.array([2.0, 2.0, 0.0, 1.0], np.float32)  # group 0 degenerate
+    res = _run(c, beta=0.0)
+    assert np.all(res["grad_f64"][:2] == 0.0)
+    assert np.all(res["A"][:2] == 0.0)
+    res_b = _run(c, beta=0.5)
+    # only the KL part remains: w = c * beta * (1 - e^d)
+    m = c["mask"].astype(bool)
+    N = m.sum()
+    d = res_b["ref_logp"] - res_b["logp"]
+    w_expect = (1.0 / N) * 0.5 * (-np.expm1(d)) * m
+    assert np.allclose(res_b["w"][:2], w_expect[:2], rtol=1e-13, atol=1e-16)
+
+
+# ----------------------------------------------------------------------------
+# row sums, masked rows, masked-token invariance
+# ----------------------------------------------------------------------------
+def test_gradient_rows_sum_to_zero_and_masked_rows_are_zero():
+    c = _case(B=6, T=7, V=50, spp=3, seed=13, scale=2.0)
+    res = _run(c)
+    g = res["grad_f64"]
+    m = c["mask"].astype(bool)
+    wmax = np.abs(res["w"]).max()
+    assert np.all(np.abs(g.sum(-1)) <= 1e-14 * wmax)
+    assert np.all(g[~m] == 0.0)
+
+
+def test_masked_token_invariance():
+    c = _case(B=4, T=6, V=13, spp=2, seed=21)
+    base = _run(c)
+    m = c["mask"].astype(bool)
+    c2 = dict(c)
+    c2["policy"] = c["policy"].copy()
+    c2["ref"] = c["ref"].copy()
+    c2["old"] = c["old"].copy()
+    c2["actions"] = c["actions"].copy()
+    c2["policy"][~m] = np.nan
+    c2["ref"][~m] = np.inf
+    c2["old"][~m] = np.nan
+    c2["actions"][~m] = 10 ** 9
+    res = _run(c2)
+    for k in ("loss", "policy_loss", "kl"):
+        assert res[k] == base[k]
+    assert np.array_equal(res["grad"], base["grad"])
+    assert np.array_equal(res["per_seq_policy"], base["per_seq_policy"])
+
+
+# ----------------------------------------------------------------------------
+# finite differences
+# ----------------------------------------------------------------------------
+def _kink_free(res, c, eps_lo=0.2, eps_hi=0.2, band=1e-4):
+    r = res["ratio"]
+    return (np.abs(r - (1 + eps_hi)) > band) & (np.abs(r - (1 - eps_lo)) > band)
+
+
+@pytest.mark.parametrize("reduction", [0, 1])
+def test_finite_difference_logits(reduction):
+    c = _case(B=4, T=3, V=6, spp=2, seed=31)
+    c["old"] = c["old"] + np.random.default_rng(0).normal(scale=0.2, size=c["old"].shape)
+    res = _run(c, reduction=reduction)
+    safe = _kink_free(res, c)
+    X = c["policy"]
+    checked = 0
+    for b in range(4):
+        for t in range(3):
+            if not c["mask"][b, t] or not safe[b, t]:
+                continue
+            for v in range(6):
+                h = 1e-6 * max(1.0, abs(X[b, t, v]))
+                Xp = X.copy(); Xp[b, t, v] += h
+                Xm = X.copy(); Xm[b, t, v] -= h
+                lp = _run(dict(c, policy=Xp), reduction=reduction)["loss"]
+                lm = _run(dict(c, policy=Xm), reduction=reduction)["loss"]
+                fd = (lp - lm) / (2 * h)
+                g = res["grad_f64"][b, t, v]
+                assert fd == pytest.approx(g, rel=1e-6, abs=1e-9), (b, t, v)
+                checked += 1
+    assert checked > 20
+
+
+def test_finite_difference_logps_path():
+    rng = np.random.default_rng(41)
+    B, T = 4, 5
+    logp = rng.normal(-2, 0.5, (B, T))
+    old = logp + rng.normal(0, 0.15, (B, T))
+    ref = logp + rng.normal(0, 0.1, (B, T))
+    mask = (rng.random((B, T)) < 0.8).astype(np.uint8)
+    A = oracle.group_advantages(rng.normal(size=B).astype(np.float32), [0, 2, 4])
+    for reduction in (0, 1):
+        res = oracle.loss_from_logps(logp, ref, old, mask, A, 0.2, 0.28, 0.04,
+                                     reduction=reduction)
+        for b in range(B):
+            for t in range(T):
+                r = res["ratio"][b, t]
+                if not mask[b, t] or abs(r - 1.28) < 1e-4 or abs(r - 0.8) < 1e-4:
+                    continue
+                h = 1e-6
+                lpp = logp.copy(); lpp[b, t] += h
+                lpm = logp.copy(); lpm[b, t] -= h
+                fp = oracle.loss_from_logps(lpp, ref, old, mask, A, 0.2, 0.28, 0.04, reduction=reduction)["loss"]
+                fm = oracle.loss_from_logps(lpm, ref, old, mask, A, 0.2, 0.28, 0.04, reduction=reduction)["loss"]
+                assert (fp - fm) / (2 * h) == pytest.approx(res["w"][b, t], rel=1e-6, abs=1e-10)
+
+
+# ----------------------------------------------------------------------------
+# reductions
+# ----------------------------------------------------------------------------
+def test_kl_nonnegative_and_beta_zero():
+    c = _case(B=6, T=8, V=20, spp=3, seed=51, scale=2.0)
+    res = _run(c)
+    assert res["kl"] > 0 and np.all(res["per_seq_kl"] >= 0)
+    res0 = _run(c, beta=0.0)
+    assert res0["loss"] == res0["policy_loss"]
+    assert res["policy_loss"] == res0["policy_loss"]
+    assert res["loss"] == pytest.approx(res["policy_loss"] + 0.04 * res["kl"], rel=1e-15)
+
+
+def test_token_mean_equals_sequence_mean_for_equal_lengths():
+    c = _case(B=4, T=6, V=10, spp=2, seed=61)
+    c["mask"] = np.zeros((4, 6), np.uint8)
+    c["mask"][:, :4] = 1
+    a = _run(c, reduction=0)
+    b = _run(c, reduction=1)
+    for k in ("loss", "policy_loss", "kl"):
+        assert a[k] == pytest.approx(b[k], rel=1e-14)
+    assert np.allclose(a["grad_f64"], b["grad_f64"], rtol=1e-13, atol=1e-18)
+
+
+def test_two_level_reduction_equals_single_loop():
+    c = _case(B=6, T=9, V=12, spp=3, seed=71)
+    for reduction in (0, 1):
+        res = _run(c, reduction=reduction)
+        m = c["mask"].astype(bool)
+        A = res["A"]
+        L = m.sum(1)
+        N, S = L.sum(), (L > 0).sum()
+        pol = kl = 0.0
+        for b in range(6):  # brute force: one pass over tokens
+            for t in range(9):
+                if not m[b, t]:
+                    continue
+                r = math.exp(res["logp"][b, t] - c["old"][b, t])
+                rc = min(max(r, 0.8), 1.2)
+                p = -min(r * A[b], rc * A[b])
+                d = res["ref_logp"][b, t] - res["logp"][b, t]
+                k = math.exp(d) - d - 1
+                cw = 1 / N if reduction == 0 else 1 / (S * L[b])
+                pol += cw * p
+                kl += cw * k
+        assert res["policy_loss"] == pytest.approx(pol, rel=1e-13, abs=1e-15)
+        assert res["kl"] == pytest.approx(kl, rel=1e-9)
+
+
+def test_empty_mask_gives_zero():
+    c = _case(B=2, T=3, V=4, spp=2, seed=81)
+    c["mask"] = np.zeros((2, 3), np.uint8)
+    res = _run(c)
+    assert res["loss"] == 0.0 and res["policy_loss"] == 0.0 and res["kl"] == 0.0
+    assert np.all(res["grad_f64"] == 0.0)
+
+
+# ----------------------------------------------------------------------------
+# hand-worked fixtures
+# ----------------------------------------------------------------------------
+_G = json.load(open(GOLDEN))
+
+
+@pytest.mark.parametrize("case", _G["cases"], ids=[c["name"] for c in _G["cases"]])
+def test_hand_worked_case(case):
+    B, T, V = case["B"], case["T"], case["V"]
+    c = dict(policy=np.array(case["policy"], np.float64), ref=np.array(case["ref"], np.float64),
+             dtype="f64", actions=np.array(case["actions"]), old=np.array(case["old"]),
+             mask=np.array(case["mask"], np.uint8), rewards=np.array(case["rewards"], np.float32),
+             bounds=_uniform_bounds(B, case["samples_per_prompt"]))
+    res = _run(c, eps_lo=case["eps_lo"], eps_hi=case["eps_hi"], beta=case["beta"],
+               reduction=case["reduction"])
+    e = case["expect"]
+    for k in ("loss", "policy_loss", "kl"):
+        assert res[k] == pytest.approx(e[k], rel=1e-12, abs=1e-15), k
+    assert np.allclose(res["per_seq_policy"], e["per_seq_policy"], atol=1e-12)
+    assert np.allclose(res["per_seq_kl"], e["per_seq_kl"], atol=1e-12)
+    assert np.array_equal(res["per_seq_active"], np.array(e["per_seq_active"], np.float64))
+    assert np.allclose(res["A"], e["A"], atol=1e-12)
+    assert np.allclose(res["grad_f64"], np.array(e["grad"]), rtol=1e-12, atol=1e-15)
+
+
+def test_length_weights_table():
+    lw = _G["length_weights"]
+    L = np.array(lw["lengths"])
+    B, T = len(L), lw["T"]
+    mask = (np.arange(T)[None] < L[:, None]).astype(np.uint8)
+    logp = np.full((B, T), -1.0)
+    A = -np.ones(B)  # g_pol = -A r = 1 with r = 1, so w = c exactly
+    for reduction, key in ((0, "token_mean_total_weight"), (1, "sequence_mean_total_weight")):
+        res = oracle.loss_from_logps(logp, None, logp, mask, A, 0.2, 0.2, 0.0, reduction=reduction)
+        assert np.allclose(res["w"].sum(1), lw[key], rtol=1e-14)
