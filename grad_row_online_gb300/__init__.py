@@ -1,0 +1,293 @@
+"""GB300 (sm_103a) fused GRPO loss: Python binding of libgrpo_gb300.so.
+
+Argument marshalling only: every step of the loss runs in the library's CUDA
+kernels (see ``include/grpo.h`` for the exact contract).  PyTorch provides
+device memory and the current stream.  If the library is missing this module
+raises; there is no fallback.
+
+    import grad_row_online_gb300 as g
+    res = g.grpo_loss_fwd_bwd(policy_logits, ref_logits, action_ids, old_logps,
+                              completion_mask, rewards, samples_per_prompt=8,
+                              clip_eps=0.2, beta=0.04)
+    res["loss"], res["policy_loss"], res["kl"], res["grad"]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import _build
+
+__all__ = ["grpo_workspace_size", "grpo_group_adv", "grpo_loss_fwd_bwd", "grpo_loss_from_logps",
+           "grpo_read_device_status", "grpo_status_string", "GrpoError", "library_path",
+           "GRPO_ADV_EPS_ADD", "GRPO_SKIP_MASKED_GRAD_ROWS"]
+
+GRPO_ADV_EPS_ADD = 1
+GRPO_SKIP_MASKED_GRAD_ROWS = 2
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+_REDUCTIONS = {"token_mean": 0, "sequence_mean": 1}
+
+
+class GrpoError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {grpo_status_string(code)} (status {code})")
+        self.code = code
+
+
+class _Groups(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int64), ("samples_per_prompt", ctypes.c_int32),
+                ("_reserved", ctypes.c_int32), ("group_boundaries", ctypes.c_void_p),
+                ("num_groups", ctypes.c_int64)]
+
+
+class _Profile(ctypes.Structure):
+    _fields_ = [("start", ctypes.c_void_p), ("stop", ctypes.c_void_p)]
+
+
+class _Params(ctypes.Structure):
+    _fields_ = [("clip_eps_lo", ctypes.c_float), ("clip_eps_hi", ctypes.c_float),
+                ("beta", ctypes.c_float), ("adv_eps", ctypes.c_float),
+                ("grad_scale", ctypes.c_float), ("reduction", ctypes.c_int32),
+                ("flags", ctypes.c_uint32), ("_reserved", ctypes.c_int32),
+                ("profile", ctypes.POINTER(_Profile))]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded C library (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"{_build.LIB} is missing: build it with __graft_entry__.build()")
+        L = ctypes.CDLL(_build.LIB)
+        vp, i64, f32, u32, sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_uint32,
+                                 ctypes.c_size_t)
+        L.grpo_workspace_size.argtypes = [i64, i64, i64]
+        L.grpo_workspace_size.restype = sz
+        L.grpo_group_adv.argtypes = [vp, ctypes.POINTER(_Groups), f32, u32, vp, vp, sz, vp]
+        L.grpo_group_adv.restype = ctypes.c_int
+        L.grpo_loss_fwd_bwd.argtypes = [vp, vp, ctypes.c_int, i64, i64, i64, vp, vp, vp, vp,
+                                        ctypes.POINTER(_Groups), ctypes.POINTER(_Params), vp, vp,
+                                        vp, vp, vp, vp, sz, vp]
+        L.grpo_loss_fwd_bwd.restype = ctypes.c_int
+        L.grpo_loss_from_logps.argtypes = [vp, vp, vp, vp, i64, i64, vp, ctypes.POINTER(_Groups),
+                                           ctypes.POINTER(_Params), vp, vp, vp, vp, vp, sz, vp]
+        L.grpo_loss_from_logps.restype = ctypes.c_int
+        L.grpo_read_device_status.argtypes = [vp, vp]
+        L.grpo_read_device_status.restype = ctypes.c_int
+        L.grpo_status_string.argtypes = [ctypes.c_int]
+        L.grpo_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def grpo_status_string(code: int) -> str:
+    return lib().grpo_status_string(int(code)).decode()
+
+
+def grpo_workspace_size(B: int, T: int, num_groups: int = 0) -> int:
+    return int(lib().grpo_workspace_size(B, T, num_groups))
+
+
+# --------------------------------------------------------------------------
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> torch.Tensor:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _groups(B: int, samples_per_prompt: int, group_boundaries) -> tuple[_Groups, object]:
+    g = _Groups()
+    g.num_seqs = B
+    g.samples_per_prompt = int(samples_per_prompt or 0)
+    keep = None
+    if group_boundaries is not None:
+        gb = group_boundaries
+        if not isinstance(gb, torch.Tensor):
+            gb = torch.tensor(list(gb), dtype=torch.int64, device="cuda")
+        _dev(gb, "group_boundaries", torch.int64)
+        g.group_boundaries = gb.data_ptr()
+        g.num_groups = gb.numel() - 1
+        keep = gb
+    return g, keep
+
+
+def _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction, flags, profile):
+    p = _Params()
+    p.clip_eps_lo = float(clip_eps)
+    p.clip_eps_hi = float(clip_eps if clip_eps_hi is None else clip_eps_hi)
+    p.beta = float(beta)
+    p.adv_eps = float(adv_eps)
+    p.grad_scale = float(grad_scale)
+    p.reduction = _REDUCTIONS[reduction] if isinstance(reduction, str) else int(reduction)
+    p.flags = int(flags)
+    prof = None
+    if profile is not None:
+        prof = _Profile(profile[0].cuda_event if hasattr(profile[0], "cuda_event") else profile[0],
+                        profile[1].cuda_event if hasattr(profile[1], "cuda_event") else profile[1])
+        p.profile = ctypes.pointer(prof)
+    return p, prof
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _workspace(B, T, G, workspace, device):
+    need = grpo_workspace_size(B, T, G)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    return workspace, need
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise GrpoError(code, what)
+
+
+# --------------------------------------------------------------------------
+def grpo_group_adv(rewards: torch.Tensor, *, samples_per_prompt: int = 0, group_boundaries=None,
+                   adv_eps: float = 1e-6, eps_add: bool = False, out: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Group-normalised advantages [B] (f32)."""
+    _dev(rewards, "rewards", torch.float32)
+    B = rewards.numel()
+    g, keep = _groups(B, samples_per_prompt, group_boundaries)
+    out = torch.empty(B, dtype=torch.float32, device=rewards.device) if out is None else out
+    ws, need = _workspace(B, 0, 0, workspace, rewards.device)
+    rc = lib().grpo_group_adv(_ptr(rewards), ctypes.byref(g), float(adv_eps),
+                              GRPO_ADV_EPS_ADD if eps_add else 0, _ptr(out), _ptr(ws),
+                              ws.numel(), _stream(stream))
+    _check(rc, "grpo_group_adv")
+    return out
+
+
+def grpo_loss_fwd_bwd(policy_logits: torch.Tensor, ref_logits: torch.Tensor,
+                      action_ids: torch.Tensor, old_logps: torch.Tensor,
+                      completion_mask: torch.Tensor, rewards: torch.Tensor, *,
+                      samples_per_prompt: int = 0, group_boundaries=None, clip_eps: float = 0.2,
+                      clip_eps_hi: Optional[float] = None, beta: float = 0.04,
+                      adv_eps: float = 1e-6, eps_add: bool = False, grad_scale: float = 1.0,
+                      reduction="token_mean", grad=True, skip_masked_grad_rows: bool = False,
+                      want_per_seq: bool = False, want_logps: bool = False,
+                      want_adv: bool = False, out3: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None, stream=None,
+                      profile=None) -> dict:
+    """Fused GRPO loss forward + dL/dlogits.
+
+    ``grad``: True (allocate), a tensor to write into (may be
+    ``policy_logits`` itself for an in-place gradient), or None/False
+    (forward only).  Returns a dict of device tensors: ``out3`` ([loss,
+    policy_loss, kl]), ``loss``, ``policy_loss``, ``kl`` (0-d views),
+    ``grad``, and the optional ``per_seq`` [3,B], ``logps`` [B,T], ``adv`` [B]."""
+    if policy_logits.dtype not in _DTYPES:
+        raise ValueError(f"unsupported logits dtype {policy_logits.dtype}")
+    _dev(policy_logits, "policy_logits")
+    _dev(ref_logits, "ref_logits", policy_logits.dtype)
+    if policy_logits.dim() != 3 or ref_logits.shape != policy_logits.shape:
+        raise ValueError("policy_logits and ref_logits must both be [B, T, V]")
+    B, T, V = policy_logits.shape
+    _dev(action_ids, "action_ids", torch.int64)
+    _dev(old_logps, "old_logps", torch.float32)
+    _dev(rewards, "rewards", torch.float32)
+    mask = _dev(completion_mask, "completion_mask")
+    if mask.dtype == torch.bool:
+        mask = mask.view(torch.uint8)
+    elif mask.dtype != torch.uint8:
+        raise ValueError("completion_mask must be bool or uint8")
+    if action_ids.shape != (B, T) or old_logps.shape != (B, T) or mask.shape != (B, T):
+        raise ValueError("action_ids, old_logps and completion_mask must be [B, T]")
+    if rewards.shape != (B,):
+        raise ValueError("rewards must be [B]")
+    dev = policy_logits.device
+    g, keep = _groups(B, samples_per_prompt, group_boundaries)
+    p, prof = _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction,
+                      (GRPO_ADV_EPS_ADD if eps_add else 0)
+                      | (GRPO_SKIP_MASKED_GRAD_ROWS if skip_masked_grad_rows else 0), profile)
+    if grad is True:
+        grad_t = torch.empty_like(policy_logits)
+    elif grad is None or grad is False:
+        grad_t = None
+    else:
+        grad_t = _dev(grad, "grad", policy_logits.dtype)
+        if grad_t.shape != policy_logits.shape:
+            raise ValueError("grad must have the shape of policy_logits")
+    out3 = torch.empty(3, dtype=torch.float32, device=dev) if out3 is None else out3
+    per_seq = torch.empty((3, B), dtype=torch.float32, device=dev) if want_per_seq else None
+    logps = torch.empty((B, T), dtype=torch.float32, device=dev) if want_logps else None
+    adv = torch.empty(B, dtype=torch.float32, device=dev) if want_adv else None
+    ws, need = _workspace(B, T, 0, workspace, dev)
+    rc = lib().grpo_loss_fwd_bwd(_ptr(policy_logits), _ptr(ref_logits), _DTYPES[policy_logits.dtype],
+                                 B, T, V, _ptr(action_ids), _ptr(old_logps), _ptr(mask),
+                                 _ptr(rewards), ctypes.byref(g), ctypes.byref(p), _ptr(grad_t),
+                                 _ptr(out3), _ptr(per_seq), _ptr(logps), _ptr(adv), _ptr(ws),
+                                 ws.numel(), _stream(stream))
+    _check(rc, "grpo_loss_fwd_bwd")
+    return {"out3": out3, "loss": out3[0], "policy_loss": out3[1], "kl": out3[2],
+            "grad": grad_t, "per_seq": per_seq, "logps": logps, "adv": adv, "workspace": ws}
+
+
+def grpo_loss_from_logps(logps: torch.Tensor, old_logps: torch.Tensor,
+                         ref_logps: Optional[torch.Tensor], completion_mask: torch.Tensor,
+                         rewards: torch.Tensor, *, samples_per_prompt: int = 0,
+                         group_boundaries=None, clip_eps: float = 0.2,
+                         clip_eps_hi: Optional[float] = None, beta: float = 0.04,
+                         adv_eps: float = 1e-6, eps_add: bool = False, grad_scale: float = 1.0,
+                         reduction="token_mean", grad=True, want_per_seq: bool = False,
+                         want_adv: bool = False, out3: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """GRPO loss from per-token log-probs; ``grad`` gives dL/dlogp [B,T]."""
+    _dev(logps, "logps", torch.float32)
+    B, T = logps.shape
+    _dev(old_logps, "old_logps", torch.float32)
+    if ref_logps is not None:
+        _dev(ref_logps, "ref_logps", torch.float32)
+    _dev(rewards, "rewards", torch.float32)
+    mask = _dev(completion_mask, "completion_mask")
+    if mask.dtype == torch.bool:
+        mask = mask.view(torch.uint8)
+    dev = logps.device
+    g, keep = _groups(B, samples_per_prompt, group_boundaries)
+    p, prof = _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction,
+                      GRPO_ADV_EPS_ADD if eps_add else 0, None)
+    if grad is True:
+        grad_t = torch.empty((B, T), dtype=torch.float32, device=dev)
+    elif grad is None or grad is False:
+        grad_t = None
+    else:
+        grad_t = _dev(grad, "grad", torch.float32)
+    out3 = torch.empty(3, dtype=torch.float32, device=dev) if out3 is None else out3
+    per_seq = torch.empty((3, B), dtype=torch.float32, device=dev) if want_per_seq else None
+    adv = torch.empty(B, dtype=torch.float32, device=dev) if want_adv else None
+    ws, need = _workspace(B, T, 0, workspace, dev)
+    rc = lib().grpo_loss_from_logps(_ptr(logps), _ptr(old_logps), _ptr(ref_logps), _ptr(mask),
+                                    B, T, _ptr(rewards), ctypes.byref(g), ctypes.byref(p),
+                                    _ptr(grad_t), _ptr(out3), _ptr(per_seq), _ptr(adv), _ptr(ws),
+                                    ws.numel(), _stream(stream))
+    _check(rc, "grpo_loss_from_logps")
+    return {"out3": out3, "loss": out3[0], "policy_loss": out3[1], "kl": out3[2],
+            "grad": grad_t, "per_seq": per_seq, "adv": adv, "workspace": ws}
+
+
+def grpo_read_device_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronises and returns the device status word of a workspace."""
+    return int(lib().grpo_read_device_status(_ptr(workspace), _stream(stream)))

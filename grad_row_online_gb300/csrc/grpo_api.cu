@@ -1,0 +1,271 @@
+// grpo_api.cu -- the C ABI of libgrpo_gb300.so (declared in include/grpo.h):
+// argument validation, workspace carving and the launch sequence.
+//
+// Every host-checkable error is found before the first CUDA call, so a
+// rejected call launches nothing.  A call enqueues, in stream order:
+//   memset of the 16-byte workspace header (status word, row counter)
+//   prep     group advantages (+ active-token counts)   grpo_prep.cu
+//   rows     fused sweep over vocabulary rows            grpo_rows.cu
+//   reduce   fixed-order reduction to the scalars        grpo_reduce.cu
+// or, for the logps-only boundary, prep + the two kernels of grpo_logps.cu.
+#include <math.h>
+#include <string.h>
+
+#include "grpo_internal.cuh"
+
+using namespace grpo;
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+size_t elem_size(grpo_dtype_t dt) { return dt == GRPO_F32 ? 4 : 2; }
+
+grpo_status_t check_params(const grpo_params_t* p) {
+  if (!p) return GRPO_ERR_NULL;
+  if (!(isfinite(p->clip_eps_lo) && isfinite(p->clip_eps_hi) && isfinite(p->beta) &&
+        isfinite(p->adv_eps) && isfinite(p->grad_scale)))
+    return GRPO_ERR_PARAM;
+  if (!(p->clip_eps_lo >= 0.f && p->clip_eps_lo < 1.f)) return GRPO_ERR_PARAM;
+  if (!(p->clip_eps_hi >= 0.f)) return GRPO_ERR_PARAM;
+  if (!(p->beta >= 0.f)) return GRPO_ERR_PARAM;
+  if (!(p->adv_eps > 0.f)) return GRPO_ERR_PARAM;
+  if (p->reduction != GRPO_TOKEN_MEAN && p->reduction != GRPO_SEQUENCE_MEAN) return GRPO_ERR_PARAM;
+  if (p->flags & ~(GRPO_ADV_EPS_ADD | GRPO_SKIP_MASKED_GRAD_ROWS)) return GRPO_ERR_PARAM;
+  return GRPO_OK;
+}
+
+// Resolves the group spec to (spp, boundaries, G).
+grpo_status_t check_groups(const grpo_groups_t* g, int64_t B, int32_t* spp,
+                           const int64_t** bounds, int64_t* G) {
+  if (!g) return GRPO_ERR_NULL;
+  if (g->num_seqs != B) return GRPO_ERR_SHAPE;
+  const bool has_spp = g->samples_per_prompt != 0;
+  const bool has_csr = g->group_boundaries != nullptr;
+  if (has_spp == has_csr || g->samples_per_prompt < 0) return GRPO_ERR_GROUP_SPEC;
+  if (has_spp) {
+    if (B % g->samples_per_prompt != 0) return GRPO_ERR_SHAPE;
+    *spp = g->samples_per_prompt;
+    *bounds = nullptr;
+    *G = B / g->samples_per_prompt;
+  } else {
+    if (g->num_groups < 0 || g->num_groups > B || (B > 0 && g->num_groups < 1))
+      return GRPO_ERR_SHAPE;
+    if (!aligned(g->group_boundaries, 8)) return GRPO_ERR_ALIGN;
+    *spp = 0;
+    *bounds = g->group_boundaries;
+    *G = g->num_groups;
+  }
+  return GRPO_OK;
+}
+
+grpo_status_t check_ws(const void* ws, size_t ws_bytes, int64_t B, int64_t T) {
+  if (!ws) return GRPO_ERR_NULL;
+  if (!aligned(ws, 256)) return GRPO_ERR_ALIGN;
+  if (ws_bytes < WsLayout(B, T).total) return GRPO_ERR_WORKSPACE;
+  return GRPO_OK;
+}
+
+// 2^(j/64) as float pairs and the three-part split of ln2/64 used by the
+// precise exponential (Tang's method); built once from libm's double exp2.
+const ExpTable& exp_table() {
+  static const ExpTable tab = [] {
+    ExpTable t;
+    for (int j = 0; j < 64; ++j) {
+      double v = exp2((double)j / 64.0);
+      t.hi[j] = (float)v;
+      t.lo[j] = (float)(v - (double)t.hi[j]);
+    }
+    const double L = 0.69314718055994530942 / 64.0;
+    const double c1 = floor(L * 131072.0 + 0.5) / 131072.0;  // 11 significant bits
+    t.c1 = (float)c1;
+    t.c2 = (float)(L - c1);
+    t.c3 = (float)(L - c1 - (double)t.c2);
+    t.inv = (float)(64.0 / 0.69314718055994530942);
+    return t;
+  }();
+  return tab;
+}
+
+grpo_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? GRPO_OK : GRPO_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" size_t grpo_workspace_size(int64_t B, int64_t T, int64_t num_groups) {
+  if (B < 0 || T < 0 || num_groups < 0) return 0;
+  return WsLayout(B, T).total;
+}
+
+extern "C" grpo_status_t grpo_group_adv(const float* rewards, const grpo_groups_t* groups,
+                                        float adv_eps, uint32_t flags, float* adv_out,
+                                        void* ws, size_t ws_bytes, void* stream) {
+  if (!groups || !adv_out) return GRPO_ERR_NULL;
+  const int64_t B = groups->num_seqs;
+  if (B < 0) return GRPO_ERR_SHAPE;
+  if (B > 0 && !rewards) return GRPO_ERR_NULL;
+  int32_t spp;
+  const int64_t* bounds;
+  int64_t G;
+  grpo_status_t st = check_groups(groups, B, &spp, &bounds, &G);
+  if (st != GRPO_OK) return st;
+  if (!(isfinite(adv_eps) && adv_eps > 0.f)) return GRPO_ERR_PARAM;
+  if (flags & ~GRPO_ADV_EPS_ADD) return GRPO_ERR_PARAM;
+  if (!aligned(rewards, 4) || !aligned(adv_out, 4)) return GRPO_ERR_ALIGN;
+  if ((st = check_ws(ws, ws_bytes, B, 0)) != GRPO_OK) return st;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  char* w = (char*)ws;
+  const WsLayout lay(B, 0);
+  WsHeader* hdr = (WsHeader*)w;
+  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return GRPO_ERR_CUDA;
+  PrepArgs pa{rewards, bounds, B, 0, G, spp, adv_eps, (int)(flags & GRPO_ADV_EPS_ADD),
+              nullptr, (double*)(w + lay.off_A), adv_out, nullptr, hdr};
+  return cuda_status(launch_prep(pa, s));
+}
+
+extern "C" grpo_status_t grpo_loss_fwd_bwd(
+    const void* policy_logits, const void* ref_logits, grpo_dtype_t dt, int64_t B, int64_t T,
+    int64_t V, const int64_t* action_ids, const float* old_logps,
+    const uint8_t* completion_mask, const float* rewards, const grpo_groups_t* groups,
+    const grpo_params_t* params, void* grad_logits, float* out3, float* per_seq,
+    float* logps_out, float* adv_out, void* ws, size_t ws_bytes, void* stream) {
+  if (dt != GRPO_F32 && dt != GRPO_BF16 && dt != GRPO_F16) return GRPO_ERR_DTYPE;
+  if (B < 0 || T < 0 || V < 1) return GRPO_ERR_SHAPE;
+  if (!out3 || !params || !groups) return GRPO_ERR_NULL;
+  const bool any_rows = B > 0 && T > 0;
+  if (any_rows && (!policy_logits || !ref_logits || !action_ids || !old_logps ||
+                   !completion_mask))
+    return GRPO_ERR_NULL;
+  if (B > 0 && !rewards) return GRPO_ERR_NULL;
+  grpo_status_t st = check_params(params);
+  if (st != GRPO_OK) return st;
+  int32_t spp;
+  const int64_t* bounds;
+  int64_t G;
+  if ((st = check_groups(groups, B, &spp, &bounds, &G)) != GRPO_OK) return st;
+  const size_t es = elem_size(dt);
+  if (!aligned(policy_logits, es) || !aligned(ref_logits, es) || !aligned(grad_logits, es) ||
+      !aligned(action_ids, 8) || !aligned(old_logps, 4) || !aligned(rewards, 4) ||
+      !aligned(out3, 4) || !aligned(per_seq, 4) || !aligned(logps_out, 4) ||
+      !aligned(adv_out, 4))
+    return GRPO_ERR_ALIGN;
+  if ((st = check_ws(ws, ws_bytes, B, T)) != GRPO_OK) return st;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  char* w = (char*)ws;
+  const WsLayout lay(B, T);
+  WsHeader* hdr = (WsHeader*)w;
+  int32_t* L = (int32_t*)(w + lay.off_L);
+  double* A = (double*)(w + lay.off_A);
+  double* slot_p = (double*)(w + lay.off_slots);
+  double* slot_k = slot_p + B * T;
+
+  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return GRPO_ERR_CUDA;
+  PrepArgs pa{rewards, bounds, B, T, G, spp, params->adv_eps,
+              (int)(params->flags & GRPO_ADV_EPS_ADD), completion_mask, A, adv_out, L, hdr};
+  cudaError_t e = launch_prep(pa, s);
+  if (e != cudaSuccess) return GRPO_ERR_CUDA;
+
+  if (any_rows) {
+    RowArgs ra;
+    ra.policy = policy_logits;
+    ra.ref = ref_logits;
+    ra.grad = grad_logits;
+    ra.actions = action_ids;
+    ra.old = old_logps;
+    ra.mask = completion_mask;
+    ra.L = L;
+    ra.A = A;
+    ra.slot_p = slot_p;
+    ra.slot_k = slot_k;
+    ra.logps_out = logps_out;
+    ra.hdr = hdr;
+    ra.B = B;
+    ra.T = T;
+    ra.V = V;
+    ra.eps_lo = params->clip_eps_lo;
+    ra.eps_hi = params->clip_eps_hi;
+    ra.beta = params->beta;
+    ra.grad_scale = params->grad_scale;
+    ra.reduction = params->reduction;
+    ra.flags = params->flags;
+    ra.precise_ok = dt == GRPO_F32;
+    ra.tab = exp_table();
+    e = launch_rows(ra, dt, params->profile, s);
+    if (e != cudaSuccess) return GRPO_ERR_CUDA;
+  }
+  ReduceArgs rd{completion_mask, L, slot_p, slot_k, B, T, params->beta, params->reduction,
+                hdr, out3, per_seq};
+  return cuda_status(launch_reduce(rd, s));
+}
+
+extern "C" grpo_status_t grpo_loss_from_logps(const float* logps, const float* old_logps,
+                                              const float* ref_logps,
+                                              const uint8_t* completion_mask, int64_t B,
+                                              int64_t T, const float* rewards,
+                                              const grpo_groups_t* groups,
+                                              const grpo_params_t* params, float* grad_logps,
+                                              float* out3, float* per_seq, float* adv_out,
+                                              void* ws, size_t ws_bytes, void* stream) {
+  if (B < 0 || T < 0) return GRPO_ERR_SHAPE;
+  if (!out3 || !params || !groups) return GRPO_ERR_NULL;
+  grpo_status_t st = check_params(params);
+  if (st != GRPO_OK) return st;
+  const bool any_rows = B > 0 && T > 0;
+  if (any_rows && (!logps || !old_logps || !completion_mask)) return GRPO_ERR_NULL;
+  if (any_rows && !ref_logps && params->beta != 0.f) return GRPO_ERR_NULL;
+  if (B > 0 && !rewards) return GRPO_ERR_NULL;
+  int32_t spp;
+  const int64_t* bounds;
+  int64_t G;
+  if ((st = check_groups(groups, B, &spp, &bounds, &G)) != GRPO_OK) return st;
+  if (!aligned(logps, 4) || !aligned(old_logps, 4) || !aligned(ref_logps, 4) ||
+      !aligned(rewards, 4) || !aligned(grad_logps, 4) || !aligned(out3, 4) ||
+      !aligned(per_seq, 4) || !aligned(adv_out, 4))
+    return GRPO_ERR_ALIGN;
+  if ((st = check_ws(ws, ws_bytes, B, T)) != GRPO_OK) return st;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  char* w = (char*)ws;
+  const WsLayout lay(B, T);
+  WsHeader* hdr = (WsHeader*)w;
+  int32_t* L = (int32_t*)(w + lay.off_L);
+  double* A = (double*)(w + lay.off_A);
+  double* seq = (double*)(w + lay.off_seq);
+  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return GRPO_ERR_CUDA;
+  PrepArgs pa{rewards, bounds, B, T, G, spp, params->adv_eps,
+              (int)(params->flags & GRPO_ADV_EPS_ADD), nullptr, A, adv_out, nullptr, hdr};
+  if (launch_prep(pa, s) != cudaSuccess) return GRPO_ERR_CUDA;
+  LogpsArgs la{logps, old_logps, ref_logps, completion_mask, A, L, seq, grad_logps, out3,
+               per_seq, hdr, B, T, params->clip_eps_lo, params->clip_eps_hi, params->beta,
+               params->grad_scale, params->reduction};
+  return cuda_status(launch_logps(la, s));
+}
+
+extern "C" grpo_status_t grpo_read_device_status(const void* ws, void* stream) {
+  if (!ws) return GRPO_ERR_NULL;
+  unsigned int h = 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return GRPO_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GRPO_ERR_CUDA;
+  return (grpo_status_t)h;
+}
+
+extern "C" const char* grpo_status_string(grpo_status_t status) {
+  switch ((int)status) {
+    case GRPO_OK: return "ok";
+    case GRPO_ERR_NULL: return "a required pointer is NULL";
+    case GRPO_ERR_SHAPE: return "invalid shape";
+    case GRPO_ERR_DTYPE: return "unsupported dtype";
+    case GRPO_ERR_ALIGN: return "misaligned pointer";
+    case GRPO_ERR_GROUP_SPEC: return "give exactly one of samples_per_prompt and group_boundaries";
+    case GRPO_ERR_PARAM: return "invalid loss parameter";
+    case GRPO_ERR_WORKSPACE: return "workspace too small";
+    case GRPO_ERR_CUDA: return "CUDA error";
+    case GRPO_ERR_ACTION_RANGE: return "action id outside [0, V) on an active token";
+    case GRPO_ERR_CSR: return "group_boundaries is not 0 = g0 < g1 < ... < gG = B";
+    case GRPO_ERR_NONFINITE_REWARD: return "non-finite reward";
+    default: return "several device-detected errors (OR of status bits)";
+  }
+}

@@ -1,0 +1,181 @@
+/*
+ * grpo.h -- C ABI of the GB300 (sm_103a) fused GRPO loss library
+ *           (libgrpo_gb300.so).
+ *
+ * What is computed (RL-Kernel "GRPO Loss" operator page, sections "Entry
+ * Point", "Tensor Contract", "Group specification", "Accuracy" and
+ * "Normalizer semantics"; dockyard_rl "GRPO and the clipped policy-gradient
+ * loss", sections "One loss, many algorithms" and "Reference-KL penalty";
+ * grpo.cpp README, section "CUDA"):
+ *
+ *   A_i      = (R_i - mean_g R) / max(std_g R, adv_eps)     population std;
+ *              A_i = 0 when every reward of the group is equal
+ *   logp     = x_a - logsumexp(x)      x = policy row, a = action id
+ *   ref_logp = y_a - logsumexp(y)      y = reference row
+ *   r        = exp(logp - old_logp)
+ *   p        = -min(r A, clip(r, 1 - eps_lo, 1 + eps_hi) A)
+ *   d        = ref_logp - logp,  k = e^d - d - 1                (k3 KL)
+ *   c        = 1 / max(N,1)                 token mean (N active tokens), or
+ *              1 / (max(S,1) L_i)           sequence mean (S live sequences)
+ *   policy_loss = sum c p,  kl = sum c k,  loss = policy_loss + beta kl
+ *   dL/dlogp    = w = grad_scale c (g_pol + beta (1 - e^d)),
+ *                 g_pol = 0 if (A>0, r>1+eps_hi) or (A<0, r<1-eps_lo), else -A r
+ *   dL/dx_v     = w (1[v = a] - softmax(x)_v)
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor arguments are DEVICE pointers to row-major contiguous
+ *     arrays owned by the caller; the library allocates nothing, keeps no
+ *     state between calls and is safe to call concurrently on different
+ *     streams with different workspaces.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns without synchronising.  Outputs are device values.
+ *   - completion_mask is one byte per token, nonzero = active.  Masked
+ *     tokens' logits, action ids and old_logps are never read: any value,
+ *     NaN included, is allowed there.
+ *   - Host-checkable errors (null pointers, shapes, parameters, alignment,
+ *     workspace size) are returned at once and nothing is launched.
+ *     Data-dependent errors found on the device (an action id outside
+ *     [0, V) on an active token, malformed CSR offsets, a non-finite reward)
+ *     set a bit in the workspace status word and make the three loss outputs
+ *     NaN; read them with grpo_read_device_status().  No kernel ever traps.
+ *   - Results are bitwise reproducible run to run: no reduction depends on
+ *     CTA scheduling.
+ */
+#ifndef GRPO_GB300_H
+#define GRPO_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GRPO_OK = 0,
+  GRPO_ERR_NULL = 1,       /* a required pointer is NULL */
+  GRPO_ERR_SHAPE = 2,      /* negative sizes, V < 1, B not a multiple of spp, ... */
+  GRPO_ERR_DTYPE = 3,      /* unknown grpo_dtype_t */
+  GRPO_ERR_ALIGN = 4,      /* a pointer is not aligned to its element size, or
+                              the workspace is not 256-byte aligned */
+  GRPO_ERR_GROUP_SPEC = 5, /* not exactly one of samples_per_prompt / boundaries */
+  GRPO_ERR_PARAM = 6,      /* eps / beta / adv_eps / grad_scale / reduction invalid */
+  GRPO_ERR_WORKSPACE = 7,  /* ws_bytes < grpo_workspace_size(...) */
+  GRPO_ERR_CUDA = 8,       /* a CUDA launch failed */
+  /* device-detected; bits of the status word (grpo_read_device_status) */
+  GRPO_ERR_ACTION_RANGE = 16,    /* active token with action id outside [0, V) */
+  GRPO_ERR_CSR = 32,             /* boundaries not 0 = g_0 < g_1 < ... < g_G = B */
+  GRPO_ERR_NONFINITE_REWARD = 64 /* a reward is NaN or infinite */
+} grpo_status_t;
+
+typedef enum { GRPO_F32 = 0, GRPO_BF16 = 1, GRPO_F16 = 2 } grpo_dtype_t;
+
+typedef enum { GRPO_TOKEN_MEAN = 0, GRPO_SEQUENCE_MEAN = 1 } grpo_reduction_t;
+
+/* Flags (grpo_params_t.flags and grpo_group_adv's flags). */
+#define GRPO_ADV_EPS_ADD 1u          /* divide by std + adv_eps instead of max(std, adv_eps) */
+#define GRPO_SKIP_MASKED_GRAD_ROWS 2u /* leave gradient rows of masked tokens untouched
+                                         (caller pre-zeroed them) instead of writing 0 */
+
+/* Group specification ("Group specification": provide exactly one of
+ * samples_per_prompt > 0, or CSR group_boundaries of length num_groups + 1
+ * with boundaries[0] = 0, boundaries[num_groups] = num_seqs and strictly
+ * increasing entries, e.g. {0, 8, 16, 24}). */
+typedef struct {
+  int64_t num_seqs;                /* B */
+  int32_t samples_per_prompt;      /* > 0: uniform groups of this size, B % spp == 0 */
+  int32_t _reserved;
+  const int64_t *group_boundaries; /* device pointer or NULL */
+  int64_t num_groups;              /* used with group_boundaries (>= 1 when B > 0) */
+} grpo_groups_t;
+
+/* Optional timing hook: when non-NULL, `start` / `stop` (cudaEvent_t handles)
+ * are recorded on the stream immediately before and after the fused row
+ * kernel, so a caller can time that kernel alone. */
+typedef struct {
+  void *start;
+  void *stop;
+} grpo_profile_t;
+
+typedef struct {
+  float clip_eps_lo;  /* eps_lo, 0 <= eps_lo < 1   (clip_eps on the pages) */
+  float clip_eps_hi;  /* eps_hi >= 0                (DAPO clip-higher when > eps_lo) */
+  float beta;         /* KL coefficient >= 0 */
+  float adv_eps;      /* > 0, 1e-6 on the pages */
+  float grad_scale;   /* finite; multiplies every gradient (1 = dL/dlogits) */
+  int32_t reduction;  /* grpo_reduction_t */
+  uint32_t flags;     /* GRPO_ADV_EPS_ADD | GRPO_SKIP_MASKED_GRAD_ROWS */
+  int32_t _reserved;
+  const grpo_profile_t *profile; /* host pointer or NULL */
+} grpo_params_t;
+
+/* Bytes of workspace the entry points below need for B sequences of T
+ * token slots in num_groups groups (any of the three entry points; a
+ * workspace of this size serves all of them).  The workspace is caller-owned
+ * device memory, 256-byte aligned, needs no initialisation, and must not be
+ * shared by calls that may run concurrently.  Returns 0 for invalid sizes. */
+size_t grpo_workspace_size(int64_t B, int64_t T, int64_t num_groups);
+
+/* Group-normalised advantages only ("Accuracy": advantages; "Group
+ * specification").  rewards [B] f32 device; adv_out [B] f32 device.
+ * flags: GRPO_ADV_EPS_ADD.  Writes the status word of `ws`. */
+grpo_status_t grpo_group_adv(const float *rewards, const grpo_groups_t *groups,
+                             float adv_eps, uint32_t flags, float *adv_out,
+                             void *ws, size_t ws_bytes, void *stream);
+
+/* The fused forward + backward from logits ("Entry Point": grpo_loss(...)
+ * then loss.backward(); "Tensor Contract").
+ *   policy_logits, ref_logits : [B,T,V] of dtype `dt`, contiguous.  ref may
+ *                               equal policy.
+ *   action_ids                : [B,T] int64.
+ *   old_logps                 : [B,T] f32.
+ *   completion_mask           : [B,T] uint8 / bool.
+ *   rewards                   : [B] f32.
+ *   grad_logits (nullable)    : [B,T,V] of dtype `dt`; receives dL/dlogits
+ *                               (overwritten, not accumulated; may equal
+ *                               policy_logits for an in-place gradient).
+ *                               NULL = forward only.
+ *   out3                      : [3] f32: loss, policy_loss, kl.
+ *   per_seq (nullable)        : [3,B] f32: per-sequence policy totals
+ *                               sum_t p, KL totals sum_t k, active counts L_i.
+ *   logps_out (nullable)      : [B,T] f32: logp of active tokens, 0 elsewhere.
+ *   adv_out (nullable)        : [B] f32: the advantages used.
+ * Pointers must be aligned to their element size; rows need not be 16-byte
+ * aligned.  B, T >= 0, V >= 1. */
+grpo_status_t grpo_loss_fwd_bwd(const void *policy_logits, const void *ref_logits,
+                                grpo_dtype_t dt, int64_t B, int64_t T, int64_t V,
+                                const int64_t *action_ids, const float *old_logps,
+                                const uint8_t *completion_mask, const float *rewards,
+                                const grpo_groups_t *groups, const grpo_params_t *params,
+                                void *grad_logits, float *out3, float *per_seq,
+                                float *logps_out, float *adv_out, void *ws,
+                                size_t ws_bytes, void *stream);
+
+/* The same loss when the per-token log-probs are already known (grpo.cpp
+ * README "CUDA": the selected-token GRPO loss; RL-Kernel "Tensor and Data
+ * Parallel": by the time the objective sees a logprob the vocabulary is
+ * reduced).
+ *   logps, old_logps : [B,T] f32.   ref_logps : [B,T] f32, NULL iff beta == 0.
+ *   completion_mask  : [B,T] uint8.  rewards : [B] f32.
+ *   grad_logps (nullable) : [B,T] f32, receives dL/dlogp (0 on masked tokens).
+ *   out3, per_seq, adv_out : as for grpo_loss_fwd_bwd. */
+grpo_status_t grpo_loss_from_logps(const float *logps, const float *old_logps,
+                                   const float *ref_logps, const uint8_t *completion_mask,
+                                   int64_t B, int64_t T, const float *rewards,
+                                   const grpo_groups_t *groups, const grpo_params_t *params,
+                                   float *grad_logps, float *out3, float *per_seq,
+                                   float *adv_out, void *ws, size_t ws_bytes, void *stream);
+
+/* Synchronises `stream` and returns the status word the last call on this
+ * workspace left (GRPO_OK or an OR of the device-detected bits), or
+ * GRPO_ERR_CUDA.  The only entry point that blocks. */
+grpo_status_t grpo_read_device_status(const void *ws, void *stream);
+
+/* Static description of a status code. */
+const char *grpo_status_string(grpo_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GRPO_GB300_H */

@@ -1,0 +1,136 @@
+"""The C ABI: the shared library loads, exports every function the headers
+declare, and rejects bad arguments on the host before any CUDA call (so
+these run without a GPU)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import grad_row_online_gb300 as g
+from grad_row_online_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    srcs = [os.path.join(_build.CSRC, s) for s in os.listdir(_build.CSRC)]
+    srcs.append(os.path.join(ROOT, "include", "grpo.h"))
+    if not os.path.exists(_build.LIB) or any(os.path.getmtime(s) > os.path.getmtime(_build.LIB)
+                                              for s in srcs):
+        _build.build()
+    return g.lib()
+
+
+def _declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*[A-Za-z_][\w \*]*?\b(grpo_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert {"grpo_group_adv", "grpo_loss_fwd_bwd", "grpo_loss_from_logps",
+            "grpo_workspace_size", "grpo_read_device_status", "grpo_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_workspace_size(lib):
+    assert g.grpo_workspace_size(8, 16) >= 256 + 2 * 8 * 16 * 8
+    assert g.grpo_workspace_size(-1, 4) == 0
+    assert g.grpo_workspace_size(0, 0) == 256 + 0 or g.grpo_workspace_size(0, 0) >= 256
+    assert g.grpo_workspace_size(1024, 4096) % 256 == 0
+
+
+def test_status_strings(lib):
+    for code in (0, 1, 2, 3, 4, 5, 6, 7, 8, 16, 32, 64, 48):
+        assert isinstance(g.grpo_status_string(code), str) and g.grpo_status_string(code)
+
+
+# ---------------------------------------------------------------------------
+# host validation (no pointer is ever dereferenced: fake addresses are fine)
+# ---------------------------------------------------------------------------
+FAKE = 1 << 20  # 16-byte aligned, never touched
+
+
+def _groups(B=8, spp=4, bounds=None, G=0):
+    gr = g._Groups()
+    gr.num_seqs = B
+    gr.samples_per_prompt = spp
+    gr.group_boundaries = bounds
+    gr.num_groups = G
+    return gr
+
+
+def _params(**kw):
+    p = g._Params()
+    p.clip_eps_lo, p.clip_eps_hi, p.beta, p.adv_eps, p.grad_scale = 0.2, 0.2, 0.04, 1e-6, 1.0
+    p.reduction, p.flags = 0, 0
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def _fwd(lib, B=8, T=16, V=64, dt=0, gr=None, p=None, ws=FAKE, ws_bytes=None, **ptr):
+    gr = gr or _groups(B)
+    p = p or _params()
+    ws_bytes = g.grpo_workspace_size(B, T) if ws_bytes is None else ws_bytes
+    a = dict(policy=FAKE, ref=FAKE, act=FAKE, old=FAKE, mask=FAKE, rew=FAKE, grad=FAKE,
+             out3=FAKE, per_seq=None, logps=None, adv=None)
+    a.update(ptr)
+    return lib.grpo_loss_fwd_bwd(a["policy"], a["ref"], dt, B, T, V, a["act"], a["old"], a["mask"],
+                                 a["rew"], ctypes.byref(gr), ctypes.byref(p), a["grad"], a["out3"],
+                                 a["per_seq"], a["logps"], a["adv"], ws, ws_bytes, None)
+
+
+def test_fwd_rejects_bad_arguments(lib):
+    assert _fwd(lib, dt=7) == 3                       # dtype
+    assert _fwd(lib, V=0) == 2                        # V < 1
+    assert _fwd(lib, B=-1) == 2
+    assert _fwd(lib, policy=None) == 1                # null input
+    assert _fwd(lib, out3=None) == 1
+    assert _fwd(lib, ws=None) == 1
+    assert _fwd(lib, B=6, gr=_groups(B=6, spp=4)) == 2      # B % spp
+    assert _fwd(lib, gr=_groups(B=9)) == 2                  # num_seqs != B
+    assert _fwd(lib, gr=_groups(spp=0)) == 5                # no group spec
+    assert _fwd(lib, gr=_groups(spp=4, bounds=FAKE, G=2)) == 5  # both
+    assert _fwd(lib, gr=_groups(spp=0, bounds=FAKE, G=0)) == 2  # empty CSR
+    assert _fwd(lib, gr=_groups(spp=0, bounds=FAKE, G=9)) == 2  # more groups than sequences
+    assert _fwd(lib, gr=_groups(spp=0, bounds=FAKE + 4, G=2)) == 4  # misaligned CSR
+    assert _fwd(lib, p=_params(clip_eps_lo=1.0)) == 6
+    assert _fwd(lib, p=_params(clip_eps_lo=-0.1)) == 6
+    assert _fwd(lib, p=_params(clip_eps_hi=-0.1)) == 6
+    assert _fwd(lib, p=_params(beta=-1.0)) == 6
+    assert _fwd(lib, p=_params(beta=float("nan"))) == 6
+    assert _fwd(lib, p=_params(adv_eps=0.0)) == 6
+    assert _fwd(lib, p=_params(grad_scale=float("inf"))) == 6
+    assert _fwd(lib, p=_params(reduction=2)) == 6
+    assert _fwd(lib, p=_params(flags=8)) == 6
+    assert _fwd(lib, dt=1, policy=FAKE + 1) == 4      # bf16 pointer not 2-byte aligned
+    assert _fwd(lib, act=FAKE + 4) == 4               # int64 ids
+    assert _fwd(lib, ws=FAKE + 16) == 4               # workspace alignment
+    assert _fwd(lib, ws_bytes=1000) == 7              # workspace size
+
+
+def test_logps_and_adv_reject_bad_arguments(lib):
+    gr, p = _groups(), _params()
+    ws = g.grpo_workspace_size(8, 16)
+    L = lib.grpo_loss_from_logps
+    assert L(FAKE, FAKE, None, FAKE, 8, 16, FAKE, ctypes.byref(gr), ctypes.byref(p), None, FAKE,
+             None, None, FAKE, ws, None) == 1  # beta > 0 without ref_logps
+    assert L(FAKE, FAKE, FAKE, FAKE, 8, 16, FAKE, ctypes.byref(gr), ctypes.byref(p), None, FAKE,
+             None, None, FAKE, 10, None) == 7
+    assert L(FAKE + 2, FAKE, FAKE, FAKE, 8, 16, FAKE, ctypes.byref(gr), ctypes.byref(p), None,
+             FAKE, None, None, FAKE, ws, None) == 4
+    A = lib.grpo_group_adv
+    assert A(FAKE, ctypes.byref(gr), ctypes.c_float(0.0), 0, FAKE, FAKE, ws, None) == 6
+    assert A(FAKE, ctypes.byref(gr), ctypes.c_float(1e-6), 4, FAKE, FAKE, ws, None) == 6
+    assert A(FAKE, ctypes.byref(gr), ctypes.c_float(1e-6), 0, None, FAKE, ws, None) == 1
+    assert A(FAKE, ctypes.byref(_groups(B=8, spp=3)), ctypes.c_float(1e-6), 0, FAKE, FAKE, ws,
+             None) == 2

@@ -1,0 +1,296 @@
+"""Parity of the CUDA library (through its C ABI) with the double-precision
+oracle on seeded inputs, at sizes the oracle finishes in seconds: several
+512-thread tiles per row, ragged tails, odd vocabularies, every dtype, both
+reductions, CSR groups, and the edge cases of the method."""
+import numpy as np
+import pytest
+import torch
+
+import grad_row_online_gb300 as g
+import oracle
+import synth
+from workload_inputs import (assert_grad_rows, assert_scalar, clip_band_rows, expect, make_case,
+                             to_device, torch_storage)
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import os
+    import __graft_entry__
+    if not os.path.exists(g.library_path()):
+        __graft_entry__.build()
+
+
+TINY = synth.WORKLOADS["tiny"]
+# multi-tile rows with a ragged vector tail, 3 groups of 4, some empty rows
+MEDIUM = synth.Workload("medium", B=12, T=10, V=5003, seed=101, sigma=2.0, ref_sigma=0.1,
+                        samples_per_prompt=4, reward_p=0.5, len_range=(0, 10),
+                        eps_lo=0.2, eps_hi=0.28, beta=0.04)
+# CSR groups, sequence mean, continuous rewards, fully masked rows
+CSR = synth.Workload("csr", B=13, T=6, V=1531, seed=102, sigma=2.0, samples_per_prompt=0,
+                     csr_size_range=(2, 5), reward="normal", len_range=(1, 6), holes=2,
+                     reduction=1)
+
+
+def run(case, dev, **kw):
+    w = case["w"]
+    args = dict(clip_eps=w.eps_lo, clip_eps_hi=w.eps_hi, beta=w.beta,
+                reduction=w.reduction, want_per_seq=True, want_logps=True, want_adv=True)
+    if w.samples_per_prompt:
+        args["samples_per_prompt"] = w.samples_per_prompt
+    else:
+        args["group_boundaries"] = dev["bounds"]
+    args.update(kw)
+    res = g.grpo_loss_fwd_bwd(dev["X"], dev["Y"], dev["acts"], dev["old"], dev["mask"], dev["R"],
+                              **args)
+    torch.cuda.synchronize()
+    return res
+
+
+def check(case, res, exp, what=""):
+    w = case["w"]
+    out = res["out3"].cpu().numpy().astype(np.float64)
+    for i, k in enumerate(("loss", "policy_loss", "kl")):
+        assert_scalar(out[i], exp[k], f"{what} {k}")
+    ps = res["per_seq"].cpu().numpy().astype(np.float64)
+    assert np.allclose(ps[0], exp["per_seq_policy"], rtol=1e-5, atol=1e-6)
+    assert np.allclose(ps[1], exp["per_seq_kl"], rtol=1e-5, atol=1e-7)
+    assert np.array_equal(ps[2], exp["per_seq_active"])
+    assert np.allclose(res["adv"].cpu().numpy(), exp["A"].astype(np.float32), rtol=1e-6, atol=1e-7)
+    m = case["mask"].astype(bool)
+    lp = res["logps"].cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(lp[m] - exp["logp"][m]) <= 4e-6 + 1e-6 * np.abs(exp["logp"][m]))
+    assert np.all(lp[~m] == 0)
+    if res["grad"] is not None:
+        got = torch_storage(res["grad"])
+        assert_grad_rows(got, exp["grad"], case["dtype"], what=f"{what} grad")
+
+
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_tiny_workload(dtype):
+    case = make_case(TINY, dtype)
+    exp = expect(case)
+    check(case, run(case, to_device(case)), exp, f"tiny/{dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_medium_multi_tile_ragged(dtype):
+    case = make_case(MEDIUM, dtype)
+    exp = expect(case)
+    check(case, run(case, to_device(case)), exp, f"medium/{dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_csr_groups_sequence_mean(dtype):
+    case = make_case(CSR, dtype)
+    assert (case["mask"].sum(1) == 0).sum() == 2
+    exp = expect(case)
+    check(case, run(case, to_device(case)), exp, f"csr/{dtype}")
+
+
+@pytest.mark.parametrize("V", [1, 2, 7, 8, 9, 4099])
+def test_small_and_odd_vocabularies(V):
+    w = TINY.with_(name=f"v{V}", V=V, seed=200 + V)
+    case = make_case(w)
+    exp = expect(case)
+    check(case, run(case, to_device(case)), exp, f"V={V}")
+
+
+def test_token_mean_and_options():
+    case = make_case(MEDIUM.with_(reduction=0), "f32")
+    dev = to_device(case)
+    for kw in (dict(eps_add=True), dict(grad_scale=0.37), dict(beta=0.0), dict(beta=0.5)):
+        exp = expect(case, eps_add=kw.get("eps_add", False), grad_scale=kw.get("grad_scale", 1.0),
+                     beta=kw.get("beta"))
+        check(case, run(case, dev, **kw), exp, str(kw))
+
+
+def test_forward_only_matches():
+    case = make_case(MEDIUM, "bf16")
+    dev = to_device(case)
+    a = run(case, dev)
+    b = run(case, dev, grad=None)
+    assert b["grad"] is None
+    assert torch.equal(a["out3"], b["out3"])
+    assert torch.equal(a["per_seq"], b["per_seq"])
+
+
+def test_in_place_gradient():
+    case = make_case(MEDIUM, "bf16")
+    dev = to_device(case)
+    ref = run(case, dev)
+    X = dev["X"].clone()
+    res = run(case, dict(dev, X=X), grad=X)
+    assert torch.equal(res["out3"], ref["out3"])
+    assert torch.equal(X, ref["grad"])
+
+
+def test_skip_masked_grad_rows():
+    case = make_case(MEDIUM, "f32")
+    dev = to_device(case)
+    ref = run(case, dev)
+    G = torch.full_like(dev["X"], 7.0)
+    run(case, dev, grad=G, skip_masked_grad_rows=True)
+    m = dev["mask"].bool()
+    assert torch.equal(G[m], ref["grad"][m])
+    assert torch.all(G[~m] == 7.0)
+    assert torch.all(ref["grad"][~m] == 0.0)
+
+
+def test_identity_ref_is_policy():
+    case = make_case(MEDIUM, "bf16")
+    dev = to_device(case)
+    res = run(case, dict(dev, Y=dev["X"]))
+    assert res["out3"][2].item() == 0.0  # KL exactly 0
+    assert torch.all(res["per_seq"][1] == 0.0)
+    exp = expect(case, ref_is_policy=True)
+    check(case, res, exp, "identity")
+
+
+def test_masked_storage_is_never_read():
+    case = make_case(MEDIUM, "f32")
+    dev = to_device(case)
+    ref = run(case, dev)
+    m = dev["mask"].bool()
+    X, Y = dev["X"].clone(), dev["Y"].clone()
+    X[~m] = float("nan")
+    Y[~m] = float("inf")
+    acts = dev["acts"].clone()
+    acts[~m] = -12345
+    old = dev["old"].clone()
+    old[~m] = float("nan")
+    res = run(case, dict(dev, X=X, Y=Y, acts=acts, old=old))
+    for k in ("out3", "per_seq", "logps", "adv", "grad"):
+        assert torch.equal(res[k], ref[k]), k
+
+
+def test_bitwise_run_to_run():
+    case = make_case(CSR, "f32")
+    dev = to_device(case)
+    a, b = run(case, dev), run(case, dev)
+    for k in ("out3", "per_seq", "logps", "grad"):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_all_masked_and_empty():
+    case = make_case(TINY, "f32")
+    dev = to_device(case)
+    res = run(case, dict(dev, mask=torch.zeros_like(dev["mask"])))
+    assert torch.all(res["out3"] == 0) and torch.all(res["grad"] == 0)
+    for B, T in ((0, 4), (4, 0)):
+        X = torch.zeros((B, T, 5), device="cuda")
+        res = g.grpo_loss_fwd_bwd(X, X, torch.zeros((B, T), dtype=torch.int64, device="cuda"),
+                                  torch.zeros((B, T), device="cuda"),
+                                  torch.zeros((B, T), dtype=torch.uint8, device="cuda"),
+                                  torch.zeros(B, device="cuda"), samples_per_prompt=2 if B else 0,
+                                  group_boundaries=None if B else [0])
+        torch.cuda.synchronize()
+        assert torch.all(res["out3"] == 0)
+
+
+def test_device_detected_errors():
+    case = make_case(TINY, "f32")
+    dev = to_device(case)
+    acts = dev["acts"].clone()
+    acts[0, 0] = TINY.V  # active token (every row has >= 4 active)
+    res = run(case, dict(dev, acts=acts))
+    assert g.grpo_read_device_status(res["workspace"]) == 16
+    assert torch.all(torch.isnan(res["out3"]))
+    R = dev["R"].clone()
+    R[3] = float("nan")
+    res = run(case, dict(dev, R=R))
+    assert g.grpo_read_device_status(res["workspace"]) == 64
+    assert torch.all(torch.isnan(res["out3"]))
+    res = run(case, dev, samples_per_prompt=0, group_boundaries=[0, 5, 5, 8])
+    assert g.grpo_read_device_status(res["workspace"]) == 32
+    # a clean call on the same workspace resets the status
+    res = run(case, dev, workspace=res["workspace"])
+    assert g.grpo_read_device_status(res["workspace"]) == 0
+
+
+def test_group_adv_entry_point():
+    w = CSR
+    R = torch.from_numpy(w.rewards()).cuda()
+    gb = torch.from_numpy(w.group_boundaries()).cuda()
+    for eps_add in (False, True):
+        A = g.grpo_group_adv(R, group_boundaries=gb, eps_add=eps_add)
+        want = oracle.group_advantages(w.rewards(), w.group_boundaries(), eps_add=eps_add)
+        assert np.allclose(A.cpu().numpy(), want.astype(np.float32), rtol=1e-6, atol=1e-7)
+    R2 = torch.from_numpy(TINY.rewards()).cuda()
+    A = g.grpo_group_adv(R2, samples_per_prompt=4)
+    want = oracle.group_advantages(TINY.rewards(), TINY.group_boundaries())
+    assert np.array_equal(A.cpu().numpy(), want.astype(np.float32))
+
+
+# ---------------------------------------------------------------------------
+# logps-only boundary
+# ---------------------------------------------------------------------------
+LOGPS_SMALL = synth.WORKLOADS["logps"].with_(name="logps_small", B=24, T=64, len_range=(8, 64))
+
+
+def _logps_case(w):
+    lp, old, ref = w.logps_inputs()
+    return dict(lp=lp, old=old, ref=ref, mask=w.completion_mask(), R=w.rewards(),
+                bounds=w.group_boundaries())
+
+
+def _logps_run(w, c, ref=True, **kw):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    args = dict(clip_eps=w.eps_lo, clip_eps_hi=w.eps_hi, beta=w.beta, reduction=w.reduction,
+                want_per_seq=True, want_adv=True)
+    if w.samples_per_prompt:
+        args["samples_per_prompt"] = w.samples_per_prompt
+    else:
+        args["group_boundaries"] = t(c["bounds"])
+    args.update(kw)
+    res = g.grpo_loss_from_logps(t(c["lp"]), t(c["old"]), t(c["ref"]) if ref else None,
+                                 t(c["mask"]), t(c["R"]), **args)
+    torch.cuda.synchronize()
+    return res
+
+
+def _logps_check(w, c, res, beta=None, reduction=None, ref=True):
+    A = oracle.group_advantages(c["R"], c["bounds"])
+    exp = oracle.loss_from_logps(c["lp"], c["ref"] if ref else None, c["old"], c["mask"], A,
+                                 w.eps_lo, w.eps_hi, w.beta if beta is None else beta,
+                                 reduction=w.reduction if reduction is None else reduction)
+    out = res["out3"].cpu().numpy().astype(np.float64)
+    for i, k in enumerate(("loss", "policy_loss", "kl")):
+        assert_scalar(out[i], exp[k], k)
+    ps = res["per_seq"].cpu().numpy().astype(np.float64)
+    assert np.allclose(ps[0], exp["per_seq_policy"], rtol=1e-5, atol=1e-5)
+    assert np.array_equal(ps[2], exp["per_seq_active"])
+    if res["grad"] is not None:
+        want = exp["w"].astype(np.float32)
+        r = exp["ratio"]
+        band = (np.abs(r - (1 - np.float32(w.eps_lo))) < 1e-6) | (np.abs(r - (1 + np.float32(w.eps_hi))) < 1e-6)
+        got = res["grad"].cpu().numpy()
+        ok = np.abs(got.astype(np.float64) - want) <= np.spacing(np.abs(want)) + 1e-9
+        assert np.all(ok | band), np.argwhere(~(ok | band))[:5]
+
+
+@pytest.mark.parametrize("mask", ["prefix", "full"])
+def test_logps_small(mask):
+    w = LOGPS_SMALL.with_(mask=mask)
+    c = _logps_case(w)
+    _logps_check(w, c, _logps_run(w, c))
+
+
+def test_logps_odd_T_sequence_mean_and_no_ref():
+    w = LOGPS_SMALL.with_(T=37, len_range=(0, 37), reduction=1)
+    c = _logps_case(w)
+    _logps_check(w, c, _logps_run(w, c))
+    _logps_check(w, c, _logps_run(w, c, ref=False, beta=0.0), beta=0.0, ref=False)
+
+
+def test_logps_large_weights_take_the_precise_path():
+    # 2 sequences, 3 tokens: weights ~0.3, far above the fp32 budget
+    w = LOGPS_SMALL.with_(B=8, T=4, len_range=(0, 2))
+    c = _logps_case(w)
+    _logps_check(w, c, _logps_run(w, c))
