@@ -194,7 +194,7 @@ extern "C" grpo_status_t grpo_loss_fwd_bwd(
     e = launch_rows(ra, dt, params->profile, s);
     if (e != cudaSuccess) return GRPO_ERR_CUDA;
   }
-  ReduceArgs rd{completion_mask, L, slot_p, slot_k, B, T, params->beta, params->reduction,
+  ReduceArgs rd{completion_mask, L, A, slot_p, slot_k, B, T, params->beta, params->reduction,
                 hdr, out3, per_seq};
   return cuda_status(launch_reduce(rd, s));
 }
@@ -266,6 +266,7 @@ extern "C" const char* grpo_status_string(grpo_status_t status) {
     case GRPO_ERR_ACTION_RANGE: return "action id outside [0, V) on an active token";
     case GRPO_ERR_CSR: return "group_boundaries is not 0 = g0 < g1 < ... < gG = B";
     case GRPO_ERR_NONFINITE_REWARD: return "non-finite reward";
+    case GRPO_ERR_TIMEOUT: return "an asynchronous copy did not complete in time";
     default: return "several device-detected errors (OR of status bits)";
   }
 }

@@ -274,6 +274,19 @@ __device__ __forceinline__ FF warp_sum_ff(float v) {
   return acc;
 }
 
+// Warp sum of float pairs, same fixed tree; result in lane 0.
+__device__ __forceinline__ FF warp_sum_ff2(FF acc) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float oh = __shfl_xor_sync(0xFFFFFFFFu, acc.hi, o);
+    const float ol = __shfl_xor_sync(0xFFFFFFFFu, acc.lo, o);
+    const FF s = two_sum(acc.hi, oh);
+    acc.hi = s.hi;
+    acc.lo = __fadd_rn(__fadd_rn(s.lo, acc.lo), ol);
+  }
+  return acc;
+}
+
 template <typename T>
 __device__ __forceinline__ T warp_sum(T v) {
 #pragma unroll
@@ -358,6 +371,7 @@ struct RowArgs {
 struct ReduceArgs {
   const uint8_t* mask;
   const int32_t* L;
+  const double* A;
   const double* slot_p;
   const double* slot_k;
   int64_t B, T;

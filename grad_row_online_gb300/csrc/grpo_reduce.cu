@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs
     P = warp_sum(P);
     K = warp_sum(K);
     const int L = a.L[i];
+    P -= a.A[i] * (double)L;  // slots hold p + A: the constant -A per token, summed here
     if (lane == 0) {
       if (a.per_seq) {
         a.per_seq[i] = (float)P;

@@ -65,7 +65,8 @@ typedef enum {
   /* device-detected; bits of the status word (grpo_read_device_status) */
   GRPO_ERR_ACTION_RANGE = 16,    /* active token with action id outside [0, V) */
   GRPO_ERR_CSR = 32,             /* boundaries not 0 = g_0 < g_1 < ... < g_G = B */
-  GRPO_ERR_NONFINITE_REWARD = 64 /* a reward is NaN or infinite */
+  GRPO_ERR_NONFINITE_REWARD = 64, /* a reward is NaN or infinite */
+  GRPO_ERR_TIMEOUT = 128          /* a bounded wait on an asynchronous copy ran out */
 } grpo_status_t;
 
 typedef enum { GRPO_F32 = 0, GRPO_BF16 = 1, GRPO_F16 = 2 } grpo_dtype_t;

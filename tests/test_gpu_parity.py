@@ -94,12 +94,34 @@ def test_csr_groups_sequence_mean(dtype):
     check(case, run(case, to_device(case)), exp, f"csr/{dtype}")
 
 
-@pytest.mark.parametrize("V", [1, 2, 7, 8, 9, 4099])
+@pytest.mark.parametrize("V", [1, 2, 4, 7, 8, 9, 16, 4099, 4100])
 def test_small_and_odd_vocabularies(V):
     w = TINY.with_(name=f"v{V}", V=V, seed=200 + V)
     case = make_case(w)
     exp = expect(case)
     check(case, run(case, to_device(case)), exp, f"V={V}")
+
+
+# long rows: many vectors per thread, a ragged vector tail, and an unaligned
+# long row
+@pytest.mark.parametrize("dtype,V", [("f32", 40000), ("bf16", 90000), ("f32", 100000),
+                                     ("f32", 200000), ("bf16", 300000), ("f32", 270001)])
+def test_long_rows(dtype, V):
+    w = TINY.with_(name=f"long{V}", B=4, T=3, V=V, seed=300 + V % 97, sigma=2.0,
+                   samples_per_prompt=2, len_range=(1, 3))
+    case = make_case(w, dtype)
+    exp = expect(case)
+    check(case, run(case, to_device(case)), exp, f"{dtype} V={V}")
+
+
+# a full mask: with equal lengths the advantages of a group cancel in the
+# policy loss, which is then a small residual of the ratios
+@pytest.mark.parametrize("dtype,V", [("f32", 5008), ("bf16", 5008), ("bf16", 90000)])
+def test_full_mask_cancellation(dtype, V):
+    w = MEDIUM.with_(name="full", V=V, mask="full", B=8 if V > 9000 else 12, T=4 if V > 9000 else 10)
+    case = make_case(w, dtype)
+    exp = expect(case)
+    check(case, run(case, to_device(case)), exp, f"full mask {dtype} V={V}")
 
 
 def test_token_mean_and_options():
@@ -111,8 +133,9 @@ def test_token_mean_and_options():
         check(case, run(case, dev, **kw), exp, str(kw))
 
 
-def test_forward_only_matches():
-    case = make_case(MEDIUM, "bf16")
+@pytest.mark.parametrize("V", [5003, 5008])
+def test_forward_only_matches(V):
+    case = make_case(MEDIUM.with_(V=V), "bf16")
     dev = to_device(case)
     a = run(case, dev)
     b = run(case, dev, grad=None)
@@ -121,8 +144,9 @@ def test_forward_only_matches():
     assert torch.equal(a["per_seq"], b["per_seq"])
 
 
-def test_in_place_gradient():
-    case = make_case(MEDIUM, "bf16")
+@pytest.mark.parametrize("V", [5003, 5008, 90001, 90000])
+def test_in_place_gradient(V):
+    case = make_case(MEDIUM.with_(V=V, B=4, T=5) if V > 9000 else MEDIUM.with_(V=V), "bf16")
     dev = to_device(case)
     ref = run(case, dev)
     X = dev["X"].clone()
@@ -131,8 +155,9 @@ def test_in_place_gradient():
     assert torch.equal(X, ref["grad"])
 
 
-def test_skip_masked_grad_rows():
-    case = make_case(MEDIUM, "f32")
+@pytest.mark.parametrize("V", [5003, 5008, 90001, 90000])
+def test_skip_masked_grad_rows(V):
+    case = make_case(MEDIUM.with_(V=V, B=4, T=5) if V > 9000 else MEDIUM.with_(V=V), "f32")
     dev = to_device(case)
     ref = run(case, dev)
     G = torch.full_like(dev["X"], 7.0)
@@ -143,8 +168,9 @@ def test_skip_masked_grad_rows():
     assert torch.all(ref["grad"][~m] == 0.0)
 
 
-def test_identity_ref_is_policy():
-    case = make_case(MEDIUM, "bf16")
+@pytest.mark.parametrize("V", [5003, 5008, 90001, 90000])
+def test_identity_ref_is_policy(V):
+    case = make_case(MEDIUM.with_(V=V, B=4, T=5) if V > 9000 else MEDIUM.with_(V=V), "bf16")
     dev = to_device(case)
     res = run(case, dict(dev, Y=dev["X"]))
     assert res["out3"][2].item() == 0.0  # KL exactly 0
@@ -153,8 +179,9 @@ def test_identity_ref_is_policy():
     check(case, res, exp, "identity")
 
 
-def test_masked_storage_is_never_read():
-    case = make_case(MEDIUM, "f32")
+@pytest.mark.parametrize("V", [5003, 5008, 90001, 90000])
+def test_masked_storage_is_never_read(V):
+    case = make_case(MEDIUM.with_(V=V, B=4, T=5) if V > 9000 else MEDIUM.with_(V=V), "f32")
     dev = to_device(case)
     ref = run(case, dev)
     m = dev["mask"].bool()
@@ -170,8 +197,9 @@ def test_masked_storage_is_never_read():
         assert torch.equal(res[k], ref[k]), k
 
 
-def test_bitwise_run_to_run():
-    case = make_case(CSR, "f32")
+@pytest.mark.parametrize("V", [1531, 1536])
+def test_bitwise_run_to_run(V):
+    case = make_case(CSR.with_(V=V), "f32")
     dev = to_device(case)
     a, b = run(case, dev), run(case, dev)
     for k in ("out3", "per_seq", "logps", "grad"):
