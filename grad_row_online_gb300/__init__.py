@@ -21,7 +21,8 @@ import torch
 
 from . import _build
 
-__all__ = ["grpo_workspace_size", "grpo_group_adv", "grpo_loss_fwd_bwd", "grpo_loss_from_logps",
+__all__ = ["grpo_workspace_size", "grpo_group_adv", "grpo_loss_fwd_bwd", "grpo_loss_fwd_bwd_static",
+           "grpo_loss_from_logps",
            "grpo_read_device_status", "grpo_status_string", "GrpoError", "library_path",
            "GRPO_ADV_EPS_ADD", "GRPO_SKIP_MASKED_GRAD_ROWS"]
 
@@ -79,6 +80,10 @@ def lib():
                                         ctypes.POINTER(_Groups), ctypes.POINTER(_Params), vp, vp,
                                         vp, vp, vp, vp, sz, vp]
         L.grpo_loss_fwd_bwd.restype = ctypes.c_int
+        L.grpo_loss_fwd_bwd_static.argtypes = [vp, vp, ctypes.c_int, i64, i64, i64, vp, vp, vp,
+                                               vp, ctypes.POINTER(_Groups),
+                                               ctypes.POINTER(_Params), vp, vp, vp, vp, vp, vp]
+        L.grpo_loss_fwd_bwd_static.restype = ctypes.c_int
         L.grpo_loss_from_logps.argtypes = [vp, vp, vp, vp, i64, i64, vp, ctypes.POINTER(_Groups),
                                            ctypes.POINTER(_Params), vp, vp, vp, vp, vp, sz, vp]
         L.grpo_loss_from_logps.restype = ctypes.c_int
@@ -244,6 +249,31 @@ def grpo_loss_fwd_bwd(policy_logits: torch.Tensor, ref_logits: torch.Tensor,
     _check(rc, "grpo_loss_fwd_bwd")
     return {"out3": out3, "loss": out3[0], "policy_loss": out3[1], "kl": out3[2],
             "grad": grad_t, "per_seq": per_seq, "logps": logps, "adv": adv, "workspace": ws}
+
+
+def grpo_loss_fwd_bwd_static(policy_logits: torch.Tensor, ref_logits: torch.Tensor,
+                             action_ids: torch.Tensor, old_logps: torch.Tensor,
+                             completion_mask: torch.Tensor, rewards: torch.Tensor, *,
+                             samples_per_prompt: int = 0, group_boundaries=None,
+                             clip_eps: float = 0.2, clip_eps_hi: Optional[float] = None,
+                             beta: float = 0.04, adv_eps: float = 1e-6, eps_add: bool = False,
+                             grad_scale: float = 1.0, reduction="token_mean",
+                             grad: Optional[torch.Tensor] = None, out3: Optional[torch.Tensor] = None,
+                             stream=None) -> int:
+    """grpo_loss_fwd_bwd with the library's fixed scratch memory instead of a
+    workspace, for callers that cannot allocate device memory at the call
+    (e.g. inside CUDA graph capture).  Every output is caller-provided:
+    `out3` ([3] f32) and, optionally, `grad` (like policy_logits).  Returns
+    the status code (0 = ok); nothing is allocated by this call."""
+    B, T, V = policy_logits.shape
+    mask = completion_mask.view(torch.uint8) if completion_mask.dtype == torch.bool else completion_mask
+    g, keep = _groups(B, samples_per_prompt, group_boundaries)
+    p, prof = _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction,
+                      GRPO_ADV_EPS_ADD if eps_add else 0, None)
+    return int(lib().grpo_loss_fwd_bwd_static(
+        _ptr(policy_logits), _ptr(ref_logits), _DTYPES[policy_logits.dtype], B, T, V,
+        _ptr(action_ids), _ptr(old_logps), _ptr(mask), _ptr(rewards), ctypes.byref(g),
+        ctypes.byref(p), _ptr(grad), _ptr(out3), None, None, None, _stream(stream)))
 
 
 def grpo_loss_from_logps(logps: torch.Tensor, old_logps: torch.Tensor,

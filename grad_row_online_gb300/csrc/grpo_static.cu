@@ -1,0 +1,69 @@
+// grpo_static.cu -- grpo_loss_fwd_bwd without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory at the point where they need
+// the loss: code that runs while a CUDA stream is being captured into a graph
+// (cudaMalloc is not a capturable operation), hosts whose device memory is
+// entirely owned by another allocator (a framework's caching pool, an
+// inference server's fixed partitions), or latency-critical loops where a
+// cudaMalloc / cudaFree pair (cudaFree synchronises the device) is not
+// acceptable.  For them, grpo_loss_fwd_bwd_static runs the same fused
+// forward + backward with its scratch memory taken from a fixed array that
+// lives in this library's device image.
+//
+// The array is file-scope device memory of kStaticScratchBytes: every GPU
+// that loads the library holds it until the process exits.  All calls share
+// it and it keeps the last call's contents; the entry point clears what must
+// start at zero (the status word and the row counter, through the same
+// 16-byte memset as the workspace path) and overwrites the rest before
+// reading it.  Because the array is shared, calls whose work overlaps on the
+// GPU (different streams, or different host threads, without ordering
+// between them) race on it: serialise them.
+#include <mutex>
+
+#include "grpo_internal.cuh"
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t)9 << 19;  // 4.5 MiB
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+// Per-device device address of g_static_scratch.  In host code the array's
+// name is only a stand-in; the address a kernel may use comes from
+// cudaGetSymbolAddress, taken once per device with that device current.
+std::mutex g_setup_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+grpo_status_t scratch_for_current_device(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GRPO_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr)
+      return GRPO_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return GRPO_OK;
+}
+
+}  // namespace
+
+extern "C" grpo_status_t grpo_loss_fwd_bwd_static(
+    const void* policy_logits, const void* ref_logits, grpo_dtype_t dt, int64_t B, int64_t T,
+    int64_t V, const int64_t* action_ids, const float* old_logps,
+    const uint8_t* completion_mask, const float* rewards, const grpo_groups_t* groups,
+    const grpo_params_t* params, void* grad_logits, float* out3, float* per_seq,
+    float* logps_out, float* adv_out, void* stream) {
+  // sizes beyond the fixed scratch are rejected before anything else runs
+  if (B < 0 || T < 0) return GRPO_ERR_SHAPE;
+  if (grpo_workspace_size(B, T, 0) > kStaticScratchBytes) return GRPO_ERR_WORKSPACE;
+  void* ws = nullptr;
+  const grpo_status_t st = scratch_for_current_device(&ws);
+  if (st != GRPO_OK) return st;
+  return grpo_loss_fwd_bwd(policy_logits, ref_logits, dt, B, T, V, action_ids, old_logps,
+                           completion_mask, rewards, groups, params, grad_logits, out3, per_seq,
+                           logps_out, adv_out, ws, kStaticScratchBytes, stream);
+}

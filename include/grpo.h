@@ -167,6 +167,30 @@ grpo_status_t grpo_loss_from_logps(const float *logps, const float *old_logps,
                                    float *grad_logps, float *out3, float *per_seq,
                                    float *adv_out, void *ws, size_t ws_bytes, void *stream);
 
+/* grpo_loss_fwd_bwd for callers that cannot allocate device memory where
+ * they need the loss -- code running while a stream is captured into a CUDA
+ * graph, hosts whose device memory belongs to another allocator, loops that
+ * cannot afford a cudaMalloc / cudaFree.  The operator pages have no
+ * counterpart: this is a deployment variant of the same computation.
+ * Arguments and results are those of grpo_loss_fwd_bwd without `ws` /
+ * `ws_bytes`: the scratch memory is a fixed 4.5 MiB array in the library's
+ * device image, present on every GPU that loads the library until the
+ * process exits.  Sizes whose grpo_workspace_size(B, T, 0) exceeds 4.5 MiB
+ * are rejected with GRPO_ERR_WORKSPACE (any B <= 8192 with B*T <= 262144
+ * fits).  No device memory is allocated.
+ * The first call on a device looks the array's device address up (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the array: calls whose GPU work may overlap
+ * (other streams or threads without ordering between them) race on it and
+ * must be serialised by the caller. */
+grpo_status_t grpo_loss_fwd_bwd_static(const void *policy_logits, const void *ref_logits,
+                                       grpo_dtype_t dt, int64_t B, int64_t T, int64_t V,
+                                       const int64_t *action_ids, const float *old_logps,
+                                       const uint8_t *completion_mask, const float *rewards,
+                                       const grpo_groups_t *groups, const grpo_params_t *params,
+                                       void *grad_logits, float *out3, float *per_seq,
+                                       float *logps_out, float *adv_out, void *stream);
+
 /* Synchronises `stream` and returns the status word the last call on this
  * workspace left (GRPO_OK or an OR of the device-detected bits), or
  * GRPO_ERR_CUDA.  The only entry point that blocks. */
