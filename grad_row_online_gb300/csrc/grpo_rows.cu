@@ -195,46 +195,56 @@ __device__ double sum_exp_precise(const T* row, int64_t V, float M, const float*
 
 // ---------------------------------------------------------------- sweep 2
 // dL/dx = w (onehot - softmax) over a row, vectors visited back to front when
-// kReverseSweep2: the lines sweep 1 read last are read first.
-template <typename T>
+// kReverseSweep2: the lines sweep 1 read last are read first.  The action
+// element is patched once per vector, outside the element loop.
+template <typename T, bool kPrecise>
 __device__ void grad_row(const T* x, T* g, int64_t V, int64_t act, const RowScalars& rs,
                          uint64_t pol_in, uint64_t pol_out) {
   constexpr int VEC = Storage<T>::kVec;
   const bool same_phase = (((uintptr_t)x ^ (uintptr_t)g) & 15) == 0;
   if (!same_phase) {  // differently aligned buffers: element by element
     for (int64_t v = threadIdx.x; v < V; v += blockDim.x)
-      Storage<T>::store1(g + v, grad_elem(Storage<T>::load1(x + v), v, rs, act));
+      Storage<T>::store1(g + v, grad_at<kPrecise>(Storage<T>::load1(x + v), v, rs, act));
     return;
   }
   const Geom<T> gm(x, V);
   if ((int)threadIdx.x < gm.head) {
     const int64_t v = threadIdx.x;
-    Storage<T>::store1(g + v, grad_elem(Storage<T>::load1(x + v), v, rs, act));
+    Storage<T>::store1(g + v, grad_at<kPrecise>(Storage<T>::load1(x + v), v, rs, act));
   }
   if ((int)threadIdx.x < gm.tail) {
     const int64_t v = gm.t0 + threadIdx.x;
-    Storage<T>::store1(g + v, grad_elem(Storage<T>::load1(x + v), v, rs, act));
+    Storage<T>::store1(g + v, grad_at<kPrecise>(Storage<T>::load1(x + v), v, rs, act));
   }
   const uint4* xv = reinterpret_cast<const uint4*>(x + gm.head);
   uint4* gv = reinterpret_cast<uint4*>(g + gm.head);
   const int64_t stride = blockDim.x;
   const int64_t n = gm.nvec;
+  // the vector holding the action element, and its lane (or none)
+  const int64_t arel = act - gm.head;
+  const int64_t aq = (arel >= 0 && arel < n * VEC) ? arel / VEC : -1;
+  const int alane = (int)(arel - aq * VEC);
   auto at = [&](int64_t k) -> int64_t { return kReverseSweep2 ? n - 1 - k : k; };
   auto emit = [&](const uint4& in, int64_t q) {
     float f[VEC];
     Storage<T>::unpack(in, f);
-    const int64_t base = gm.head + q * VEC;
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) f[j] = grad_elem(f[j], base + j, rs, act);
+    for (int j = 0; j < VEC; ++j) f[j] = grad_elem<kPrecise>(f[j], rs);
+    if (q == aq) {
+#pragma unroll
+      for (int j = 0; j < VEC; ++j)
+        if (j == alane) f[j] = rs.ga;
+    }
     st_hint(gv + q, Storage<T>::pack(f), pol_out);
   };
+  constexpr int U = kGradUnroll;
   int64_t k = threadIdx.x;
-  for (; k + (kUnroll - 1) * stride < n; k += kUnroll * stride) {
-    uint4 v[kUnroll];
+  for (; k + (U - 1) * stride < n; k += U * stride) {
+    uint4 v[U];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) v[u] = ld_hint(xv + at(k + u * stride), pol_in);
+    for (int u = 0; u < U; ++u) v[u] = ld_hint(xv + at(k + u * stride), pol_in);
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) emit(v[u], at(k + u * stride));
+    for (int u = 0; u < U; ++u) emit(v[u], at(k + u * stride));
   }
   for (; k < n; k += stride) emit(ld_hint(xv + at(k), pol_in), at(k));
 }
@@ -372,7 +382,10 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(cons
       }
       if (want_grad) {
         const RowScalars rs = s_rs;
-        grad_row<T>(x, grow, a.V, act, rs, stream, stream);
+        if (rs.precise)
+          grad_row<T, true>(x, grow, a.V, act, rs, stream, stream);
+        else
+          grad_row<T, false>(x, grow, a.V, act, rs, stream, stream);
       }
     }
     __syncthreads();  // everyone is done with s_rs / s_next of this row

@@ -11,7 +11,8 @@ namespace grpo {
 static constexpr int kRowThreads = 256;
 static constexpr int kRowBlocksPerSM = 4;
 static constexpr int kUnroll = 4;        // 16-byte vectors in flight per thread, one row
-static constexpr int kPairUnroll = 2;    // ... per row when policy and reference stream together
+static constexpr int kPairUnroll = 3;    // ... per row when policy and reference stream together
+static constexpr int kGradUnroll = 4;    // ... in the gradient sweep
 static constexpr bool kReverseSweep2 = true;
 // Refinement.  The fast logsumexp of a row has an absolute error below
 // kFastErrBound (the normaliser's relative error, below 2^-19, plus the
@@ -222,12 +223,18 @@ static __device__ __forceinline__ RowScalars finish_precise(const RowArgs& a, do
 }
 
 // ---------------------------------------------------------------- sweep 2
-__device__ __forceinline__ float grad_elem(float x, int64_t v, const RowScalars& rs, int64_t act) {
+// -w softmax_v; in a refined row, elements above kElemPrecise in double
+template <bool kPrecise>
+__device__ __forceinline__ float grad_elem(float x, const RowScalars& rs) {
   const float p = ex2_fast(__fmaf_rn(x, kLog2e, -rs.LL));
   float g = __fmul_rn(rs.wneg, p);
-  if (rs.precise && fabsf(g) > kElemPrecise) g = (float)(-rs.w * exp((double)x - rs.lse_p));
-  if (v == act) g = rs.ga;
+  if (kPrecise && fabsf(g) > kElemPrecise) g = (float)(-rs.w * exp((double)x - rs.lse_p));
   return g;
+}
+// the element v of a row (the action element is w (1 - p_a))
+template <bool kPrecise>
+__device__ __forceinline__ float grad_at(float x, int64_t v, const RowScalars& rs, int64_t act) {
+  return v == act ? rs.ga : grad_elem<kPrecise>(x, rs);
 }
 
 }  // namespace grpo
