@@ -36,7 +36,7 @@ METRIC = "active tokens/s and HBM GB/s (% of roofline), fused GRPO fwd+bwd, 1 GB
 UNIT = "active tokens/s"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "rows_kernel_large_vocab.md")
 ROWS_SOURCES = [os.path.join(ROOT, "grad_row_online_gb300", "csrc", f)
-                for f in ("grpo_rows.cu", "grpo_internal.cuh")]
+                for f in ("grpo_rows.cu", "grpo_rows_common.cuh", "grpo_internal.cuh")]
 
 
 def rows_source_hash() -> str:

@@ -119,7 +119,7 @@ extern "C" grpo_status_t grpo_group_adv(const float* rewards, const grpo_groups_
   WsHeader* hdr = (WsHeader*)w;
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return GRPO_ERR_CUDA;
   PrepArgs pa{rewards, bounds, B, 0, G, spp, adv_eps, (int)(flags & GRPO_ADV_EPS_ADD),
-              nullptr, (double*)(w + lay.off_A), adv_out, nullptr, hdr};
+              nullptr, 0, (double*)(w + lay.off_A), adv_out, nullptr, hdr};
   return cuda_status(launch_prep(pa, s));
 }
 
@@ -162,7 +162,7 @@ extern "C" grpo_status_t grpo_loss_fwd_bwd(
 
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return GRPO_ERR_CUDA;
   PrepArgs pa{rewards, bounds, B, T, G, spp, params->adv_eps,
-              (int)(params->flags & GRPO_ADV_EPS_ADD), completion_mask, A, adv_out, L, hdr};
+              (int)(params->flags & GRPO_ADV_EPS_ADD), completion_mask, 1, A, adv_out, L, hdr};
   cudaError_t e = launch_prep(pa, s);
   if (e != cudaSuccess) return GRPO_ERR_CUDA;
 
@@ -194,8 +194,8 @@ extern "C" grpo_status_t grpo_loss_fwd_bwd(
     e = launch_rows(ra, dt, params->profile, s);
     if (e != cudaSuccess) return GRPO_ERR_CUDA;
   }
-  ReduceArgs rd{completion_mask, L, A, slot_p, slot_k, B, T, params->beta, params->reduction,
-                hdr, out3, per_seq};
+  ReduceArgs rd{completion_mask, L, A, (double*)(w + lay.off_seq), slot_p, slot_k, B, T,
+                params->beta, params->reduction, hdr, out3, per_seq};
   return cuda_status(launch_reduce(rd, s));
 }
 
@@ -234,7 +234,7 @@ extern "C" grpo_status_t grpo_loss_from_logps(const float* logps, const float* o
   double* seq = (double*)(w + lay.off_seq);
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return GRPO_ERR_CUDA;
   PrepArgs pa{rewards, bounds, B, T, G, spp, params->adv_eps,
-              (int)(params->flags & GRPO_ADV_EPS_ADD), nullptr, A, adv_out, nullptr, hdr};
+              (int)(params->flags & GRPO_ADV_EPS_ADD), nullptr, 0, A, adv_out, nullptr, hdr};
   if (launch_prep(pa, s) != cudaSuccess) return GRPO_ERR_CUDA;
   LogpsArgs la{logps, old_logps, ref_logps, completion_mask, A, L, seq, grad_logps, out3,
                per_seq, hdr, B, T, params->clip_eps_lo, params->clip_eps_hi, params->beta,

@@ -22,9 +22,9 @@ namespace grpo {
 //   slots    double[2 B T]    per-token policy / KL terms (logits path)
 // ----------------------------------------------------------------------------
 struct WsHeader {
-  unsigned int status;
-  unsigned int pad0;
-  unsigned long long row_counter;
+  unsigned int status;        // device-detected error bits
+  unsigned int done_ctas;     // reduce: CTAs finished (the last one forms the scalar)
+  unsigned long long row_counter;  // rows: next row to claim
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -340,7 +340,8 @@ struct PrepArgs {
   int32_t spp;
   float adv_eps;
   int eps_add;
-  const uint8_t* mask;  // NULL -> no mask scan
+  const uint8_t* mask;  // the completion mask (may be NULL when T == 0)
+  int count;            // 1: also count active tokens per sequence into L
   double* A;
   float* adv_out;  // nullable
   int32_t* L;      // used when mask != NULL
@@ -372,6 +373,7 @@ struct ReduceArgs {
   const uint8_t* mask;
   const int32_t* L;
   const double* A;
+  double* seq;  // [2B] per-sequence totals
   const double* slot_p;
   const double* slot_k;
   int64_t B, T;

@@ -1,5 +1,6 @@
 // grpo_prep.cu -- group-normalised advantages and per-sequence active-token
-// counts.  One CTA per group.
+// counts, in one launch: CTAs [0, G) take a group each, CTAs [G, G+B) the
+// mask of one sequence each.
 //
 // RL-Kernel "GRPO Loss" page, "Accuracy": advantages are the group's rewards
 // minus their mean over the population standard deviation clamped at
@@ -19,6 +20,34 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
   __shared__ double s_red[32 * 3];
   __shared__ float s_fred[32];
   __shared__ int s_bad;
+  if ((int64_t)blockIdx.x >= a.G) {  // active-token count of one sequence
+    const int64_t i = blockIdx.x - a.G;
+    const uint8_t* m = a.mask + i * a.T;
+    int cnt = 0;
+    const uintptr_t addr = (uintptr_t)m;
+    int64_t head = (int64_t)((16 - (addr & 15)) & 15);
+    if (head > a.T) head = a.T;
+    const int64_t nvec = (a.T - head) / 16;
+    const int64_t tail0 = head + nvec * 16;
+    for (int64_t t = threadIdx.x; t < head; t += blockDim.x) cnt += m[t] != 0;
+    for (int64_t t = tail0 + threadIdx.x; t < a.T; t += blockDim.x) cnt += m[t] != 0;
+    const uint4* mv = reinterpret_cast<const uint4*>(m + head);
+    for (int64_t k = threadIdx.x; k < nvec; k += blockDim.x) {
+      const uint4 v = __ldg(mv + k);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        // count nonzero bytes: set the top bit of each nonzero byte
+        const uint32_t x = w[q];
+        const uint32_t nz = ((x & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | x;
+        cnt += __popc(nz & 0x80808080u);
+      }
+    }
+    int c1[1] = {cnt};
+    block_sum<int, 1>(c1, reinterpret_cast<int*>(s_red));
+    if (threadIdx.x == 0) a.L[i] = c1[0];
+    return;
+  }
   const int64_t g = blockIdx.x;
 
   if (threadIdx.x == 0) s_bad = 0;
@@ -84,39 +113,12 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepArgs a) {
     if (a.adv_out) a.adv_out[i] = (float)Ai;
   }
 
-  // ---- active-token counts of the group's sequences ----
-  if (a.mask == nullptr) return;
-  for (int64_t i = lo; i < hi; ++i) {
-    const uint8_t* m = a.mask + i * a.T;
-    int cnt = 0;
-    const uintptr_t addr = (uintptr_t)m;
-    int64_t head = (int64_t)((16 - (addr & 15)) & 15);
-    if (head > a.T) head = a.T;
-    const int64_t nvec = (a.T - head) / 16;
-    const int64_t tail0 = head + nvec * 16;
-    for (int64_t t = threadIdx.x; t < head; t += blockDim.x) cnt += m[t] != 0;
-    for (int64_t t = tail0 + threadIdx.x; t < a.T; t += blockDim.x) cnt += m[t] != 0;
-    const uint4* mv = reinterpret_cast<const uint4*>(m + head);
-    for (int64_t k = threadIdx.x; k < nvec; k += blockDim.x) {
-      uint4 v = __ldg(mv + k);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        // count nonzero bytes: set the top bit of each nonzero byte
-        uint32_t x = w[q];
-        uint32_t nz = ((x & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | x;
-        cnt += __popc(nz & 0x80808080u);
-      }
-    }
-    int c1[1] = {cnt};
-    block_sum<int, 1>(c1, reinterpret_cast<int*>(s_red));
-    if (threadIdx.x == 0) a.L[i] = c1[0];
-  }
 }
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
-  if (a.G <= 0) return cudaSuccess;
-  prep_kernel<<<(unsigned)a.G, kPrepThreads, 0, s>>>(a);
+  const int64_t grid = a.G + (a.count ? a.B : 0);
+  if (grid <= 0) return cudaSuccess;
+  prep_kernel<<<(unsigned)grid, kPrepThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -5,92 +5,92 @@
 // sequence total, then the B sequence totals to the scalar -- and the
 // normaliser of "Normalizer semantics": the global active-token count (token
 // mean) or the per-sequence count followed by a mean over live sequences.
-// The summation order is fixed by the code (lane-strided partial sums, an
-// xor-shuffle tree, a fixed warp order), never by scheduling, so the result
-// is bitwise reproducible.  Single CTA: the per-token slots are B*T doubles,
-// a few hundred kilobytes for vocabulary-sized rows.
+//
+// One CTA per sequence forms its totals; the CTA that finishes last (an
+// atomic ticket, one per CTA, that nobody waits on) forms the scalar from the
+// B totals.  Every sum has an order fixed by the code (thread-strided partial
+// sums, xor-shuffle trees, warps in index order, sequences in index order),
+// never by scheduling, so the result is bitwise reproducible.
 #include "grpo_internal.cuh"
 
 namespace grpo {
 
-static constexpr int kReduceThreads = 1024;
+static constexpr int kReduceThreads = 256;
 
 __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs a) {
-  __shared__ double s_d[32 * 3];
-  __shared__ long long s_l[64];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nw = blockDim.x >> 5;
+  __shared__ double s_d[32 * 2];
+  __shared__ long long s_l[32 * 2];
+  __shared__ bool s_last;
+  const int64_t i = blockIdx.x;
 
-  long long ns[2] = {0, 0};
-  for (int64_t i = threadIdx.x; i < a.B; i += blockDim.x) {
-    int L = a.L[i];
-    ns[0] += L;
-    ns[1] += L > 0;
-  }
-  block_sum<long long, 2>(ns, s_l);
-  const long long N = ns[0], S = ns[1];
-
-  // level 1: warp w owns sequences w, w + nw, ...; its lanes take the token
-  // slots t = lane, lane + 32, ... in order, then an xor-shuffle tree gives
-  // the sequence totals P_i, K_i.  Lane 0 folds them, in sequence order, into
-  // this warp's share of the scalar numerator.
-  double pol = 0.0, kl = 0.0;
-  for (int64_t i = warp; i < a.B; i += nw) {
+  // level 1: sequence i.  Slots hold p + A (the policy term plus its constant
+  // part, see the row kernel); the constant -A_i per token is added here.
+  if (i < a.B) {
     const uint8_t* m = a.mask + i * a.T;
     const double* sp = a.slot_p + i * a.T;
     const double* sk = a.slot_k + i * a.T;
-    double P = 0.0, K = 0.0;
-    for (int64_t t = lane; t < a.T; t += 32)
+    double v[2] = {0.0, 0.0};
+    for (int64_t t = threadIdx.x; t < a.T; t += blockDim.x)
       if (m[t]) {
-        P += sp[t];
-        K += sk[t];
+        v[0] += sp[t];
+        v[1] += sk[t];
       }
-    P = warp_sum(P);
-    K = warp_sum(K);
-    const int L = a.L[i];
-    P -= a.A[i] * (double)L;  // slots hold p + A: the constant -A per token, summed here
-    if (lane == 0) {
+    block_sum<double, 2>(v, s_d);
+    if (threadIdx.x == 0) {
+      const int L = a.L[i];
+      const double P = v[0] - a.A[i] * (double)L;
+      a.seq[i] = P;
+      a.seq[a.B + i] = v[1];
       if (a.per_seq) {
         a.per_seq[i] = (float)P;
-        a.per_seq[a.B + i] = (float)K;
+        a.per_seq[a.B + i] = (float)v[1];
         a.per_seq[2 * a.B + i] = (float)L;
       }
-      if (a.reduction == GRPO_TOKEN_MEAN) {
-        pol += P;
-        kl += K;
-      } else if (L > 0) {
-        pol += P / (double)L;
-        kl += K / (double)L;
-      }
+      __threadfence();
+      const unsigned ticket = atomicAdd(&a.hdr->done_ctas, 1u);
+      s_last = ticket == gridDim.x - 1;
     }
-  }
-  // level 2: warps in fixed order
-  __syncthreads();
-  if (lane == 0) {
-    s_d[warp] = pol;
-    s_d[32 + warp] = kl;
+  } else if (threadIdx.x == 0) {
+    s_last = true;  // B == 0: a single CTA writes the zero loss
   }
   __syncthreads();
-  if (warp == 0) {
-    double p = lane < nw ? s_d[lane] : 0.0;
-    double k = lane < nw ? s_d[32 + lane] : 0.0;
-    p = warp_sum(p);
-    k = warp_sum(k);
-    if (lane == 0) {
-      const double den = a.reduction == GRPO_TOKEN_MEAN ? (double)(N > 0 ? N : 1)
-                                                        : (double)(S > 0 ? S : 1);
-      const double P = p / den, K = k / den;
-      float o0 = (float)(P + (double)a.beta * K), o1 = (float)P, o2 = (float)K;
-      if (a.hdr->status != 0u) o0 = o1 = o2 = NAN;
-      a.out3[0] = o0;
-      a.out3[1] = o1;
-      a.out3[2] = o2;
+  if (!s_last) return;
+  __threadfence();
+
+  // level 2: the scalar, over the B sequence totals in index order
+  long long ns[2] = {0, 0};
+  double u[2] = {0.0, 0.0};
+  for (int64_t j = threadIdx.x; j < a.B; j += blockDim.x) {
+    const int L = a.L[j];
+    const double P = ((volatile double*)a.seq)[j], K = ((volatile double*)a.seq)[a.B + j];
+    ns[0] += L;
+    ns[1] += L > 0;
+    if (a.reduction == GRPO_TOKEN_MEAN) {
+      u[0] += P;
+      u[1] += K;
+    } else if (L > 0) {
+      u[0] += P / (double)L;
+      u[1] += K / (double)L;
     }
+  }
+  block_sum<long long, 2>(ns, s_l);
+  block_sum<double, 2>(u, s_d);
+  if (threadIdx.x == 0) {
+    const long long N = ns[0], S = ns[1];
+    const double den = a.reduction == GRPO_TOKEN_MEAN ? (double)(N > 0 ? N : 1)
+                                                      : (double)(S > 0 ? S : 1);
+    const double P = u[0] / den, K = u[1] / den;
+    float o0 = (float)(P + (double)a.beta * K), o1 = (float)P, o2 = (float)K;
+    if (((volatile unsigned*)&a.hdr->status)[0] != 0u) o0 = o1 = o2 = NAN;
+    a.out3[0] = o0;
+    a.out3[1] = o1;
+    a.out3[2] = o2;
   }
 }
 
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t s) {
-  reduce_kernel<<<1, kReduceThreads, 0, s>>>(a);
+  const int64_t grid = a.B > 0 ? a.B : 1;
+  reduce_kernel<<<(unsigned)grid, kReduceThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

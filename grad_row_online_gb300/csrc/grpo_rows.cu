@@ -53,9 +53,11 @@ __device__ __forceinline__ void lse_elements(const T* row, int64_t e0, int64_t e
 // Online normaliser of one row over its 16-byte vectors (kUnroll in flight
 // per thread) plus its unaligned head / tail scalars.
 template <typename T>
-__device__ __forceinline__ void lse_row(const T* row, int64_t V, OnlineLse& st, uint64_t pol) {
+__device__ __forceinline__ void lse_row(const T* row, int64_t V, OnlineLse& st, uint64_t pol,
+                                        uint4* keep) {
   constexpr int VEC = Storage<T>::kVec;
   const Geom<T> g(row, V);
+  const int64_t nsm = keep ? (g.nvec < kPolicySmemVecs ? g.nvec : kPolicySmemVecs) : 0;
   lse_elements<T>(row, 0, g.head, st);
   lse_elements<T>(row, g.t0, V, st);
   const uint4* vb = reinterpret_cast<const uint4*>(row + g.head);
@@ -66,6 +68,9 @@ __device__ __forceinline__ void lse_row(const T* row, int64_t V, OnlineLse& st, 
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) v[u] = ld_hint(vb + k + u * stride, pol);
 #pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (k + u * stride < nsm) keep[k + u * stride] = v[u];
+#pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       float f[VEC];
       Storage<T>::unpack(v[u], f);
@@ -74,7 +79,9 @@ __device__ __forceinline__ void lse_row(const T* row, int64_t V, OnlineLse& st, 
   }
   for (; k < g.nvec; k += stride) {
     float f[VEC];
-    Storage<T>::unpack(ld_hint(vb + k, pol), f);
+    const uint4 v = ld_hint(vb + k, pol);
+    if (k < nsm) keep[k] = v;
+    Storage<T>::unpack(v, f);
     st.update<VEC>(f);
   }
 }
@@ -88,14 +95,16 @@ __device__ __forceinline__ void lse_row(const T* row, int64_t V, OnlineLse& st, 
 // other.
 template <typename T>
 __device__ __forceinline__ void lse_pair(const T* x, const T* y, int64_t V, OnlineLse& sx,
-                                         OnlineLse& sy, uint64_t pol_x, uint64_t pol_y) {
+                                         OnlineLse& sy, uint64_t pol_x, uint64_t pol_y,
+                                         uint4* keep) {
   constexpr int VEC = Storage<T>::kVec;
   const Geom<T> gx(x, V), gy(y, V);
   if (gy.head != gx.head) {
-    lse_row<T>(x, V, sx, pol_x);
-    lse_row<T>(y, V, sy, pol_y);
+    lse_row<T>(x, V, sx, pol_x, keep);
+    lse_row<T>(y, V, sy, pol_y, nullptr);
     return;
   }
+  const int64_t nsm = keep ? (gx.nvec < kPolicySmemVecs ? gx.nvec : kPolicySmemVecs) : 0;
   // head / tail scalars, as one padded vector per thread
   const bool h = (int)threadIdx.x < gx.head;
   const bool t = (int)threadIdx.x < gx.tail;
@@ -127,6 +136,9 @@ __device__ __forceinline__ void lse_pair(const T* x, const T* y, int64_t V, Onli
       vy[u] = ld_hint(yv + k + u * stride, pol_y);
     }
 #pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (k + u * stride < nsm) keep[k + u * stride] = vx[u];
+#pragma unroll
     for (int u = 0; u < U; ++u) {
       float f[VEC];
       Storage<T>::unpack(vx[u], f);
@@ -137,7 +149,9 @@ __device__ __forceinline__ void lse_pair(const T* x, const T* y, int64_t V, Onli
   }
   for (; k < gx.nvec; k += stride) {
     float f[VEC];
-    Storage<T>::unpack(ld_hint(xv + k, pol_x), f);
+    const uint4 v = ld_hint(xv + k, pol_x);
+    if (k < nsm) keep[k] = v;
+    Storage<T>::unpack(v, f);
     sx.update<VEC>(f);
     Storage<T>::unpack(ld_hint(yv + k, pol_y), f);
     sy.update<VEC>(f);
@@ -199,7 +213,7 @@ __device__ double sum_exp_precise(const T* row, int64_t V, float M, const float*
 // element is patched once per vector, outside the element loop.
 template <typename T, bool kPrecise>
 __device__ void grad_row(const T* x, T* g, int64_t V, int64_t act, const RowScalars& rs,
-                         uint64_t pol_in, uint64_t pol_out) {
+                         uint64_t pol_in, uint64_t pol_out, const uint4* kept) {
   constexpr int VEC = Storage<T>::kVec;
   const bool same_phase = (((uintptr_t)x ^ (uintptr_t)g) & 15) == 0;
   if (!same_phase) {  // differently aligned buffers: element by element
@@ -224,7 +238,6 @@ __device__ void grad_row(const T* x, T* g, int64_t V, int64_t act, const RowScal
   const int64_t arel = act - gm.head;
   const int64_t aq = (arel >= 0 && arel < n * VEC) ? arel / VEC : -1;
   const int alane = (int)(arel - aq * VEC);
-  auto at = [&](int64_t k) -> int64_t { return kReverseSweep2 ? n - 1 - k : k; };
   auto emit = [&](const uint4& in, int64_t q) {
     float f[VEC];
     Storage<T>::unpack(in, f);
@@ -237,16 +250,22 @@ __device__ void grad_row(const T* x, T* g, int64_t V, int64_t act, const RowScal
     }
     st_hint(gv + q, Storage<T>::pack(f), pol_out);
   };
+  // vectors [0, nsm) were kept in shared memory by sweep 1; the rest, in the
+  // sweep order, from global memory (mostly L2)
+  const int64_t nsm = n < kPolicySmemVecs ? n : kPolicySmemVecs;
+  const int64_t ng = n - nsm;
+  auto atg = [&](int64_t k) -> int64_t { return kReverseSweep2 ? n - 1 - k : nsm + k; };
   constexpr int U = kGradUnroll;
   int64_t k = threadIdx.x;
-  for (; k + (U - 1) * stride < n; k += U * stride) {
+  for (; k + (U - 1) * stride < ng; k += U * stride) {
     uint4 v[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) v[u] = ld_hint(xv + at(k + u * stride), pol_in);
+    for (int u = 0; u < U; ++u) v[u] = ld_hint(xv + atg(k + u * stride), pol_in);
 #pragma unroll
-    for (int u = 0; u < U; ++u) emit(v[u], at(k + u * stride));
+    for (int u = 0; u < U; ++u) emit(v[u], atg(k + u * stride));
   }
-  for (; k < n; k += stride) emit(ld_hint(xv + at(k), pol_in), at(k));
+  for (; k < ng; k += stride) emit(ld_hint(xv + atg(k), pol_in), atg(k));
+  for (int64_t q = threadIdx.x; q < nsm; q += stride) emit(kept[q], q);
 }
 
 // zeros over a gradient row
@@ -263,6 +282,7 @@ __device__ void zero_row(T* g, int64_t V, uint64_t pol) {
 // ------------------------------------------------------------------ kernel
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(const RowArgs a) {
+  extern __shared__ __align__(16) uint4 s_keep[];  // kPolicySmemVecs vectors
   __shared__ float s_f[64];
   __shared__ FF s_zs[64];
   __shared__ double s_d[64];
@@ -338,7 +358,8 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(cons
       OnlineLse sp, sr;
       sp.init();
       sr.init();
-      lse_pair<T>(x, y, a.V, sp, sr, want_grad ? keep : stream, stream);
+      lse_pair<T>(x, y, a.V, sp, sr, want_grad ? keep : stream, stream,
+                  want_grad ? s_keep : nullptr);
       float Mp, Mr;
       FF Zp = {0.f, 0.f}, Zr = {0.f, 0.f};
       combine_ff(sp, sr, s_f, s_zs, Mp, Mr, Zp, Zr);
@@ -383,9 +404,9 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(cons
       if (want_grad) {
         const RowScalars rs = s_rs;
         if (rs.precise)
-          grad_row<T, true>(x, grow, a.V, act, rs, stream, stream);
+          grad_row<T, true>(x, grow, a.V, act, rs, stream, stream, s_keep);
         else
-          grad_row<T, false>(x, grow, a.V, act, rs, stream, stream);
+          grad_row<T, false>(x, grow, a.V, act, rs, stream, stream, s_keep);
       }
     }
     __syncthreads();  // everyone is done with s_rs / s_next of this row
@@ -402,15 +423,19 @@ static cudaError_t launch_t(const RowArgs& a, const grpo_profile_t* prof, cudaSt
   if (e != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
+  e = cudaFuncSetAttribute(rows_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kPolicySmemBytes);
+  if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rows_kernel<T>, kRowThreads, 0);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rows_kernel<T>, kRowThreads,
+                                                    kPolicySmemBytes);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   int64_t grid = (int64_t)sms * per_sm;
   const int64_t rows = a.B * a.T;
   if (grid > rows) grid = rows;
   if (prof && prof->start) cudaEventRecord((cudaEvent_t)prof->start, s);
-  rows_kernel<T><<<(unsigned)grid, kRowThreads, 0, s>>>(a);
+  rows_kernel<T><<<(unsigned)grid, kRowThreads, kPolicySmemBytes, s>>>(a);
   e = cudaGetLastError();
   if (prof && prof->stop) cudaEventRecord((cudaEvent_t)prof->stop, s);
   return e;

@@ -14,6 +14,11 @@ static constexpr int kUnroll = 4;        // 16-byte vectors in flight per thread
 static constexpr int kPairUnroll = 3;    // ... per row when policy and reference stream together
 static constexpr int kGradUnroll = 4;    // ... in the gradient sweep
 static constexpr bool kReverseSweep2 = true;
+// The first kPolicySmemBytes of the policy row are kept in shared memory
+// between the sweeps: with sweep 2 back to front they are the lines read
+// longest ago, the ones L2 would have lost.
+static constexpr int kPolicySmemBytes = 40 * 1024;
+static constexpr int kPolicySmemVecs = kPolicySmemBytes / 16;
 // Refinement.  The fast logsumexp of a row has an absolute error below
 // kFastErrBound (the normaliser's relative error, below 2^-19, plus the
 // float-float finish's ~1e-7).  An element of the fp32 gradient stays within
