@@ -6,9 +6,12 @@ One step = one call of grpo_loss_fwd_bwd over the whole workload (group
 advantages, both vocabulary sweeps, the gradient, the reduction).  Default
 workload: the large-vocabulary configuration (B=16, T=2048, V=151936, bf16).
 Inputs are synthetic (seeded generator) and larger than L2, so no flush is
-needed between steps.  Under torchrun every rank runs an independent replica
-(the loss of one batch does not shard without its reduction; see the design
-notes), so scaling is weak and `value` sums the replicas.
+needed between steps (the logps-only workload rotates over copies whose total
+is larger than L2).  The timed steps are queued behind a head start of plain
+device work, so the device events time the device and not the Python call
+overhead of short steps; `e2e` times the whole host path.  Under torchrun
+every rank runs an independent replica (the loss of one batch does not shard
+without its reduction), so scaling is weak and `value` sums the replicas.
 
 --impl reference times the double-precision CPU oracle (the only reference
 implementation of this method) on a bounded sample of the same workload.
@@ -178,26 +181,6 @@ def oracle_threads() -> int:
     return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
 
 
-def cpu_baseline(w: synth.Workload, budget_s: float = 12.0) -> dict:
-    active = np.nonzero(w.completion_mask().reshape(-1))[0]
-    cores = oracle_threads()
-    rows = np.random.default_rng(0).choice(active, min(len(active), max(cores * 2, 16)),
-                                           replace=False)
-    cache = {}
-    oracle_sample_step(w, rows[:2], {})  # load the library
-    t0 = time.perf_counter()
-    n = oracle_sample_step(w, rows, cache)
-    first = time.perf_counter() - t0
-    reps = max(1, int(budget_s / max(first, 1e-3)) - 1)
-    t0 = time.perf_counter()
-    for _ in range(reps):
-        n += oracle_sample_step(w, rows, cache)
-    el = first + time.perf_counter() - t0
-    return {"value": n / el, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{len(rows)} random active rows of {w.name} (policy+ref log-softmax, "
-                      f"token terms, gradient rows), {reps + 1} passes, {el:.1f} s"}
-
-
 # ---------------------------------------------------------------------------
 def dist_setup():
     import torch
@@ -230,39 +213,312 @@ def barrier(ws: int):
         dist.barrier()
 
 
+def aggregate_value(active: int, steps: int, world: int, elapsed_ms_max: float) -> float:
+    """Whole-job throughput: the active tokens every rank processed over the
+    slowest rank's time (replicas: each rank runs the full workload)."""
+    return active * steps * world / (elapsed_ms_max / 1e3)
+
+
+# ---------------------------------------------------------------------------
+# the oracle as the reference arm / CPU baseline
+# ---------------------------------------------------------------------------
+def oracle_logps_step(w: synth.Workload, cache: dict) -> int:
+    """One pass of the oracle over the whole logps-only workload (inputs
+    generated once, not timed).  Returns tokens processed."""
+    import oracle
+    if "lp" not in cache:
+        cache["lp"], cache["old"], cache["ref"] = w.logps_inputs()
+        cache["mask"] = w.completion_mask()
+        cache["R"], cache["gb"] = w.rewards(), w.group_boundaries()
+    A = oracle.group_advantages(cache["R"], cache["gb"])
+    oracle.loss_from_logps(cache["lp"], cache["ref"], cache["old"], cache["mask"], A, w.eps_lo,
+                           w.eps_hi, w.beta, reduction=w.reduction)
+    return int(cache["mask"].sum())
+
+
+def reference_sample(w: synth.Workload):
+    """(step function, sample description) of the oracle on a bounded sample."""
+    cores = oracle_threads()
+    if w.V == 0:
+        cache = {}
+        return (lambda: oracle_logps_step(w, cache)), f"the whole {w.name} workload per step"
+    active = np.nonzero(w.completion_mask().reshape(-1))[0]
+    rows = np.random.default_rng(0).choice(active, min(len(active), max(cores * 2, 16)),
+                                           replace=False)
+    cache = {}
+    return (lambda: oracle_sample_step(w, rows, cache)), \
+        f"{len(rows)} random active rows of {w.name} per step (policy+ref log-softmax, token " \
+        f"terms, gradient rows)"
+
+
+def cpu_baseline(w: synth.Workload, budget_s: float = 12.0) -> dict:
+    step, what = reference_sample(w)
+    step()  # load the library, generate the inputs
+    n, t0, passes = 0, time.perf_counter(), 0
+    while True:
+        n += step()
+        passes += 1
+        el = time.perf_counter() - t0
+        if el > budget_s or passes >= 10000:
+            break
+    return {"value": n / el, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"{what}; {passes} passes, {el:.1f} s"}
+
+
 def run_reference(args, w, ws, rank):
     if rank != 0:
         return
-    cores = oracle_threads()
-    active = np.nonzero(w.completion_mask().reshape(-1))[0]
-    rows = np.random.default_rng(0).choice(active, min(len(active), max(cores, 8)), replace=False)
-    cache = {}
-    oracle_sample_step(w, rows, cache)
-    times = []
+    step, what = reference_sample(w)
+    step()
+    times, n = [], 0
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        oracle_sample_step(w, rows, cache)
+        k = step()
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
+            n += k
     total = sum(times)
-    value = len(rows) * len(times) / total
+    value = n / total
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(w),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"each step: {len(rows)} random active rows of {w.name}"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_threads(),
+                             "kind": "oracle", "sample": what},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
+def l2_note(w: synth.Workload) -> str:
+    if w.V:
+        return "inputs larger than L2 (no flush needed)"
+    # logps, old, ref, grad (f32) and the mask per slot, rewards per sequence
+    per_copy = w.B * w.T * (4 * 4 + 1) + 4 * w.B
+    return (f"inputs rotate over {LogpsCase.COPIES} copies "
+            f"({LogpsCase.COPIES * per_copy / 1e6:.0f} MB, larger than L2)")
+
+
 def workload_config(w: synth.Workload) -> dict:
     act = int(w.completion_mask().sum())
-    cfg = {"workload": f"{w.name}: B={w.B} T={w.T} V={w.V} {w.dtype}", "B": w.B, "T": w.T,
-           "V": w.V, "active_tokens": act, "samples_per_prompt": w.samples_per_prompt or None,
+    note = l2_note(w)
+    cfg = {"workload": f"{w.name}: B={w.B} T={w.T}" + (f" V={w.V} {w.dtype}" if w.V else " logps f32"),
+           "B": w.B, "T": w.T, "V": w.V or None, "active_tokens": act,
+           "samples_per_prompt": w.samples_per_prompt or None,
            "reduction": ["token_mean", "sequence_mean"][w.reduction],
-           "parallelism": "replicas", "l2": "inputs larger than L2 (no flush needed)"}
+           "parallelism": "replicas", "l2": note,
+           "timing": "device events around the steps, queued behind a head start of "
+                     "plain device work so that host call overhead is not timed"}
     return cfg
+
+
+# ---------------------------------------------------------------------------
+# the two boundaries under test
+# ---------------------------------------------------------------------------
+class LogitsCase:
+    """grpo_loss_fwd_bwd on a logits workload (inputs larger than L2)."""
+
+    launches_per_step = 3  # prep, rows, reduce
+    kernel = "rows_kernel (fused sweeps)"
+
+    def __init__(self, w, device):
+        import torch
+        import grad_row_online_gb300 as g
+        self.g, self.w, self.device = g, w, device
+        self.inp = device_inputs(w, device)
+        self.kw = loss_kwargs(w, self.inp)
+        self.active = int(self.inp["mask"].sum().item())
+        self.grad = torch.empty_like(self.inp["X"])
+        self.out3 = torch.empty(3, dtype=torch.float32, device=device)
+        self.wsp = torch.empty(g.grpo_workspace_size(w.B, w.T), dtype=torch.uint8, device=device)
+        s_in = 2 if w.dtype == "bf16" else 4
+        # policy read twice, ref once, grad written once, per active row
+        self.alg_bytes = 4.0 * w.V * s_in * self.active
+
+    def step(self, k=0, prof=None):
+        i = self.inp
+        self.g.grpo_loss_fwd_bwd(i["X"], i["Y"], i["acts"], i["old"], i["mask"], i["R"],
+                                 grad=self.grad, out3=self.out3, workspace=self.wsp, profile=prof,
+                                 **self.kw)
+
+    def e2e_setup(self):
+        import torch
+        self.host = {}
+        for k, v in self.inp.items():
+            self.host[k] = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+            self.host[k].copy_(v)
+        self.dev_in = {k: torch.empty_like(v) for k, v in self.inp.items()}
+        self.dev_in["bounds"] = self.inp["bounds"]
+        self.kw_e = loss_kwargs(self.w, self.dev_in)
+        self.loss_host = torch.empty(3, dtype=torch.float32).pin_memory()
+        return sum(v.numel() * v.element_size() for k, v in self.host.items() if k != "bounds")
+
+    def e2e_step(self):
+        d = self.dev_in
+        for k in ("X", "Y", "acts", "old", "mask", "R"):
+            d[k].copy_(self.host[k], non_blocking=True)
+        self.g.grpo_loss_fwd_bwd(d["X"], d["Y"], d["acts"], d["old"], d["mask"], d["R"],
+                                 grad=self.grad, out3=self.out3, workspace=self.wsp, **self.kw_e)
+        self.loss_host.copy_(self.out3, non_blocking=True)
+
+
+class LogpsCase:
+    """grpo_loss_from_logps on the logps-only workload.  One copy of its
+    inputs (54 MB) fits in L2, so the timed steps rotate over COPIES copies
+    (with their own gradient buffers): a step's inputs were last touched
+    COPIES - 1 steps earlier, with more than L2's capacity read and written
+    since."""
+
+    COPIES = 4
+    launches_per_step = 2  # prep, logps_kernel
+    kernel = "logps_kernel"
+
+    def __init__(self, w, device):
+        import torch
+        import grad_row_online_gb300 as g
+        self.g, self.w, self.device = g, w, device
+        lp, old, ref = w.logps_inputs()
+        host = dict(lp=lp, old=old, ref=ref, mask=w.completion_mask(), R=w.rewards())
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        self.copies = [{k: t(v) for k, v in host.items()} for _ in range(self.COPIES)]
+        for c in self.copies:
+            c["grad"] = torch.empty((w.B, w.T), dtype=torch.float32, device=device)
+        self.inp = self.copies[0]
+        self.grad = self.inp["grad"]
+        self.active = int(self.inp["mask"].sum().item())
+        self.out3 = torch.empty(3, dtype=torch.float32, device=device)
+        self.wsp = torch.empty(g.grpo_workspace_size(w.B, w.T), dtype=torch.uint8, device=device)
+        # logp / old / ref of active tokens, the mask, dL/dlogp of every slot
+        self.alg_bytes = 12.0 * self.active + 5.0 * w.B * w.T
+
+    def _call(self, i, prof=None):
+        w = self.w
+        self.g.grpo_loss_from_logps(i["lp"], i["old"], i["ref"], i["mask"], i["R"],
+                                    samples_per_prompt=w.samples_per_prompt, clip_eps=w.eps_lo,
+                                    clip_eps_hi=w.eps_hi, beta=w.beta, reduction=w.reduction,
+                                    grad=i["grad"], out3=self.out3, workspace=self.wsp,
+                                    profile=prof)
+
+    def step(self, k=0, prof=None):
+        self._call(self.copies[k % self.COPIES], prof)
+
+    def e2e_setup(self):
+        import torch
+        self.host = {}
+        for k, v in self.inp.items():
+            if k == "grad":
+                continue
+            self.host[k] = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+            self.host[k].copy_(v)
+        self.dev_in = {k: torch.empty_like(v) for k, v in self.inp.items()}
+        self.loss_host = torch.empty(3, dtype=torch.float32).pin_memory()
+        return sum(v.numel() * v.element_size() for v in self.host.values())
+
+    def e2e_step(self):
+        for k in self.host:
+            self.dev_in[k].copy_(self.host[k], non_blocking=True)
+        self._call(self.dev_in)
+        self.loss_host.copy_(self.out3, non_blocking=True)
+
+
+def head_start(device, seconds: float):
+    """Queue about `seconds` of plain device work (zero-fills of a 1 GB
+    buffer) ahead of the timed region, so that the host has enqueued the
+    timed steps before the device reaches them: the events then time the
+    device, not the Python call overhead of short steps."""
+    import torch
+    buf = torch.empty(1 << 30, dtype=torch.uint8, device=device)
+    seconds = min(seconds, 0.05)
+    n = max(1, int(seconds / 160e-6) + 1)  # one 1 GB fill takes about 160 us
+    for _ in range(n):
+        buf.zero_()
+    return buf
+
+
+def run_gpu(args, w, ws, rank, local):
+    import torch
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    case = (LogpsCase if w.V == 0 else LogitsCase)(w, device)
+    stream = torch.cuda.current_stream(device)
+
+    t0 = time.perf_counter()
+    for k in range(args.warmup):
+        case.step(k)
+    host_per_step = (time.perf_counter() - t0) / max(args.warmup, 1)
+    torch.cuda.synchronize(device)
+    assert case.g.grpo_read_device_status(case.wsp) == 0
+
+    def ev():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()  # created now, recorded again inside the timed region
+        return e
+    kev = [(ev(), ev()) for _ in range(args.steps)]   # main kernel (recorded by the library)
+    e_start, e_stop = ev(), ev()
+    torch.cuda.synchronize(device)
+
+    uuid = getattr(torch.cuda.get_device_properties(device), "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else local)
+    barrier(ws)
+    torch.cuda.synchronize(device)
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    hs = head_start(device, 2.0 * host_per_step * args.steps + 1e-3)
+    e_start.record(stream)
+    for k in range(args.steps):
+        case.step(k, kev[k])
+    e_stop.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(ws)
+    clk = clocks.stop() if rank == 0 else None
+    del hs
+    elapsed_ms = e_start.elapsed_time(e_stop)
+    kernel_ms = [a.elapsed_time(b) for a, b in kev]
+    elapsed_ms = max_over_ranks(elapsed_ms, ws, device)
+    ms_per_step = elapsed_ms / args.steps
+    value = aggregate_value(case.active, args.steps, ws, elapsed_ms)
+
+    # ---- end to end: pinned host inputs -> device -> loss -> host ----
+    e2e_steps = min(args.e2e_steps, args.steps)
+    h2d = case.e2e_setup()
+    case.e2e_step()
+    torch.cuda.synchronize(device)
+    barrier(ws)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        case.e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, device)
+    e2e_value = aggregate_value(case.active, e2e_steps, ws, e2e_ms)
+
+    if rank != 0:
+        barrier(ws)
+        return
+    kern_avg_s = statistics.mean(kernel_ms) / 1e3
+    peak, peak_kind = measured_peak()
+    achieved = case.alg_bytes / kern_avg_s / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype if w.V else "f32",
+        "data": "synthetic", "config": workload_config(w),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(w.name) if w.V else None,
+                     "kernel": case.kernel, "peak_source": f"{peak_kind} hbm_gbs",
+                     "bytes_per_launch": case.alg_bytes, "avg_launch_ms": kern_avg_s * 1e3},
+        "step_gbs_algorithmic": case.alg_bytes / (ms_per_step / 1e3) / 1e9,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": 12, "steps": e2e_steps},
+        "gpu_launches": case.launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline and ws == 1:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+    barrier(ws)
 
 
 def main():
@@ -271,7 +527,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="large_vocab",
-                    choices=["fused", "large_vocab", "var_groups"])
+                    choices=["fused", "large_vocab", "var_groups", "logps", "logps_full"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -288,120 +544,7 @@ def main():
     if args.impl == "reference":
         run_reference(args, w, ws, rank)
         return
-
-    import torch
-    import grad_row_online_gb300 as g
-    device = torch.device("cuda", local)
-    torch.cuda.set_device(device)
-    inp = device_inputs(w, device)
-    kw = loss_kwargs(w, inp)
-    B, T, V = w.B, w.T, w.V
-    s_in = 2 if w.dtype == "bf16" else 4
-    active = int(inp["mask"].sum().item())
-    grad = torch.empty_like(inp["X"])
-    out3 = torch.empty(3, dtype=torch.float32, device=device)
-    wsp = torch.empty(g.grpo_workspace_size(B, T), dtype=torch.uint8, device=device)
-    stream = torch.cuda.current_stream(device)
-
-    def step(prof=None):
-        g.grpo_loss_fwd_bwd(inp["X"], inp["Y"], inp["acts"], inp["old"], inp["mask"], inp["R"],
-                            grad=grad, out3=out3, workspace=wsp, profile=prof, **kw)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(device)
-    assert g.grpo_read_device_status(wsp) == 0
-
-    # row-kernel events, created up front (recorded by the library)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    for a, b in evs:
-        a.record(); b.record()
-    torch.cuda.synchronize(device)
-
-    uuid = getattr(torch.cuda.get_device_properties(device), "uuid", None)
-    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else local)
-    barrier(ws)
-    torch.cuda.synchronize(device)
-    if rank == 0:
-        clocks.start()
-        time.sleep(0.3)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_stop = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        step(evs[i])
-    t_stop.record(stream)
-    torch.cuda.synchronize(device)
-    barrier(ws)
-    clk = clocks.stop() if rank == 0 else None
-    elapsed_ms = t_start.elapsed_time(t_stop)
-    rows_ms = [a.elapsed_time(b) for a, b in evs]
-    elapsed_ms = max_over_ranks(elapsed_ms, ws, device)
-    ms_per_step = elapsed_ms / args.steps
-    value = active * args.steps * ws / (elapsed_ms / 1e3)
-
-    # ---- end to end: pinned host inputs -> device -> loss -> host ----
-    e2e_steps = min(args.e2e_steps, args.steps)
-    host = {}
-    for k, v in inp.items():
-        host[k] = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
-        host[k].copy_(v)
-    h2d = sum(v.numel() * v.element_size() for k, v in host.items() if k != "bounds")
-    loss_host = torch.empty(3, dtype=torch.float32).pin_memory()
-    dev_in = {k: torch.empty_like(v) for k, v in inp.items()}
-    dev_in["bounds"] = inp["bounds"]
-    kw_e = loss_kwargs(w, dev_in)
-
-    def e2e_step():
-        for k in ("X", "Y", "acts", "old", "mask", "R"):
-            dev_in[k].copy_(host[k], non_blocking=True)
-        g.grpo_loss_fwd_bwd(dev_in["X"], dev_in["Y"], dev_in["acts"], dev_in["old"],
-                            dev_in["mask"], dev_in["R"], grad=grad, out3=out3, workspace=wsp,
-                            **kw_e)
-        loss_host.copy_(out3, non_blocking=True)
-
-    e2e_step()
-    torch.cuda.synchronize(device)
-    barrier(ws)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(device)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, device)
-    e2e_value = active * e2e_steps * ws / (e2e_ms / 1e3)
-
-    if rank != 0:
-        barrier(ws)
-        return
-
-    alg_bytes = 4.0 * V * s_in * active  # policy read twice, ref once, grad written once
-    rows_avg_s = statistics.mean(rows_ms) / 1e3
-    peak, peak_kind = measured_peak()
-    achieved = alg_bytes / rows_avg_s / 1e9
-    traffic = profiled_traffic(w.name)
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": workload_config(w),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "rows_kernel (fused sweeps)", "peak_source": f"{peak_kind} hbm_gbs",
-                     "bytes_per_launch": alg_bytes, "avg_launch_ms": rows_avg_s * 1e3},
-        "step_gbs_algorithmic": alg_bytes / (ms_per_step / 1e3) / 1e9,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": 12, "steps": e2e_steps},
-        "gpu_launches": 3 * args.steps,
-        "clocks": clk,
-    }
-    if not args.no_cpu_baseline and ws == 1:
-        line["cpu_baseline"] = cpu_baseline(w)
-    print(json.dumps(line), flush=True)
-    barrier(ws)
+    run_gpu(args, w, ws, rank, local)
 
 
 if __name__ == "__main__":

@@ -284,7 +284,8 @@ def grpo_loss_from_logps(logps: torch.Tensor, old_logps: torch.Tensor,
                          adv_eps: float = 1e-6, eps_add: bool = False, grad_scale: float = 1.0,
                          reduction="token_mean", grad=True, want_per_seq: bool = False,
                          want_adv: bool = False, out3: Optional[torch.Tensor] = None,
-                         workspace: Optional[torch.Tensor] = None, stream=None) -> dict:
+                         workspace: Optional[torch.Tensor] = None, stream=None,
+                         profile=None) -> dict:
     """GRPO loss from per-token log-probs; ``grad`` gives dL/dlogp [B,T]."""
     _dev(logps, "logps", torch.float32)
     B, T = logps.shape
@@ -298,7 +299,7 @@ def grpo_loss_from_logps(logps: torch.Tensor, old_logps: torch.Tensor,
     dev = logps.device
     g, keep = _groups(B, samples_per_prompt, group_boundaries)
     p, prof = _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction,
-                      GRPO_ADV_EPS_ADD if eps_add else 0, None)
+                      GRPO_ADV_EPS_ADD if eps_add else 0, profile)
     if grad is True:
         grad_t = torch.empty((B, T), dtype=torch.float32, device=dev)
     elif grad is None or grad is False:

@@ -18,23 +18,29 @@ namespace grpo {
 //   header   256 B   status word, row counter
 //   L        int32 [B]        active tokens per sequence
 //   A        double[B]        advantages
-//   seq      double[2B]       per-sequence policy / KL totals (logps path)
+//   Aff      float2[B]        the same advantages as float pairs (hi, lo)
+//   seq      double[2B]       per-sequence policy / KL totals (logits path);
+//                             the logps path keeps float-pair totals there,
+//                             float4 {P.hi, P.lo, K.hi, K.lo} per sequence
 //   slots    double[2 B T]    per-token policy / KL terms (logits path)
 // ----------------------------------------------------------------------------
 struct WsHeader {
-  unsigned int status;        // device-detected error bits
-  unsigned int done_ctas;     // reduce: CTAs finished (the last one forms the scalar)
+  unsigned int status;             // device-detected error bits
+  unsigned int done_ctas;          // reduce: CTAs finished (the last one forms the scalar)
   unsigned long long row_counter;  // rows: next row to claim
+  unsigned long long N;            // active tokens  (prep: integer atomics, exact)
+  unsigned long long S;            // live sequences (idem)
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t off_L, off_A, off_seq, off_slots, total;
+  size_t off_L, off_A, off_Aff, off_seq, off_slots, total;
   __host__ __device__ WsLayout(int64_t B, int64_t T) {
     off_L = 256;
     off_A = off_L + align256(sizeof(int32_t) * (size_t)B);
-    off_seq = off_A + align256(sizeof(double) * (size_t)B);
+    off_Aff = off_A + align256(sizeof(double) * (size_t)B);
+    off_seq = off_Aff + align256(sizeof(float) * 2 * (size_t)B);
     off_slots = off_seq + align256(sizeof(double) * 2 * (size_t)B);
     total = off_slots + align256(sizeof(double) * 2 * (size_t)B * (size_t)T);
   }
@@ -221,6 +227,36 @@ __device__ __forceinline__ FF fast_two_sum(float a, float b) {  // |a| >= |b|
   return {s, __fsub_rn(b, __fsub_rn(s, a))};
 }
 
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+  FF s = two_sum(a.hi, b.hi);
+  s.lo = __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo));
+  return fast_two_sum(s.hi, s.lo);
+}
+__device__ __forceinline__ FF ff_neg(FF a) { return {-a.hi, -a.lo}; }
+__device__ __forceinline__ FF ff_scale(FF a, float f) {  // a * f
+  const float ph = __fmul_rn(a.hi, f);
+  const float pl = __fmaf_rn(a.hi, f, -ph);
+  return fast_two_sum(ph, __fmaf_rn(a.lo, f, pl));
+}
+__device__ __forceinline__ float ff_float(FF a) { return __fadd_rn(a.hi, a.lo); }
+// a / b: the fp32 quotient of the leading parts, then one correction from
+// the remainder a - q1 b (formed with an exact product).
+__device__ __forceinline__ FF ff_div(FF a, FF b) {
+  const float q1 = __fdiv_rn(a.hi, b.hi);
+  const float p = __fmul_rn(q1, b.hi);
+  const float pe = __fmaf_rn(q1, b.hi, -p);
+  const FF r = two_sum(a.hi, -p);
+  const float rem = __fadd_rn(r.hi, __fadd_rn(__fsub_rn(r.lo, pe),
+                                              __fsub_rn(a.lo, __fmul_rn(q1, b.lo))));
+  return fast_two_sum(q1, __fdiv_rn(rem, b.hi));
+}
+// A non-negative integer below 2^48 as an exact float pair.
+__device__ __forceinline__ FF ff_from_u64(unsigned long long n) {
+  const float hi = __ull2float_rn(n);
+  const long long rest = (long long)n - (long long)hi;
+  return {hi, (float)rest};
+}
+
 // thi / tlo: the 2^(j/64) table, staged in shared memory by the caller.
 __device__ __forceinline__ FF exp_ff(float t_hi, float t_lo, const float* thi,
                                      const float* tlo, const ExpTable& tb) {
@@ -330,6 +366,39 @@ __device__ __forceinline__ float block_max(float v, float* scratch) {
   return warp_max(x);
 }
 
+// This thread's share of the level-2 sums over the B sequence totals
+// (seq[0..B) policy, seq[B..2B) KL), in a fixed order: the token mean adds
+// the totals, the sequence mean adds total / L_i over live sequences.  The
+// totals were written by other CTAs of the same launch (made visible by
+// their __threadfence before the ticket), so they are read from L2 (ld.cg),
+// eight at a time to keep the loads in flight.
+__device__ __forceinline__ void seq_totals(const double* seq, const int32_t* Ls, int64_t B,
+                                           int reduction, double (&u)[2]) {
+  constexpr int kBatch = 8;
+  const int64_t stride = blockDim.x;
+  for (int64_t j0 = threadIdx.x; j0 < B; j0 += kBatch * stride) {
+    double P[kBatch], K[kBatch];
+    int L[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int64_t j = j0 + k * stride;
+      P[k] = j < B ? __ldcg(seq + j) : 0.0;
+      K[k] = j < B ? __ldcg(seq + B + j) : 0.0;
+      L[k] = j < B ? __ldcg(Ls + j) : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      if (reduction == GRPO_TOKEN_MEAN) {
+        u[0] += P[k];
+        u[1] += K[k];
+      } else if (L[k] > 0) {
+        u[0] += P[k] / (double)L[k];
+        u[1] += K[k] / (double)L[k];
+      }
+    }
+  }
+}
+
 // ----------------------------------------------------------------------------
 // kernels (defined in the .cu files)
 // ----------------------------------------------------------------------------
@@ -343,6 +412,7 @@ struct PrepArgs {
   const uint8_t* mask;  // the completion mask (may be NULL when T == 0)
   int count;            // 1: also count active tokens per sequence into L
   double* A;
+  float2* Aff;     // nullable: the advantages as float pairs
   float* adv_out;  // nullable
   int32_t* L;      // used when mask != NULL
   WsHeader* hdr;
@@ -390,8 +460,9 @@ struct LogpsArgs {
   const float* ref;  // nullable
   const uint8_t* mask;
   const double* A;
+  const float2* Aff;  // the advantages as float pairs
   int32_t* L;
-  double* seq;  // [2B]
+  float4* seq;  // [B] {P.hi, P.lo, K.hi, K.lo}
   float* grad;  // nullable
   float* out3;
   float* per_seq;  // nullable
@@ -405,6 +476,6 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 cudaError_t launch_rows(const RowArgs& a, grpo_dtype_t dt, const grpo_profile_t* prof,
                         cudaStream_t s);
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t s);
-cudaError_t launch_logps(const LogpsArgs& a, cudaStream_t s);
+cudaError_t launch_logps(const LogpsArgs& a, const grpo_profile_t* prof, cudaStream_t s);
 
 }  // namespace grpo

@@ -4,64 +4,102 @@
 // probs, reduced inside each block (never with per-token atomics); RL-Kernel
 // "GRPO Loss" page, "Accuracy" for the per-token terms and "Tensor and Data
 // Parallel" for the two nested reductions (token slots -> sequence totals ->
-// scalar).  Two kernels:
-//   seq kernel   one CTA per sequence: the sequence's active-token count and
-//                its policy / KL totals (fp32 per token, Kahan per thread,
-//                double across the block, fixed order);
-//   grad kernel  block 0 reduces the B sequence totals to the scalar
-//                outputs; all blocks write dL/dlogp = w for every token.
-// The whole cost is one pass over logps / old_logps / ref_logps / mask.
+// scalar).
+//
+// One kernel, after prep has counted the active tokens (L_i, N and S in the
+// workspace): one CTA per sequence evaluates each active token's policy and
+// KL terms once, writes dL/dlogp for every slot (0 on masked ones) and forms
+// the sequence's totals in a fixed order; the CTA that finishes last (an
+// atomic ticket that nobody waits on) forms the scalar from the B totals in
+// index order.  The whole cost is one pass over logps / old_logps /
+// ref_logps / mask plus the gradient write.
+//
+// Arithmetic: fp32 per token, Kahan sums per thread, float pairs (two_sum)
+// for every sum above that.  No fp64 on the common path: GB300's fp64 pipe
+// is a small fraction of its fp32 rate, and a few dozen fp64 operations per
+// CTA measurably lengthened this kernel.
 #include "grpo_internal.cuh"
 
 namespace grpo {
 
-static constexpr int kSeqThreads = 256;
-static constexpr int kGradThreads = 256;
+static constexpr int kLogpsThreads = 128;
 static constexpr float kWPrecise = 0x1p-11f;
 
-// k3 = e^d - d - 1 in fp32: a short series where e^d - 1 and d nearly
-// cancel, the library expm1 elsewhere.
-__device__ __forceinline__ float k3f(float d) {
-  if (fabsf(d) < 0.0625f) {
-    float q = __fmaf_rn(d, 1.0f / 720.0f, 1.0f / 120.0f);
-    q = __fmaf_rn(d, q, 1.0f / 24.0f);
-    q = __fmaf_rn(d, q, 1.0f / 6.0f);
-    q = __fmaf_rn(d, q, 0.5f);
-    return __fmul_rn(__fmul_rn(d, d), q);
+// e^d - 1 and k3 = e^d - d - 1 together.  With Q(d) = sum_{n>=2} d^(n-2)/n!,
+// e^d - 1 = d + d^2 Q(d) and k3 = d^2 Q(d).
+//
+// Q_poly: Q through its d^7/9! term.  For |d| < 1/2 the first omitted term,
+// d^8/10!, is below 2e-9 of Q, so Q_poly is Q to fp32 rounding.
+__device__ __forceinline__ float Q_poly(float d) {
+  float q = __fmaf_rn(d, 1.0f / 362880.0f, 1.0f / 40320.0f);
+  q = __fmaf_rn(d, q, 1.0f / 5040.0f);
+  q = __fmaf_rn(d, q, 1.0f / 720.0f);
+  q = __fmaf_rn(d, q, 1.0f / 120.0f);
+  q = __fmaf_rn(d, q, 1.0f / 24.0f);
+  q = __fmaf_rn(d, q, 1.0f / 6.0f);
+  return __fmaf_rn(d, q, 0.5f);
+}
+
+struct Em {
+  float em;  // e^d - 1
+  float k3;  // e^d - d - 1
+};
+// Any d: Q_poly inside |d| < 1/2, the library expm1f outside (where
+// k3 = (e^d - 1) - d no longer cancels).
+__device__ __forceinline__ Em expm1_k3(float d) {
+  Em r;
+  if (fabsf(d) < 0.5f) {
+    const float q = Q_poly(d), d2 = __fmul_rn(d, d);
+    r.k3 = __fmul_rn(d2, q);
+    r.em = __fmaf_rn(d2, q, d);
+  } else {
+    r.em = expm1f(d);
+    r.k3 = __fsub_rn(r.em, d);
   }
-  return expm1f(d) - d;
+  return r;
 }
 
 struct TokTerms {
-  float q;  // policy term minus its constant part: p = -A + q
+  float q;  // policy term plus A: p = -A + q
   float k;  // KL term
   float g;  // g_pol + beta g_kl
 };
 
 // p = -min(rA, clip(r)A) = -A - min((r-1)A, (clip(r)-1)A).  The constant -A
-// is summed per sequence in double (-A_i L_i): with a full mask the A_i of a
-// group cancel exactly there, which an fp32 A rounded per token would break.
-// The remainder uses r - 1 = expm1(d), accurate where r is close to 1.
+// enters once per sequence, as -A_i L_i in float pairs from the float-pair
+// advantage: with a full mask the A_i of a group cancel there, which an fp32
+// A rounded per token would break.
+// The remainder uses r - 1 = e^(logp-old) - 1, accurate where r is near 1.
 __device__ __forceinline__ TokTerms tok_terms(float lp, float o, float rf, float A,
                                               const LogpsArgs& a) {
   TokTerms t;
-  const float em = expm1f(__fsub_rn(lp, o));  // r - 1
-  const float r = em + 1.0f;
-  const float unc = em * A;
-  const float cl = fminf(fmaxf(em, -a.eps_lo), a.eps_hi) * A;
+  const float em = expm1_k3(__fsub_rn(lp, o)).em;  // r - 1
+  const float unc = __fmul_rn(em, A);
+  const float cl = __fmul_rn(fminf(fmaxf(em, -a.eps_lo), a.eps_hi), A);
   t.q = -fminf(unc, cl);
-  const float d = a.ref ? __fsub_rn(rf, lp) : 0.0f;
-  t.k = k3f(d);
+  const Em kd = expm1_k3(a.ref ? __fsub_rn(rf, lp) : 0.0f);
+  t.k = kd.k3;
   const bool clipped = (A > 0.f && em > a.eps_hi) || (A < 0.f && em < -a.eps_lo);
-  const float gpol = clipped ? 0.f : -A * r;
-  t.g = gpol + a.beta * (-expm1f(d));
+  const float gpol = clipped ? 0.f : -__fmul_rn(A, __fadd_rn(em, 1.0f));
+  t.g = __fmaf_rn(-a.beta, kd.em, gpol);
   return t;
 }
 
 // dL/dlogp in double, for tokens whose gradient is large enough that the
-// fp32 evaluation could be off by more than its rounding allowance.
-__device__ __forceinline__ float w_precise(float lp, float o, float rf, double A, double c,
-                                           const LogpsArgs& a) {
+// fp32 evaluation could be off by more than its rounding allowance.  Rare,
+// so it also forms the token weight c itself.
+struct SeqCtx {
+  float A, gc;        // advantage and grad_scale * c, rounded to fp32
+  int64_t b;          // the sequence
+  int L;              // its active tokens
+  unsigned long long N, S;
+};
+__device__ __noinline__ float w_precise(float lp, float o, float rf, const SeqCtx& x,
+                                        const LogpsArgs& a) {
+  const double A = a.A[x.b];
+  const double c = a.reduction == GRPO_TOKEN_MEAN
+                       ? 1.0 / (double)(x.N > 0 ? x.N : 1)
+                       : 1.0 / ((double)(x.S > 0 ? x.S : 1) * (double)x.L);
   const double r = exp((double)lp - (double)o);
   const double lo = 1.0 - (double)a.eps_lo, hi = 1.0 + (double)a.eps_hi;
   const double gpol = ((A > 0.0 && r > hi) || (A < 0.0 && r < lo)) ? 0.0 : -A * r;
@@ -70,182 +108,309 @@ __device__ __forceinline__ float w_precise(float lp, float o, float rf, double A
 }
 
 __device__ __forceinline__ void kahan(float& s, float& c, float x) {
-  float y = __fsub_rn(x, c);
-  float t = __fadd_rn(s, y);
+  const float y = __fsub_rn(x, c);
+  const float t = __fadd_rn(s, y);
   c = __fsub_rn(__fsub_rn(t, s), y);
   s = t;
 }
 
 __device__ __forceinline__ bool vec_ok(const LogpsArgs& a) {
-  uintptr_t m = (uintptr_t)a.logps | (uintptr_t)a.old | (uintptr_t)a.ref | (uintptr_t)a.grad;
+  const uintptr_t m = (uintptr_t)a.logps | (uintptr_t)a.old | (uintptr_t)a.ref | (uintptr_t)a.grad;
   return (a.T % 4 == 0) && ((m & 15) == 0) && (((uintptr_t)a.mask & 3) == 0);
 }
 
-__global__ void __launch_bounds__(kSeqThreads) logps_seq_kernel(const LogpsArgs a) {
-  __shared__ double s_d[64];
-  __shared__ int s_i[32];
+// Per-thread sums: q and k each as a Kahan pair.  A vector's four active
+// tokens are added in fp32 first and enter the Kahan sum once.
+struct Acc {
+  float sq = 0.f, cq = 0.f, sk = 0.f, ck = 0.f;
+};
+
+__device__ __forceinline__ float token_w(float lp, float o, float rf, const TokTerms& t,
+                                         const SeqCtx& x, const LogpsArgs& a) {
+  float w = __fmul_rn(x.gc, t.g);
+  if (fabsf(w) > kWPrecise) w = w_precise(lp, o, rf, x, a);
+  return w;
+}
+
+// Per-CTA constants of the fast path.  With s = sign(A) (+1 for A = 0) and
+// lim = eps_hi (A > 0) or eps_lo (A <= 0):
+//   min(rA, clip(r)A) = A + |A| min(s(r-1), lim)    (so q = -|A| min(s em, lim))
+//   the token is clipped  <=>  s em > lim
+// which is the clipped-surrogate case split with the sign of A taken out.
+struct FastCtx {
+  float2 s2, neg_absA2, negA2, gc2, neg_beta2;
+  float lim;
+  float g2_max;  // (kWPrecise / gc)^2: a vector whose sum of g^2 stays below
+                 // it has every |w| <= kWPrecise
+};
+
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+
+// Q_poly on two lanes with packed fp32x2 arithmetic.
+__device__ __forceinline__ float2 Q_poly2(float2 d) {
+  float2 q = __ffma2_rn(d, f2(1.0f / 362880.0f), f2(1.0f / 40320.0f));
+  q = __ffma2_rn(d, q, f2(1.0f / 5040.0f));
+  q = __ffma2_rn(d, q, f2(1.0f / 720.0f));
+  q = __ffma2_rn(d, q, f2(1.0f / 120.0f));
+  q = __ffma2_rn(d, q, f2(1.0f / 24.0f));
+  q = __ffma2_rn(d, q, f2(1.0f / 6.0f));
+  return __ffma2_rn(d, q, f2(0.5f));
+}
+
+// Two active tokens on the fast path (every operation but the clip on
+// packed fp32x2).  Accumulates q and k, and the sums behind the range check.
+__device__ __forceinline__ float2 pair_fast(float2 lp, float2 od, float2 rf, bool has_ref,
+                                            const FastCtx& f, float2& vq, float2& vk,
+                                            float2& d2sum, float2& g2sum) {
+  const float2 dp = __ffma2_rn(od, f2(-1.f), lp);  // logp - old
+  const float2 Qp = Q_poly2(dp), ddp = __fmul2_rn(dp, dp);
+  const float2 em = __ffma2_rn(ddp, Qp, dp);       // r - 1
+  const float2 dr = has_ref ? __ffma2_rn(lp, f2(-1.f), rf) : f2(0.f);  // ref - logp
+  const float2 Qr = Q_poly2(dr), ddr = __fmul2_rn(dr, dr);
+  const float2 k = __fmul2_rn(ddr, Qr);            // k3
+  const float2 emr = __ffma2_rn(ddr, Qr, dr);      // e^(ref-logp) - 1
+  const float2 se = __fmul2_rn(f.s2, em);
+  const float2 mn = make_float2(fminf(se.x, f.lim), fminf(se.y, f.lim));
+  const float2 q = __fmul2_rn(f.neg_absA2, mn);
+  float2 gp = __fmul2_rn(f.negA2, __fadd2_rn(em, f2(1.f)));  // -A r
+  gp.x = se.x > f.lim ? 0.f : gp.x;
+  gp.y = se.y > f.lim ? 0.f : gp.y;
+  const float2 g = __ffma2_rn(f.neg_beta2, emr, gp);
+  vq = __fadd2_rn(vq, q);
+  vk = __fadd2_rn(vk, k);
+  d2sum = __fadd2_rn(d2sum, __fadd2_rn(ddp, ddr));
+  g2sum = __ffma2_rn(g, g, g2sum);
+  return __fmul2_rn(f.gc2, g);
+}
+
+// One vector of four active slots on the fast path.  Returns false when a
+// token needs the general path: a log ratio outside |d| < 1/2 (caught by
+// the vector's sum of d^2 reaching 1/4), or a gradient above kWPrecise
+// (caught by its sum of g^2); NaNs fail the check too.
+__device__ __forceinline__ bool vec_fast(const float4& l4, const float4& o4, const float4& r4,
+                                         bool has_ref, const FastCtx& f, float (&w)[4],
+                                         float& vq, float& vk) {
+  float2 sq = f2(0.f), sk = f2(0.f), d2 = f2(0.f), g2 = f2(0.f);
+  const float2 w01 = pair_fast(make_float2(l4.x, l4.y), make_float2(o4.x, o4.y),
+                               make_float2(r4.x, r4.y), has_ref, f, sq, sk, d2, g2);
+  const float2 w23 = pair_fast(make_float2(l4.z, l4.w), make_float2(o4.z, o4.w),
+                               make_float2(r4.z, r4.w), has_ref, f, sq, sk, d2, g2);
+  w[0] = w01.x;
+  w[1] = w01.y;
+  w[2] = w23.x;
+  w[3] = w23.y;
+  vq = __fadd_rn(sq.x, sq.y);
+  vk = __fadd_rn(sk.x, sk.y);
+  return __fadd_rn(d2.x, d2.y) < 0.25f && __fadd_rn(g2.x, g2.y) <= f.g2_max;
+}
+
+// Every byte of a mask word nonzero.
+__device__ __forceinline__ bool all_active(uint32_t mw) {
+  return ((((mw & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | mw) & 0x80808080u) == 0x80808080u;
+}
+
+// The same vector on the general path, token by token.
+__device__ __forceinline__ void vec_general(uint32_t mw, const float4& l4, const float4& o4,
+                                            const float4& r4, const SeqCtx& x,
+                                            const LogpsArgs& a, float (&w)[4], float& vq,
+                                            float& vk) {
+  const float lp[4] = {l4.x, l4.y, l4.z, l4.w};
+  const float od[4] = {o4.x, o4.y, o4.z, o4.w};
+  const float rf[4] = {r4.x, r4.y, r4.z, r4.w};
+  vq = 0.f;
+  vk = 0.f;
+#pragma unroll 1
+  for (int j = 0; j < 4; ++j) {
+    w[j] = 0.f;
+    if ((mw >> (8 * j)) & 0xFFu) {
+      const TokTerms t = tok_terms(lp[j], od[j], rf[j], x.A, a);
+      vq = __fadd_rn(vq, t.q);
+      vk = __fadd_rn(vk, t.k);
+      w[j] = token_w(lp[j], od[j], rf[j], t, x, a);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs a) {
+  __shared__ FF s_ff[2][kLogpsThreads / 32];
+  __shared__ bool s_last;
   const int64_t b = blockIdx.x;
-  const float A = (float)a.A[b];
-  const int64_t base = b * a.T;
-  float sp = 0.f, cp = 0.f, sk = 0.f, ck = 0.f;
-  int cnt = 0;
-  if (vec_ok(a)) {
-    const int64_t nv = a.T / 4;
-    for (int64_t q = threadIdx.x; q < nv; q += blockDim.x) {
-      const uint32_t mw = __ldg(reinterpret_cast<const uint32_t*>(a.mask + base) + q);
-      if (mw == 0u) continue;  // masked storage is not read
-      const float4 lp = __ldg(reinterpret_cast<const float4*>(a.logps + base) + q);
-      const float4 od = __ldg(reinterpret_cast<const float4*>(a.old + base) + q);
-      float4 rf = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (a.ref) rf = __ldg(reinterpret_cast<const float4*>(a.ref + base) + q);
-      const float l4[4] = {lp.x, lp.y, lp.z, lp.w}, o4[4] = {od.x, od.y, od.z, od.w};
-      const float r4[4] = {rf.x, rf.y, rf.z, rf.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if ((mw >> (8 * j)) & 0xFFu) {
-          TokTerms t = tok_terms(l4[j], o4[j], r4[j], A, a);
-          kahan(sp, cp, t.q);
-          kahan(sk, ck, t.k);
-          ++cnt;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (b < a.B) {
+    SeqCtx x;
+    x.b = b;
+    x.N = a.hdr->N;
+    x.S = a.hdr->S;
+    x.L = a.L[b];
+    const float2 Ab = a.Aff[b];
+    x.A = Ab.x;
+    // grad_scale * c in fp32: c = 1/max(N,1) or 1/(max(S,1) L_b); the
+    // products and quotient are rounded in fp32, well inside the gradient's
+    // rounding allowance
+    const float den = a.reduction == GRPO_TOKEN_MEAN
+                          ? __ull2float_rn(x.N > 0 ? x.N : 1)
+                          : __fmul_rn(__ull2float_rn(x.S > 0 ? x.S : 1), (float)x.L);
+    x.gc = x.L > 0 ? __fdiv_rn(a.grad_scale, den) : 0.f;
+    const bool has_ref = a.ref != nullptr;
+    FastCtx f;
+    const float sgn = x.A > 0.f ? 1.f : -1.f;
+    f.s2 = f2(sgn);
+    f.neg_absA2 = f2(-fabsf(x.A));
+    f.negA2 = f2(-x.A);
+    f.gc2 = f2(x.gc);
+    f.neg_beta2 = f2(-a.beta);
+    f.lim = x.A > 0.f ? a.eps_hi : a.eps_lo;
+    {
+      const float gm = x.gc > 0.f ? __fdiv_rn(kWPrecise, x.gc) : INFINITY;
+      f.g2_max = __fmul_rn(gm, gm);
+    }
+    const int64_t base = b * a.T;
+    Acc acc;
+    if (vec_ok(a)) {
+      const int64_t nv = a.T / 4;
+      const uint32_t* mrow = reinterpret_cast<const uint32_t*>(a.mask + base);
+      const float4* lrow = reinterpret_cast<const float4*>(a.logps + base);
+      const float4* orow = reinterpret_cast<const float4*>(a.old + base);
+      const float4* rrow = reinterpret_cast<const float4*>(a.ref + base);
+      float4* grow = reinterpret_cast<float4*>(a.grad + base);
+      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      // Software pipeline, one vector per thread per iteration: the data of
+      // vector v+1 (whose mask word arrived an iteration earlier) and the
+      // mask word of v+2 are in flight while v is evaluated.  Masked vectors
+      // are not read.
+      constexpr int kS = kLogpsThreads;
+      int64_t v = threadIdx.x;
+      uint32_t m0 = v < nv ? __ldg(mrow + v) : 0u;
+      uint32_t m1 = v + kS < nv ? __ldg(mrow + v + kS) : 0u;
+      float4 l0 = z4, o0 = z4, r0 = z4;
+      if (m0 != 0u) {
+        l0 = __ldg(lrow + v);
+        o0 = __ldg(orow + v);
+        if (a.ref) r0 = __ldg(rrow + v);
+      }
+      for (; v < nv; v += kS) {
+        float4 l1 = z4, o1 = z4, r1 = z4;
+        if (m1 != 0u) {
+          l1 = __ldg(lrow + v + kS);
+          o1 = __ldg(orow + v + kS);
+          if (a.ref) r1 = __ldg(rrow + v + kS);
         }
-    }
-  } else {
-    for (int64_t t = threadIdx.x; t < a.T; t += blockDim.x) {
-      if (!a.mask[base + t]) continue;
-      TokTerms tt = tok_terms(a.logps[base + t], a.old[base + t],
-                              a.ref ? a.ref[base + t] : 0.f, A, a);
-      kahan(sp, cp, tt.q);
-      kahan(sk, ck, tt.k);
-      ++cnt;
-    }
-  }
-  double v[2] = {(double)sp - (double)cp, (double)sk - (double)ck};
-  block_sum<double, 2>(v, s_d);
-  int n[1] = {cnt};
-  block_sum<int, 1>(n, s_i);
-  if (threadIdx.x == 0) {
-    a.seq[b] = v[0] - a.A[b] * (double)n[0];
-    a.seq[a.B + b] = v[1];
-    a.L[b] = n[0];
-  }
-}
-
-__global__ void __launch_bounds__(kGradThreads) logps_grad_kernel(const LogpsArgs a) {
-  __shared__ double s_d[64];
-  __shared__ long long s_l[64];
-  long long ns[2] = {0, 0};
-  for (int64_t i = threadIdx.x; i < a.B; i += blockDim.x) {
-    int L = a.L[i];
-    ns[0] += L;
-    ns[1] += L > 0;
-  }
-  block_sum<long long, 2>(ns, s_l);
-  const long long N = ns[0], S = ns[1];
-
-  if (blockIdx.x == 0) {  // the scalar, in fixed order
-    double v[2] = {0.0, 0.0};
-    for (int64_t i = threadIdx.x; i < a.B; i += blockDim.x) {
-      const double P = a.seq[i], K = a.seq[a.B + i];
-      const int L = a.L[i];
-      if (a.reduction == GRPO_TOKEN_MEAN) {
-        v[0] += P;
-        v[1] += K;
-      } else if (L > 0) {
-        v[0] += P / (double)L;
-        v[1] += K / (double)L;
+        const uint32_t m2 = v + 2 * kS < nv ? __ldg(mrow + v + 2 * kS) : 0u;
+        float w[4] = {0.f, 0.f, 0.f, 0.f};
+        if (m0 != 0u) {
+          float vq, vk;
+          if (!(all_active(m0) && vec_fast(l0, o0, r0, has_ref, f, w, vq, vk)))
+            vec_general(m0, l0, o0, r0, x, a, w, vq, vk);
+          kahan(acc.sq, acc.cq, vq);
+          kahan(acc.sk, acc.ck, vk);
+        }
+        if (a.grad) grow[v] = make_float4(w[0], w[1], w[2], w[3]);
+        m0 = m1;
+        m1 = m2;
+        l0 = l1;
+        o0 = o1;
+        r0 = r1;
       }
-      if (a.per_seq) {
-        a.per_seq[i] = (float)P;
-        a.per_seq[a.B + i] = (float)K;
-        a.per_seq[2 * a.B + i] = (float)L;
+    } else {
+      for (int64_t t = threadIdx.x; t < a.T; t += blockDim.x) {
+        float w = 0.f;
+        if (a.mask[base + t]) {
+          const float lp = a.logps[base + t], o = a.old[base + t];
+          const float rf = a.ref ? a.ref[base + t] : 0.f;
+          const TokTerms tt = tok_terms(lp, o, rf, x.A, a);
+          kahan(acc.sq, acc.cq, tt.q);
+          kahan(acc.sk, acc.ck, tt.k);
+          w = token_w(lp, o, rf, tt, x, a);
+        }
+        if (a.grad) a.grad[base + t] = w;
       }
     }
-    block_sum<double, 2>(v, s_d);
+    // the sequence's totals as float pairs: threads' Kahan sums, a fixed
+    // xor tree per warp, warps in index order
+    FF fq = warp_sum_ff2(FF{acc.sq, -acc.cq}), fk = warp_sum_ff2(FF{acc.sk, -acc.ck});
+    if (lane == 0) {
+      s_ff[0][warp] = fq;
+      s_ff[1][warp] = fk;
+    }
+    __syncthreads();
     if (threadIdx.x == 0) {
-      const double den = a.reduction == GRPO_TOKEN_MEAN ? (double)(N > 0 ? N : 1)
-                                                        : (double)(S > 0 ? S : 1);
-      const double P = v[0] / den, K = v[1] / den;
-      float o0 = (float)(P + (double)a.beta * K), o1 = (float)P, o2 = (float)K;
-      if (a.hdr->status != 0u) o0 = o1 = o2 = NAN;
-      a.out3[0] = o0;
-      a.out3[1] = o1;
-      a.out3[2] = o2;
-    }
-  }
-  if (a.grad == nullptr) return;
-
-  const double c_tok = 1.0 / (double)(N > 0 ? N : 1);
-  const double inv_S = 1.0 / (double)(S > 0 ? S : 1);
-  const int64_t BT = a.B * a.T;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  auto weight = [&](int64_t b) -> double {
-    return a.reduction == GRPO_TOKEN_MEAN ? c_tok : inv_S / (double)a.L[b];
-  };
-  if (vec_ok(a)) {
-    const int64_t nv = BT / 4;
-    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < nv; q += stride) {
-      const uint32_t mw = __ldg(reinterpret_cast<const uint32_t*>(a.mask) + q);
-      float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (mw != 0u) {
-        const int64_t b = (4 * q) / a.T;
-        const double c = weight(b);
-        const double Ad = a.A[b];
-        const float A = (float)Ad;
-        const float gc = (float)((double)a.grad_scale * c);
-        const float4 lp = __ldg(reinterpret_cast<const float4*>(a.logps) + q);
-        const float4 od = __ldg(reinterpret_cast<const float4*>(a.old) + q);
-        float4 rf = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (a.ref) rf = __ldg(reinterpret_cast<const float4*>(a.ref) + q);
-        const float l4[4] = {lp.x, lp.y, lp.z, lp.w}, o4[4] = {od.x, od.y, od.z, od.w};
-        const float r4[4] = {rf.x, rf.y, rf.z, rf.w};
-        float w4[4];
+      fq = s_ff[0][0];
+      fk = s_ff[1][0];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          w4[j] = 0.f;
-          if ((mw >> (8 * j)) & 0xFFu) {
-            float w = gc * tok_terms(l4[j], o4[j], r4[j], A, a).g;
-            if (fabsf(w) > kWPrecise) w = w_precise(l4[j], o4[j], r4[j], Ad, c, a);
-            w4[j] = w;
-          }
-        }
-        out = make_float4(w4[0], w4[1], w4[2], w4[3]);
+      for (int k = 1; k < kLogpsThreads / 32; ++k) {
+        fq = ff_add(fq, s_ff[0][k]);
+        fk = ff_add(fk, s_ff[1][k]);
       }
-      reinterpret_cast<float4*>(a.grad)[q] = out;
-    }
-  } else {
-    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < BT; j += stride) {
-      float w = 0.f;
-      if (a.mask[j]) {
-        const int64_t b = j / a.T;
-        const double c = weight(b);
-        const double Ad = a.A[b];
-        const float rf = a.ref ? a.ref[j] : 0.f;
-        w = (float)((double)a.grad_scale * c) * tok_terms(a.logps[j], a.old[j], rf, (float)Ad, a).g;
-        if (fabsf(w) > kWPrecise) w = w_precise(a.logps[j], a.old[j], rf, Ad, c, a);
+      // P_b = sum q - A_b L_b (the product exact up to ~2^-48 relative)
+      const FF P = ff_add(fq, ff_neg(ff_scale(FF{Ab.x, Ab.y}, (float)x.L)));
+      a.seq[b] = make_float4(P.hi, P.lo, fk.hi, fk.lo);
+      if (a.per_seq) {
+        a.per_seq[b] = ff_float(P);
+        a.per_seq[a.B + b] = ff_float(fk);
+        a.per_seq[2 * a.B + b] = (float)x.L;
       }
-      a.grad[j] = w;
+      __threadfence();
+      s_last = atomicAdd(&a.hdr->done_ctas, 1u) == gridDim.x - 1;
     }
+  } else if (threadIdx.x == 0) {
+    s_last = true;  // B == 0: a single CTA writes the zero loss
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // The scalar over the B sequence totals, in float pairs: each thread's
+  // sequences in index order, a fixed xor tree, warps in index order.  The
+  // totals were written by other CTAs of this launch (visible through their
+  // fence before the ticket), so they are read from L2.
+  FF u[2] = {{0.f, 0.f}, {0.f, 0.f}};
+  for (int64_t j = threadIdx.x; j < a.B; j += blockDim.x) {
+    const float4 t = __ldcg(a.seq + j);
+    FF P = {t.x, t.y}, K = {t.z, t.w};
+    if (a.reduction != GRPO_TOKEN_MEAN) {
+      const int L = __ldcg(a.L + j);
+      if (L == 0) continue;
+      const FF Lf = {(float)L, 0.f};
+      P = ff_div(P, Lf);
+      K = ff_div(K, Lf);
+    }
+    u[0] = ff_add(u[0], P);
+    u[1] = ff_add(u[1], K);
+  }
+  u[0] = warp_sum_ff2(u[0]);
+  u[1] = warp_sum_ff2(u[1]);
+  if (lane == 0) {
+    s_ff[0][warp] = u[0];
+    s_ff[1][warp] = u[1];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    FF P = s_ff[0][0], K = s_ff[1][0];
+#pragma unroll
+    for (int k = 1; k < kLogpsThreads / 32; ++k) {
+      P = ff_add(P, s_ff[0][k]);
+      K = ff_add(K, s_ff[1][k]);
+    }
+    const unsigned long long N = a.B > 0 ? a.hdr->N : 0, S = a.B > 0 ? a.hdr->S : 0;
+    const FF den = ff_from_u64(a.reduction == GRPO_TOKEN_MEAN ? (N > 0 ? N : 1) : (S > 0 ? S : 1));
+    P = ff_div(P, den);
+    K = ff_div(K, den);
+    float o0 = ff_float(ff_add(P, ff_scale(K, a.beta))), o1 = ff_float(P), o2 = ff_float(K);
+    if (((volatile unsigned*)&a.hdr->status)[0] != 0u) o0 = o1 = o2 = NAN;
+    a.out3[0] = o0;
+    a.out3[1] = o1;
+    a.out3[2] = o2;
   }
 }
 
-cudaError_t launch_logps(const LogpsArgs& a, cudaStream_t s) {
-  if (a.B > 0) {
-    logps_seq_kernel<<<(unsigned)a.B, kSeqThreads, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  int64_t grid = 1;
-  if (a.grad) {
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t work = (a.B * a.T + 4 * kGradThreads - 1) / (4 * kGradThreads);
-    grid = (int64_t)sms * 8;
-    if (grid > work) grid = work;
-    if (grid < 1) grid = 1;
-  }
-  logps_grad_kernel<<<(unsigned)grid, kGradThreads, 0, s>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_logps(const LogpsArgs& a, const grpo_profile_t* prof, cudaStream_t s) {
+  if (prof && prof->start) cudaEventRecord((cudaEvent_t)prof->start, s);
+  const int64_t grid = a.B > 0 ? a.B : 1;
+  logps_kernel<<<(unsigned)grid, kLogpsThreads, 0, s>>>(a);
+  const cudaError_t e = cudaGetLastError();
+  if (prof && prof->stop) cudaEventRecord((cudaEvent_t)prof->stop, s);
+  return e;
 }
 
 }  // namespace grpo

@@ -19,7 +19,6 @@ static constexpr int kReduceThreads = 256;
 
 __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs a) {
   __shared__ double s_d[32 * 2];
-  __shared__ long long s_l[32 * 2];
   __shared__ bool s_last;
   const int64_t i = blockIdx.x;
 
@@ -58,25 +57,12 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs
   __threadfence();
 
   // level 2: the scalar, over the B sequence totals in index order
-  long long ns[2] = {0, 0};
   double u[2] = {0.0, 0.0};
-  for (int64_t j = threadIdx.x; j < a.B; j += blockDim.x) {
-    const int L = a.L[j];
-    const double P = ((volatile double*)a.seq)[j], K = ((volatile double*)a.seq)[a.B + j];
-    ns[0] += L;
-    ns[1] += L > 0;
-    if (a.reduction == GRPO_TOKEN_MEAN) {
-      u[0] += P;
-      u[1] += K;
-    } else if (L > 0) {
-      u[0] += P / (double)L;
-      u[1] += K / (double)L;
-    }
-  }
-  block_sum<long long, 2>(ns, s_l);
+  seq_totals(a.seq, a.L, a.B, a.reduction, u);
   block_sum<double, 2>(u, s_d);
   if (threadIdx.x == 0) {
-    const long long N = ns[0], S = ns[1];
+    // N = active tokens, S = live sequences, as prep counted them
+    const long long N = a.B > 0 ? a.hdr->N : 0, S = a.B > 0 ? a.hdr->S : 0;
     const double den = a.reduction == GRPO_TOKEN_MEAN ? (double)(N > 0 ? N : 1)
                                                       : (double)(S > 0 ? S : 1);
     const double P = u[0] / den, K = u[1] / den;

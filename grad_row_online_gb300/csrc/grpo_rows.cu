@@ -297,20 +297,11 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(cons
     s_thi[threadIdx.x] = a.tab.hi[threadIdx.x];
     s_tlo[threadIdx.x] = a.tab.lo[threadIdx.x];
   }
-  // N = active tokens, S = live sequences (every CTA, fixed order)
-  {
-    long long ns[2] = {0, 0};
-    for (int64_t i = threadIdx.x; i < a.B; i += blockDim.x) {
-      const int L = a.L[i];
-      ns[0] += L;
-      ns[1] += L > 0;
-    }
-    block_sum<long long, 2>(ns, reinterpret_cast<long long*>(s_d));
-    if (threadIdx.x == 0) {
-      s_NS[0] = ns[0];
-      s_NS[1] = ns[1];
-      s_next = (long long)atomicAdd(&a.hdr->row_counter, 1ull);
-    }
+  // N = active tokens, S = live sequences: counted by prep, read here once
+  if (threadIdx.x == 0) {
+    s_NS[0] = a.hdr->N;
+    s_NS[1] = a.hdr->S;
+    s_next = (long long)atomicAdd(&a.hdr->row_counter, 1ull);
   }
   __syncthreads();
   const long long N = s_NS[0], S = s_NS[1];

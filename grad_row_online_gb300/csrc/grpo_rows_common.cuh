@@ -58,20 +58,6 @@ struct Geom {
   }
 };
 
-// ------------------------------------------------------ float-float helpers
-__device__ __forceinline__ FF ff_add(FF a, FF b) {
-  FF s = two_sum(a.hi, b.hi);
-  s.lo = __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo));
-  return fast_two_sum(s.hi, s.lo);
-}
-__device__ __forceinline__ FF ff_neg(FF a) { return {-a.hi, -a.lo}; }
-__device__ __forceinline__ FF ff_scale(FF a, float f) {  // a * f
-  const float ph = __fmul_rn(a.hi, f);
-  const float pl = __fmaf_rn(a.hi, f, -ph);
-  return fast_two_sum(ph, __fmaf_rn(a.lo, f, pl));
-}
-__device__ __forceinline__ float ff_float(FF a) { return __fadd_rn(a.hi, a.lo); }
-
 // ln 2 as a float pair
 constexpr float kLn2Hi = 0.693147182464599609375f;
 constexpr float kLn2Lo = -1.904654323148236e-09f;

@@ -13,9 +13,8 @@
 // The array is file-scope device memory of kStaticScratchBytes: every GPU
 // that loads the library holds it until the process exits.  All calls share
 // it and it keeps the last call's contents; the entry point clears what must
-// start at zero (the status word and the row counter, through the same
-// 16-byte memset as the workspace path) and overwrites the rest before
-// reading it.  Because the array is shared, calls whose work overlaps on the
+// start at zero (the header's status word and counters, through the same
+// memset as the workspace path) and overwrites the rest before reading it.  Because the array is shared, calls whose work overlaps on the
 // GPU (different streams, or different host threads, without ordering
 // between them) race on it: serialise them.
 #include <mutex>

@@ -91,8 +91,9 @@ typedef struct {
 } grpo_groups_t;
 
 /* Optional timing hook: when non-NULL, `start` / `stop` (cudaEvent_t handles)
- * are recorded on the stream immediately before and after the fused row
- * kernel, so a caller can time that kernel alone. */
+ * are recorded on the stream immediately before and after the main kernel
+ * work of a call -- the fused row kernel of grpo_loss_fwd_bwd, the two
+ * per-token kernels of grpo_loss_from_logps -- so a caller can time it alone. */
 typedef struct {
   void *start;
   void *stop;

@@ -1,0 +1,43 @@
+"""The multi-process path of bench.py on CPU: two gloo ranks rendezvous
+through the environment (as torchrun sets it), time-aggregate with the
+max over ranks, and form the whole-job throughput of two replicas."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank: int, port: int, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      LOCAL_RANK=str(rank), WORLD_SIZE="2", CUDA_VISIBLE_DEVICES="")
+    import torch.distributed as dist
+    import bench
+    ws, r, local = bench.dist_setup()
+    assert (ws, r) == (2, rank) and dist.get_backend() == "gloo"
+    slowest = bench.max_over_ranks(10.0 + 5.0 * rank, ws, "cpu")  # per-rank step times (ms)
+    bench.barrier(ws)
+    q.put((rank, slowest, bench.aggregate_value(1000, 4, ws, slowest)))
+    dist.destroy_process_group()
+
+
+def test_two_rank_harness_on_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, slowest, value in got:
+        assert slowest == 15.0  # both ranks see the slower rank's time
+        assert value == pytest.approx(1000 * 4 * 2 / 0.015)  # two replicas' tokens / max time
