@@ -119,7 +119,7 @@ extern "C" grpo_status_t grpo_group_adv(const float* rewards, const grpo_groups_
   WsHeader* hdr = (WsHeader*)w;
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return GRPO_ERR_CUDA;
   PrepArgs pa{rewards, bounds, B, 0, G, spp, adv_eps, (int)(flags & GRPO_ADV_EPS_ADD),
-              nullptr, 0, (double*)(w + lay.off_A), nullptr, adv_out, nullptr, hdr};
+              nullptr, 0, (double*)(w + lay.off_A), nullptr, adv_out, nullptr, nullptr, hdr};
   return cuda_status(launch_prep(pa, s));
 }
 
@@ -163,7 +163,7 @@ extern "C" grpo_status_t grpo_loss_fwd_bwd(
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return GRPO_ERR_CUDA;
   PrepArgs pa{rewards, bounds, B, T, G, spp, params->adv_eps,
               (int)(params->flags & GRPO_ADV_EPS_ADD), completion_mask, 1, A, nullptr, adv_out, L,
-              hdr};
+              nullptr, hdr};
   cudaError_t e = launch_prep(pa, s);
   if (e != cudaSuccess) return GRPO_ERR_CUDA;
 
@@ -233,13 +233,14 @@ extern "C" grpo_status_t grpo_loss_from_logps(const float* logps, const float* o
   int32_t* L = (int32_t*)(w + lay.off_L);
   double* A = (double*)(w + lay.off_A);
   float2* Aff = (float2*)(w + lay.off_Aff);
+  int2* rng = (int2*)(w + lay.off_rng);
   float4* seq = (float4*)(w + lay.off_seq);
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return GRPO_ERR_CUDA;
   PrepArgs pa{rewards, bounds, B, T, G, spp, params->adv_eps,
               (int)(params->flags & GRPO_ADV_EPS_ADD), completion_mask, 1, A, Aff, adv_out, L,
-              hdr};
+              rng, hdr};
   if (launch_prep(pa, s) != cudaSuccess) return GRPO_ERR_CUDA;
-  LogpsArgs la{logps, old_logps, ref_logps, completion_mask, A, Aff, L, seq, grad_logps, out3,
+  LogpsArgs la{logps, old_logps, ref_logps, completion_mask, A, Aff, rng, L, seq, grad_logps, out3,
                per_seq, hdr, B, T, params->clip_eps_lo, params->clip_eps_hi, params->beta,
                params->grad_scale, params->reduction};
   return cuda_status(launch_logps(la, params->profile, s));

@@ -19,6 +19,8 @@ namespace grpo {
 //   L        int32 [B]        active tokens per sequence
 //   A        double[B]        advantages
 //   Aff      float2[B]        the same advantages as float pairs (hi, lo)
+//   range    int2[B]          first active token and last active token + 1
+//                             ({0, 0} for an empty sequence)
 //   seq      double[2B]       per-sequence policy / KL totals (logits path);
 //                             the logps path keeps float-pair totals there,
 //                             float4 {P.hi, P.lo, K.hi, K.lo} per sequence
@@ -35,12 +37,13 @@ struct WsHeader {
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t off_L, off_A, off_Aff, off_seq, off_slots, total;
+  size_t off_L, off_A, off_Aff, off_rng, off_seq, off_slots, total;
   __host__ __device__ WsLayout(int64_t B, int64_t T) {
     off_L = 256;
     off_A = off_L + align256(sizeof(int32_t) * (size_t)B);
     off_Aff = off_A + align256(sizeof(double) * (size_t)B);
-    off_seq = off_Aff + align256(sizeof(float) * 2 * (size_t)B);
+    off_rng = off_Aff + align256(sizeof(float) * 2 * (size_t)B);
+    off_seq = off_rng + align256(sizeof(int32_t) * 2 * (size_t)B);
     off_slots = off_seq + align256(sizeof(double) * 2 * (size_t)B);
     total = off_slots + align256(sizeof(double) * 2 * (size_t)B * (size_t)T);
   }
@@ -414,7 +417,8 @@ struct PrepArgs {
   double* A;
   float2* Aff;     // nullable: the advantages as float pairs
   float* adv_out;  // nullable
-  int32_t* L;      // used when mask != NULL
+  int32_t* L;      // used when counting
+  int2* range;     // nullable: active range per sequence (when counting)
   WsHeader* hdr;
 };
 
@@ -461,6 +465,7 @@ struct LogpsArgs {
   const uint8_t* mask;
   const double* A;
   const float2* Aff;  // the advantages as float pairs
+  const int2* range;  // active range per sequence
   int32_t* L;
   float4* seq;  // [B] {P.hi, P.lo, K.hi, K.lo}
   float* grad;  // nullable

@@ -18,6 +18,8 @@
 // for every sum above that.  No fp64 on the common path: GB300's fp64 pipe
 // is a small fraction of its fp32 rate, and a few dozen fp64 operations per
 // CTA measurably lengthened this kernel.
+#include <atomic>
+
 #include "grpo_internal.cuh"
 
 namespace grpo {
@@ -231,11 +233,97 @@ __device__ __forceinline__ void vec_general(uint32_t mw, const float4& l4, const
   }
 }
 
-__global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs a) {
+// One vector of four slots: its gradient, and its q / k sums into the
+// thread's Kahan pairs.  Fully active vectors take the fast path when their
+// range check passes; everything else the general path.
+__device__ __forceinline__ void process_vec(uint32_t mw, const float4& l, const float4& o,
+                                            const float4& r, bool has_ref, const FastCtx& f,
+                                            const SeqCtx& x, const LogpsArgs& a, Acc& acc,
+                                            float (&w)[4]) {
+  w[0] = w[1] = w[2] = w[3] = 0.f;
+  if (mw == 0u) return;
+  float vq, vk;
+  if (!(all_active(mw) && vec_fast(l, o, r, has_ref, f, w, vq, vk)))
+    vec_general(mw, l, o, r, x, a, w, vq, vk);
+  kahan(acc.sq, acc.cq, vq);
+  kahan(acc.sk, acc.ck, vk);
+}
+
+// ---- staging through shared memory with bulk asynchronous copies ----
+// The active range of the sequence, widened to 16-token boundaries, moves
+// in chunks of kChunk tokens (logps, old, ref and the mask bytes: four
+// cp.async.bulk copies completing on one mbarrier); kDepth chunks are in
+// flight while one is evaluated.
+static constexpr int kChunk = 4 * kLogpsThreads;  // one float4 per thread
+static constexpr int kDepth = 4;
+static constexpr uint32_t kWaitLimit = 1u << 22;  // try_wait rounds before giving up
+
+struct Stage {
+  float4 lp[kChunk / 4];
+  float4 od[kChunk / 4];
+  float4 rf[kChunk / 4];
+  uint32_t mk[kChunk / 4];
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for a phase of `bar`; false if it did not complete in time.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// Staging applies when every copy is 16-byte aligned: float rows on 16-byte
+// boundaries with T % 16 == 0 puts each 16-token chunk start on a 64-byte
+// (data) and 16-byte (mask) boundary.
+__device__ __forceinline__ bool staged_ok(const LogpsArgs& a) {
+  const uintptr_t m = (uintptr_t)a.logps | (uintptr_t)a.old | (uintptr_t)a.ref |
+                      (uintptr_t)a.grad | (uintptr_t)a.mask;
+  return a.range != nullptr && (a.T % 16 == 0) && ((m & 15) == 0);
+}
+
+__global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs a) {
   __shared__ FF s_ff[2][kLogpsThreads / 32];
   __shared__ bool s_last;
+  __shared__ __align__(16) Stage s_st[kDepth];
+  __shared__ __align__(8) uint64_t s_full[kDepth];
   const int64_t b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t pol = l2_evict_first();  // every input byte is read once
+  if (threadIdx.x == 0) {
+    for (int d = 0; d < kDepth; ++d) mbar_init(&s_full[d], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
 
   if (b < a.B) {
     SeqCtx x;
@@ -267,7 +355,54 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
     }
     const int64_t base = b * a.T;
     Acc acc;
-    if (vec_ok(a)) {
+    if (staged_ok(a)) {
+      const int2 rg = a.range[b];
+      const int64_t lo = rg.x & ~15, hi = min((int64_t)((rg.y + 15) & ~15), a.T);
+      const int nchunks = (int)((hi - lo + kChunk - 1) / kChunk);
+      const uint32_t nref = has_ref ? 1u : 0u;
+      auto issue = [&](int c) {  // thread 0 only
+        const int64_t st = lo + (int64_t)c * kChunk;
+        const uint32_t len = (uint32_t)min((int64_t)kChunk, hi - st);
+        Stage& S = s_st[c % kDepth];
+        uint64_t* bar = &s_full[c % kDepth];
+        mbar_expect_tx(bar, len * (4u * (2u + nref) + 1u));
+        bulk_g2s(S.lp, a.logps + base + st, 4u * len, bar, pol);
+        bulk_g2s(S.od, a.old + base + st, 4u * len, bar, pol);
+        if (has_ref) bulk_g2s(S.rf, a.ref + base + st, 4u * len, bar, pol);
+        bulk_g2s(S.mk, a.mask + base + st, len, bar, pol);
+      };
+      if (threadIdx.x == 0)
+        for (int c = 0; c < nchunks && c < kDepth; ++c) issue(c);
+      // slots outside the widened active range hold no active token
+      float4* grow = reinterpret_cast<float4*>(a.grad + base);
+      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (a.grad) {
+        for (int64_t v = threadIdx.x; v < lo / 4; v += kLogpsThreads) grow[v] = z4;
+        for (int64_t v = hi / 4 + threadIdx.x; v < a.T / 4; v += kLogpsThreads) grow[v] = z4;
+      }
+      bool timed_out = false;
+      for (int c = 0; c < nchunks; ++c) {
+        const int slot = c % kDepth;
+        const int64_t st = lo + (int64_t)c * kChunk;
+        const int len = (int)min((int64_t)kChunk, hi - st);
+        bool ready = mbar_wait(&s_full[slot], (uint32_t)(c / kDepth) & 1u);
+        if (!ready) {  // never expected: record it, then give the copy a second chance
+          timed_out = true;
+          ready = mbar_wait(&s_full[slot], (uint32_t)(c / kDepth) & 1u);
+        }
+        const int v = threadIdx.x;
+        if (ready && 4 * v < len) {
+          const Stage& S = s_st[slot];
+          float w[4];
+          process_vec(S.mk[v], S.lp[v], S.od[v], has_ref ? S.rf[v] : z4, has_ref, f, x, a, acc,
+                      w);
+          if (a.grad) grow[st / 4 + v] = make_float4(w[0], w[1], w[2], w[3]);
+        }
+        __syncthreads();  // the slot is free again
+        if (threadIdx.x == 0 && c + kDepth < nchunks) issue(c + kDepth);
+      }
+      if (timed_out) atomicOr(&a.hdr->status, (unsigned)GRPO_ERR_TIMEOUT);
+    } else if (vec_ok(a)) {
       const int64_t nv = a.T / 4;
       const uint32_t* mrow = reinterpret_cast<const uint32_t*>(a.mask + base);
       const float4* lrow = reinterpret_cast<const float4*>(a.logps + base);
@@ -297,14 +432,8 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
           if (a.ref) r1 = __ldg(rrow + v + kS);
         }
         const uint32_t m2 = v + 2 * kS < nv ? __ldg(mrow + v + 2 * kS) : 0u;
-        float w[4] = {0.f, 0.f, 0.f, 0.f};
-        if (m0 != 0u) {
-          float vq, vk;
-          if (!(all_active(m0) && vec_fast(l0, o0, r0, has_ref, f, w, vq, vk)))
-            vec_general(m0, l0, o0, r0, x, a, w, vq, vk);
-          kahan(acc.sq, acc.cq, vq);
-          kahan(acc.sk, acc.ck, vk);
-        }
+        float w[4];
+        process_vec(m0, l0, o0, r0, has_ref, f, x, a, acc, w);
         if (a.grad) grow[v] = make_float4(w[0], w[1], w[2], w[3]);
         m0 = m1;
         m1 = m2;
@@ -364,19 +493,30 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
   // sequences in index order, a fixed xor tree, warps in index order.  The
   // totals were written by other CTAs of this launch (visible through their
   // fence before the ticket), so they are read from L2.
+  // Loads go out kBatch at a time, so the L2 latency is paid once per batch.
+  constexpr int kBatch = 8;
   FF u[2] = {{0.f, 0.f}, {0.f, 0.f}};
-  for (int64_t j = threadIdx.x; j < a.B; j += blockDim.x) {
-    const float4 t = __ldcg(a.seq + j);
-    FF P = {t.x, t.y}, K = {t.z, t.w};
-    if (a.reduction != GRPO_TOKEN_MEAN) {
-      const int L = __ldcg(a.L + j);
-      if (L == 0) continue;
-      const FF Lf = {(float)L, 0.f};
-      P = ff_div(P, Lf);
-      K = ff_div(K, Lf);
+  for (int64_t j0 = threadIdx.x; j0 < a.B; j0 += kBatch * kLogpsThreads) {
+    float4 t[kBatch];
+    int L[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int64_t j = j0 + (int64_t)k * kLogpsThreads;
+      t[k] = j < a.B ? __ldcg(a.seq + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      L[k] = j < a.B ? a.L[j] : 0;  // written by prep, an earlier launch
     }
-    u[0] = ff_add(u[0], P);
-    u[1] = ff_add(u[1], K);
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      FF P = {t[k].x, t[k].y}, K = {t[k].z, t[k].w};
+      if (a.reduction != GRPO_TOKEN_MEAN) {
+        if (L[k] == 0) continue;
+        const FF Lf = {(float)L[k], 0.f};
+        P = ff_div(P, Lf);
+        K = ff_div(K, Lf);
+      }
+      u[0] = ff_add(u[0], P);
+      u[1] = ff_add(u[1], K);
+    }
   }
   u[0] = warp_sum_ff2(u[0]);
   u[1] = warp_sum_ff2(u[1]);
@@ -405,10 +545,23 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
 }
 
 cudaError_t launch_logps(const LogpsArgs& a, const grpo_profile_t* prof, cudaStream_t s) {
+  // eight 27 KB CTAs per SM need the largest shared-memory carveout; the
+  // attribute is set once per device (setting it again costs host time)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::atomic<unsigned long long> carveout_set{0};
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(carveout_set.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(logps_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    carveout_set.fetch_or(bit, std::memory_order_acq_rel);
+  }
   if (prof && prof->start) cudaEventRecord((cudaEvent_t)prof->start, s);
   const int64_t grid = a.B > 0 ? a.B : 1;
   logps_kernel<<<(unsigned)grid, kLogpsThreads, 0, s>>>(a);
-  const cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (prof && prof->stop) cudaEventRecord((cudaEvent_t)prof->stop, s);
   return e;
 }

@@ -19,29 +19,48 @@ namespace grpo {
 static constexpr int kPrepWarps = 8;
 static constexpr int kPrepThreads = 32 * kPrepWarps;
 
-// Nonzero bytes of one 32-bit word: the top bit of each nonzero byte is set
-// by (x & 0x7F) + 0x7F or by x itself.
-__device__ __forceinline__ int nonzero_bytes(uint32_t x) {
-  return __popc((((x & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | x) & 0x80808080u);
-}
+// Nonzero bytes of a 32-bit word are found through their top bits: the top
+// bit of each nonzero byte is set by (x & 0x7F) + 0x7F or by x itself.
 
-// Active tokens of one sequence, summed by one warp (every lane gets it).
-__device__ __forceinline__ int warp_count(const uint8_t* m, int64_t T, int lane) {
-  int cnt = 0;
+// Active tokens of one sequence, scanned by one warp: the count and the
+// first and last active positions (-1 when there are none); every lane gets
+// them.
+struct SeqScan {
+  int count, first, last;
+};
+__device__ __forceinline__ void scan_word(uint32_t x, int pos, SeqScan& s) {
+  const uint32_t nz = (((x & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | x) & 0x80808080u;
+  s.count += __popc(nz);
+  if (nz) {
+    s.first = min(s.first, pos + ((__ffs(nz) - 1) >> 3));
+    s.last = max(s.last, pos + ((31 - __clz(nz)) >> 3));
+  }
+}
+__device__ __forceinline__ SeqScan warp_scan(const uint8_t* m, int64_t T, int lane) {
+  SeqScan s{0, 0x7FFFFFFF, -1};
   const uintptr_t addr = (uintptr_t)m;
   int64_t head = (int64_t)((16 - (addr & 15)) & 15);
   if (head > T) head = T;
   const int64_t nvec = (T - head) / 16;
   const int64_t tail0 = head + nvec * 16;
-  for (int64_t t = lane; t < head; t += 32) cnt += m[t] != 0;
-  for (int64_t t = tail0 + lane; t < T; t += 32) cnt += m[t] != 0;
+  for (int64_t t = lane; t < head; t += 32)
+    if (m[t]) { ++s.count; s.first = min(s.first, (int)t); s.last = max(s.last, (int)t); }
+  for (int64_t t = tail0 + lane; t < T; t += 32)
+    if (m[t]) { ++s.count; s.first = min(s.first, (int)t); s.last = max(s.last, (int)t); }
   const uint4* mv = reinterpret_cast<const uint4*>(m + head);
-#pragma unroll 4
+#pragma unroll 8
   for (int64_t k = lane; k < nvec; k += 32) {
     const uint4 v = __ldg(mv + k);
-    cnt += nonzero_bytes(v.x) + nonzero_bytes(v.y) + nonzero_bytes(v.z) + nonzero_bytes(v.w);
+    const int pos = (int)(head + 16 * k);
+    scan_word(v.x, pos, s);
+    scan_word(v.y, pos + 4, s);
+    scan_word(v.z, pos + 8, s);
+    scan_word(v.w, pos + 12, s);
   }
-  return warp_sum(cnt);
+  s.count = warp_sum(s.count);
+  s.first = __reduce_min_sync(0xFFFFFFFFu, s.first);
+  s.last = __reduce_max_sync(0xFFFFFFFFu, s.last);
+  return s;
 }
 
 // Advantages of one group, by one warp.  Every sum runs over the lanes'
@@ -118,8 +137,12 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
   const int64_t i = ((int64_t)blockIdx.x - group_ctas) * kPrepWarps + warp;
   int L = 0;
   if (i < a.B) {
-    L = warp_count(a.mask + i * a.T, a.T, lane);
-    if (lane == 0) a.L[i] = L;
+    const SeqScan sc = warp_scan(a.mask + i * a.T, a.T, lane);
+    L = sc.count;
+    if (lane == 0) {
+      a.L[i] = L;
+      if (a.range) a.range[i] = L > 0 ? make_int2(sc.first, sc.last + 1) : make_int2(0, 0);
+    }
   }
   if (lane == 0) s_L[warp] = L;
   __syncthreads();

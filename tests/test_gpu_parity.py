@@ -317,6 +317,33 @@ def test_logps_odd_T_sequence_mean_and_no_ref():
     _logps_check(w, c, _logps_run(w, c, ref=False, beta=0.0), beta=0.0, ref=False)
 
 
+def _mask_pattern(B, T, pattern, seed):
+    rng = np.random.default_rng(seed)
+    t = np.arange(T)[None, :]
+    if pattern == "random":  # ~70% active, nonzero bytes of several values
+        m = (rng.random((B, T)) < 0.7) * rng.choice([1, 7, 255], size=(B, T))
+    elif pattern == "suffix":  # a masked prefix, then active to a ragged end
+        lo = rng.integers(0, T, size=B)[:, None]
+        hi = rng.integers(0, T + 1, size=B)[:, None]
+        m = (t >= lo) & (t < np.maximum(hi, lo + 1))
+    else:  # "single": one active token per sequence (none in sequence 0)
+        m = t == rng.integers(0, T, size=B)[:, None]
+        m[0] = False
+    return np.ascontiguousarray(m.astype(np.uint8))
+
+
+@pytest.mark.parametrize("T", [2064, 100])
+@pytest.mark.parametrize("pattern", ["random", "suffix", "single"])
+def test_logps_mask_patterns(T, pattern):
+    # T=2064: rows staged through shared memory in five chunks (the ring of
+    # four wraps, the last chunk is partial); T=100: the register path
+    w = LOGPS_SMALL.with_(B=16, T=T)
+    c = _logps_case(w)
+    c["mask"] = _mask_pattern(w.B, w.T, pattern, seed=T)
+    for reduction in (0, 1):
+        _logps_check(w, c, _logps_run(w, c, reduction=reduction), reduction=reduction)
+
+
 def test_logps_large_weights_take_the_precise_path():
     # 2 sequences, 3 tokens: weights ~0.3, far above the fp32 budget
     w = LOGPS_SMALL.with_(B=8, T=4, len_range=(0, 2))
