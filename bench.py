@@ -37,28 +37,36 @@ import synth  # noqa: E402
 
 METRIC = "active tokens/s and HBM GB/s (% of roofline), fused GRPO fwd+bwd, 1 GB300"
 UNIT = "active tokens/s"
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "rows_kernel_large_vocab.md")
-ROWS_SOURCES = [os.path.join(ROOT, "grad_row_online_gb300", "csrc", f)
-                for f in ("grpo_rows.cu", "grpo_rows_common.cuh", "grpo_internal.cuh")]
+CSRC = os.path.join(ROOT, "grad_row_online_gb300", "csrc")
+# workload -> (committed ncu summary, sources of the kernel it profiles)
+PROFILES = {
+    "large_vocab": ("rows_kernel_large_vocab.md",
+                    ("grpo_rows.cu", "grpo_rows_common.cuh", "grpo_internal.cuh")),
+    "logps": ("logps_kernel_logps.md", ("grpo_logps.cu", "grpo_internal.cuh")),
+}
 
 
-def rows_source_hash() -> str:
+def source_hash(files) -> str:
     h = hashlib.sha256()
-    for f in ROWS_SOURCES:
-        h.update(open(f, "rb").read())
+    for f in files:
+        h.update(open(os.path.join(CSRC, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload: str):
-    """DRAM bytes per launch of the row kernel from the committed ncu summary,
-    if it was taken on the current kernel source for this workload."""
-    if not os.path.exists(PROFILE_SUMMARY):
+    """DRAM bytes per launch of the workload's main kernel from its committed
+    ncu summary, if that was taken on the current kernel source."""
+    if workload not in PROFILES:
         return None
-    text = open(PROFILE_SUMMARY).read()
+    name, files = PROFILES[workload]
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
     src = re.search(r"kernel_source_sha:\s*(\w+)", text)
     wl = re.search(r"workload:\s*(\w+)", text)
     tb = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not (src and wl and tb) or src.group(1) != rows_source_hash() or wl.group(1) != workload:
+    if not (src and wl and tb) or src.group(1) != source_hash(files) or wl.group(1) != workload:
         return None
     return float(tb.group(1))
 
@@ -506,7 +514,7 @@ def run_gpu(args, w, ws, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype if w.V else "f32",
         "data": "synthetic", "config": workload_config(w),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": profiled_traffic(w.name) if w.V else None,
+                     "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                      "kernel": case.kernel, "peak_source": f"{peak_kind} hbm_gbs",
                      "bytes_per_launch": case.alg_bytes, "avg_launch_ms": kern_avg_s * 1e3},
         "step_gbs_algorithmic": case.alg_bytes / (ms_per_step / 1e3) / 1e9,
