@@ -11,8 +11,9 @@ defines them:
 
   1. group advantages from the rewards           (``group_advantages``)
   2. log-softmax of the policy / reference rows  (``log_softmax_rows``)
-  3. ratio, clipped surrogate, k3 KL, weights, the two-level reduction and
-     dL/dlogp                                     (``loss_from_logps``)
+  3. ratio, clipped surrogate (or CISPO, or the dual clip), the KL estimator
+     (k3, k1 or k2), weights, the two-level reduction, dL/dlogp and the clip
+     counters                                     (``loss_from_logps``)
   4. dL/dlogits = w (onehot - softmax)            (``grad_rows``)
 
 Parity pins: every function here is checked against closed forms, library
@@ -32,7 +33,9 @@ _SO = os.path.join(_HERE, "liboracle.so")
 
 F32, BF16, F16, F64 = 0, 1, 2, 3
 DTYPE_CODE = {"f32": F32, "bf16": BF16, "f16": F16, "f64": F64}
-TOKEN_MEAN, SEQUENCE_MEAN = 0, 1
+TOKEN_MEAN, SEQUENCE_MEAN, FIXED_CONSTANT = 0, 1, 2
+KL_TYPES = {"k3": 0, "k1": 1, "k2": 2}
+SURROGATES = {"clip": 0, "cispo": 1}
 
 
 def build_commands() -> list[list[str]]:
@@ -59,7 +62,7 @@ def lib():
         L.oracle_group_advantages.restype = ci
         L.oracle_log_softmax_rows.argtypes = [vp, ci, i64, i64, vp, vp, vp]
         L.oracle_loss_from_logps.argtypes = [i64, i64, vp, vp, vp, vp, vp, dbl, dbl, dbl, dbl,
-                                             ci, vp, vp, vp, vp]
+                                             ci, ci, ci, dbl, dbl, vp, vp, vp, vp, vp]
         L.oracle_grad_rows.argtypes = [vp, ci, i64, i64, vp, vp, vp, ci, vp, vp]
         L.oracle_round_to.argtypes = [vp, i64, ci, vp]
         _lib = L
@@ -109,26 +112,38 @@ def log_softmax_rows(rows, dtype: str, actions=None):
 
 
 def loss_from_logps(logp, ref_logp, old, mask, A, eps_lo, eps_hi, beta,
-                    grad_scale: float = 1.0, reduction: int = TOKEN_MEAN):
+                    grad_scale: float = 1.0, reduction: int = TOKEN_MEAN, kl: str = "k3",
+                    surrogate: str = "clip", dual_clip_c: float | None = None,
+                    norm_constant: float | None = None):
     """Loss, per-sequence totals and dL/dlogp from per-token log-probs.
     logp / ref_logp / old: [B,T] (any float type, widened to double);
-    ref_logp may be None (no KL term)."""
+    ref_logp may be None (no KL term).  Variants: kl in {"k3", "k1", "k2"},
+    surrogate in {"clip", "cispo"}, the dual clip constant c > 1, and the
+    fixed-constant normaliser (reduction FIXED_CONSTANT with norm_constant)."""
     lp = _c(logp, np.float64)
     B, T = lp.shape
     rl = None if ref_logp is None else _c(ref_logp, np.float64)
     od = _c(old, np.float64)
     m = _c(mask, np.uint8)
     Ad = _c(A, np.float64)
+    if reduction == FIXED_CONSTANT and not (norm_constant and norm_constant > 0):
+        raise ValueError("the fixed-constant normaliser needs norm_constant > 0")
+    if dual_clip_c is not None and (dual_clip_c <= 1.0 or surrogate != "clip"):
+        raise ValueError("the dual clip needs c > 1 and the clipped surrogate")
     out3 = np.zeros(3, dtype=np.float64)
     per_seq = np.zeros(3 * B, dtype=np.float64)
     w = np.zeros((B, T), dtype=np.float64)
     ratio = np.zeros((B, T), dtype=np.float64)
+    counts = np.zeros(3, dtype=np.int64)
     lib().oracle_loss_from_logps(B, T, _p(lp), _p(rl), _p(od), _p(m), _p(Ad), float(eps_lo),
                                  float(eps_hi), float(beta), float(grad_scale), int(reduction),
-                                 _p(out3), _p(per_seq), _p(w), _p(ratio))
+                                 KL_TYPES[kl], SURROGATES[surrogate], float(dual_clip_c or 0.0),
+                                 float(norm_constant or 0.0), _p(out3), _p(per_seq), _p(w),
+                                 _p(ratio), _p(counts))
     return {"loss": out3[0], "policy_loss": out3[1], "kl": out3[2],
             "per_seq_policy": per_seq[:B], "per_seq_kl": per_seq[B:2 * B],
-            "per_seq_active": per_seq[2 * B:], "w": w, "ratio": ratio}
+            "per_seq_active": per_seq[2 * B:], "w": w, "ratio": ratio,
+            "clip_counts": counts}
 
 
 def grad_rows(rows, dtype: str, actions, lse, w, out_dtype: str | None = None):
@@ -167,8 +182,11 @@ def widen(a, dtype: str) -> np.ndarray:
 
 def fused(policy, ref, dtype: str, actions, old, mask, rewards, bounds, eps_lo, eps_hi,
           beta, adv_eps: float = 1e-6, eps_add: bool = False, grad_scale: float = 1.0,
-          reduction: int = TOKEN_MEAN, out_dtype: str | None = None, want_grad: bool = True):
+          reduction: int = TOKEN_MEAN, out_dtype: str | None = None, want_grad: bool = True,
+          **variant):
     """The whole fused path for in-memory [B,T,V] inputs (small sizes).
+    `variant` (kl, surrogate, dual_clip_c, norm_constant) goes to
+    loss_from_logps unchanged.
 
     Masked rows are never read: their logits, actions and old_logps may hold
     anything.  Returns a dict with loss, policy_loss, kl, per-sequence
@@ -191,7 +209,8 @@ def fused(policy, ref, dtype: str, actions, old, mask, rewards, bounds, eps_lo, 
     oldd = np.zeros(B * T)
     oldd[act] = np.asarray(old, dtype=np.float64).reshape(-1)[act]
     res = loss_from_logps(logp.reshape(B, T), None if ref is None else ref_logp.reshape(B, T),
-                          oldd.reshape(B, T), m, A, eps_lo, eps_hi, beta, grad_scale, reduction)
+                          oldd.reshape(B, T), m, A, eps_lo, eps_hi, beta, grad_scale, reduction,
+                          **variant)
     res["A"] = A
     res["logp"] = logp.reshape(B, T)
     res["ref_logp"] = ref_logp.reshape(B, T)

@@ -201,8 +201,10 @@ void oracle_log_softmax_rows(const void *rows, int dtype, int64_t nrows, int64_t
  *   policy p = -min(r A, clip(r, 1 - eps_lo, 1 + eps_hi) A)   [RK], [DY]
  *   k3     k = e^d - d - 1 = expm1(d) - d, d = ref - logp     [DY] KL penalty
  * Weights c_it ([RK] "Normalizer semantics"; [GC] length-normalization table):
- *   token mean (0):    1 / max(N, 1),          N = number of active tokens
- *   sequence mean (1): 1 / (max(S, 1) * L_i),  S = sequences with L_i > 0
+ *   token mean (0):     1 / max(N, 1),          N = number of active tokens
+ *   sequence mean (1):  1 / (max(S, 1) * L_i),  S = sequences with L_i > 0
+ *   fixed constant (2): 1 / C for a declared C > 0 (the Dr.GRPO form, [RK]
+ *                       "Normalizer semantics", fixed_constant mode)
  *   policy_loss = sum c p, kl = sum c k, loss = policy_loss + beta kl.
  * Reduction as two nested sums ([RK] "Tensor and Data Parallel", step 3):
  * token slots -> per-sequence totals (P_i, K_i) -> the scalar.
@@ -211,6 +213,24 @@ void oracle_log_softmax_rows(const void *rows, int dtype, int64_t nrows, int64_t
  *   g_pol = 0 if (A > 0 and r > 1 + eps_hi) or (A < 0 and r < 1 - eps_lo),
  *           else -A r;
  *   g_kl  = d k / d logp = 1 - e^d = -expm1(d).
+ *
+ * Variants ([DY] "One loss, many algorithms", "CISPO", "Reference-KL
+ * penalty"; [RX] "REINFORCE++" and "REINFORCE++-baseline"):
+ *   kl_type 1, k1 (the log ratio):  k = logp - ref = -d,  g_kl = 1
+ *   kl_type 2, k2:                  k = (logp - ref)^2 / 2 = d^2 / 2,
+ *                                   g_kl = logp - ref = -d
+ *   dual clip c > 1 (A < 0 only; "a lower bound on negative-advantage
+ *     terms"):  p = -max(min(r A, clip(r) A), c A), which for A < 0 is
+ *     -A min(max(r, 1 - eps_lo), c); g_pol is also 0 where r > c.
+ *   surrogate 1, CISPO:  p = -A sg(clip(r)) logp, so g_pol = -A clip(r)
+ *     (the clipped weight sits behind a stop-gradient; every token keeps a
+ *     gradient through logp).  Not combined with the dual clip.
+ * Clip counters (counts, nullable, [3]): tokens clipped at the upper bound,
+ * at the lower bound, and by the dual clip.  For the clipped surrogate the
+ * first two are (A > 0 and r > 1 + eps_hi) and (A < 0 and r < 1 - eps_lo) --
+ * the tokens whose policy gradient the clip removes; for CISPO they are the
+ * tokens whose weight clip(r) differs from r (r > 1 + eps_hi, r < 1 - eps_lo).
+ *
  * ref_logp may be NULL: the KL term is then 0.
  * out3 = {loss, policy_loss, kl}; per_seq = [P (B) | K (B) | L (B)];
  * w, ratio (nullable) are [B,T] with 0 on masked tokens. */
@@ -218,10 +238,12 @@ void oracle_loss_from_logps(int64_t B, int64_t T, const double *logp,
                             const double *ref_logp, const double *old,
                             const uint8_t *mask, const double *A, double eps_lo,
                             double eps_hi, double beta, double grad_scale,
-                            int reduction, double *out3, double *per_seq,
-                            double *w, double *ratio) {
+                            int reduction, int kl_type, int surrogate, double dual_c,
+                            double norm_const, double *out3, double *per_seq,
+                            double *w, double *ratio, int64_t *counts) {
   double *P = per_seq, *K = per_seq + B, *Ls = per_seq + 2 * B;
   int64_t N = 0, S = 0;
+  int64_t n_hi = 0, n_lo = 0, n_dual = 0;
   for (int64_t i = 0; i < B; ++i) {
     int64_t L = 0;
     for (int64_t t = 0; t < T; ++t)
@@ -235,8 +257,10 @@ void oracle_loss_from_logps(int64_t B, int64_t T, const double *logp,
     double c;
     if (reduction == 0)
       c = 1.0 / (double)(N > 0 ? N : 1);
-    else
+    else if (reduction == 1)
       c = Ls[i] > 0 ? 1.0 / ((double)(S > 0 ? S : 1) * Ls[i]) : 0.0;
+    else
+      c = 1.0 / norm_const;
     for (int64_t t = 0; t < T; ++t) {
       int64_t j = i * T + t;
       if (!mask[j]) {
@@ -246,14 +270,43 @@ void oracle_loss_from_logps(int64_t B, int64_t T, const double *logp,
       }
       double r = exp(logp[j] - old[j]);
       double a = A[i];
-      double unclipped = r * a;
       double rc = r < 1.0 - eps_lo ? 1.0 - eps_lo : (r > 1.0 + eps_hi ? 1.0 + eps_hi : r);
-      double clipped = rc * a;
-      double p = -(unclipped < clipped ? unclipped : clipped);
+      double p, gpol;
+      if (surrogate == 1) { /* CISPO */
+        p = -a * rc * logp[j];
+        gpol = -a * rc;
+        if (r > 1.0 + eps_hi) ++n_hi;
+        if (r < 1.0 - eps_lo) ++n_lo;
+      } else {
+        double unclipped = r * a;
+        double clipped = rc * a;
+        double obj = unclipped < clipped ? unclipped : clipped;
+        int hi = a > 0.0 && r > 1.0 + eps_hi;
+        int lo = a < 0.0 && r < 1.0 - eps_lo;
+        int dual = dual_c > 0.0 && a < 0.0 && r > dual_c;
+        if (dual_c > 0.0 && a < 0.0 && dual_c * a > obj) obj = dual_c * a;
+        p = -obj;
+        gpol = (hi || lo || dual) ? 0.0 : -a * r;
+        n_hi += hi;
+        n_lo += lo;
+        n_dual += dual;
+      }
       double d = ref_logp ? ref_logp[j] - logp[j] : 0.0;
-      double k = expm1(d) - d;
-      double gpol = ((a > 0.0 && r > 1.0 + eps_hi) || (a < 0.0 && r < 1.0 - eps_lo)) ? 0.0 : -a * r;
-      double gkl = -expm1(d);
+      double k, gkl;
+      if (kl_type == 1) {
+        k = -d;
+        gkl = 1.0;
+      } else if (kl_type == 2) {
+        k = 0.5 * d * d;
+        gkl = -d;
+      } else {
+        k = expm1(d) - d;
+        gkl = -expm1(d);
+      }
+      if (!ref_logp) {
+        k = 0.0;
+        gkl = 0.0;
+      }
       Pi += p;
       Ki += k;
       if (w) w[j] = grad_scale * c * (gpol + beta * gkl);
@@ -263,8 +316,8 @@ void oracle_loss_from_logps(int64_t B, int64_t T, const double *logp,
     K[i] = Ki;
   }
   double pol = 0.0, kl = 0.0;
-  if (reduction == 0) {
-    double n = (double)(N > 0 ? N : 1);
+  if (reduction == 0 || reduction == 2) {
+    double n = reduction == 0 ? (double)(N > 0 ? N : 1) : norm_const;
     for (int64_t i = 0; i < B; ++i) {
       pol += P[i];
       kl += K[i];
@@ -284,6 +337,11 @@ void oracle_loss_from_logps(int64_t B, int64_t T, const double *logp,
   out3[0] = pol + beta * kl;
   out3[1] = pol;
   out3[2] = kl;
+  if (counts) {
+    counts[0] = n_hi;
+    counts[1] = n_lo;
+    counts[2] = n_dual;
+  }
 }
 
 /* -------------------------------------------------------- gradient rows

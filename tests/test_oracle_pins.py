@@ -439,8 +439,10 @@ def test_hand_worked_case(case):
              mask=np.array(case["mask"], np.uint8), rewards=np.array(case["rewards"], np.float32),
              bounds=_uniform_bounds(B, case["samples_per_prompt"]))
     res = _run(c, eps_lo=case["eps_lo"], eps_hi=case["eps_hi"], beta=case["beta"],
-               reduction=case["reduction"])
+               reduction=case["reduction"], **case.get("variant", {}))
     e = case["expect"]
+    if "clip_counts" in e:
+        assert list(res["clip_counts"]) == e["clip_counts"]
     for k in ("loss", "policy_loss", "kl"):
         assert res[k] == pytest.approx(e[k], rel=1e-12, abs=1e-15), k
     assert np.allclose(res["per_seq_policy"], e["per_seq_policy"], atol=1e-12)
