@@ -29,7 +29,9 @@ __all__ = ["grpo_workspace_size", "grpo_group_adv", "grpo_loss_fwd_bwd", "grpo_l
 GRPO_ADV_EPS_ADD = 1
 GRPO_SKIP_MASKED_GRAD_ROWS = 2
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
-_REDUCTIONS = {"token_mean": 0, "sequence_mean": 1}
+_REDUCTIONS = {"token_mean": 0, "sequence_mean": 1, "fixed_constant": 2}
+_KL_TYPES = {"k3": 0, "k1": 1, "k2": 2}
+_SURROGATES = {"clip": 0, "cispo": 1}
 
 
 class GrpoError(RuntimeError):
@@ -52,8 +54,10 @@ class _Params(ctypes.Structure):
     _fields_ = [("clip_eps_lo", ctypes.c_float), ("clip_eps_hi", ctypes.c_float),
                 ("beta", ctypes.c_float), ("adv_eps", ctypes.c_float),
                 ("grad_scale", ctypes.c_float), ("reduction", ctypes.c_int32),
-                ("flags", ctypes.c_uint32), ("_reserved", ctypes.c_int32),
-                ("profile", ctypes.POINTER(_Profile))]
+                ("flags", ctypes.c_uint32), ("kl_type", ctypes.c_int32),
+                ("surrogate", ctypes.c_int32), ("dual_clip_c", ctypes.c_float),
+                ("norm_constant", ctypes.c_float), ("_reserved", ctypes.c_int32),
+                ("profile", ctypes.POINTER(_Profile)), ("clip_counts", ctypes.c_void_p)]
 
 
 _lib = None
@@ -134,8 +138,16 @@ def _groups(B: int, samples_per_prompt: int, group_boundaries) -> tuple[_Groups,
     return g, keep
 
 
-def _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction, flags, profile):
+def _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction, flags, profile,
+            kl="k3", surrogate="clip", dual_clip_c=None, norm_constant=None, clip_counts=None):
     p = _Params()
+    p.kl_type = _KL_TYPES[kl]
+    p.surrogate = _SURROGATES[surrogate]
+    p.dual_clip_c = float(dual_clip_c or 0.0)
+    p.norm_constant = float(norm_constant or 0.0)
+    if clip_counts is not None:
+        _dev(clip_counts, "clip_counts", torch.int64)
+        p.clip_counts = clip_counts.data_ptr()
     p.clip_eps_lo = float(clip_eps)
     p.clip_eps_hi = float(clip_eps if clip_eps_hi is None else clip_eps_hi)
     p.beta = float(beta)
@@ -196,14 +208,20 @@ def grpo_loss_fwd_bwd(policy_logits: torch.Tensor, ref_logits: torch.Tensor,
                       want_per_seq: bool = False, want_logps: bool = False,
                       want_adv: bool = False, out3: Optional[torch.Tensor] = None,
                       workspace: Optional[torch.Tensor] = None, stream=None,
-                      profile=None) -> dict:
+                      profile=None, kl: str = "k3", surrogate: str = "clip",
+                      dual_clip_c: Optional[float] = None, norm_constant: Optional[float] = None,
+                      want_clip_counts: bool = False) -> dict:
     """Fused GRPO loss forward + dL/dlogits.
 
     ``grad``: True (allocate), a tensor to write into (may be
     ``policy_logits`` itself for an in-place gradient), or None/False
-    (forward only).  Returns a dict of device tensors: ``out3`` ([loss,
-    policy_loss, kl]), ``loss``, ``policy_loss``, ``kl`` (0-d views),
-    ``grad``, and the optional ``per_seq`` [3,B], ``logps`` [B,T], ``adv`` [B]."""
+    (forward only).  Variants: ``kl`` in {"k3", "k1", "k2"}, ``surrogate``
+    in {"clip", "cispo"}, ``dual_clip_c`` (> 1), ``reduction=
+    "fixed_constant"`` with ``norm_constant``.  Returns a dict of device
+    tensors: ``out3`` ([loss, policy_loss, kl]), ``loss``, ``policy_loss``,
+    ``kl`` (0-d views), ``grad``, and the optional ``per_seq`` [3,B],
+    ``logps`` [B,T], ``adv`` [B], ``clip_counts`` [3] (int64: clipped at the
+    upper bound, at the lower bound, by the dual clip)."""
     if policy_logits.dtype not in _DTYPES:
         raise ValueError(f"unsupported logits dtype {policy_logits.dtype}")
     _dev(policy_logits, "policy_logits")
@@ -225,9 +243,11 @@ def grpo_loss_fwd_bwd(policy_logits: torch.Tensor, ref_logits: torch.Tensor,
         raise ValueError("rewards must be [B]")
     dev = policy_logits.device
     g, keep = _groups(B, samples_per_prompt, group_boundaries)
+    counts = torch.empty(3, dtype=torch.int64, device=dev) if want_clip_counts else None
     p, prof = _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction,
                       (GRPO_ADV_EPS_ADD if eps_add else 0)
-                      | (GRPO_SKIP_MASKED_GRAD_ROWS if skip_masked_grad_rows else 0), profile)
+                      | (GRPO_SKIP_MASKED_GRAD_ROWS if skip_masked_grad_rows else 0), profile,
+                      kl, surrogate, dual_clip_c, norm_constant, counts)
     if grad is True:
         grad_t = torch.empty_like(policy_logits)
     elif grad is None or grad is False:
@@ -248,7 +268,8 @@ def grpo_loss_fwd_bwd(policy_logits: torch.Tensor, ref_logits: torch.Tensor,
                                  ws.numel(), _stream(stream))
     _check(rc, "grpo_loss_fwd_bwd")
     return {"out3": out3, "loss": out3[0], "policy_loss": out3[1], "kl": out3[2],
-            "grad": grad_t, "per_seq": per_seq, "logps": logps, "adv": adv, "workspace": ws}
+            "grad": grad_t, "per_seq": per_seq, "logps": logps, "adv": adv,
+            "clip_counts": counts, "workspace": ws}
 
 
 def grpo_loss_fwd_bwd_static(policy_logits: torch.Tensor, ref_logits: torch.Tensor,
@@ -285,8 +306,12 @@ def grpo_loss_from_logps(logps: torch.Tensor, old_logps: torch.Tensor,
                          reduction="token_mean", grad=True, want_per_seq: bool = False,
                          want_adv: bool = False, out3: Optional[torch.Tensor] = None,
                          workspace: Optional[torch.Tensor] = None, stream=None,
-                         profile=None) -> dict:
-    """GRPO loss from per-token log-probs; ``grad`` gives dL/dlogp [B,T]."""
+                         profile=None, kl: str = "k3", surrogate: str = "clip",
+                         dual_clip_c: Optional[float] = None,
+                         norm_constant: Optional[float] = None,
+                         want_clip_counts: bool = False) -> dict:
+    """GRPO loss from per-token log-probs; ``grad`` gives dL/dlogp [B,T].
+    Variants and outputs as in grpo_loss_fwd_bwd."""
     _dev(logps, "logps", torch.float32)
     B, T = logps.shape
     _dev(old_logps, "old_logps", torch.float32)
@@ -298,8 +323,10 @@ def grpo_loss_from_logps(logps: torch.Tensor, old_logps: torch.Tensor,
         mask = mask.view(torch.uint8)
     dev = logps.device
     g, keep = _groups(B, samples_per_prompt, group_boundaries)
+    counts = torch.empty(3, dtype=torch.int64, device=dev) if want_clip_counts else None
     p, prof = _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction,
-                      GRPO_ADV_EPS_ADD if eps_add else 0, profile)
+                      GRPO_ADV_EPS_ADD if eps_add else 0, profile, kl, surrogate, dual_clip_c,
+                      norm_constant, counts)
     if grad is True:
         grad_t = torch.empty((B, T), dtype=torch.float32, device=dev)
     elif grad is None or grad is False:
@@ -316,7 +343,8 @@ def grpo_loss_from_logps(logps: torch.Tensor, old_logps: torch.Tensor,
                                     ws.numel(), _stream(stream))
     _check(rc, "grpo_loss_from_logps")
     return {"out3": out3, "loss": out3[0], "policy_loss": out3[1], "kl": out3[2],
-            "grad": grad_t, "per_seq": per_seq, "adv": adv, "workspace": ws}
+            "grad": grad_t, "per_seq": per_seq, "adv": adv, "clip_counts": counts,
+            "workspace": ws}
 
 
 def grpo_read_device_status(workspace: torch.Tensor, stream=None) -> int:

@@ -30,9 +30,33 @@ grpo_status_t check_params(const grpo_params_t* p) {
   if (!(p->clip_eps_hi >= 0.f)) return GRPO_ERR_PARAM;
   if (!(p->beta >= 0.f)) return GRPO_ERR_PARAM;
   if (!(p->adv_eps > 0.f)) return GRPO_ERR_PARAM;
-  if (p->reduction != GRPO_TOKEN_MEAN && p->reduction != GRPO_SEQUENCE_MEAN) return GRPO_ERR_PARAM;
+  if (p->reduction != GRPO_TOKEN_MEAN && p->reduction != GRPO_SEQUENCE_MEAN &&
+      p->reduction != GRPO_FIXED_CONSTANT)
+    return GRPO_ERR_PARAM;
+  if (p->reduction == GRPO_FIXED_CONSTANT && !(isfinite(p->norm_constant) && p->norm_constant > 0.f))
+    return GRPO_ERR_PARAM;
   if (p->flags & ~(GRPO_ADV_EPS_ADD | GRPO_SKIP_MASKED_GRAD_ROWS)) return GRPO_ERR_PARAM;
+  if (p->kl_type != GRPO_KL_K3 && p->kl_type != GRPO_KL_K1 && p->kl_type != GRPO_KL_K2)
+    return GRPO_ERR_PARAM;
+  if (p->surrogate != GRPO_SURROGATE_CLIP && p->surrogate != GRPO_SURROGATE_CISPO)
+    return GRPO_ERR_PARAM;
+  if (p->dual_clip_c != 0.f) {  // off, or c > 1 with the clipped surrogate
+    if (!(isfinite(p->dual_clip_c) && p->dual_clip_c > 1.f)) return GRPO_ERR_PARAM;
+    if (p->surrogate != GRPO_SURROGATE_CLIP) return GRPO_ERR_PARAM;
+  }
+  if (p->clip_counts && ((uintptr_t)p->clip_counts & 7)) return GRPO_ERR_ALIGN;
   return GRPO_OK;
+}
+
+Variant variant_of(const grpo_params_t* p) {
+  Variant v;
+  v.eps_lo = p->clip_eps_lo;
+  v.eps_hi = p->clip_eps_hi;
+  v.beta = p->beta;
+  v.dual_c = p->dual_clip_c;
+  v.kl_type = p->kl_type;
+  v.surrogate = p->surrogate;
+  return v;
 }
 
 // Resolves the group spec to (spp, boundaries, G).
@@ -192,11 +216,15 @@ extern "C" grpo_status_t grpo_loss_fwd_bwd(
     ra.flags = params->flags;
     ra.precise_ok = dt == GRPO_F32;
     ra.tab = exp_table();
+    ra.var = variant_of(params);
+    ra.norm_c = params->norm_constant;
     e = launch_rows(ra, dt, params->profile, s);
     if (e != cudaSuccess) return GRPO_ERR_CUDA;
   }
   ReduceArgs rd{completion_mask, L, A, (double*)(w + lay.off_seq), slot_p, slot_k, B, T,
-                params->beta, params->reduction, hdr, out3, per_seq};
+                params->beta, params->reduction, hdr, out3, per_seq,
+                variant_of(params).splits_A() ? 1 : 0, params->norm_constant,
+                params->clip_counts};
   return cuda_status(launch_reduce(rd, s));
 }
 
@@ -242,7 +270,8 @@ extern "C" grpo_status_t grpo_loss_from_logps(const float* logps, const float* o
   if (launch_prep(pa, s) != cudaSuccess) return GRPO_ERR_CUDA;
   LogpsArgs la{logps, old_logps, ref_logps, completion_mask, A, Aff, rng, L, seq, grad_logps, out3,
                per_seq, hdr, B, T, params->clip_eps_lo, params->clip_eps_hi, params->beta,
-               params->grad_scale, params->reduction};
+               params->grad_scale, params->reduction, variant_of(params),
+               params->norm_constant, params->clip_counts};
   return cuda_status(launch_logps(la, params->profile, s));
 }
 

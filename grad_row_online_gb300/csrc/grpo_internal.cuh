@@ -32,6 +32,7 @@ struct WsHeader {
   unsigned long long row_counter;  // rows: next row to claim
   unsigned long long N;            // active tokens  (prep: integer atomics, exact)
   unsigned long long S;            // live sequences (idem)
+  unsigned long long clip[3];      // clipped tokens: upper, lower, dual (integer atomics)
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -370,8 +371,9 @@ __device__ __forceinline__ float block_max(float v, float* scratch) {
 }
 
 // This thread's share of the level-2 sums over the B sequence totals
-// (seq[0..B) policy, seq[B..2B) KL), in a fixed order: the token mean adds
-// the totals, the sequence mean adds total / L_i over live sequences.  The
+// (seq[0..B) policy, seq[B..2B) KL), in a fixed order: the token mean and
+// the fixed constant add the totals, the sequence mean adds total / L_i over
+// live sequences.  The
 // totals were written by other CTAs of the same launch (made visible by
 // their __threadfence before the ticket), so they are read from L2 (ld.cg),
 // eight at a time to keep the loads in flight.
@@ -391,7 +393,7 @@ __device__ __forceinline__ void seq_totals(const double* seq, const int32_t* Ls,
     }
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
-      if (reduction == GRPO_TOKEN_MEAN) {
+      if (reduction != GRPO_SEQUENCE_MEAN) {
         u[0] += P[k];
         u[1] += K[k];
       } else if (L[k] > 0) {
@@ -400,6 +402,99 @@ __device__ __forceinline__ void seq_totals(const double* seq, const int32_t* Ls,
       }
     }
   }
+}
+
+// ----------------------------------------------------------------------------
+// the per-token epilogue and its variants
+// ----------------------------------------------------------------------------
+// The loss variant of a call (dockyard_rl "One loss, many algorithms",
+// "CISPO", "Reference-KL penalty"; Relax "REINFORCE++-baseline" for k2).
+struct Variant {
+  float eps_lo, eps_hi, beta;
+  float dual_c;  // 0: off; > 1: the dual clip on negative-advantage tokens
+  int kl_type;   // grpo_kl_t
+  int surrogate; // grpo_surrogate_t
+  __host__ __device__ bool is_default() const {
+    return kl_type == GRPO_KL_K3 && surrogate == GRPO_SURROGATE_CLIP && dual_c == 0.f;
+  }
+  // the policy term's constant -A is summed per sequence (clipped surrogate)
+  __host__ __device__ bool splits_A() const { return surrogate == GRPO_SURROGATE_CLIP; }
+};
+
+template <typename F>
+struct TokEpi {
+  F q;       // clipped surrogate: the policy term plus A (p = q - A); CISPO: p
+  F k;       // the KL estimator
+  F g;       // g_pol + beta g_kl = d(p + beta k)/d logp
+  int clip;  // 0, or the clip that removed / clipped the token: 1 upper, 2 lower, 3 dual
+};
+
+// One token's scalars from em = r - 1, the log-prob lp, d = ref_logp - logp,
+// emd = e^d - 1 and k3 = e^d - d - 1 (the caller evaluates these three with
+// the accuracy its precision needs).  Clipped surrogate:
+//   p + A = -min((r-1)A, (clip(r)-1)A), and with the dual clip (A < 0)
+//   p + A = -max(min(...), (c-1)A); g_pol = 0 where a clip binds, else -A r.
+// CISPO: p = -A clip(r) lp, g_pol = -A clip(r).
+// KL: k3 = e^d - d - 1 (g_kl = -(e^d - 1)), k1 = -d (g_kl = 1),
+//     k2 = d^2/2 (g_kl = -d); no reference: k = g_kl = 0.
+template <typename F>
+__device__ __forceinline__ TokEpi<F> token_epilogue(F em, F lp, F d, F emd, F k3, bool has_ref,
+                                                    F A, const Variant& v) {
+  TokEpi<F> t;
+  const F lo = -(F)v.eps_lo, hi = (F)v.eps_hi;  // bounds on r - 1
+  const F emc = em < lo ? lo : (em > hi ? hi : em);
+  F gpol;
+  if (v.surrogate == GRPO_SURROGATE_CISPO) {
+    const F rc = (F)1 + emc;
+    t.q = -A * rc * lp;
+    gpol = -A * rc;
+    t.clip = em > hi ? 1 : (em < lo ? 2 : 0);
+  } else {
+    const F unc = em * A, cl = emc * A;
+    F m = unc < cl ? unc : cl;
+    bool dual = false;
+    if (v.dual_c > 0.f && A < (F)0) {
+      const F cm1 = (F)v.dual_c - (F)1;
+      const F dc = cm1 * A;
+      if (dc > m) m = dc;
+      dual = em > cm1;
+    }
+    t.q = -m;
+    const bool up = A > (F)0 && em > hi, down = A < (F)0 && em < lo;
+    gpol = (up || down || dual) ? (F)0 : -A * (em + (F)1);
+    t.clip = up ? 1 : (down ? 2 : (dual ? 3 : 0));
+  }
+  F gkl;
+  if (!has_ref) {
+    t.k = (F)0;
+    gkl = (F)0;
+  } else if (v.kl_type == GRPO_KL_K1) {
+    t.k = -d;
+    gkl = (F)1;
+  } else if (v.kl_type == GRPO_KL_K2) {
+    t.k = d * d * (F)0.5;
+    gkl = -d;
+  } else {
+    t.k = k3;
+    gkl = -emd;
+  }
+  t.g = gpol + (F)v.beta * gkl;
+  return t;
+}
+
+// d g_kl / d ref_logp in magnitude (= d g_kl / d logp), for error budgets:
+// e^d for k3, 0 for k1, 1 for k2.
+__device__ __forceinline__ float kl_slope(int kl_type, float emd) {
+  return kl_type == GRPO_KL_K1 ? 0.f : (kl_type == GRPO_KL_K2 ? 1.f : 1.f + emd);
+}
+
+// This CTA's clip counts into the workspace header (one atomic per nonzero
+// count; integer sums are exact in any order).  Call with the CTA's totals
+// from one thread.
+__device__ __forceinline__ void add_clip_counts(WsHeader* hdr, const unsigned (&n)[3]) {
+#pragma unroll
+  for (int j = 0; j < 3; ++j)
+    if (n[j]) atomicAdd(&hdr->clip[j], (unsigned long long)n[j]);
 }
 
 // ----------------------------------------------------------------------------
@@ -441,6 +536,8 @@ struct RowArgs {
   unsigned flags;
   int precise_ok;  // fp32 gradient output: rows may take the precise path
   ExpTable tab;
+  Variant var;
+  float norm_c;  // GRPO_FIXED_CONSTANT's constant
 };
 
 struct ReduceArgs {
@@ -456,6 +553,9 @@ struct ReduceArgs {
   WsHeader* hdr;
   float* out3;
   float* per_seq;  // nullable
+  int split_A;      // the clipped surrogate: add -A_i L_i per sequence
+  float norm_c;     // GRPO_FIXED_CONSTANT's constant
+  unsigned long long* counts_out;  // nullable [3]
 };
 
 struct LogpsArgs {
@@ -475,6 +575,9 @@ struct LogpsArgs {
   int64_t B, T;
   float eps_lo, eps_hi, beta, grad_scale;
   int reduction;
+  Variant var;
+  float norm_c;  // GRPO_FIXED_CONSTANT's constant
+  unsigned long long* counts_out;  // nullable [3]
 };
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);

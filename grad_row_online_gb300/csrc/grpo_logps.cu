@@ -61,30 +61,18 @@ __device__ __forceinline__ Em expm1_k3(float d) {
   return r;
 }
 
-struct TokTerms {
-  float q;  // policy term plus A: p = -A + q
-  float k;  // KL term
-  float g;  // g_pol + beta g_kl
-};
-
-// p = -min(rA, clip(r)A) = -A - min((r-1)A, (clip(r)-1)A).  The constant -A
-// enters once per sequence, as -A_i L_i in float pairs from the float-pair
-// advantage: with a full mask the A_i of a group cancel there, which an fp32
-// A rounded per token would break.
-// The remainder uses r - 1 = e^(logp-old) - 1, accurate where r is near 1.
-__device__ __forceinline__ TokTerms tok_terms(float lp, float o, float rf, float A,
-                                              const LogpsArgs& a) {
-  TokTerms t;
+// One token on the general path: the ratio and the KL argument through
+// expm1_k3 (accurate near 0), then the variant's epilogue.  For the clipped
+// surrogate p = -A - min((r-1)A, (clip(r)-1)A): the constant -A enters once
+// per sequence, as -A_i L_i in float pairs from the float-pair advantage
+// (with a full mask the A_i of a group cancel there, which an fp32 A rounded
+// per token would break).
+__device__ __forceinline__ TokEpi<float> tok_terms(float lp, float o, float rf, float A,
+                                                   const LogpsArgs& a) {
   const float em = expm1_k3(__fsub_rn(lp, o)).em;  // r - 1
-  const float unc = __fmul_rn(em, A);
-  const float cl = __fmul_rn(fminf(fmaxf(em, -a.eps_lo), a.eps_hi), A);
-  t.q = -fminf(unc, cl);
-  const Em kd = expm1_k3(a.ref ? __fsub_rn(rf, lp) : 0.0f);
-  t.k = kd.k3;
-  const bool clipped = (A > 0.f && em > a.eps_hi) || (A < 0.f && em < -a.eps_lo);
-  const float gpol = clipped ? 0.f : -__fmul_rn(A, __fadd_rn(em, 1.0f));
-  t.g = __fmaf_rn(-a.beta, kd.em, gpol);
-  return t;
+  const float d = a.ref ? __fsub_rn(rf, lp) : 0.0f;
+  const Em kd = expm1_k3(d);
+  return token_epilogue<float>(em, lp, d, kd.em, kd.k3, a.ref != nullptr, A, a.var);
 }
 
 // dL/dlogp in double, for tokens whose gradient is large enough that the
@@ -99,14 +87,15 @@ struct SeqCtx {
 __device__ __noinline__ float w_precise(float lp, float o, float rf, const SeqCtx& x,
                                         const LogpsArgs& a) {
   const double A = a.A[x.b];
-  const double c = a.reduction == GRPO_TOKEN_MEAN
-                       ? 1.0 / (double)(x.N > 0 ? x.N : 1)
-                       : 1.0 / ((double)(x.S > 0 ? x.S : 1) * (double)x.L);
-  const double r = exp((double)lp - (double)o);
-  const double lo = 1.0 - (double)a.eps_lo, hi = 1.0 + (double)a.eps_hi;
-  const double gpol = ((A > 0.0 && r > hi) || (A < 0.0 && r < lo)) ? 0.0 : -A * r;
+  const double c = a.reduction == GRPO_TOKEN_MEAN      ? 1.0 / (double)(x.N > 0 ? x.N : 1)
+                   : a.reduction == GRPO_SEQUENCE_MEAN ? 1.0 / ((double)(x.S > 0 ? x.S : 1) * (double)x.L)
+                                                       : 1.0 / (double)a.norm_c;
+  const double em = expm1((double)lp - (double)o);
   const double d = a.ref ? (double)rf - (double)lp : 0.0;
-  return (float)((double)a.grad_scale * c * (gpol + (double)a.beta * -expm1(d)));
+  const double emd = expm1(d);
+  const TokEpi<double> t =
+      token_epilogue<double>(em, (double)lp, d, emd, emd - d, a.ref != nullptr, A, a.var);
+  return (float)((double)a.grad_scale * c * t.g);
 }
 
 __device__ __forceinline__ void kahan(float& s, float& c, float x) {
@@ -125,9 +114,16 @@ __device__ __forceinline__ bool vec_ok(const LogpsArgs& a) {
 // tokens are added in fp32 first and enter the Kahan sum once.
 struct Acc {
   float sq = 0.f, cq = 0.f, sk = 0.f, ck = 0.f;
+  unsigned nc[3] = {0u, 0u, 0u};  // clipped tokens: upper, lower, dual
+  // (constant indices only, so the counters stay in registers)
+  __device__ __forceinline__ void count(int clip, unsigned n = 1u) {
+    if (clip == 1) nc[0] += n;
+    else if (clip == 2) nc[1] += n;
+    else if (clip == 3) nc[2] += n;
+  }
 };
 
-__device__ __forceinline__ float token_w(float lp, float o, float rf, const TokTerms& t,
+__device__ __forceinline__ float token_w(float lp, float o, float rf, const TokEpi<float>& t,
                                          const SeqCtx& x, const LogpsArgs& a) {
   float w = __fmul_rn(x.gc, t.g);
   if (fabsf(w) > kWPrecise) w = w_precise(lp, o, rf, x, a);
@@ -140,6 +136,8 @@ __device__ __forceinline__ float token_w(float lp, float o, float rf, const TokT
 //   the token is clipped  <=>  s em > lim
 // which is the clipped-surrogate case split with the sign of A taken out.
 struct FastCtx {
+  bool on;     // the call's loss is the default variant (clipped surrogate, k3)
+  int clip_kind;  // how a clipped token counts: 1 upper (A > 0), 2 lower (A < 0), 0 not
   float2 s2, neg_absA2, negA2, gc2, neg_beta2;
   float lim;
   float g2_max;  // (kWPrecise / gc)^2: a vector whose sum of g^2 stays below
@@ -163,7 +161,7 @@ __device__ __forceinline__ float2 Q_poly2(float2 d) {
 // packed fp32x2).  Accumulates q and k, and the sums behind the range check.
 __device__ __forceinline__ float2 pair_fast(float2 lp, float2 od, float2 rf, bool has_ref,
                                             const FastCtx& f, float2& vq, float2& vk,
-                                            float2& d2sum, float2& g2sum) {
+                                            float2& d2sum, float2& g2sum, int& nclip) {
   const float2 dp = __ffma2_rn(od, f2(-1.f), lp);  // logp - old
   const float2 Qp = Q_poly2(dp), ddp = __fmul2_rn(dp, dp);
   const float2 em = __ffma2_rn(ddp, Qp, dp);       // r - 1
@@ -175,8 +173,10 @@ __device__ __forceinline__ float2 pair_fast(float2 lp, float2 od, float2 rf, boo
   const float2 mn = make_float2(fminf(se.x, f.lim), fminf(se.y, f.lim));
   const float2 q = __fmul2_rn(f.neg_absA2, mn);
   float2 gp = __fmul2_rn(f.negA2, __fadd2_rn(em, f2(1.f)));  // -A r
-  gp.x = se.x > f.lim ? 0.f : gp.x;
-  gp.y = se.y > f.lim ? 0.f : gp.y;
+  const bool cx = se.x > f.lim, cy = se.y > f.lim;
+  gp.x = cx ? 0.f : gp.x;
+  gp.y = cy ? 0.f : gp.y;
+  nclip += (int)cx + (int)cy;
   const float2 g = __ffma2_rn(f.neg_beta2, emr, gp);
   vq = __fadd2_rn(vq, q);
   vk = __fadd2_rn(vk, k);
@@ -191,12 +191,13 @@ __device__ __forceinline__ float2 pair_fast(float2 lp, float2 od, float2 rf, boo
 // (caught by its sum of g^2); NaNs fail the check too.
 __device__ __forceinline__ bool vec_fast(const float4& l4, const float4& o4, const float4& r4,
                                          bool has_ref, const FastCtx& f, float (&w)[4],
-                                         float& vq, float& vk) {
+                                         float& vq, float& vk, int& nclip) {
   float2 sq = f2(0.f), sk = f2(0.f), d2 = f2(0.f), g2 = f2(0.f);
+  nclip = 0;
   const float2 w01 = pair_fast(make_float2(l4.x, l4.y), make_float2(o4.x, o4.y),
-                               make_float2(r4.x, r4.y), has_ref, f, sq, sk, d2, g2);
+                               make_float2(r4.x, r4.y), has_ref, f, sq, sk, d2, g2, nclip);
   const float2 w23 = pair_fast(make_float2(l4.z, l4.w), make_float2(o4.z, o4.w),
-                               make_float2(r4.z, r4.w), has_ref, f, sq, sk, d2, g2);
+                               make_float2(r4.z, r4.w), has_ref, f, sq, sk, d2, g2, nclip);
   w[0] = w01.x;
   w[1] = w01.y;
   w[2] = w23.x;
@@ -215,7 +216,7 @@ __device__ __forceinline__ bool all_active(uint32_t mw) {
 __device__ __forceinline__ void vec_general(uint32_t mw, const float4& l4, const float4& o4,
                                             const float4& r4, const SeqCtx& x,
                                             const LogpsArgs& a, float (&w)[4], float& vq,
-                                            float& vk) {
+                                            float& vk, Acc& acc) {
   const float lp[4] = {l4.x, l4.y, l4.z, l4.w};
   const float od[4] = {o4.x, o4.y, o4.z, o4.w};
   const float rf[4] = {r4.x, r4.y, r4.z, r4.w};
@@ -225,9 +226,10 @@ __device__ __forceinline__ void vec_general(uint32_t mw, const float4& l4, const
   for (int j = 0; j < 4; ++j) {
     w[j] = 0.f;
     if ((mw >> (8 * j)) & 0xFFu) {
-      const TokTerms t = tok_terms(lp[j], od[j], rf[j], x.A, a);
+      const TokEpi<float> t = tok_terms(lp[j], od[j], rf[j], x.A, a);
       vq = __fadd_rn(vq, t.q);
       vk = __fadd_rn(vk, t.k);
+      acc.count(t.clip);
       w[j] = token_w(lp[j], od[j], rf[j], t, x, a);
     }
   }
@@ -243,8 +245,12 @@ __device__ __forceinline__ void process_vec(uint32_t mw, const float4& l, const 
   w[0] = w[1] = w[2] = w[3] = 0.f;
   if (mw == 0u) return;
   float vq, vk;
-  if (!(all_active(mw) && vec_fast(l, o, r, has_ref, f, w, vq, vk)))
-    vec_general(mw, l, o, r, x, a, w, vq, vk);
+  int nclip;
+  if (f.on && all_active(mw) && vec_fast(l, o, r, has_ref, f, w, vq, vk, nclip)) {
+    acc.count(f.clip_kind, (unsigned)nclip);
+  } else {
+    vec_general(mw, l, o, r, x, a, w, vq, vk, acc);
+  }
   kahan(acc.sq, acc.cq, vq);
   kahan(acc.sk, acc.ck, vk);
 }
@@ -313,6 +319,7 @@ __device__ __forceinline__ bool staged_ok(const LogpsArgs& a) {
 
 __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs a) {
   __shared__ FF s_ff[2][kLogpsThreads / 32];
+  __shared__ unsigned s_nc[3][kLogpsThreads / 32];
   __shared__ bool s_last;
   __shared__ __align__(16) Stage s_st[kDepth];
   __shared__ __align__(8) uint64_t s_full[kDepth];
@@ -333,15 +340,18 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
     x.L = a.L[b];
     const float2 Ab = a.Aff[b];
     x.A = Ab.x;
-    // grad_scale * c in fp32: c = 1/max(N,1) or 1/(max(S,1) L_b); the
+    // grad_scale * c in fp32: c = 1/max(N,1), 1/(max(S,1) L_b) or 1/C; the
     // products and quotient are rounded in fp32, well inside the gradient's
     // rounding allowance
-    const float den = a.reduction == GRPO_TOKEN_MEAN
-                          ? __ull2float_rn(x.N > 0 ? x.N : 1)
-                          : __fmul_rn(__ull2float_rn(x.S > 0 ? x.S : 1), (float)x.L);
+    const float den =
+        a.reduction == GRPO_TOKEN_MEAN      ? __ull2float_rn(x.N > 0 ? x.N : 1)
+        : a.reduction == GRPO_SEQUENCE_MEAN ? __fmul_rn(__ull2float_rn(x.S > 0 ? x.S : 1), (float)x.L)
+                                            : a.norm_c;
     x.gc = x.L > 0 ? __fdiv_rn(a.grad_scale, den) : 0.f;
     const bool has_ref = a.ref != nullptr;
     FastCtx f;
+    f.on = a.var.is_default();
+    f.clip_kind = x.A > 0.f ? 1 : (x.A < 0.f ? 2 : 0);
     const float sgn = x.A > 0.f ? 1.f : -1.f;
     f.s2 = f2(sgn);
     f.neg_absA2 = f2(-fabsf(x.A));
@@ -447,9 +457,10 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
         if (a.mask[base + t]) {
           const float lp = a.logps[base + t], o = a.old[base + t];
           const float rf = a.ref ? a.ref[base + t] : 0.f;
-          const TokTerms tt = tok_terms(lp, o, rf, x.A, a);
+          const TokEpi<float> tt = tok_terms(lp, o, rf, x.A, a);
           kahan(acc.sq, acc.cq, tt.q);
           kahan(acc.sk, acc.ck, tt.k);
+          acc.count(tt.clip);
           w = token_w(lp, o, rf, tt, x, a);
         }
         if (a.grad) a.grad[base + t] = w;
@@ -458,9 +469,16 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
     // the sequence's totals as float pairs: threads' Kahan sums, a fixed
     // xor tree per warp, warps in index order
     FF fq = warp_sum_ff2(FF{acc.sq, -acc.cq}), fk = warp_sum_ff2(FF{acc.sk, -acc.ck});
+    unsigned nc[3] = {0u, 0u, 0u};
+    if (a.counts_out) {
+#pragma unroll
+      for (int j = 0; j < 3; ++j) nc[j] = warp_sum(acc.nc[j]);
+    }
     if (lane == 0) {
       s_ff[0][warp] = fq;
       s_ff[1][warp] = fk;
+#pragma unroll
+      for (int j = 0; j < 3; ++j) s_nc[j][warp] = nc[j];
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -471,13 +489,22 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
         fq = ff_add(fq, s_ff[0][k]);
         fk = ff_add(fk, s_ff[1][k]);
       }
-      // P_b = sum q - A_b L_b (the product exact up to ~2^-48 relative)
-      const FF P = ff_add(fq, ff_neg(ff_scale(FF{Ab.x, Ab.y}, (float)x.L)));
+      // P_b = sum q - A_b L_b for the clipped surrogate (the product exact
+      // up to ~2^-48 relative); CISPO's q is the policy term itself
+      const FF P = a.var.splits_A() ? ff_add(fq, ff_neg(ff_scale(FF{Ab.x, Ab.y}, (float)x.L))) : fq;
       a.seq[b] = make_float4(P.hi, P.lo, fk.hi, fk.lo);
       if (a.per_seq) {
         a.per_seq[b] = ff_float(P);
         a.per_seq[a.B + b] = ff_float(fk);
         a.per_seq[2 * a.B + b] = (float)x.L;
+      }
+      if (a.counts_out) {
+        unsigned n[3];
+        for (int j = 0; j < 3; ++j) {
+          n[j] = 0u;
+          for (int k = 0; k < kLogpsThreads / 32; ++k) n[j] += s_nc[j][k];
+        }
+        add_clip_counts(a.hdr, n);
       }
       __threadfence();
       s_last = atomicAdd(&a.hdr->done_ctas, 1u) == gridDim.x - 1;
@@ -508,7 +535,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
       FF P = {t[k].x, t[k].y}, K = {t[k].z, t[k].w};
-      if (a.reduction != GRPO_TOKEN_MEAN) {
+      if (a.reduction == GRPO_SEQUENCE_MEAN) {
         if (L[k] == 0) continue;
         const FF Lf = {(float)L[k], 0.f};
         P = ff_div(P, Lf);
@@ -533,7 +560,9 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
       K = ff_add(K, s_ff[1][k]);
     }
     const unsigned long long N = a.B > 0 ? a.hdr->N : 0, S = a.B > 0 ? a.hdr->S : 0;
-    const FF den = ff_from_u64(a.reduction == GRPO_TOKEN_MEAN ? (N > 0 ? N : 1) : (S > 0 ? S : 1));
+    const FF den = a.reduction == GRPO_FIXED_CONSTANT
+                       ? FF{a.norm_c, 0.f}
+                       : ff_from_u64(a.reduction == GRPO_TOKEN_MEAN ? (N > 0 ? N : 1) : (S > 0 ? S : 1));
     P = ff_div(P, den);
     K = ff_div(K, den);
     float o0 = ff_float(ff_add(P, ff_scale(K, a.beta))), o1 = ff_float(P), o2 = ff_float(K);
@@ -541,6 +570,8 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
     a.out3[0] = o0;
     a.out3[1] = o1;
     a.out3[2] = o2;
+    if (a.counts_out)  // every CTA added its counts before taking its ticket
+      for (int j = 0; j < 3; ++j) a.counts_out[j] = __ldcg(&a.hdr->clip[j]);
   }
 }
 

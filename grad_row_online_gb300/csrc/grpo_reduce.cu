@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs
     block_sum<double, 2>(v, s_d);
     if (threadIdx.x == 0) {
       const int L = a.L[i];
-      const double P = v[0] - a.A[i] * (double)L;
+      const double P = a.split_A ? v[0] - a.A[i] * (double)L : v[0];
       a.seq[i] = P;
       a.seq[a.B + i] = v[1];
       if (a.per_seq) {
@@ -63,14 +63,17 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs
   if (threadIdx.x == 0) {
     // N = active tokens, S = live sequences, as prep counted them
     const long long N = a.B > 0 ? a.hdr->N : 0, S = a.B > 0 ? a.hdr->S : 0;
-    const double den = a.reduction == GRPO_TOKEN_MEAN ? (double)(N > 0 ? N : 1)
-                                                      : (double)(S > 0 ? S : 1);
+    const double den = a.reduction == GRPO_TOKEN_MEAN      ? (double)(N > 0 ? N : 1)
+                       : a.reduction == GRPO_SEQUENCE_MEAN ? (double)(S > 0 ? S : 1)
+                                                           : (double)a.norm_c;
     const double P = u[0] / den, K = u[1] / den;
     float o0 = (float)(P + (double)a.beta * K), o1 = (float)P, o2 = (float)K;
     if (((volatile unsigned*)&a.hdr->status)[0] != 0u) o0 = o1 = o2 = NAN;
     a.out3[0] = o0;
     a.out3[1] = o1;
     a.out3[2] = o2;
+    if (a.counts_out)  // every row kernel CTA added its counts before this launch
+      for (int j = 0; j < 3; ++j) a.counts_out[j] = a.hdr->clip[j];
   }
 }
 

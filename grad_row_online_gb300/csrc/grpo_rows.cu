@@ -305,9 +305,12 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(cons
   }
   __syncthreads();
   const long long N = s_NS[0], S = s_NS[1];
-  // token weight: 1/max(N,1) (token mean) or 1/(max(S,1) L_i) (sequence mean)
-  const double c_tok = 1.0 / (double)(N > 0 ? N : 1);
+  // token weight: 1/max(N,1) (token mean), 1/(max(S,1) L_i) (sequence mean)
+  // or 1/C (fixed constant)
+  const double c_tok = a.reduction == GRPO_FIXED_CONSTANT ? 1.0 / (double)a.norm_c
+                                                          : 1.0 / (double)(N > 0 ? N : 1);
   const double inv_S = 1.0 / (double)(S > 0 ? S : 1);
+  unsigned n_clip[3] = {0u, 0u, 0u};  // thread 0: this CTA's clipped rows
   const int64_t BT = a.B * a.T;
   const bool want_grad = a.grad != nullptr;
   const bool zero_masked = want_grad && !(a.flags & GRPO_SKIP_MASKED_GRAD_ROWS);
@@ -342,7 +345,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(cons
         ya = Storage<T>::load1(y + act);
         o = __ldg(a.old + row);
         Ab = a.A[b];
-        c = a.reduction == GRPO_TOKEN_MEAN ? c_tok : inv_S / (double)a.L[b];
+        c = a.reduction == GRPO_SEQUENCE_MEAN ? inv_S / (double)a.L[b] : c_tok;
       }
 
       // sweep 1, the block combine, the fast finish
@@ -391,6 +394,9 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(cons
         a.slot_p[row] = s_rs.q;
         a.slot_k[row] = s_rs.k;
         if (a.logps_out) a.logps_out[row] = (float)s_rs.logp;
+        if (s_rs.clip == 1) ++n_clip[0];
+        else if (s_rs.clip == 2) ++n_clip[1];
+        else if (s_rs.clip == 3) ++n_clip[2];
       }
       if (want_grad) {
         const RowScalars rs = s_rs;
@@ -405,6 +411,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(cons
     __syncthreads();
     row = s_next;
   }
+  if (threadIdx.x == 0) add_clip_counts(a.hdr, n_clip);
 }
 
 template <typename T>

@@ -38,6 +38,7 @@ struct RowScalars {
   float wneg;         // -w as float
   float ga;           // gradient at the action element
   int precise;      // bit 0: policy row refined, bit 1: reference row refined
+  int clip;         // 0, or the clip that bound: 1 upper, 2 lower, 3 dual
 };
 
 // vector geometry of a row: `head` scalars up to the first 16-byte boundary,
@@ -145,26 +146,30 @@ __device__ __forceinline__ RowScalars finish_fast(const RowArgs& a, float MLp, F
   const float emd = expm1f(d);
   const float emlp = expm1f(lpf);
   const float ratio = __fadd_rn(1.0f, rm1);
-  const float lo_b = -a.eps_lo, hi_b = a.eps_hi;  // bounds on r - 1
-  const float unc = __fmul_rn(rm1, A);
-  const float cl = __fmul_rn(fminf(fmaxf(rm1, lo_b), hi_b), A);
-  const bool clipped = (A > 0.f && rm1 > hi_b) || (A < 0.f && rm1 < lo_b);
-  const float gpol = clipped ? 0.f : -__fmul_rn(A, ratio);
+  const TokEpi<float> t = token_epilogue<float>(rm1, lpf, d, emd, k3_from(d, emd), true, A, a.var);
   const float gc = __fmul_rn(a.grad_scale, c);
-  const float w = __fmul_rn(gc, __fmaf_rn(-a.beta, emd, gpol));
+  const float w = __fmul_rn(gc, t.g);
   r.lse_p = (double)lse_p.hi + (double)lse_p.lo;
-  r.q = (double)(-fminf(unc, cl));
-  r.k = (double)k3_from(d, emd);
+  r.q = (double)t.q;
+  r.k = (double)t.k;
   r.logp = (double)lp.hi + (double)lp.lo;
   r.w = (double)w;
   r.wneg = -w;
   r.LL = ff_float(Pp);
   r.ga = -__fmul_rn(w, emlp);
   r.precise = 0;
+  r.clip = t.clip;
   if (want_grad && a.precise_ok) {
-    const float s_ref = fabsf(gc) * a.beta * (1.0f + emd);
+    // sensitivities of w to the two rows' logsumexp: the KL part's slope
+    // (both rows), the policy part's |A| r (policy row), w itself (p_a)
+    const float s_ref = fabsf(gc) * a.beta * kl_slope(a.var.kl_type, emd);
     const float s_pol = fabsf(w) + fabsf(gc) * fabsf(A) * ratio + s_ref;
     r.precise = (s_pol * kFastErrBound > kTau ? 1 : 0) | (s_ref * kFastErrBound > kTau ? 2 : 0);
+    // k1's value is d itself (and k2's gradient is d): an error in one row's
+    // logsumexp enters the KL term at full weight and, summed over tokens of
+    // either sign, is not damped; refining the policy row alone would leave
+    // the reference row's rounding in d uncancelled, so both rows go together
+    if ((r.precise & 1) && a.var.kl_type != GRPO_KL_K3) r.precise |= 2;
   }
   return r;
 }
@@ -193,23 +198,18 @@ static __device__ __forceinline__ RowScalars finish_precise(const RowArgs& a, do
   const double emd = __shfl_sync(0xFFFFFFFFu, em, 1);
   const double emlp = __shfl_sync(0xFFFFFFFFu, em, 2);
   RowScalars r;
-  const double ratio = 1.0 + rm1;
-  const double lo_b = -(double)a.eps_lo, hi_b = (double)a.eps_hi;
-  const double unc = rm1 * A;
-  const double rc = rm1 < lo_b ? lo_b : (rm1 > hi_b ? hi_b : rm1);
-  const double cl = rc * A;
-  const bool clipped = (A > 0.0 && rm1 > hi_b) || (A < 0.0 && rm1 < lo_b);
-  const double gpol = clipped ? 0.0 : -A * ratio;
-  const double w = (double)a.grad_scale * c * (gpol - (double)a.beta * emd);
+  const TokEpi<double> t = token_epilogue<double>(rm1, lp, d, emd, emd - d, true, A, a.var);
+  const double w = (double)a.grad_scale * c * t.g;
   r.lse_p = lse_p;
-  r.q = -(unc < cl ? unc : cl);
-  r.k = emd - d;
+  r.q = t.q;
+  r.k = t.k;
   r.logp = lp;
   r.w = w;
   r.wneg = (float)(-w);
   r.LL = (float)(lse_p * (double)kLog2e);
   r.ga = (float)(-w * emlp);
   r.precise = 1;
+  r.clip = t.clip;
   return r;
 }
 

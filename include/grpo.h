@@ -59,7 +59,7 @@ typedef enum {
   GRPO_ERR_ALIGN = 4,      /* a pointer is not aligned to its element size, or
                               the workspace is not 256-byte aligned */
   GRPO_ERR_GROUP_SPEC = 5, /* not exactly one of samples_per_prompt / boundaries */
-  GRPO_ERR_PARAM = 6,      /* eps / beta / adv_eps / grad_scale / reduction invalid */
+  GRPO_ERR_PARAM = 6,      /* eps / beta / adv_eps / grad_scale / reduction / variant invalid */
   GRPO_ERR_WORKSPACE = 7,  /* ws_bytes < grpo_workspace_size(...) */
   GRPO_ERR_CUDA = 8,       /* a CUDA launch failed */
   /* device-detected; bits of the status word (grpo_read_device_status) */
@@ -71,7 +71,30 @@ typedef enum {
 
 typedef enum { GRPO_F32 = 0, GRPO_BF16 = 1, GRPO_F16 = 2 } grpo_dtype_t;
 
-typedef enum { GRPO_TOKEN_MEAN = 0, GRPO_SEQUENCE_MEAN = 1 } grpo_reduction_t;
+/* Normaliser ("Normalizer semantics"): the global active-token count, the
+ * per-sequence count then the mean over live sequences, or a declared
+ * constant (the Dr.GRPO form, independent of the mask). */
+typedef enum {
+  GRPO_TOKEN_MEAN = 0,
+  GRPO_SEQUENCE_MEAN = 1,
+  GRPO_FIXED_CONSTANT = 2 /* c = 1 / grpo_params_t.norm_constant for every active token */
+} grpo_reduction_t;
+
+/* Reference-KL estimator (dockyard_rl "Reference-KL penalty"; Relax
+ * "REINFORCE++" and "REINFORCE++-baseline"), d = ref_logp - logp; the
+ * gradient is the pathwise derivative of each formula. */
+typedef enum {
+  GRPO_KL_K3 = 0, /* e^d - d - 1 (low-variance, unbiased)     d/dlogp: 1 - e^d */
+  GRPO_KL_K1 = 1, /* logp - ref_logp (the log ratio)          d/dlogp: 1 */
+  GRPO_KL_K2 = 2  /* (logp - ref_logp)^2 / 2                  d/dlogp: logp - ref_logp */
+} grpo_kl_t;
+
+/* Policy surrogate (dockyard_rl "One loss, many algorithms", "CISPO"). */
+typedef enum {
+  GRPO_SURROGATE_CLIP = 0, /* -min(r A, clip(r) A), optionally dual-clipped */
+  GRPO_SURROGATE_CISPO = 1 /* -A sg(clip(r)) logp: every token keeps a gradient
+                              -A clip(r) through logp */
+} grpo_surrogate_t;
 
 /* Flags (grpo_params_t.flags and grpo_group_adv's flags). */
 #define GRPO_ADV_EPS_ADD 1u          /* divide by std + adv_eps instead of max(std, adv_eps) */
@@ -92,13 +115,16 @@ typedef struct {
 
 /* Optional timing hook: when non-NULL, `start` / `stop` (cudaEvent_t handles)
  * are recorded on the stream immediately before and after the main kernel
- * work of a call -- the fused row kernel of grpo_loss_fwd_bwd, the two
- * per-token kernels of grpo_loss_from_logps -- so a caller can time it alone. */
+ * of a call -- the fused row kernel of grpo_loss_fwd_bwd, the per-token
+ * kernel of grpo_loss_from_logps -- so a caller can time it alone. */
 typedef struct {
   void *start;
   void *stop;
 } grpo_profile_t;
 
+/* Call parameters.  Zero-initialising the variant fields (kl_type,
+ * surrogate, dual_clip_c, norm_constant, clip_counts) gives the GRPO loss
+ * of the operator page: the clipped surrogate with k3 and no dual clip. */
 typedef struct {
   float clip_eps_lo;  /* eps_lo, 0 <= eps_lo < 1   (clip_eps on the pages) */
   float clip_eps_hi;  /* eps_hi >= 0                (DAPO clip-higher when > eps_lo) */
@@ -107,8 +133,24 @@ typedef struct {
   float grad_scale;   /* finite; multiplies every gradient (1 = dL/dlogits) */
   int32_t reduction;  /* grpo_reduction_t */
   uint32_t flags;     /* GRPO_ADV_EPS_ADD | GRPO_SKIP_MASKED_GRAD_ROWS */
+  int32_t kl_type;    /* grpo_kl_t */
+  int32_t surrogate;  /* grpo_surrogate_t */
+  float dual_clip_c;  /* 0: off.  > 1: dual clip ("ratio_clip_c", a lower bound
+                         on negative-advantage terms): for A < 0 the objective is
+                         max(min(r A, clip(r) A), c A), whose policy gradient is 0
+                         where r > c.  Only with GRPO_SURROGATE_CLIP. */
+  float norm_constant; /* GRPO_FIXED_CONSTANT: the declared constant, finite and
+                          > 0; ignored by the other reductions */
   int32_t _reserved;
   const grpo_profile_t *profile; /* host pointer or NULL */
+  unsigned long long *clip_counts; /* device [3] or NULL: overwritten with the
+                          number of active tokens clipped at the upper bound,
+                          at the lower bound, and by the dual clip.  Clipped
+                          surrogate: (A > 0, r > 1 + eps_hi), (A < 0,
+                          r < 1 - eps_lo), (A < 0, r > c) -- the tokens whose
+                          policy gradient a clip removes.  CISPO: r > 1 + eps_hi,
+                          r < 1 - eps_lo (the weight clip(r) differs from r),
+                          whatever the sign of A; the third is 0. */
 } grpo_params_t;
 
 /* Bytes of workspace the entry points below need for B sequences of T

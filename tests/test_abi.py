@@ -110,8 +110,19 @@ def test_fwd_rejects_bad_arguments(lib):
     assert _fwd(lib, p=_params(beta=float("nan"))) == 6
     assert _fwd(lib, p=_params(adv_eps=0.0)) == 6
     assert _fwd(lib, p=_params(grad_scale=float("inf"))) == 6
-    assert _fwd(lib, p=_params(reduction=2)) == 6
+    assert _fwd(lib, p=_params(reduction=3)) == 6
     assert _fwd(lib, p=_params(flags=8)) == 6
+    # loss variants
+    assert _fwd(lib, p=_params(reduction=2)) == 6  # fixed constant without a constant
+    assert _fwd(lib, p=_params(reduction=2, norm_constant=-1.0)) == 6
+    assert _fwd(lib, p=_params(reduction=2, norm_constant=float("inf"))) == 6
+    assert _fwd(lib, p=_params(kl_type=3)) == 6
+    assert _fwd(lib, p=_params(kl_type=-1)) == 6
+    assert _fwd(lib, p=_params(surrogate=2)) == 6
+    assert _fwd(lib, p=_params(dual_clip_c=1.0)) == 6  # c must exceed 1
+    assert _fwd(lib, p=_params(dual_clip_c=float("nan"))) == 6
+    assert _fwd(lib, p=_params(surrogate=1, dual_clip_c=3.0)) == 6  # not with CISPO
+    assert _fwd(lib, p=_params(clip_counts=FAKE + 4)) == 4  # misaligned counter array
     assert _fwd(lib, dt=1, policy=FAKE + 1) == 4      # bf16 pointer not 2-byte aligned
     assert _fwd(lib, act=FAKE + 4) == 4               # int64 ids
     assert _fwd(lib, ws=FAKE + 16) == 4               # workspace alignment
