@@ -22,7 +22,8 @@ import torch
 from . import _build
 
 __all__ = ["grpo_workspace_size", "grpo_group_adv", "grpo_loss_fwd_bwd", "grpo_loss_fwd_bwd_static",
-           "grpo_loss_from_logps",
+           "grpo_loss_from_logps", "grpo_count_active", "grpo_loss_finalize", "Shard",
+           "totals_buffer", "SEQ_TOTAL_BYTES",
            "grpo_read_device_status", "grpo_status_string", "GrpoError", "library_path",
            "GRPO_ADV_EPS_ADD", "GRPO_SKIP_MASKED_GRAD_ROWS"]
 
@@ -32,6 +33,27 @@ _DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 _REDUCTIONS = {"token_mean": 0, "sequence_mean": 1, "fixed_constant": 2}
 _KL_TYPES = {"k3": 0, "k1": 1, "k2": 2}
 _SURROGATES = {"clip": 0, "cispo": 1}
+
+
+SEQ_TOTAL_BYTES = 32  # one grpo_seq_total_t record
+
+
+class Shard:
+    """A data-parallel shard of the batch: the call's token arguments cover
+    sequences [seq_begin, seq_begin + B) of a batch whose rewards and groups
+    are passed whole; ``global_counts`` (int64 [2] on the device: N, S of
+    the batch) sets the token weights, and the call writes its per-sequence
+    totals into ``totals`` (``totals_buffer(B)``) instead of the loss."""
+
+    def __init__(self, seq_begin: int, global_counts: torch.Tensor, totals: torch.Tensor):
+        self.seq_begin = int(seq_begin)
+        self.global_counts = global_counts
+        self.totals = totals
+
+
+def totals_buffer(B: int, device="cuda") -> torch.Tensor:
+    """Device memory for B per-sequence total records (uint8 [B, 32])."""
+    return torch.empty((B, SEQ_TOTAL_BYTES), dtype=torch.uint8, device=device)
 
 
 class GrpoError(RuntimeError):
@@ -50,6 +72,11 @@ class _Profile(ctypes.Structure):
     _fields_ = [("start", ctypes.c_void_p), ("stop", ctypes.c_void_p)]
 
 
+class _Shard(ctypes.Structure):
+    _fields_ = [("seq_begin", ctypes.c_int64), ("global_counts", ctypes.c_void_p),
+                ("totals_out", ctypes.c_void_p)]
+
+
 class _Params(ctypes.Structure):
     _fields_ = [("clip_eps_lo", ctypes.c_float), ("clip_eps_hi", ctypes.c_float),
                 ("beta", ctypes.c_float), ("adv_eps", ctypes.c_float),
@@ -57,7 +84,8 @@ class _Params(ctypes.Structure):
                 ("flags", ctypes.c_uint32), ("kl_type", ctypes.c_int32),
                 ("surrogate", ctypes.c_int32), ("dual_clip_c", ctypes.c_float),
                 ("norm_constant", ctypes.c_float), ("_reserved", ctypes.c_int32),
-                ("profile", ctypes.POINTER(_Profile)), ("clip_counts", ctypes.c_void_p)]
+                ("profile", ctypes.POINTER(_Profile)), ("shard", ctypes.POINTER(_Shard)),
+                ("clip_counts", ctypes.c_void_p)]
 
 
 _lib = None
@@ -91,6 +119,10 @@ def lib():
         L.grpo_loss_from_logps.argtypes = [vp, vp, vp, vp, i64, i64, vp, ctypes.POINTER(_Groups),
                                            ctypes.POINTER(_Params), vp, vp, vp, vp, vp, sz, vp]
         L.grpo_loss_from_logps.restype = ctypes.c_int
+        L.grpo_count_active.argtypes = [vp, i64, i64, vp, vp]
+        L.grpo_count_active.restype = ctypes.c_int
+        L.grpo_loss_finalize.argtypes = [vp, i64, vp, ctypes.POINTER(_Params), vp, vp]
+        L.grpo_loss_finalize.restype = ctypes.c_int
         L.grpo_read_device_status.argtypes = [vp, vp]
         L.grpo_read_device_status.restype = ctypes.c_int
         L.grpo_status_string.argtypes = [ctypes.c_int]
@@ -139,8 +171,14 @@ def _groups(B: int, samples_per_prompt: int, group_boundaries) -> tuple[_Groups,
 
 
 def _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction, flags, profile,
-            kl="k3", surrogate="clip", dual_clip_c=None, norm_constant=None, clip_counts=None):
+            kl="k3", surrogate="clip", dual_clip_c=None, norm_constant=None, clip_counts=None,
+            shard: Optional[Shard] = None):
     p = _Params()
+    if shard is not None:
+        _dev(shard.global_counts, "global_counts", torch.int64)
+        _dev(shard.totals, "totals", torch.uint8)
+        p._shard = _Shard(shard.seq_begin, shard.global_counts.data_ptr(), shard.totals.data_ptr())
+        p.shard = ctypes.pointer(p._shard)
     p.kl_type = _KL_TYPES[kl]
     p.surrogate = _SURROGATES[surrogate]
     p.dual_clip_c = float(dual_clip_c or 0.0)
@@ -210,7 +248,7 @@ def grpo_loss_fwd_bwd(policy_logits: torch.Tensor, ref_logits: torch.Tensor,
                       workspace: Optional[torch.Tensor] = None, stream=None,
                       profile=None, kl: str = "k3", surrogate: str = "clip",
                       dual_clip_c: Optional[float] = None, norm_constant: Optional[float] = None,
-                      want_clip_counts: bool = False) -> dict:
+                      want_clip_counts: bool = False, shard: Optional[Shard] = None) -> dict:
     """Fused GRPO loss forward + dL/dlogits.
 
     ``grad``: True (allocate), a tensor to write into (may be
@@ -221,7 +259,9 @@ def grpo_loss_fwd_bwd(policy_logits: torch.Tensor, ref_logits: torch.Tensor,
     tensors: ``out3`` ([loss, policy_loss, kl]), ``loss``, ``policy_loss``,
     ``kl`` (0-d views), ``grad``, and the optional ``per_seq`` [3,B],
     ``logps`` [B,T], ``adv`` [B], ``clip_counts`` [3] (int64: clipped at the
-    upper bound, at the lower bound, by the dual clip)."""
+    upper bound, at the lower bound, by the dual clip).  With ``shard``
+    (see ``Shard``) ``rewards`` and the groups span the whole batch, the
+    token tensors the shard's sequences, and ``out3`` is not written."""
     if policy_logits.dtype not in _DTYPES:
         raise ValueError(f"unsupported logits dtype {policy_logits.dtype}")
     _dev(policy_logits, "policy_logits")
@@ -239,15 +279,16 @@ def grpo_loss_fwd_bwd(policy_logits: torch.Tensor, ref_logits: torch.Tensor,
         raise ValueError("completion_mask must be bool or uint8")
     if action_ids.shape != (B, T) or old_logps.shape != (B, T) or mask.shape != (B, T):
         raise ValueError("action_ids, old_logps and completion_mask must be [B, T]")
-    if rewards.shape != (B,):
+    if shard is None and rewards.shape != (B,):
         raise ValueError("rewards must be [B]")
     dev = policy_logits.device
-    g, keep = _groups(B, samples_per_prompt, group_boundaries)
+    g, keep = _groups(rewards.numel() if shard is not None else B, samples_per_prompt,
+                      group_boundaries)
     counts = torch.empty(3, dtype=torch.int64, device=dev) if want_clip_counts else None
     p, prof = _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction,
                       (GRPO_ADV_EPS_ADD if eps_add else 0)
                       | (GRPO_SKIP_MASKED_GRAD_ROWS if skip_masked_grad_rows else 0), profile,
-                      kl, surrogate, dual_clip_c, norm_constant, counts)
+                      kl, surrogate, dual_clip_c, norm_constant, counts, shard)
     if grad is True:
         grad_t = torch.empty_like(policy_logits)
     elif grad is None or grad is False:
@@ -260,7 +301,7 @@ def grpo_loss_fwd_bwd(policy_logits: torch.Tensor, ref_logits: torch.Tensor,
     per_seq = torch.empty((3, B), dtype=torch.float32, device=dev) if want_per_seq else None
     logps = torch.empty((B, T), dtype=torch.float32, device=dev) if want_logps else None
     adv = torch.empty(B, dtype=torch.float32, device=dev) if want_adv else None
-    ws, need = _workspace(B, T, 0, workspace, dev)
+    ws, need = _workspace(rewards.numel() if shard is not None else B, T, 0, workspace, dev)
     rc = lib().grpo_loss_fwd_bwd(_ptr(policy_logits), _ptr(ref_logits), _DTYPES[policy_logits.dtype],
                                  B, T, V, _ptr(action_ids), _ptr(old_logps), _ptr(mask),
                                  _ptr(rewards), ctypes.byref(g), ctypes.byref(p), _ptr(grad_t),
@@ -309,9 +350,9 @@ def grpo_loss_from_logps(logps: torch.Tensor, old_logps: torch.Tensor,
                          profile=None, kl: str = "k3", surrogate: str = "clip",
                          dual_clip_c: Optional[float] = None,
                          norm_constant: Optional[float] = None,
-                         want_clip_counts: bool = False) -> dict:
+                         want_clip_counts: bool = False, shard: Optional[Shard] = None) -> dict:
     """GRPO loss from per-token log-probs; ``grad`` gives dL/dlogp [B,T].
-    Variants and outputs as in grpo_loss_fwd_bwd."""
+    Variants, outputs and ``shard`` as in grpo_loss_fwd_bwd."""
     _dev(logps, "logps", torch.float32)
     B, T = logps.shape
     _dev(old_logps, "old_logps", torch.float32)
@@ -322,11 +363,12 @@ def grpo_loss_from_logps(logps: torch.Tensor, old_logps: torch.Tensor,
     if mask.dtype == torch.bool:
         mask = mask.view(torch.uint8)
     dev = logps.device
-    g, keep = _groups(B, samples_per_prompt, group_boundaries)
+    Bg = rewards.numel() if shard is not None else B
+    g, keep = _groups(Bg, samples_per_prompt, group_boundaries)
     counts = torch.empty(3, dtype=torch.int64, device=dev) if want_clip_counts else None
     p, prof = _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction,
                       GRPO_ADV_EPS_ADD if eps_add else 0, profile, kl, surrogate, dual_clip_c,
-                      norm_constant, counts)
+                      norm_constant, counts, shard)
     if grad is True:
         grad_t = torch.empty((B, T), dtype=torch.float32, device=dev)
     elif grad is None or grad is False:
@@ -336,7 +378,7 @@ def grpo_loss_from_logps(logps: torch.Tensor, old_logps: torch.Tensor,
     out3 = torch.empty(3, dtype=torch.float32, device=dev) if out3 is None else out3
     per_seq = torch.empty((3, B), dtype=torch.float32, device=dev) if want_per_seq else None
     adv = torch.empty(B, dtype=torch.float32, device=dev) if want_adv else None
-    ws, need = _workspace(B, T, 0, workspace, dev)
+    ws, need = _workspace(Bg, T, 0, workspace, dev)
     rc = lib().grpo_loss_from_logps(_ptr(logps), _ptr(old_logps), _ptr(ref_logps), _ptr(mask),
                                     B, T, _ptr(rewards), ctypes.byref(g), ctypes.byref(p),
                                     _ptr(grad_t), _ptr(out3), _ptr(per_seq), _ptr(adv), _ptr(ws),
@@ -345,6 +387,36 @@ def grpo_loss_from_logps(logps: torch.Tensor, old_logps: torch.Tensor,
     return {"out3": out3, "loss": out3[0], "policy_loss": out3[1], "kl": out3[2],
             "grad": grad_t, "per_seq": per_seq, "adv": adv, "clip_counts": counts,
             "workspace": ws}
+
+
+def grpo_count_active(completion_mask: torch.Tensor, out: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
+    """N (active tokens) and S (sequences with one) of a [B,T] mask, as an
+    int64 [2] device tensor: a shard's contribution to the batch counts."""
+    mask = _dev(completion_mask, "completion_mask")
+    if mask.dtype == torch.bool:
+        mask = mask.view(torch.uint8)
+    B, T = mask.shape
+    out = torch.empty(2, dtype=torch.int64, device=mask.device) if out is None else out
+    _check(lib().grpo_count_active(_ptr(mask), B, T, _ptr(out), _stream(stream)),
+           "grpo_count_active")
+    return out
+
+
+def grpo_loss_finalize(totals: torch.Tensor, global_counts: torch.Tensor, *, beta: float = 0.04,
+                       reduction="token_mean", norm_constant: Optional[float] = None,
+                       out3: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """[loss, policy_loss, kl] from the whole batch's per-sequence totals
+    (every shard's ``totals`` concatenated in shard order, uint8 [B, 32])
+    and the batch counts -- bit-identical to the unsharded call."""
+    _dev(totals, "totals", torch.uint8)
+    _dev(global_counts, "global_counts", torch.int64)
+    B = totals.shape[0]
+    p, _ = _params(0.2, None, beta, 1e-6, 1.0, reduction, 0, None, norm_constant=norm_constant)
+    out3 = torch.empty(3, dtype=torch.float32, device=totals.device) if out3 is None else out3
+    _check(lib().grpo_loss_finalize(_ptr(totals), B, _ptr(global_counts), ctypes.byref(p),
+                                    _ptr(out3), _stream(stream)), "grpo_loss_finalize")
+    return out3
 
 
 def grpo_read_device_status(workspace: torch.Tensor, stream=None) -> int:

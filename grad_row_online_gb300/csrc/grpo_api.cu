@@ -3,11 +3,14 @@
 //
 // Every host-checkable error is found before the first CUDA call, so a
 // rejected call launches nothing.  A call enqueues, in stream order:
-//   memset of the 16-byte workspace header (status word, row counter)
+//   memset of the workspace header (status word, counters)
 //   prep     group advantages (+ active-token counts)   grpo_prep.cu
 //   rows     fused sweep over vocabulary rows            grpo_rows.cu
 //   reduce   fixed-order reduction to the scalars        grpo_reduce.cu
-// or, for the logps-only boundary, prep + the two kernels of grpo_logps.cu.
+// or, for the logps-only boundary, prep + the kernel of grpo_logps.cu.
+// A shard call (grpo_shard_t) runs the same kernels on its sequences, with
+// the whole batch's groups and counts, and leaves the scalar to
+// grpo_loss_finalize.
 #include <math.h>
 #include <string.h>
 
@@ -113,6 +116,34 @@ const ExpTable& exp_table() {
 
 grpo_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? GRPO_OK : GRPO_ERR_CUDA; }
 
+// A call's place in the batch: the whole batch, or a shard (grpo_shard_t)
+// whose groups and rewards span Bg sequences while its token arguments cover
+// B of them from seq_begin on.
+struct Placement {
+  int64_t Bg = 0, seq_begin = 0;
+  const unsigned long long* NS = nullptr;  // the batch counts, when given
+  SeqTotal* totals = nullptr;              // the shard's records, when sharded
+  bool shard = false;
+};
+grpo_status_t placement_of(const grpo_params_t* p, const grpo_groups_t* g, int64_t B,
+                           Placement* pl) {
+  if (!p->shard) {
+    pl->Bg = B;
+    return GRPO_OK;
+  }
+  const grpo_shard_t* sh = p->shard;
+  pl->shard = true;
+  pl->Bg = g->num_seqs;
+  pl->seq_begin = sh->seq_begin;
+  if (pl->seq_begin < 0 || pl->Bg < 0 || pl->seq_begin > pl->Bg || B > pl->Bg - pl->seq_begin)
+    return GRPO_ERR_SHAPE;
+  if (!sh->global_counts || (B > 0 && !sh->totals_out)) return GRPO_ERR_NULL;
+  if (!aligned(sh->global_counts, 8) || !aligned(sh->totals_out, 16)) return GRPO_ERR_ALIGN;
+  pl->NS = sh->global_counts;
+  pl->totals = reinterpret_cast<SeqTotal*>(sh->totals_out);
+  return GRPO_OK;
+}
+
 }  // namespace
 
 extern "C" size_t grpo_workspace_size(int64_t B, int64_t T, int64_t num_groups) {
@@ -142,8 +173,9 @@ extern "C" grpo_status_t grpo_group_adv(const float* rewards, const grpo_groups_
   const WsLayout lay(B, 0);
   WsHeader* hdr = (WsHeader*)w;
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return GRPO_ERR_CUDA;
-  PrepArgs pa{rewards, bounds, B, 0, G, spp, adv_eps, (int)(flags & GRPO_ADV_EPS_ADD),
-              nullptr, 0, (double*)(w + lay.off_A), nullptr, adv_out, nullptr, nullptr, hdr};
+  PrepArgs pa{rewards, bounds, B, 0, G, B, 0, &hdr->N, spp, adv_eps,
+              (int)(flags & GRPO_ADV_EPS_ADD), nullptr, 0, (double*)(w + lay.off_A), nullptr,
+              adv_out, nullptr, nullptr, hdr};
   return cuda_status(launch_prep(pa, s));
 }
 
@@ -155,37 +187,42 @@ extern "C" grpo_status_t grpo_loss_fwd_bwd(
     float* logps_out, float* adv_out, void* ws, size_t ws_bytes, void* stream) {
   if (dt != GRPO_F32 && dt != GRPO_BF16 && dt != GRPO_F16) return GRPO_ERR_DTYPE;
   if (B < 0 || T < 0 || V < 1) return GRPO_ERR_SHAPE;
-  if (!out3 || !params || !groups) return GRPO_ERR_NULL;
+  if (!params || !groups) return GRPO_ERR_NULL;
   const bool any_rows = B > 0 && T > 0;
   if (any_rows && (!policy_logits || !ref_logits || !action_ids || !old_logps ||
                    !completion_mask))
     return GRPO_ERR_NULL;
-  if (B > 0 && !rewards) return GRPO_ERR_NULL;
   grpo_status_t st = check_params(params);
   if (st != GRPO_OK) return st;
+  Placement pl;
+  if ((st = placement_of(params, groups, B, &pl)) != GRPO_OK) return st;
+  if (!out3 && !pl.shard) return GRPO_ERR_NULL;
+  if (pl.Bg > 0 && !rewards) return GRPO_ERR_NULL;
   int32_t spp;
   const int64_t* bounds;
   int64_t G;
-  if ((st = check_groups(groups, B, &spp, &bounds, &G)) != GRPO_OK) return st;
+  if ((st = check_groups(groups, pl.Bg, &spp, &bounds, &G)) != GRPO_OK) return st;
   const size_t es = elem_size(dt);
   if (!aligned(policy_logits, es) || !aligned(ref_logits, es) || !aligned(grad_logits, es) ||
       !aligned(action_ids, 8) || !aligned(old_logps, 4) || !aligned(rewards, 4) ||
       !aligned(out3, 4) || !aligned(per_seq, 4) || !aligned(logps_out, 4) ||
       !aligned(adv_out, 4))
     return GRPO_ERR_ALIGN;
-  if ((st = check_ws(ws, ws_bytes, B, T)) != GRPO_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, pl.Bg, T)) != GRPO_OK) return st;
 
   cudaStream_t s = (cudaStream_t)stream;
   char* w = (char*)ws;
-  const WsLayout lay(B, T);
+  const WsLayout lay(pl.Bg, T);
   WsHeader* hdr = (WsHeader*)w;
   int32_t* L = (int32_t*)(w + lay.off_L);
-  double* A = (double*)(w + lay.off_A);
+  double* A = (double*)(w + lay.off_A);  // [Bg]: every group's advantages
   double* slot_p = (double*)(w + lay.off_slots);
   double* slot_k = slot_p + B * T;
+  const unsigned long long* NS = pl.NS ? pl.NS : &hdr->N;
+  SeqTotal* totals = pl.shard ? pl.totals : (SeqTotal*)(w + lay.off_seq);
 
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return GRPO_ERR_CUDA;
-  PrepArgs pa{rewards, bounds, B, T, G, spp, params->adv_eps,
+  PrepArgs pa{rewards, bounds, B, T, G, pl.Bg, pl.seq_begin, &hdr->N, spp, params->adv_eps,
               (int)(params->flags & GRPO_ADV_EPS_ADD), completion_mask, 1, A, nullptr, adv_out, L,
               nullptr, hdr};
   cudaError_t e = launch_prep(pa, s);
@@ -200,11 +237,12 @@ extern "C" grpo_status_t grpo_loss_fwd_bwd(
     ra.old = old_logps;
     ra.mask = completion_mask;
     ra.L = L;
-    ra.A = A;
+    ra.A = A + pl.seq_begin;
     ra.slot_p = slot_p;
     ra.slot_k = slot_k;
     ra.logps_out = logps_out;
     ra.hdr = hdr;
+    ra.NS = NS;
     ra.B = B;
     ra.T = T;
     ra.V = V;
@@ -221,10 +259,10 @@ extern "C" grpo_status_t grpo_loss_fwd_bwd(
     e = launch_rows(ra, dt, params->profile, s);
     if (e != cudaSuccess) return GRPO_ERR_CUDA;
   }
-  ReduceArgs rd{completion_mask, L, A, (double*)(w + lay.off_seq), slot_p, slot_k, B, T,
-                params->beta, params->reduction, hdr, out3, per_seq,
+  ReduceArgs rd{completion_mask, L, A + pl.seq_begin, totals, slot_p, slot_k, B, T,
+                params->beta, params->reduction, hdr, NS, out3, per_seq,
                 variant_of(params).splits_A() ? 1 : 0, params->norm_constant,
-                params->clip_counts};
+                params->clip_counts, pl.shard ? 1 : 0};
   return cuda_status(launch_reduce(rd, s));
 }
 
@@ -237,42 +275,75 @@ extern "C" grpo_status_t grpo_loss_from_logps(const float* logps, const float* o
                                               float* out3, float* per_seq, float* adv_out,
                                               void* ws, size_t ws_bytes, void* stream) {
   if (B < 0 || T < 0) return GRPO_ERR_SHAPE;
-  if (!out3 || !params || !groups) return GRPO_ERR_NULL;
+  if (!params || !groups) return GRPO_ERR_NULL;
   grpo_status_t st = check_params(params);
   if (st != GRPO_OK) return st;
   const bool any_rows = B > 0 && T > 0;
   if (any_rows && (!logps || !old_logps || !completion_mask)) return GRPO_ERR_NULL;
   if (any_rows && !ref_logps && params->beta != 0.f) return GRPO_ERR_NULL;
-  if (B > 0 && !rewards) return GRPO_ERR_NULL;
+  Placement pl;
+  if ((st = placement_of(params, groups, B, &pl)) != GRPO_OK) return st;
+  if (!out3 && !pl.shard) return GRPO_ERR_NULL;
+  if (pl.Bg > 0 && !rewards) return GRPO_ERR_NULL;
   int32_t spp;
   const int64_t* bounds;
   int64_t G;
-  if ((st = check_groups(groups, B, &spp, &bounds, &G)) != GRPO_OK) return st;
+  if ((st = check_groups(groups, pl.Bg, &spp, &bounds, &G)) != GRPO_OK) return st;
   if (!aligned(logps, 4) || !aligned(old_logps, 4) || !aligned(ref_logps, 4) ||
       !aligned(rewards, 4) || !aligned(grad_logps, 4) || !aligned(out3, 4) ||
       !aligned(per_seq, 4) || !aligned(adv_out, 4))
     return GRPO_ERR_ALIGN;
-  if ((st = check_ws(ws, ws_bytes, B, T)) != GRPO_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, pl.Bg, T)) != GRPO_OK) return st;
 
   cudaStream_t s = (cudaStream_t)stream;
   char* w = (char*)ws;
-  const WsLayout lay(B, T);
+  const WsLayout lay(pl.Bg, T);
   WsHeader* hdr = (WsHeader*)w;
   int32_t* L = (int32_t*)(w + lay.off_L);
-  double* A = (double*)(w + lay.off_A);
-  float2* Aff = (float2*)(w + lay.off_Aff);
+  double* A = (double*)(w + lay.off_A);     // [Bg]: every group's advantages
+  float2* Aff = (float2*)(w + lay.off_Aff);  // [Bg]
   int2* rng = (int2*)(w + lay.off_rng);
-  float4* seq = (float4*)(w + lay.off_seq);
+  const unsigned long long* NS = pl.NS ? pl.NS : &hdr->N;
+  SeqTotal* totals = pl.shard ? pl.totals : (SeqTotal*)(w + lay.off_seq);
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return GRPO_ERR_CUDA;
-  PrepArgs pa{rewards, bounds, B, T, G, spp, params->adv_eps,
+  PrepArgs pa{rewards, bounds, B, T, G, pl.Bg, pl.seq_begin, &hdr->N, spp, params->adv_eps,
               (int)(params->flags & GRPO_ADV_EPS_ADD), completion_mask, 1, A, Aff, adv_out, L,
               rng, hdr};
   if (launch_prep(pa, s) != cudaSuccess) return GRPO_ERR_CUDA;
-  LogpsArgs la{logps, old_logps, ref_logps, completion_mask, A, Aff, rng, L, seq, grad_logps, out3,
+  LogpsArgs la{logps, old_logps, ref_logps, completion_mask, A + pl.seq_begin,
+               Aff + pl.seq_begin, rng, L, totals, grad_logps, out3,
                per_seq, hdr, B, T, params->clip_eps_lo, params->clip_eps_hi, params->beta,
                params->grad_scale, params->reduction, variant_of(params),
-               params->norm_constant, params->clip_counts};
+               params->norm_constant, params->clip_counts, NS, pl.shard ? 1 : 0};
   return cuda_status(launch_logps(la, params->profile, s));
+}
+
+extern "C" grpo_status_t grpo_count_active(const uint8_t* completion_mask, int64_t B, int64_t T,
+                                           unsigned long long* counts_out, void* stream) {
+  if (B < 0 || T < 0) return GRPO_ERR_SHAPE;
+  if (!counts_out || (B > 0 && T > 0 && !completion_mask)) return GRPO_ERR_NULL;
+  if (!aligned(counts_out, 8)) return GRPO_ERR_ALIGN;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemsetAsync(counts_out, 0, 2 * sizeof(unsigned long long), s) != cudaSuccess)
+    return GRPO_ERR_CUDA;
+  PrepArgs pa{nullptr, nullptr, B, T, 0, B, 0, counts_out, 0, 1.f, 0, completion_mask, 1,
+              nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  return cuda_status(launch_prep(pa, s));
+}
+
+extern "C" grpo_status_t grpo_loss_finalize(const grpo_seq_total_t* totals, int64_t B,
+                                            const unsigned long long* global_counts,
+                                            const grpo_params_t* params, float* out3,
+                                            void* stream) {
+  if (B < 0) return GRPO_ERR_SHAPE;
+  if (!params || !out3 || !global_counts || (B > 0 && !totals)) return GRPO_ERR_NULL;
+  grpo_status_t st = check_params(params);
+  if (st != GRPO_OK) return st;
+  if (!aligned(totals, 16) || !aligned(global_counts, 8) || !aligned(out3, 4))
+    return GRPO_ERR_ALIGN;
+  return cuda_status(launch_finalize(reinterpret_cast<const SeqTotal*>(totals), B, global_counts,
+                                     params->reduction, params->norm_constant, params->beta,
+                                     out3, (cudaStream_t)stream));
 }
 
 extern "C" grpo_status_t grpo_read_device_status(const void* ws, void* stream) {

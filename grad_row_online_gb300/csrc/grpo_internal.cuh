@@ -21,9 +21,9 @@ namespace grpo {
 //   Aff      float2[B]        the same advantages as float pairs (hi, lo)
 //   range    int2[B]          first active token and last active token + 1
 //                             ({0, 0} for an empty sequence)
-//   seq      double[2B]       per-sequence policy / KL totals (logits path);
-//                             the logps path keeps float-pair totals there,
-//                             float4 {P.hi, P.lo, K.hi, K.lo} per sequence
+//   seq      SeqTotal[B]      per-sequence totals (the records of
+//                             grpo_seq_total_t: double totals on the logits
+//                             path, float pairs on the logps path)
 //   slots    double[2 B T]    per-token policy / KL terms (logits path)
 // ----------------------------------------------------------------------------
 struct WsHeader {
@@ -45,7 +45,7 @@ struct WsLayout {
     off_Aff = off_A + align256(sizeof(double) * (size_t)B);
     off_rng = off_Aff + align256(sizeof(float) * 2 * (size_t)B);
     off_seq = off_rng + align256(sizeof(int32_t) * 2 * (size_t)B);
-    off_slots = off_seq + align256(sizeof(double) * 2 * (size_t)B);
+    off_slots = off_seq + align256((size_t)32 * (size_t)B);
     total = off_slots + align256(sizeof(double) * 2 * (size_t)B * (size_t)T);
   }
 };
@@ -370,40 +370,6 @@ __device__ __forceinline__ float block_max(float v, float* scratch) {
   return warp_max(x);
 }
 
-// This thread's share of the level-2 sums over the B sequence totals
-// (seq[0..B) policy, seq[B..2B) KL), in a fixed order: the token mean and
-// the fixed constant add the totals, the sequence mean adds total / L_i over
-// live sequences.  The
-// totals were written by other CTAs of the same launch (made visible by
-// their __threadfence before the ticket), so they are read from L2 (ld.cg),
-// eight at a time to keep the loads in flight.
-__device__ __forceinline__ void seq_totals(const double* seq, const int32_t* Ls, int64_t B,
-                                           int reduction, double (&u)[2]) {
-  constexpr int kBatch = 8;
-  const int64_t stride = blockDim.x;
-  for (int64_t j0 = threadIdx.x; j0 < B; j0 += kBatch * stride) {
-    double P[kBatch], K[kBatch];
-    int L[kBatch];
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int64_t j = j0 + k * stride;
-      P[k] = j < B ? __ldcg(seq + j) : 0.0;
-      K[k] = j < B ? __ldcg(seq + B + j) : 0.0;
-      L[k] = j < B ? __ldcg(Ls + j) : 0;
-    }
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      if (reduction != GRPO_SEQUENCE_MEAN) {
-        u[0] += P[k];
-        u[1] += K[k];
-      } else if (L[k] > 0) {
-        u[0] += P[k] / (double)L[k];
-        u[1] += K[k] / (double)L[k];
-      }
-    }
-  }
-}
-
 // ----------------------------------------------------------------------------
 // the per-token epilogue and its variants
 // ----------------------------------------------------------------------------
@@ -498,12 +464,167 @@ __device__ __forceinline__ void add_clip_counts(WsHeader* hdr, const unsigned (&
 }
 
 // ----------------------------------------------------------------------------
+// per-sequence totals and the final scalar
+// ----------------------------------------------------------------------------
+// One sequence's totals (grpo_seq_total_t, 32 bytes).  kind 1: P, K as
+// doubles (logits path); kind 2: P and K as float pairs in the first 16
+// bytes (logps path).
+struct __align__(16) SeqTotal {
+  double P, K;
+  long long L;
+  int kind;
+  int pad;
+};
+static_assert(sizeof(SeqTotal) == 32, "grpo_seq_total_t is 32 bytes");
+enum : int { kTotalsDouble = 1, kTotalsFF = 2 };
+
+__device__ __forceinline__ void put_total(SeqTotal* r, double P, double K, int L) {
+  SeqTotal t;
+  t.P = P;
+  t.K = K;
+  t.L = L;
+  t.kind = kTotalsDouble;
+  t.pad = 0;
+  *r = t;
+}
+__device__ __forceinline__ void put_total(SeqTotal* r, FF P, FF K, int L) {
+  uint4* q = reinterpret_cast<uint4*>(r);
+  q[0] = make_uint4(__float_as_uint(P.hi), __float_as_uint(P.lo), __float_as_uint(K.hi),
+                    __float_as_uint(K.lo));
+  q[1] = make_uint4((unsigned)L, 0u, (unsigned)kTotalsFF, 0u);
+}
+
+// The final scalar from B records, by the first kFinalThreads threads of a
+// CTA (every thread of the CTA calls it: it holds __syncthreads).  Each
+// thread takes records j = t, t + 128, ... in index order (loads batched
+// eight at a time, from L2: the records may come from other CTAs of the
+// same launch), then a fixed xor tree per warp and the four warps in index
+// order.  The token mean and the fixed constant add the totals; the sequence
+// mean adds total / L over live sequences; then one division by N, S or C.
+// The order depends only on the index, so an unsharded call and
+// grpo_loss_finalize over the same records produce the same bits.
+// kind 1 sums in double, kind 2 in float pairs.  A record of another kind,
+// or a nonzero `bad`, gives NaN outputs.  Thread 0 writes out3.
+constexpr int kFinalThreads = 128;
+struct FinalSmem {
+  double d[2][kFinalThreads / 32];
+  FF f[2][kFinalThreads / 32];
+  int mixed;
+};
+static __device__ __noinline__ void final_scalar(const SeqTotal* recs, int64_t B, unsigned long long N,
+                             unsigned long long S, int reduction, float norm_c, float beta,
+                             bool bad, float* out3, FinalSmem& sm) {
+  constexpr int kBatch = 8;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int kind = B > 0 ? __ldcg(&recs[0].kind) : kTotalsDouble;
+  if (t == 0) sm.mixed = 0;
+  __syncthreads();
+  double ud[2] = {0.0, 0.0};
+  FF uf[2] = {{0.f, 0.f}, {0.f, 0.f}};
+  if (t < kFinalThreads) {
+    for (int64_t j0 = t; j0 < B; j0 += kBatch * kFinalThreads) {
+      uint4 lo[kBatch], hi[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int64_t j = j0 + (int64_t)k * kFinalThreads;
+        const uint4* q = reinterpret_cast<const uint4*>(recs + (j < B ? j : 0));
+        lo[k] = j < B ? __ldcg(q) : make_uint4(0u, 0u, 0u, 0u);
+        hi[k] = j < B ? __ldcg(q + 1) : make_uint4(0u, 0u, (unsigned)kind, 0u);
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int L = (int)hi[k].x;
+        if ((int)hi[k].z != kind) sm.mixed = 1;
+        if (kind == kTotalsDouble) {
+          double P = __hiloint2double((int)lo[k].y, (int)lo[k].x);
+          double K = __hiloint2double((int)lo[k].w, (int)lo[k].z);
+          if (reduction == GRPO_SEQUENCE_MEAN) {
+            if (L == 0) continue;
+            P /= (double)L;
+            K /= (double)L;
+          }
+          ud[0] += P;
+          ud[1] += K;
+        } else {
+          FF P = {__uint_as_float(lo[k].x), __uint_as_float(lo[k].y)};
+          FF K = {__uint_as_float(lo[k].z), __uint_as_float(lo[k].w)};
+          if (reduction == GRPO_SEQUENCE_MEAN) {
+            if (L == 0) continue;
+            const FF Lf = {(float)L, 0.f};
+            P = ff_div(P, Lf);
+            K = ff_div(K, Lf);
+          }
+          uf[0] = ff_add(uf[0], P);
+          uf[1] = ff_add(uf[1], K);
+        }
+      }
+    }
+    if (kind == kTotalsDouble) {
+      ud[0] = warp_sum(ud[0]);
+      ud[1] = warp_sum(ud[1]);
+      if (lane == 0) {
+        sm.d[0][warp] = ud[0];
+        sm.d[1][warp] = ud[1];
+      }
+    } else {
+      uf[0] = warp_sum_ff2(uf[0]);
+      uf[1] = warp_sum_ff2(uf[1]);
+      if (lane == 0) {
+        sm.f[0][warp] = uf[0];
+        sm.f[1][warp] = uf[1];
+      }
+    }
+  }
+  __syncthreads();
+  if (t != 0) return;
+  float o0, o1, o2;
+  if (kind == kTotalsDouble) {
+    double P = sm.d[0][0], K = sm.d[1][0];
+#pragma unroll
+    for (int k = 1; k < kFinalThreads / 32; ++k) {
+      P += sm.d[0][k];
+      K += sm.d[1][k];
+    }
+    const double den = reduction == GRPO_TOKEN_MEAN      ? (double)(N > 0 ? N : 1)
+                       : reduction == GRPO_SEQUENCE_MEAN ? (double)(S > 0 ? S : 1)
+                                                         : (double)norm_c;
+    P /= den;
+    K /= den;
+    o0 = (float)(P + (double)beta * K);
+    o1 = (float)P;
+    o2 = (float)K;
+  } else {
+    FF P = sm.f[0][0], K = sm.f[1][0];
+#pragma unroll
+    for (int k = 1; k < kFinalThreads / 32; ++k) {
+      P = ff_add(P, sm.f[0][k]);
+      K = ff_add(K, sm.f[1][k]);
+    }
+    const FF den = reduction == GRPO_FIXED_CONSTANT
+                       ? FF{norm_c, 0.f}
+                       : ff_from_u64(reduction == GRPO_TOKEN_MEAN ? (N > 0 ? N : 1) : (S > 0 ? S : 1));
+    P = ff_div(P, den);
+    K = ff_div(K, den);
+    o0 = ff_float(ff_add(P, ff_scale(K, beta)));
+    o1 = ff_float(P);
+    o2 = ff_float(K);
+  }
+  if (bad || sm.mixed || (kind != kTotalsDouble && kind != kTotalsFF)) o0 = o1 = o2 = NAN;
+  out3[0] = o0;
+  out3[1] = o1;
+  out3[2] = o2;
+}
+
+// ----------------------------------------------------------------------------
 // kernels (defined in the .cu files)
 // ----------------------------------------------------------------------------
 struct PrepArgs {
-  const float* rewards;
+  const float* rewards;   // [Bg]
   const int64_t* bounds;  // NULL -> uniform groups of spp
-  int64_t B, T, G;
+  int64_t B, T, G;        // B: sequences whose masks are scanned (a shard's)
+  int64_t Bg;             // sequences the groups cover (the whole batch)
+  int64_t seq_begin;      // the scanned sequences' first index in the batch
+  unsigned long long* NS; // [2]: N and S receive the scanned counts (atomics)
   int32_t spp;
   float adv_eps;
   int eps_add;
@@ -512,9 +633,9 @@ struct PrepArgs {
   double* A;
   float2* Aff;     // nullable: the advantages as float pairs
   float* adv_out;  // nullable
-  int32_t* L;      // used when counting
+  int32_t* L;      // nullable: per-sequence counts (when counting)
   int2* range;     // nullable: active range per sequence (when counting)
-  WsHeader* hdr;
+  WsHeader* hdr;   // status word (may be NULL when G == 0)
 };
 
 struct RowArgs {
@@ -530,6 +651,7 @@ struct RowArgs {
   double* slot_k;
   float* logps_out;  // nullable
   WsHeader* hdr;
+  const unsigned long long* NS;  // [2]: N and S of the whole batch
   int64_t B, T, V;
   float eps_lo, eps_hi, beta, grad_scale;
   int reduction;
@@ -544,18 +666,20 @@ struct ReduceArgs {
   const uint8_t* mask;
   const int32_t* L;
   const double* A;
-  double* seq;  // [2B] per-sequence totals
+  SeqTotal* seq;  // [B] per-sequence totals
   const double* slot_p;
   const double* slot_k;
   int64_t B, T;
   float beta;
   int reduction;
   WsHeader* hdr;
+  const unsigned long long* NS;  // [2]: N and S of the whole batch
   float* out3;
   float* per_seq;  // nullable
   int split_A;      // the clipped surrogate: add -A_i L_i per sequence
   float norm_c;     // GRPO_FIXED_CONSTANT's constant
   unsigned long long* counts_out;  // nullable [3]
+  int shard;        // 1: write the totals only (the scalar comes from grpo_loss_finalize)
 };
 
 struct LogpsArgs {
@@ -567,7 +691,7 @@ struct LogpsArgs {
   const float2* Aff;  // the advantages as float pairs
   const int2* range;  // active range per sequence
   int32_t* L;
-  float4* seq;  // [B] {P.hi, P.lo, K.hi, K.lo}
+  SeqTotal* seq;  // [B] per-sequence totals
   float* grad;  // nullable
   float* out3;
   float* per_seq;  // nullable
@@ -578,6 +702,8 @@ struct LogpsArgs {
   Variant var;
   float norm_c;  // GRPO_FIXED_CONSTANT's constant
   unsigned long long* counts_out;  // nullable [3]
+  const unsigned long long* NS;    // [2]: N and S of the whole batch
+  int shard;     // 1: write the totals only (the scalar comes from grpo_loss_finalize)
 };
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
@@ -585,5 +711,7 @@ cudaError_t launch_rows(const RowArgs& a, grpo_dtype_t dt, const grpo_profile_t*
                         cudaStream_t s);
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t s);
 cudaError_t launch_logps(const LogpsArgs& a, const grpo_profile_t* prof, cudaStream_t s);
+cudaError_t launch_finalize(const SeqTotal* recs, int64_t B, const unsigned long long* NS,
+                            int reduction, float norm_c, float beta, float* out3, cudaStream_t s);
 
 }  // namespace grpo

@@ -25,6 +25,7 @@
 namespace grpo {
 
 static constexpr int kLogpsThreads = 128;
+static_assert(kLogpsThreads >= kFinalThreads, "the last CTA runs final_scalar");
 static constexpr float kWPrecise = 0x1p-11f;
 
 // e^d - 1 and k3 = e^d - d - 1 together.  With Q(d) = sum_{n>=2} d^(n-2)/n!,
@@ -320,6 +321,7 @@ __device__ __forceinline__ bool staged_ok(const LogpsArgs& a) {
 __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs a) {
   __shared__ FF s_ff[2][kLogpsThreads / 32];
   __shared__ unsigned s_nc[3][kLogpsThreads / 32];
+  __shared__ FinalSmem s_fin;
   __shared__ bool s_last;
   __shared__ __align__(16) Stage s_st[kDepth];
   __shared__ __align__(8) uint64_t s_full[kDepth];
@@ -335,8 +337,8 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
   if (b < a.B) {
     SeqCtx x;
     x.b = b;
-    x.N = a.hdr->N;
-    x.S = a.hdr->S;
+    x.N = a.NS[0];
+    x.S = a.NS[1];
     x.L = a.L[b];
     const float2 Ab = a.Aff[b];
     x.A = Ab.x;
@@ -492,7 +494,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
       // P_b = sum q - A_b L_b for the clipped surrogate (the product exact
       // up to ~2^-48 relative); CISPO's q is the policy term itself
       const FF P = a.var.splits_A() ? ff_add(fq, ff_neg(ff_scale(FF{Ab.x, Ab.y}, (float)x.L))) : fq;
-      a.seq[b] = make_float4(P.hi, P.lo, fk.hi, fk.lo);
+      put_total(a.seq + b, P, fk, x.L);
       if (a.per_seq) {
         a.per_seq[b] = ff_float(P);
         a.per_seq[a.B + b] = ff_float(fk);
@@ -515,64 +517,14 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  if (threadIdx.x == 0 && a.counts_out)  // every CTA added its counts before its ticket
+    for (int j = 0; j < 3; ++j) a.counts_out[j] = __ldcg(&a.hdr->clip[j]);
+  if (a.shard) return;  // the scalar comes from grpo_loss_finalize over all shards' totals
 
-  // The scalar over the B sequence totals, in float pairs: each thread's
-  // sequences in index order, a fixed xor tree, warps in index order.  The
-  // totals were written by other CTAs of this launch (visible through their
-  // fence before the ticket), so they are read from L2.
-  // Loads go out kBatch at a time, so the L2 latency is paid once per batch.
-  constexpr int kBatch = 8;
-  FF u[2] = {{0.f, 0.f}, {0.f, 0.f}};
-  for (int64_t j0 = threadIdx.x; j0 < a.B; j0 += kBatch * kLogpsThreads) {
-    float4 t[kBatch];
-    int L[kBatch];
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int64_t j = j0 + (int64_t)k * kLogpsThreads;
-      t[k] = j < a.B ? __ldcg(a.seq + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-      L[k] = j < a.B ? a.L[j] : 0;  // written by prep, an earlier launch
-    }
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      FF P = {t[k].x, t[k].y}, K = {t[k].z, t[k].w};
-      if (a.reduction == GRPO_SEQUENCE_MEAN) {
-        if (L[k] == 0) continue;
-        const FF Lf = {(float)L[k], 0.f};
-        P = ff_div(P, Lf);
-        K = ff_div(K, Lf);
-      }
-      u[0] = ff_add(u[0], P);
-      u[1] = ff_add(u[1], K);
-    }
-  }
-  u[0] = warp_sum_ff2(u[0]);
-  u[1] = warp_sum_ff2(u[1]);
-  if (lane == 0) {
-    s_ff[0][warp] = u[0];
-    s_ff[1][warp] = u[1];
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    FF P = s_ff[0][0], K = s_ff[1][0];
-#pragma unroll
-    for (int k = 1; k < kLogpsThreads / 32; ++k) {
-      P = ff_add(P, s_ff[0][k]);
-      K = ff_add(K, s_ff[1][k]);
-    }
-    const unsigned long long N = a.B > 0 ? a.hdr->N : 0, S = a.B > 0 ? a.hdr->S : 0;
-    const FF den = a.reduction == GRPO_FIXED_CONSTANT
-                       ? FF{a.norm_c, 0.f}
-                       : ff_from_u64(a.reduction == GRPO_TOKEN_MEAN ? (N > 0 ? N : 1) : (S > 0 ? S : 1));
-    P = ff_div(P, den);
-    K = ff_div(K, den);
-    float o0 = ff_float(ff_add(P, ff_scale(K, a.beta))), o1 = ff_float(P), o2 = ff_float(K);
-    if (((volatile unsigned*)&a.hdr->status)[0] != 0u) o0 = o1 = o2 = NAN;
-    a.out3[0] = o0;
-    a.out3[1] = o1;
-    a.out3[2] = o2;
-    if (a.counts_out)  // every CTA added its counts before taking its ticket
-      for (int j = 0; j < 3; ++j) a.counts_out[j] = __ldcg(&a.hdr->clip[j]);
-  }
+  // the scalar over the B sequence records, in index order
+  const bool bad = ((volatile unsigned*)&a.hdr->status)[0] != 0u;
+  final_scalar(a.seq, a.B, a.B > 0 ? a.NS[0] : 0ull, a.B > 0 ? a.NS[1] : 0ull, a.reduction,
+               a.norm_c, a.beta, bad, a.out3, s_fin);
 }
 
 cudaError_t launch_logps(const LogpsArgs& a, const grpo_profile_t* prof, cudaStream_t s) {

@@ -1,7 +1,8 @@
 // grpo_prep.cu -- group-normalised advantages and per-sequence active-token
 // counts, in one launch of 8-warp CTAs: the first ceil(G/8) CTAs give one
 // warp to each group, the rest (when counting) one warp to the mask of each
-// sequence.
+// sequence.  In a shard call the groups span the whole batch (Bg sequences;
+// advantages are replicated) while the masks are the shard's B sequences.
 //
 // RL-Kernel "GRPO Loss" page, "Accuracy": advantages are the group's rewards
 // minus their mean over the population standard deviation clamped at
@@ -73,14 +74,14 @@ __device__ void warp_group(const PrepArgs& a, int64_t g, int lane) {
   } else {
     lo = a.bounds[g];
     hi = a.bounds[g + 1];
-    bool bad = !(lo >= 0 && hi > lo && hi <= a.B);
+    bool bad = !(lo >= 0 && hi > lo && hi <= a.Bg);
     if (g == 0 && lo != 0) bad = true;
-    if (g == a.G - 1 && hi != a.B) bad = true;
+    if (g == a.G - 1 && hi != a.Bg) bad = true;
     if (bad) {
       if (lane == 0) atomicOr(&a.hdr->status, (unsigned)GRPO_ERR_CSR);
       // keep every index in range; the outputs are NaN through the status word
-      lo = lo < 0 ? 0 : (lo > a.B ? a.B : lo);
-      hi = hi < lo ? lo : (hi > a.B ? a.B : hi);
+      lo = lo < 0 ? 0 : (lo > a.Bg ? a.Bg : lo);
+      hi = hi < lo ? lo : (hi > a.Bg ? a.Bg : hi);
     }
   }
   const int64_t n = hi - lo;
@@ -120,7 +121,8 @@ __device__ void warp_group(const PrepArgs& a, int64_t g, int lane) {
       const float hi = (float)Ai;
       a.Aff[i] = make_float2(hi, (float)(Ai - (double)hi));
     }
-    if (a.adv_out) a.adv_out[i] = (float)Ai;
+    if (a.adv_out && i >= a.seq_begin && i < a.seq_begin + a.B)
+      a.adv_out[i - a.seq_begin] = (float)Ai;
   }
 }
 
@@ -140,7 +142,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
     const SeqScan sc = warp_scan(a.mask + i * a.T, a.T, lane);
     L = sc.count;
     if (lane == 0) {
-      a.L[i] = L;
+      if (a.L) a.L[i] = L;
       if (a.range) a.range[i] = L > 0 ? make_int2(sc.first, sc.last + 1) : make_int2(0, 0);
     }
   }
@@ -153,8 +155,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
       n += (unsigned long long)s_L[k];
       s += s_L[k] > 0;
     }
-    if (n) atomicAdd(&a.hdr->N, n);
-    if (s) atomicAdd(&a.hdr->S, s);
+    if (n) atomicAdd(&a.NS[0], n);
+    if (s) atomicAdd(&a.NS[1], s);
   }
 }
 

@@ -11,6 +11,12 @@
 // B totals.  Every sum has an order fixed by the code (thread-strided partial
 // sums, xor-shuffle trees, warps in index order, sequences in index order),
 // never by scheduling, so the result is bitwise reproducible.
+//
+// Sequence sharding (same page, steps 2-6): a shard call writes its
+// sequences' totals and stops; finalize_kernel forms the scalar from the
+// totals of all shards, concatenated in shard order, with the same
+// final_scalar code the unsharded last CTA runs -- the same bits at any
+// degree.
 #include "grpo_internal.cuh"
 
 namespace grpo {
@@ -19,11 +25,12 @@ static constexpr int kReduceThreads = 256;
 
 __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs a) {
   __shared__ double s_d[32 * 2];
+  __shared__ FinalSmem s_fin;
   __shared__ bool s_last;
   const int64_t i = blockIdx.x;
 
-  // level 1: sequence i.  Slots hold p + A (the policy term plus its constant
-  // part, see the row kernel); the constant -A_i per token is added here.
+  // level 1: sequence i.  Slots hold the policy term plus A for the clipped
+  // surrogate (see the row kernel); the constant -A_i per token is added here.
   if (i < a.B) {
     const uint8_t* m = a.mask + i * a.T;
     const double* sp = a.slot_p + i * a.T;
@@ -38,48 +45,55 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs
     if (threadIdx.x == 0) {
       const int L = a.L[i];
       const double P = a.split_A ? v[0] - a.A[i] * (double)L : v[0];
-      a.seq[i] = P;
-      a.seq[a.B + i] = v[1];
+      put_total(a.seq + i, P, v[1], L);
       if (a.per_seq) {
         a.per_seq[i] = (float)P;
         a.per_seq[a.B + i] = (float)v[1];
         a.per_seq[2 * a.B + i] = (float)L;
       }
-      __threadfence();
-      const unsigned ticket = atomicAdd(&a.hdr->done_ctas, 1u);
-      s_last = ticket == gridDim.x - 1;
+      if (i == 0 && a.counts_out)  // the row kernel's CTAs added their counts before this launch
+        for (int j = 0; j < 3; ++j) a.counts_out[j] = a.hdr->clip[j];
+      if (a.shard) {
+        s_last = false;  // the scalar comes from grpo_loss_finalize over all shards' totals
+      } else {
+        __threadfence();
+        const unsigned ticket = atomicAdd(&a.hdr->done_ctas, 1u);
+        s_last = ticket == gridDim.x - 1;
+      }
     }
   } else if (threadIdx.x == 0) {
-    s_last = true;  // B == 0: a single CTA writes the zero loss
+    s_last = !a.shard;  // B == 0: a single CTA writes the zero loss
+    if (a.counts_out)
+      for (int j = 0; j < 3; ++j) a.counts_out[j] = a.hdr->clip[j];
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
 
-  // level 2: the scalar, over the B sequence totals in index order
-  double u[2] = {0.0, 0.0};
-  seq_totals(a.seq, a.L, a.B, a.reduction, u);
-  block_sum<double, 2>(u, s_d);
-  if (threadIdx.x == 0) {
-    // N = active tokens, S = live sequences, as prep counted them
-    const long long N = a.B > 0 ? a.hdr->N : 0, S = a.B > 0 ? a.hdr->S : 0;
-    const double den = a.reduction == GRPO_TOKEN_MEAN      ? (double)(N > 0 ? N : 1)
-                       : a.reduction == GRPO_SEQUENCE_MEAN ? (double)(S > 0 ? S : 1)
-                                                           : (double)a.norm_c;
-    const double P = u[0] / den, K = u[1] / den;
-    float o0 = (float)(P + (double)a.beta * K), o1 = (float)P, o2 = (float)K;
-    if (((volatile unsigned*)&a.hdr->status)[0] != 0u) o0 = o1 = o2 = NAN;
-    a.out3[0] = o0;
-    a.out3[1] = o1;
-    a.out3[2] = o2;
-    if (a.counts_out)  // every row kernel CTA added its counts before this launch
-      for (int j = 0; j < 3; ++j) a.counts_out[j] = a.hdr->clip[j];
-  }
+  // level 2: the scalar, over the B sequence records in index order
+  const bool bad = ((volatile unsigned*)&a.hdr->status)[0] != 0u;
+  final_scalar(a.seq, a.B, a.B > 0 ? a.NS[0] : 0ull, a.B > 0 ? a.NS[1] : 0ull, a.reduction,
+               a.norm_c, a.beta, bad, a.out3, s_fin);
 }
 
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t s) {
   const int64_t grid = a.B > 0 ? a.B : 1;
   reduce_kernel<<<(unsigned)grid, kReduceThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+__global__ void __launch_bounds__(kFinalThreads) finalize_kernel(const SeqTotal* recs, int64_t B,
+                                                                const unsigned long long* NS,
+                                                                int reduction, float norm_c,
+                                                                float beta, float* out3) {
+  __shared__ FinalSmem s_fin;
+  final_scalar(recs, B, B > 0 ? NS[0] : 0ull, B > 0 ? NS[1] : 0ull, reduction, norm_c, beta,
+               false, out3, s_fin);
+}
+
+cudaError_t launch_finalize(const SeqTotal* recs, int64_t B, const unsigned long long* NS,
+                            int reduction, float norm_c, float beta, float* out3, cudaStream_t s) {
+  finalize_kernel<<<1, kFinalThreads, 0, s>>>(recs, B, NS, reduction, norm_c, beta, out3);
   return cudaGetLastError();
 }
 

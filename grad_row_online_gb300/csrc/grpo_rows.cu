@@ -297,10 +297,11 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(cons
     s_thi[threadIdx.x] = a.tab.hi[threadIdx.x];
     s_tlo[threadIdx.x] = a.tab.lo[threadIdx.x];
   }
-  // N = active tokens, S = live sequences: counted by prep, read here once
+  // N = active tokens, S = live sequences of the whole batch (counted by prep,
+  // or given by a shard call), read here once
   if (threadIdx.x == 0) {
-    s_NS[0] = a.hdr->N;
-    s_NS[1] = a.hdr->S;
+    s_NS[0] = a.NS[0];
+    s_NS[1] = a.NS[1];
     s_next = (long long)atomicAdd(&a.hdr->row_counter, 1ull);
   }
   __syncthreads();

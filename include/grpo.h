@@ -122,6 +122,34 @@ typedef struct {
   void *stop;
 } grpo_profile_t;
 
+/* One sequence's totals in the exact form the final reduction consumes
+ * (policy and KL totals and the active count; opaque).  A data-parallel
+ * shard writes one record per sequence it owns; concatenated in shard
+ * order they are the whole batch's, and grpo_loss_finalize turns them into
+ * the three loss outputs. */
+typedef struct {
+  unsigned char opaque[32];
+} grpo_seq_total_t;
+
+/* A data-parallel shard of the batch (RL-Kernel "Tensor and Data Parallel"):
+ * a rank owns a contiguous range of whole sequences.  With a shard, a call's
+ * rewards and group specification describe the WHOLE batch (advantages are
+ * replicated: every rank normalises every group over the same rewards and
+ * keeps its own slice), while the token arguments (logits or log-probs,
+ * action_ids, old_logps, completion_mask, gradients, per_seq, adv_out)
+ * cover only the shard's B sequences, starting at sequence seq_begin of the
+ * batch.  The token weights use the whole batch's counts; only per-sequence
+ * totals cross a rank boundary.  Whatever the partition, every gradient,
+ * per-sequence total and loss output is bit-identical to the unsharded
+ * call's. */
+typedef struct {
+  int64_t seq_begin;                        /* the shard's first sequence in the batch */
+  const unsigned long long *global_counts;  /* device [2]: N (active tokens) and S (live
+                                               sequences) of the whole batch, e.g. the sum
+                                               over shards of grpo_count_active */
+  grpo_seq_total_t *totals_out;             /* device [B]: the shard's per-sequence totals */
+} grpo_shard_t;
+
 /* Call parameters.  Zero-initialising the variant fields (kl_type,
  * surrogate, dual_clip_c, norm_constant, clip_counts) gives the GRPO loss
  * of the operator page: the clipped surrogate with k3 and no dual clip. */
@@ -143,6 +171,7 @@ typedef struct {
                           > 0; ignored by the other reductions */
   int32_t _reserved;
   const grpo_profile_t *profile; /* host pointer or NULL */
+  const grpo_shard_t *shard;     /* host pointer or NULL (the whole batch) */
   unsigned long long *clip_counts; /* device [3] or NULL: overwritten with the
                           number of active tokens clipped at the upper bound,
                           at the lower bound, and by the dual clip.  Clipped
@@ -155,7 +184,8 @@ typedef struct {
 
 /* Bytes of workspace the entry points below need for B sequences of T
  * token slots in num_groups groups (any of the three entry points; a
- * workspace of this size serves all of them).  The workspace is caller-owned
+ * workspace of this size serves all of them).  A shard call (grpo_shard_t)
+ * needs grpo_workspace_size(total sequences of the batch, T, 0).  The workspace is caller-owned
  * device memory, 256-byte aligned, needs no initialisation, and must not be
  * shared by calls that may run concurrently.  Returns 0 for invalid sizes. */
 size_t grpo_workspace_size(int64_t B, int64_t T, int64_t num_groups);
@@ -179,7 +209,8 @@ grpo_status_t grpo_group_adv(const float *rewards, const grpo_groups_t *groups,
  *                               (overwritten, not accumulated; may equal
  *                               policy_logits for an in-place gradient).
  *                               NULL = forward only.
- *   out3                      : [3] f32: loss, policy_loss, kl.
+ *   out3                      : [3] f32: loss, policy_loss, kl (not written,
+ *                               and may be NULL, in a shard call).
  *   per_seq (nullable)        : [3,B] f32: per-sequence policy totals
  *                               sum_t p, KL totals sum_t k, active counts L_i.
  *   logps_out (nullable)      : [B,T] f32: logp of active tokens, 0 elsewhere.
@@ -233,6 +264,27 @@ grpo_status_t grpo_loss_fwd_bwd_static(const void *policy_logits, const void *re
                                        const grpo_groups_t *groups, const grpo_params_t *params,
                                        void *grad_logits, float *out3, float *per_seq,
                                        float *logps_out, float *adv_out, void *stream);
+
+/* Sequence sharding ("Tensor and Data Parallel", steps 2-6).  A rank that
+ * owns B sequences of T slots counts them: counts_out (device [2]) receives
+ * N = sum of active tokens and S = sequences with at least one, as exact
+ * integers; the whole batch's counts are the sums over ranks.  The paper's
+ * normaliser "divides by a global active-token count, gathered as integers
+ * so it is exact at every degree". */
+grpo_status_t grpo_count_active(const uint8_t *completion_mask, int64_t B, int64_t T,
+                                unsigned long long *counts_out, void *stream);
+
+/* The loss outputs from the whole batch's per-sequence totals: the records
+ * of every shard concatenated in shard order (B records, all from the same
+ * entry point: grpo_loss_fwd_bwd or grpo_loss_from_logps), the batch counts
+ * (device [2], as in grpo_shard_t) and the same params (reduction,
+ * norm_constant, beta).  out3 = {loss, policy_loss, kl}, computed by the
+ * same code, in the same order, as an unsharded call; so the result is
+ * bit-identical to it ("all_reduce is excluded on purpose": the sum runs
+ * in declared sequence order). */
+grpo_status_t grpo_loss_finalize(const grpo_seq_total_t *totals, int64_t B,
+                                 const unsigned long long *global_counts,
+                                 const grpo_params_t *params, float *out3, void *stream);
 
 /* Synchronises `stream` and returns the status word the last call on this
  * workspace left (GRPO_OK or an OR of the device-detected bits), or

@@ -145,3 +145,41 @@ def test_logps_and_adv_reject_bad_arguments(lib):
     assert A(FAKE, ctypes.byref(gr), ctypes.c_float(1e-6), 0, None, FAKE, ws, None) == 1
     assert A(FAKE, ctypes.byref(_groups(B=8, spp=3)), ctypes.c_float(1e-6), 0, FAKE, FAKE, ws,
              None) == 2
+
+
+def test_shard_entry_points_reject_bad_arguments(lib):
+    # grpo_count_active / grpo_loss_finalize host checks
+    assert lib.grpo_count_active(FAKE, -1, 4, FAKE, None) == 2
+    assert lib.grpo_count_active(FAKE, 2, 4, None, None) == 1
+    assert lib.grpo_count_active(None, 2, 4, FAKE, None) == 1
+    assert lib.grpo_count_active(FAKE, 2, 4, FAKE + 4, None) == 4
+    p = _params()
+    assert lib.grpo_loss_finalize(FAKE, -1, FAKE, ctypes.byref(p), FAKE, None) == 2
+    assert lib.grpo_loss_finalize(None, 4, FAKE, ctypes.byref(p), FAKE, None) == 1
+    assert lib.grpo_loss_finalize(FAKE, 4, None, ctypes.byref(p), FAKE, None) == 1
+    assert lib.grpo_loss_finalize(FAKE, 4, FAKE, ctypes.byref(p), None, None) == 1
+    assert lib.grpo_loss_finalize(FAKE + 8, 4, FAKE, ctypes.byref(p), FAKE, None) == 4
+    assert lib.grpo_loss_finalize(FAKE, 4, FAKE, ctypes.byref(_params(reduction=5)), FAKE,
+                                  None) == 6
+
+
+def _sharded(seq_begin, counts=FAKE, totals=FAKE):
+    sh = g._Shard(seq_begin, counts, totals)
+    p = _params()
+    p._sh = sh
+    p.shard = ctypes.pointer(sh)
+    return p
+
+
+def test_shard_placement_is_checked(lib):
+    # a shard of 4 sequences of a batch of 8 (groups and rewards span the batch)
+    gr = _groups(8)
+    ws = g.grpo_workspace_size(8, 16)
+    assert _fwd(lib, B=4, gr=gr, p=_sharded(5), ws_bytes=ws) == 2   # runs past the batch
+    assert _fwd(lib, B=4, gr=gr, p=_sharded(-1), ws_bytes=ws) == 2
+    assert _fwd(lib, B=4, gr=gr, p=_sharded(0, counts=None), ws_bytes=ws) == 1
+    assert _fwd(lib, B=4, gr=gr, p=_sharded(0, totals=None), ws_bytes=ws) == 1
+    assert _fwd(lib, B=4, gr=gr, p=_sharded(0, totals=FAKE + 8), ws_bytes=ws) == 4
+    assert _fwd(lib, B=4, gr=gr, p=_sharded(0, counts=FAKE + 4), ws_bytes=ws) == 4
+    # the workspace must cover the whole batch
+    assert _fwd(lib, B=4, gr=gr, p=_sharded(0), ws_bytes=g.grpo_workspace_size(4, 16)) == 7

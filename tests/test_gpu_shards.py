@@ -1,0 +1,183 @@
+"""Sequence-sharded determinism (RL-Kernel "GRPO Loss", "Tensor and Data
+Parallel"): a batch split into K contiguous shards of whole sequences --
+emulated as K "ranks" on one GPU, each with its own workspace -- gives
+bit-identical gradients, per-sequence totals and loss outputs to the
+unsharded call, for every K, with advantage groups straddling shards.  The
+exchange is what the page describes: the active-token counts gathered as
+integers, the per-sequence totals concatenated in shard order."""
+import numpy as np
+import pytest
+import torch
+
+import grad_row_online_gb300 as g
+import synth
+from workload_inputs import make_case, to_device
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import os
+    import __graft_entry__
+    if not os.path.exists(g.library_path()):
+        __graft_entry__.build()
+
+
+# 12 sequences in groups of 4; ragged lengths, some empty sequences
+BATCH = synth.Workload("shards", B=12, T=10, V=3001, seed=121, sigma=2.0, ref_sigma=0.2,
+                       samples_per_prompt=4, reward_p=0.5, len_range=(0, 10), eps_lo=0.2,
+                       eps_hi=0.28, beta=0.1, old_sigma=0.3)
+PARTITIONS = {
+    "1": [12],
+    "2": [6, 6],
+    "straddle": [5, 7],           # shard boundary inside a group
+    "3-uneven": [1, 8, 3],
+    "with-empty": [0, 12, 0],
+    "12": [1] * 12,
+}
+OPTIONS = {
+    "token-mean": dict(),
+    "sequence-mean": dict(reduction="sequence_mean"),
+    "fixed-k2-dual": dict(reduction="fixed_constant", norm_constant=40.0, kl="k2",
+                          dual_clip_c=1.4),
+}
+
+
+def _bounds(sizes):
+    out, s = [], 0
+    for n in sizes:
+        out.append((s, s + n))
+        s += n
+    return out
+
+
+def _sharded_logits(dev, w, sizes, opts):
+    """Run every shard, exchange counts and totals, finalize."""
+    parts = _bounds(sizes)
+    counts = [g.grpo_count_active(dev["mask"][a:b]) for a, b in parts]
+    global_counts = torch.stack(counts).sum(0)  # integer sums: exact in any order
+    grads, per_seq, totals, clips = [], [], [], []
+    for a, b in parts:
+        tot = g.totals_buffer(b - a)
+        res = g.grpo_loss_fwd_bwd(dev["X"][a:b], dev["Y"][a:b], dev["acts"][a:b],
+                                  dev["old"][a:b], dev["mask"][a:b], dev["R"],
+                                  samples_per_prompt=w.samples_per_prompt, clip_eps=w.eps_lo,
+                                  clip_eps_hi=w.eps_hi, beta=w.beta, want_per_seq=True,
+                                  want_clip_counts=True,
+                                  shard=g.Shard(a, global_counts, tot), **opts)
+        grads.append(res["grad"])
+        per_seq.append(res["per_seq"])
+        totals.append(tot)
+        clips.append(res["clip_counts"])
+    all_totals = torch.cat(totals)  # shard order = sequence order
+    out3 = g.grpo_loss_finalize(all_totals, global_counts, beta=w.beta,
+                                reduction=opts.get("reduction", "token_mean"),
+                                norm_constant=opts.get("norm_constant"))
+    torch.cuda.synchronize()
+    return dict(out3=out3, grad=torch.cat(grads), per_seq=torch.cat(per_seq, dim=1),
+                totals=all_totals, clips=torch.stack(clips).sum(0), counts=global_counts)
+
+
+@pytest.mark.parametrize("opt", list(OPTIONS))
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_logits_shards_are_bitwise_identical(dtype, opt):
+    w = BATCH
+    case = make_case(w, dtype)
+    dev = to_device(case)
+    opts = OPTIONS[opt]
+    whole = g.grpo_loss_fwd_bwd(dev["X"], dev["Y"], dev["acts"], dev["old"], dev["mask"],
+                                dev["R"], samples_per_prompt=w.samples_per_prompt,
+                                clip_eps=w.eps_lo, clip_eps_hi=w.eps_hi, beta=w.beta,
+                                want_per_seq=True, want_clip_counts=True, **opts)
+    torch.cuda.synchronize()
+    ref = _sharded_logits(dev, w, PARTITIONS["1"], opts)
+    # one shard through finalize reproduces the plain call
+    assert torch.equal(ref["out3"], whole["out3"])
+    assert torch.equal(ref["grad"], whole["grad"])
+    assert torch.equal(ref["per_seq"], whole["per_seq"])
+    assert torch.equal(ref["clips"], whole["clip_counts"])
+    assert int(ref["counts"][0]) == int(case["mask"].sum())
+    for name, sizes in PARTITIONS.items():
+        got = _sharded_logits(dev, w, sizes, opts)
+        for k in ("out3", "grad", "per_seq", "totals", "clips", "counts"):
+            assert torch.equal(got[k], ref[k]), (name, k)
+
+
+LOGPS = synth.WORKLOADS["logps"].with_(name="logps_shards", B=12, T=64, len_range=(0, 64),
+                                      samples_per_prompt=4, old_sigma=0.3, ref_logp_sigma=0.1,
+                                      beta=0.1)
+
+
+def _sharded_logps(t, w, sizes, opts):
+    parts = _bounds(sizes)
+    counts = [g.grpo_count_active(t["mask"][a:b]) for a, b in parts]
+    global_counts = torch.stack(counts).sum(0)
+    grads, totals = [], []
+    for a, b in parts:
+        tot = g.totals_buffer(b - a)
+        res = g.grpo_loss_from_logps(t["lp"][a:b], t["old"][a:b], t["ref"][a:b], t["mask"][a:b],
+                                     t["R"], samples_per_prompt=w.samples_per_prompt,
+                                     clip_eps=w.eps_lo, clip_eps_hi=w.eps_hi, beta=w.beta,
+                                     shard=g.Shard(a, global_counts, tot), **opts)
+        grads.append(res["grad"])
+        totals.append(tot)
+    all_totals = torch.cat(totals)
+    out3 = g.grpo_loss_finalize(all_totals, global_counts, beta=w.beta,
+                                reduction=opts.get("reduction", "token_mean"),
+                                norm_constant=opts.get("norm_constant"))
+    torch.cuda.synchronize()
+    return dict(out3=out3, grad=torch.cat(grads), totals=all_totals)
+
+
+@pytest.mark.parametrize("opt", list(OPTIONS))
+@pytest.mark.parametrize("T", [64, 100, 37])  # staged, register and scalar paths
+def test_logps_shards_are_bitwise_identical(T, opt):
+    w = LOGPS.with_(T=T, len_range=(0, T))
+    lp, old, ref = w.logps_inputs()
+    host = dict(lp=lp, old=old, ref=ref, mask=w.completion_mask(), R=w.rewards())
+    t = {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in host.items()}
+    opts = OPTIONS[opt]
+    whole = g.grpo_loss_from_logps(t["lp"], t["old"], t["ref"], t["mask"], t["R"],
+                                   samples_per_prompt=w.samples_per_prompt, clip_eps=w.eps_lo,
+                                   clip_eps_hi=w.eps_hi, beta=w.beta, **opts)
+    torch.cuda.synchronize()
+    ref_run = _sharded_logps(t, w, PARTITIONS["1"], opts)
+    assert torch.equal(ref_run["out3"], whole["out3"])
+    assert torch.equal(ref_run["grad"], whole["grad"])
+    for name, sizes in PARTITIONS.items():
+        got = _sharded_logps(t, w, sizes, opts)
+        for k in ("out3", "grad", "totals"):
+            assert torch.equal(got[k], ref_run[k]), (name, k)
+
+
+def test_count_active_matches_the_mask():
+    m = torch.from_numpy(BATCH.completion_mask()).cuda()
+    m[3] = 0
+    c = g.grpo_count_active(m)
+    torch.cuda.synchronize()
+    L = m.sum(1)
+    assert int(c[0]) == int(L.sum()) and int(c[1]) == int((L > 0).sum())
+    empty = g.grpo_count_active(m[:0])
+    assert empty.tolist() == [0, 0]
+
+
+def test_dp_helper_single_rank_matches_the_plain_call():
+    from grad_row_online_gb300 import dp
+    w = BATCH
+    case = make_case(w, "bf16")
+    dev = to_device(case)
+    args = dict(policy=dev["X"], ref=dev["Y"], acts=dev["acts"], old=dev["old"],
+                mask=dev["mask"], R=dev["R"])
+    res = dp.sequence_sharded_loss(g.grpo_loss_fwd_bwd, args, dev["mask"], 0, beta=w.beta,
+                                   samples_per_prompt=w.samples_per_prompt, clip_eps=w.eps_lo,
+                                   clip_eps_hi=w.eps_hi)
+    whole = g.grpo_loss_fwd_bwd(dev["X"], dev["Y"], dev["acts"], dev["old"], dev["mask"],
+                                dev["R"], samples_per_prompt=w.samples_per_prompt,
+                                clip_eps=w.eps_lo, clip_eps_hi=w.eps_hi, beta=w.beta)
+    torch.cuda.synchronize()
+    assert torch.equal(res["out3"], whole["out3"])
+    assert torch.equal(res["grad"], whole["grad"])
