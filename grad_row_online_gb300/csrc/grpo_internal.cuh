@@ -497,7 +497,7 @@ __device__ __forceinline__ void put_total(SeqTotal* r, FF P, FF K, int L) {
 // The final scalar from B records, by the first kFinalThreads threads of a
 // CTA (every thread of the CTA calls it: it holds __syncthreads).  Each
 // thread takes records j = t, t + 128, ... in index order (loads batched
-// eight at a time, from L2: the records may come from other CTAs of the
+// four at a time, from L2: the records may come from other CTAs of the
 // same launch), then a fixed xor tree per warp and the four warps in index
 // order.  The token mean and the fixed constant add the totals; the sequence
 // mean adds total / L over live sequences; then one division by N, S or C.
@@ -511,10 +511,10 @@ struct FinalSmem {
   FF f[2][kFinalThreads / 32];
   int mixed;
 };
-static __device__ __noinline__ void final_scalar(const SeqTotal* recs, int64_t B, unsigned long long N,
+static __device__ __forceinline__ void final_scalar(const SeqTotal* recs, int64_t B, unsigned long long N,
                              unsigned long long S, int reduction, float norm_c, float beta,
                              bool bad, float* out3, FinalSmem& sm) {
-  constexpr int kBatch = 8;
+  constexpr int kBatch = 4;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int kind = B > 0 ? __ldcg(&recs[0].kind) : kTotalsDouble;
   if (t == 0) sm.mixed = 0;
