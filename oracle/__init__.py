@@ -62,7 +62,7 @@ def lib():
         L.oracle_group_advantages.restype = ci
         L.oracle_log_softmax_rows.argtypes = [vp, ci, i64, i64, vp, vp, vp]
         L.oracle_loss_from_logps.argtypes = [i64, i64, vp, vp, vp, vp, vp, dbl, dbl, dbl, dbl,
-                                             ci, ci, ci, dbl, dbl, vp, vp, vp, vp, vp]
+                                             ci, ci, ci, dbl, dbl, ci, vp, vp, vp, vp, vp]
         L.oracle_grad_rows.argtypes = [vp, ci, i64, i64, vp, vp, vp, ci, vp, vp]
         L.oracle_round_to.argtypes = [vp, i64, ci, vp]
         _lib = L
@@ -114,12 +114,14 @@ def log_softmax_rows(rows, dtype: str, actions=None):
 def loss_from_logps(logp, ref_logp, old, mask, A, eps_lo, eps_hi, beta,
                     grad_scale: float = 1.0, reduction: int = TOKEN_MEAN, kl: str = "k3",
                     surrogate: str = "clip", dual_clip_c: float | None = None,
-                    norm_constant: float | None = None):
+                    norm_constant: float | None = None, ratio_level: str = "token"):
     """Loss, per-sequence totals and dL/dlogp from per-token log-probs.
     logp / ref_logp / old: [B,T] (any float type, widened to double);
     ref_logp may be None (no KL term).  Variants: kl in {"k3", "k1", "k2"},
     surrogate in {"clip", "cispo"}, the dual clip constant c > 1, and the
-    fixed-constant normaliser (reduction FIXED_CONSTANT with norm_constant)."""
+    fixed-constant normaliser (reduction FIXED_CONSTANT with norm_constant),
+    and ratio_level "sequence" (GSPO: one ratio per sequence, sequence mean
+    only, not with CISPO)."""
     lp = _c(logp, np.float64)
     B, T = lp.shape
     rl = None if ref_logp is None else _c(ref_logp, np.float64)
@@ -130,6 +132,10 @@ def loss_from_logps(logp, ref_logp, old, mask, A, eps_lo, eps_hi, beta,
         raise ValueError("the fixed-constant normaliser needs norm_constant > 0")
     if dual_clip_c is not None and (dual_clip_c <= 1.0 or surrogate != "clip"):
         raise ValueError("the dual clip needs c > 1 and the clipped surrogate")
+    if ratio_level not in ("token", "sequence"):
+        raise ValueError("ratio_level is 'token' or 'sequence'")
+    if ratio_level == "sequence" and (reduction != SEQUENCE_MEAN or surrogate != "clip"):
+        raise ValueError("sequence-level ratios need the sequence mean and the clipped surrogate")
     out3 = np.zeros(3, dtype=np.float64)
     per_seq = np.zeros(3 * B, dtype=np.float64)
     w = np.zeros((B, T), dtype=np.float64)
@@ -138,8 +144,8 @@ def loss_from_logps(logp, ref_logp, old, mask, A, eps_lo, eps_hi, beta,
     lib().oracle_loss_from_logps(B, T, _p(lp), _p(rl), _p(od), _p(m), _p(Ad), float(eps_lo),
                                  float(eps_hi), float(beta), float(grad_scale), int(reduction),
                                  KL_TYPES[kl], SURROGATES[surrogate], float(dual_clip_c or 0.0),
-                                 float(norm_constant or 0.0), _p(out3), _p(per_seq), _p(w),
-                                 _p(ratio), _p(counts))
+                                 float(norm_constant or 0.0), int(ratio_level == "sequence"),
+                                 _p(out3), _p(per_seq), _p(w), _p(ratio), _p(counts))
     return {"loss": out3[0], "policy_loss": out3[1], "kl": out3[2],
             "per_seq_policy": per_seq[:B], "per_seq_kl": per_seq[B:2 * B],
             "per_seq_active": per_seq[2 * B:], "w": w, "ratio": ratio,

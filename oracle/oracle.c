@@ -225,6 +225,14 @@ void oracle_log_softmax_rows(const void *rows, int dtype, int64_t nrows, int64_t
  *   surrogate 1, CISPO:  p = -A sg(clip(r)) logp, so g_pol = -A clip(r)
  *     (the clipped weight sits behind a stop-gradient; every token keeps a
  *     gradient through logp).  Not combined with the dual clip.
+ *   sequence-level ratio (seq_ratio 1, GSPO; Relax "REINFORCE++ /
+ *     REINFORCE++-baseline" algorithm table, and dockyard_rl
+ *     "sequence_level_importance_ratios"): every active token of sequence i
+ *     uses rho_i = exp((1/L_i) sum_t (logp - old)) in place of its own r,
+ *     then the clipped surrogate; the policy gradient of token t is
+ *     d/dlogp_it of the sequence-mean loss, c_it (-A rho_i) (0 when rho_i is
+ *     clipped), because each of the L_i equal terms carries rho_i / L_i.
+ *     Sequence mean only (the page rejects the global-token reduction).
  * Clip counters (counts, nullable, [3]): tokens clipped at the upper bound,
  * at the lower bound, and by the dual clip.  For the clipped surrogate the
  * first two are (A > 0 and r > 1 + eps_hi) and (A < 0 and r < 1 - eps_lo) --
@@ -239,7 +247,7 @@ void oracle_loss_from_logps(int64_t B, int64_t T, const double *logp,
                             const uint8_t *mask, const double *A, double eps_lo,
                             double eps_hi, double beta, double grad_scale,
                             int reduction, int kl_type, int surrogate, double dual_c,
-                            double norm_const, double *out3, double *per_seq,
+                            double norm_const, int seq_ratio, double *out3, double *per_seq,
                             double *w, double *ratio, int64_t *counts) {
   double *P = per_seq, *K = per_seq + B, *Ls = per_seq + 2 * B;
   int64_t N = 0, S = 0;
@@ -261,6 +269,13 @@ void oracle_loss_from_logps(int64_t B, int64_t T, const double *logp,
       c = Ls[i] > 0 ? 1.0 / ((double)(S > 0 ? S : 1) * Ls[i]) : 0.0;
     else
       c = 1.0 / norm_const;
+    double rho = 1.0; /* GSPO: the sequence's ratio */
+    if (seq_ratio && Ls[i] > 0) {
+      double s = 0.0;
+      for (int64_t t = 0; t < T; ++t)
+        if (mask[i * T + t]) s += logp[i * T + t] - old[i * T + t];
+      rho = exp(s / Ls[i]);
+    }
     for (int64_t t = 0; t < T; ++t) {
       int64_t j = i * T + t;
       if (!mask[j]) {
@@ -268,7 +283,7 @@ void oracle_loss_from_logps(int64_t B, int64_t T, const double *logp,
         if (ratio) ratio[j] = 0.0;
         continue;
       }
-      double r = exp(logp[j] - old[j]);
+      double r = seq_ratio ? rho : exp(logp[j] - old[j]);
       double a = A[i];
       double rc = r < 1.0 - eps_lo ? 1.0 - eps_lo : (r > 1.0 + eps_hi ? 1.0 + eps_hi : r);
       double p, gpol;

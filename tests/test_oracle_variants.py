@@ -240,3 +240,58 @@ def test_clip_counters_match_zero_gradient_tokens(dual):
     assert res["clip_counts"][1] + res["clip_counts"][2] == (zero & (Ab < 0)).sum()
     if dual is None:
         assert res["clip_counts"][2] == 0
+
+
+# ----------------------------------------------------------------------------
+# GSPO: one ratio per sequence
+# ----------------------------------------------------------------------------
+def test_gspo_finite_differences():
+    # the gradient of token t carries the coupling through rho_i: perturbing
+    # one log-prob moves every token's term of its sequence
+    logp, old, ref, mask, A = _logps_case(29, old_sd=0.3)
+    kw = dict(reduction=oracle.SEQUENCE_MEAN, ratio_level="sequence")
+    res = _loss(logp, old, ref, mask, A, **kw)
+    near = _near_kink(res["ratio"], A)
+    checked = 0
+    for b in range(logp.shape[0]):
+        if near[b][mask[b].astype(bool)].any():
+            continue
+        for t in range(logp.shape[1]):
+            if not mask[b, t]:
+                continue
+            h = 1e-6
+            lpp = logp.copy(); lpp[b, t] += h
+            lpm = logp.copy(); lpm[b, t] -= h
+            fd = (_loss(lpp, old, ref, mask, A, **kw)["loss"]
+                  - _loss(lpm, old, ref, mask, A, **kw)["loss"]) / (2 * h)
+            assert fd == pytest.approx(res["w"][b, t], rel=1e-6, abs=1e-10), (b, t)
+            checked += 1
+    assert checked > 15
+
+
+def test_gspo_reduces_to_token_ratios():
+    logp, old, ref, mask, A = _logps_case(31, T=9)
+    kw = dict(reduction=oracle.SEQUENCE_MEAN)
+    # single-token sequences: rho_i is the token's own ratio, bit for bit
+    one = np.zeros_like(mask)
+    one[:, 3] = 1
+    a = _loss(logp, old, ref, one, A, **kw)
+    b = _loss(logp, old, ref, one, A, ratio_level="sequence", **kw)
+    for k in ("loss", "policy_loss", "kl"):
+        assert a[k] == b[k]
+    assert np.array_equal(a["w"], b["w"])
+    # equal log ratios within each sequence: the same loss up to rounding
+    same = logp - (logp[:, :1] - old[:, :1])
+    c = _loss(logp, same, ref, mask, A, **kw)
+    d = _loss(logp, same, ref, mask, A, ratio_level="sequence", **kw)
+    assert d["loss"] == pytest.approx(c["loss"], rel=1e-13)
+    assert np.allclose(d["w"], c["w"], rtol=1e-12, atol=1e-18)
+
+
+def test_gspo_rejects_token_level_reductions_and_cispo():
+    logp, old, ref, mask, A = _logps_case(1)
+    with pytest.raises(ValueError):
+        _loss(logp, old, ref, mask, A, ratio_level="sequence")  # token mean
+    with pytest.raises(ValueError):
+        _loss(logp, old, ref, mask, A, ratio_level="sequence", reduction=oracle.SEQUENCE_MEAN,
+              surrogate="cispo")
