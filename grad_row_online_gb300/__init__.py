@@ -83,7 +83,7 @@ class _Params(ctypes.Structure):
                 ("grad_scale", ctypes.c_float), ("reduction", ctypes.c_int32),
                 ("flags", ctypes.c_uint32), ("kl_type", ctypes.c_int32),
                 ("surrogate", ctypes.c_int32), ("dual_clip_c", ctypes.c_float),
-                ("norm_constant", ctypes.c_float), ("_reserved", ctypes.c_int32),
+                ("norm_constant", ctypes.c_float), ("ratio_level", ctypes.c_int32),
                 ("profile", ctypes.POINTER(_Profile)), ("shard", ctypes.POINTER(_Shard)),
                 ("clip_counts", ctypes.c_void_p)]
 
@@ -172,8 +172,9 @@ def _groups(B: int, samples_per_prompt: int, group_boundaries) -> tuple[_Groups,
 
 def _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction, flags, profile,
             kl="k3", surrogate="clip", dual_clip_c=None, norm_constant=None, clip_counts=None,
-            shard: Optional[Shard] = None):
+            shard: Optional[Shard] = None, ratio_level: str = "token"):
     p = _Params()
+    p.ratio_level = {"token": 0, "sequence": 1}[ratio_level]
     if shard is not None:
         _dev(shard.global_counts, "global_counts", torch.int64)
         _dev(shard.totals, "totals", torch.uint8)
@@ -248,14 +249,16 @@ def grpo_loss_fwd_bwd(policy_logits: torch.Tensor, ref_logits: torch.Tensor,
                       workspace: Optional[torch.Tensor] = None, stream=None,
                       profile=None, kl: str = "k3", surrogate: str = "clip",
                       dual_clip_c: Optional[float] = None, norm_constant: Optional[float] = None,
-                      want_clip_counts: bool = False, shard: Optional[Shard] = None) -> dict:
+                      want_clip_counts: bool = False, shard: Optional[Shard] = None,
+                      ratio_level: str = "token") -> dict:
     """Fused GRPO loss forward + dL/dlogits.
 
     ``grad``: True (allocate), a tensor to write into (may be
     ``policy_logits`` itself for an in-place gradient), or None/False
     (forward only).  Variants: ``kl`` in {"k3", "k1", "k2"}, ``surrogate``
     in {"clip", "cispo"}, ``dual_clip_c`` (> 1), ``reduction=
-    "fixed_constant"`` with ``norm_constant``.  Returns a dict of device
+    "fixed_constant"`` with ``norm_constant``, ``ratio_level="sequence"``
+    (GSPO, with ``reduction="sequence_mean"``).  Returns a dict of device
     tensors: ``out3`` ([loss, policy_loss, kl]), ``loss``, ``policy_loss``,
     ``kl`` (0-d views), ``grad``, and the optional ``per_seq`` [3,B],
     ``logps`` [B,T], ``adv`` [B], ``clip_counts`` [3] (int64: clipped at the
@@ -288,7 +291,7 @@ def grpo_loss_fwd_bwd(policy_logits: torch.Tensor, ref_logits: torch.Tensor,
     p, prof = _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction,
                       (GRPO_ADV_EPS_ADD if eps_add else 0)
                       | (GRPO_SKIP_MASKED_GRAD_ROWS if skip_masked_grad_rows else 0), profile,
-                      kl, surrogate, dual_clip_c, norm_constant, counts, shard)
+                      kl, surrogate, dual_clip_c, norm_constant, counts, shard, ratio_level)
     if grad is True:
         grad_t = torch.empty_like(policy_logits)
     elif grad is None or grad is False:
@@ -350,7 +353,8 @@ def grpo_loss_from_logps(logps: torch.Tensor, old_logps: torch.Tensor,
                          profile=None, kl: str = "k3", surrogate: str = "clip",
                          dual_clip_c: Optional[float] = None,
                          norm_constant: Optional[float] = None,
-                         want_clip_counts: bool = False, shard: Optional[Shard] = None) -> dict:
+                         want_clip_counts: bool = False, shard: Optional[Shard] = None,
+                         ratio_level: str = "token") -> dict:
     """GRPO loss from per-token log-probs; ``grad`` gives dL/dlogp [B,T].
     Variants, outputs and ``shard`` as in grpo_loss_fwd_bwd."""
     _dev(logps, "logps", torch.float32)
@@ -368,7 +372,7 @@ def grpo_loss_from_logps(logps: torch.Tensor, old_logps: torch.Tensor,
     counts = torch.empty(3, dtype=torch.int64, device=dev) if want_clip_counts else None
     p, prof = _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction,
                       GRPO_ADV_EPS_ADD if eps_add else 0, profile, kl, surrogate, dual_clip_c,
-                      norm_constant, counts, shard)
+                      norm_constant, counts, shard, ratio_level)
     if grad is True:
         grad_t = torch.empty((B, T), dtype=torch.float32, device=dev)
     elif grad is None or grad is False:

@@ -47,6 +47,10 @@ grpo_status_t check_params(const grpo_params_t* p) {
     if (!(isfinite(p->dual_clip_c) && p->dual_clip_c > 1.f)) return GRPO_ERR_PARAM;
     if (p->surrogate != GRPO_SURROGATE_CLIP) return GRPO_ERR_PARAM;
   }
+  if (p->ratio_level != 0 && p->ratio_level != 1) return GRPO_ERR_PARAM;
+  if (p->ratio_level == 1 &&
+      (p->reduction != GRPO_SEQUENCE_MEAN || p->surrogate != GRPO_SURROGATE_CLIP))
+    return GRPO_ERR_PARAM;  // GSPO is sequence-level only
   if (p->clip_counts && ((uintptr_t)p->clip_counts & 7)) return GRPO_ERR_ALIGN;
   return GRPO_OK;
 }
@@ -59,6 +63,7 @@ Variant variant_of(const grpo_params_t* p) {
   v.dual_c = p->dual_clip_c;
   v.kl_type = p->kl_type;
   v.surrogate = p->surrogate;
+  v.seq_ratio = p->ratio_level;
   return v;
 }
 
@@ -228,6 +233,7 @@ extern "C" grpo_status_t grpo_loss_fwd_bwd(
   cudaError_t e = launch_prep(pa, s);
   if (e != cudaSuccess) return GRPO_ERR_CUDA;
 
+  const Variant var = variant_of(params);
   if (any_rows) {
     RowArgs ra;
     ra.policy = policy_logits;
@@ -254,15 +260,30 @@ extern "C" grpo_status_t grpo_loss_fwd_bwd(
     ra.flags = params->flags;
     ra.precise_ok = dt == GRPO_F32;
     ra.tab = exp_table();
-    ra.var = variant_of(params);
+    ra.var = var;
     ra.norm_c = params->norm_constant;
+    if (var.seq_ratio) {  // GSPO: sweep 1, the per-sequence step, sweep 2
+      if (launch_gspo_rows(ra, dt, 1, params->profile, s) != cudaSuccess) return GRPO_ERR_CUDA;
+      ReduceArgs rd{completion_mask, L, A + pl.seq_begin, totals, slot_p, slot_k, B, T,
+                    params->beta, params->reduction, hdr, NS, out3, per_seq, 1,
+                    params->norm_constant, params->clip_counts, pl.shard ? 1 : 0, var, old_logps,
+                    params->grad_scale};
+      if (launch_reduce(rd, s) != cudaSuccess) return GRPO_ERR_CUDA;
+      if (grad_logits && launch_gspo_rows(ra, dt, 2, params->profile, s) != cudaSuccess)
+        return GRPO_ERR_CUDA;
+      if (!grad_logits && params->profile && params->profile->stop)
+        cudaEventRecord((cudaEvent_t)params->profile->stop, s);
+      return GRPO_OK;
+    }
     e = launch_rows(ra, dt, params->profile, s);
     if (e != cudaSuccess) return GRPO_ERR_CUDA;
   }
+  Variant rv = var;
+  rv.seq_ratio = 0;  // no rows: nothing for the GSPO step to do
   ReduceArgs rd{completion_mask, L, A + pl.seq_begin, totals, slot_p, slot_k, B, T,
                 params->beta, params->reduction, hdr, NS, out3, per_seq,
-                variant_of(params).splits_A() ? 1 : 0, params->norm_constant,
-                params->clip_counts, pl.shard ? 1 : 0};
+                var.splits_A() ? 1 : 0, params->norm_constant,
+                params->clip_counts, pl.shard ? 1 : 0, rv, old_logps, params->grad_scale};
   return cuda_status(launch_reduce(rd, s));
 }
 

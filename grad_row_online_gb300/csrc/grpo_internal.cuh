@@ -30,6 +30,7 @@ struct WsHeader {
   unsigned int status;             // device-detected error bits
   unsigned int done_ctas;          // reduce: CTAs finished (the last one forms the scalar)
   unsigned long long row_counter;  // rows: next row to claim
+  unsigned long long row_counter2; // GSPO's second row sweep: next row to claim
   unsigned long long N;            // active tokens  (prep: integer atomics, exact)
   unsigned long long S;            // live sequences (idem)
   unsigned long long clip[3];      // clipped tokens: upper, lower, dual (integer atomics)
@@ -380,8 +381,10 @@ struct Variant {
   float dual_c;  // 0: off; > 1: the dual clip on negative-advantage tokens
   int kl_type;   // grpo_kl_t
   int surrogate; // grpo_surrogate_t
+  int seq_ratio; // 1: GSPO, one ratio per sequence (em is then the sequence's rho - 1)
   __host__ __device__ bool is_default() const {
-    return kl_type == GRPO_KL_K3 && surrogate == GRPO_SURROGATE_CLIP && dual_c == 0.f;
+    return kl_type == GRPO_KL_K3 && surrogate == GRPO_SURROGATE_CLIP && dual_c == 0.f &&
+           seq_ratio == 0;
   }
   // the policy term's constant -A is summed per sequence (clipped surrogate)
   __host__ __device__ bool splits_A() const { return surrogate == GRPO_SURROGATE_CLIP; }
@@ -668,7 +671,7 @@ struct ReduceArgs {
   const double* A;
   SeqTotal* seq;  // [B] per-sequence totals
   const double* slot_p;
-  const double* slot_k;
+  double* slot_k;
   int64_t B, T;
   float beta;
   int reduction;
@@ -680,6 +683,11 @@ struct ReduceArgs {
   float norm_c;     // GRPO_FIXED_CONSTANT's constant
   unsigned long long* counts_out;  // nullable [3]
   int shard;        // 1: write the totals only (the scalar comes from grpo_loss_finalize)
+  // GSPO (var.seq_ratio): the slots hold logp and d = ref_logp - logp; this
+  // kernel forms rho_i, the per-token terms and w (written over d)
+  Variant var;
+  const float* old;
+  float grad_scale;
 };
 
 struct LogpsArgs {
@@ -710,6 +718,8 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 cudaError_t launch_rows(const RowArgs& a, grpo_dtype_t dt, const grpo_profile_t* prof,
                         cudaStream_t s);
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t s);
+cudaError_t launch_gspo_rows(const RowArgs& a, grpo_dtype_t dt, int phase,
+                             const grpo_profile_t* prof, cudaStream_t s);
 cudaError_t launch_logps(const LogpsArgs& a, const grpo_profile_t* prof, cudaStream_t s);
 cudaError_t launch_finalize(const SeqTotal* recs, int64_t B, const unsigned long long* NS,
                             int reduction, float norm_c, float beta, float* out3, cudaStream_t s);

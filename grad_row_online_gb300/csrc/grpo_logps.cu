@@ -68,9 +68,11 @@ __device__ __forceinline__ Em expm1_k3(float d) {
 // per sequence, as -A_i L_i in float pairs from the float-pair advantage
 // (with a full mask the A_i of a group cancel there, which an fp32 A rounded
 // per token would break).
+// (em_seq: GSPO's rho_i - 1 for the whole sequence, used in place of the
+// token's own ratio when the call asks for sequence-level ratios.)
 __device__ __forceinline__ TokEpi<float> tok_terms(float lp, float o, float rf, float A,
-                                                   const LogpsArgs& a) {
-  const float em = expm1_k3(__fsub_rn(lp, o)).em;  // r - 1
+                                                   const LogpsArgs& a, float em_seq) {
+  const float em = a.var.seq_ratio ? em_seq : expm1_k3(__fsub_rn(lp, o)).em;  // r - 1
   const float d = a.ref ? __fsub_rn(rf, lp) : 0.0f;
   const Em kd = expm1_k3(d);
   return token_epilogue<float>(em, lp, d, kd.em, kd.k3, a.ref != nullptr, A, a.var);
@@ -84,6 +86,8 @@ struct SeqCtx {
   int64_t b;          // the sequence
   int L;              // its active tokens
   unsigned long long N, S;
+  float em_seq;       // GSPO: rho_i - 1 (fp32 and double)
+  double em_seq_d;
 };
 __device__ __noinline__ float w_precise(float lp, float o, float rf, const SeqCtx& x,
                                         const LogpsArgs& a) {
@@ -91,7 +95,7 @@ __device__ __noinline__ float w_precise(float lp, float o, float rf, const SeqCt
   const double c = a.reduction == GRPO_TOKEN_MEAN      ? 1.0 / (double)(x.N > 0 ? x.N : 1)
                    : a.reduction == GRPO_SEQUENCE_MEAN ? 1.0 / ((double)(x.S > 0 ? x.S : 1) * (double)x.L)
                                                        : 1.0 / (double)a.norm_c;
-  const double em = expm1((double)lp - (double)o);
+  const double em = a.var.seq_ratio ? x.em_seq_d : expm1((double)lp - (double)o);
   const double d = a.ref ? (double)rf - (double)lp : 0.0;
   const double emd = expm1(d);
   const TokEpi<double> t =
@@ -227,7 +231,7 @@ __device__ __forceinline__ void vec_general(uint32_t mw, const float4& l4, const
   for (int j = 0; j < 4; ++j) {
     w[j] = 0.f;
     if ((mw >> (8 * j)) & 0xFFu) {
-      const TokEpi<float> t = tok_terms(lp[j], od[j], rf[j], x.A, a);
+      const TokEpi<float> t = tok_terms(lp[j], od[j], rf[j], x.A, a, x.em_seq);
       vq = __fadd_rn(vq, t.q);
       vk = __fadd_rn(vk, t.k);
       acc.count(t.clip);
@@ -322,6 +326,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
   __shared__ FF s_ff[2][kLogpsThreads / 32];
   __shared__ unsigned s_nc[3][kLogpsThreads / 32];
   __shared__ FinalSmem s_fin;
+  __shared__ double s_em[1];
   __shared__ bool s_last;
   __shared__ __align__(16) Stage s_st[kDepth];
   __shared__ __align__(8) uint64_t s_full[kDepth];
@@ -366,6 +371,27 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
       f.g2_max = __fmul_rn(gm, gm);
     }
     const int64_t base = b * a.T;
+    x.em_seq = 0.f;
+    x.em_seq_d = 0.0;
+    if (a.var.seq_ratio) {
+      // GSPO: rho_i = exp(mean over the active tokens of logp - old), before
+      // any token's term (Kahan sums per thread, float pairs across the CTA)
+      float ss = 0.f, sc = 0.f;
+      for (int64_t t = threadIdx.x; t < a.T; t += blockDim.x)
+        if (a.mask[base + t]) kahan(ss, sc, __fsub_rn(a.logps[base + t], a.old[base + t]));
+      const FF wsum = warp_sum_ff2(FF{ss, -sc});
+      if (lane == 0) s_ff[0][warp] = wsum;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        FF tot = s_ff[0][0];
+        for (int k = 1; k < kLogpsThreads / 32; ++k) tot = ff_add(tot, s_ff[0][k]);
+        const double em = x.L > 0 ? expm1(((double)tot.hi + (double)tot.lo) / (double)x.L) : 0.0;
+        s_em[0] = em;
+      }
+      __syncthreads();
+      x.em_seq_d = s_em[0];
+      x.em_seq = (float)x.em_seq_d;
+    }
     Acc acc;
     if (staged_ok(a)) {
       const int2 rg = a.range[b];
@@ -459,7 +485,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
         if (a.mask[base + t]) {
           const float lp = a.logps[base + t], o = a.old[base + t];
           const float rf = a.ref ? a.ref[base + t] : 0.f;
-          const TokEpi<float> tt = tok_terms(lp, o, rf, x.A, a);
+          const TokEpi<float> tt = tok_terms(lp, o, rf, x.A, a, x.em_seq);
           kahan(acc.sq, acc.cq, tt.q);
           kahan(acc.sk, acc.ck, tt.k);
           acc.count(tt.clip);

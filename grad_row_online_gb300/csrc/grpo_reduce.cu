@@ -25,6 +25,8 @@ static constexpr int kReduceThreads = 256;
 
 __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs a) {
   __shared__ double s_d[32 * 2];
+  __shared__ unsigned s_u[3 * 32];
+  __shared__ double s_em;
   __shared__ FinalSmem s_fin;
   __shared__ bool s_last;
   const int64_t i = blockIdx.x;
@@ -34,16 +36,44 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs
   if (i < a.B) {
     const uint8_t* m = a.mask + i * a.T;
     const double* sp = a.slot_p + i * a.T;
-    const double* sk = a.slot_k + i * a.T;
+    double* sk = a.slot_k + i * a.T;
+    const int L = a.L[i];
     double v[2] = {0.0, 0.0};
-    for (int64_t t = threadIdx.x; t < a.T; t += blockDim.x)
-      if (m[t]) {
-        v[0] += sp[t];
-        v[1] += sk[t];
-      }
+    unsigned nc[3] = {0u, 0u, 0u};
+    if (a.var.seq_ratio) {
+      // GSPO: the slots hold logp and d = ref_logp - logp.  rho_i first (a
+      // fixed-order sum over the sequence), then every token's terms with
+      // rho_i in place of its own ratio, and w = dL/dlogp written over d.
+      double s1[1] = {0.0};
+      for (int64_t t = threadIdx.x; t < a.T; t += blockDim.x)
+        if (m[t]) s1[0] += sp[t] - (double)a.old[i * a.T + t];
+      block_sum<double, 1>(s1, s_d);
+      if (threadIdx.x == 0) s_em = L > 0 ? expm1(s1[0] / (double)L) : 0.0;
+      __syncthreads();
+      const double em = s_em, A = a.A[i];
+      const unsigned long long S = a.NS[1];
+      const double c = L > 0 ? 1.0 / ((double)(S > 0 ? S : 1) * (double)L) : 0.0;
+      for (int64_t t = threadIdx.x; t < a.T; t += blockDim.x)
+        if (m[t]) {
+          const double lp = sp[t], d = sk[t], emd = expm1(d);
+          const TokEpi<double> te = token_epilogue<double>(em, lp, d, emd, emd - d, true, A, a.var);
+          v[0] += te.q;
+          v[1] += te.k;
+          sk[t] = (double)a.grad_scale * c * te.g;
+          if (te.clip == 1) ++nc[0];
+          else if (te.clip == 2) ++nc[1];
+          else if (te.clip == 3) ++nc[2];
+        }
+    } else {
+      for (int64_t t = threadIdx.x; t < a.T; t += blockDim.x)
+        if (m[t]) {
+          v[0] += sp[t];
+          v[1] += sk[t];
+        }
+    }
     block_sum<double, 2>(v, s_d);
+    if (a.var.seq_ratio && a.counts_out) block_sum<unsigned, 3>(nc, s_u);
     if (threadIdx.x == 0) {
-      const int L = a.L[i];
       const double P = a.split_A ? v[0] - a.A[i] * (double)L : v[0];
       put_total(a.seq + i, P, v[1], L);
       if (a.per_seq) {
@@ -51,24 +81,22 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs
         a.per_seq[a.B + i] = (float)v[1];
         a.per_seq[2 * a.B + i] = (float)L;
       }
-      if (i == 0 && a.counts_out)  // the row kernel's CTAs added their counts before this launch
-        for (int j = 0; j < 3; ++j) a.counts_out[j] = a.hdr->clip[j];
-      if (a.shard) {
-        s_last = false;  // the scalar comes from grpo_loss_finalize over all shards' totals
-      } else {
-        __threadfence();
-        const unsigned ticket = atomicAdd(&a.hdr->done_ctas, 1u);
-        s_last = ticket == gridDim.x - 1;
-      }
+      if (a.var.seq_ratio && a.counts_out) add_clip_counts(a.hdr, nc);
+      __threadfence();
+      const unsigned ticket = atomicAdd(&a.hdr->done_ctas, 1u);
+      s_last = ticket == gridDim.x - 1;
     }
   } else if (threadIdx.x == 0) {
-    s_last = !a.shard;  // B == 0: a single CTA writes the zero loss
-    if (a.counts_out)
-      for (int j = 0; j < 3; ++j) a.counts_out[j] = a.hdr->clip[j];
+    s_last = true;  // B == 0: a single CTA
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  // the clip counts: the row kernel added its before this launch, the GSPO
+  // step above before each CTA's ticket
+  if (threadIdx.x == 0 && a.counts_out)
+    for (int j = 0; j < 3; ++j) a.counts_out[j] = __ldcg(&a.hdr->clip[j]);
+  if (a.shard) return;  // the scalar comes from grpo_loss_finalize over all shards' totals
 
   // level 2: the scalar, over the B sequence records in index order
   const bool bad = ((volatile unsigned*)&a.hdr->status)[0] != 0u;

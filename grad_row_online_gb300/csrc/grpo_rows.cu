@@ -252,7 +252,7 @@ __device__ void grad_row(const T* x, T* g, int64_t V, int64_t act, const RowScal
   };
   // vectors [0, nsm) were kept in shared memory by sweep 1; the rest, in the
   // sweep order, from global memory (mostly L2)
-  const int64_t nsm = n < kPolicySmemVecs ? n : kPolicySmemVecs;
+  const int64_t nsm = kept ? (n < kPolicySmemVecs ? n : kPolicySmemVecs) : 0;
   const int64_t ng = n - nsm;
   auto atg = [&](int64_t k) -> int64_t { return kReverseSweep2 ? n - 1 - k : nsm + k; };
   constexpr int U = kGradUnroll;
@@ -413,6 +413,179 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(cons
     row = s_next;
   }
   if (threadIdx.x == 0) add_clip_counts(a.hdr, n_clip);
+}
+
+// ------------------------------------------------------------------ GSPO
+// Sequence-level ratios need every token's log-prob of a sequence before any
+// gradient of it, so the fused row pass splits in two around the
+// per-sequence step in grpo_reduce.cu:
+//   gspo_sweep1_kernel  sweep 1 and the finish of every active row: logp and
+//                       d = ref_logp - logp into the two token slots (both
+//                       rows refined to double when the gradient is fp32);
+//   (reduce)            rho_i, the per-token terms and w into the slots;
+//   gspo_sweep2_kernel  sweep 2 of every row from (logp, w): the gradient,
+//                       zeros on masked rows.
+// Rows are claimed from two device counters, as in rows_kernel.
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) gspo_sweep1_kernel(const RowArgs a) {
+  __shared__ float s_f[64];
+  __shared__ FF s_zs[64];
+  __shared__ double s_d[64];
+  __shared__ float s_thi[64], s_tlo[64];
+  __shared__ RowScalars s_rs;
+  __shared__ float s_M[2];
+  __shared__ long long s_next;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x < 64) {
+    s_thi[threadIdx.x] = a.tab.hi[threadIdx.x];
+    s_tlo[threadIdx.x] = a.tab.lo[threadIdx.x];
+  }
+  if (threadIdx.x == 0) s_next = (long long)atomicAdd(&a.hdr->row_counter, 1ull);
+  __syncthreads();
+  const int64_t BT = a.B * a.T;
+  const bool refine = a.precise_ok && a.grad != nullptr;
+  const uint64_t stream = l2_evict_first();
+  int64_t row = s_next;
+  while (row < BT) {
+    long long claim = 0;
+    if (threadIdx.x == 0) claim = (long long)atomicAdd(&a.hdr->row_counter, 1ull);
+    const T* x = reinterpret_cast<const T*>(a.policy) + row * a.V;
+    const T* y = reinterpret_cast<const T*>(a.ref) + row * a.V;
+    const bool active = a.mask[row] != 0;
+    const int64_t act = active ? a.actions[row] : 0;
+    if (!active) {
+      if (threadIdx.x == 0 && a.logps_out) a.logps_out[row] = 0.f;
+    } else if (act < 0 || act >= a.V) {
+      if (threadIdx.x == 0) {
+        atomicOr(&a.hdr->status, (unsigned)GRPO_ERR_ACTION_RANGE);
+        a.slot_p[row] = NAN;
+        a.slot_k[row] = NAN;
+        if (a.logps_out) a.logps_out[row] = NAN;
+      }
+    } else {
+      float xa = 0.f, ya = 0.f, o = 0.f;
+      if (threadIdx.x == 0) {
+        xa = Storage<T>::load1(x + act);
+        ya = Storage<T>::load1(y + act);
+        o = __ldg(a.old + row);
+      }
+      OnlineLse sp, sr;
+      sp.init();
+      sr.init();
+      lse_pair<T>(x, y, a.V, sp, sr, stream, stream, nullptr);
+      float Mp, Mr;
+      FF Zp = {0.f, 0.f}, Zr = {0.f, 0.f};
+      combine_ff(sp, sr, s_f, s_zs, Mp, Mr, Zp, Zr);
+      if (threadIdx.x == 0) {
+        s_rs = finish_fast(a, __fmul_rn(Mp, kLog2e), Zp, __fmul_rn(Mr, kLog2e), Zr, xa, ya, o,
+                           0.f, 0.f, false);
+        s_M[0] = Mp;
+        s_M[1] = Mr;
+      }
+      __syncthreads();
+      if (refine) {  // block-uniform: both rows in double (the ratio is a sequence mean)
+        const float RMp = s_M[0], RMr = s_M[1];
+        const double zp = sum_exp_precise<T>(x, a.V, RMp, s_thi, s_tlo, a.tab, s_d);
+        const double zr = sum_exp_precise<T>(y, a.V, RMr, s_thi, s_tlo, a.tab, s_d);
+        if (warp == 0) {
+          const RowScalars rs = finish_precise(a, (double)RMp, zp, (double)RMr, zr, xa, ya, o,
+                                               0.0, 0.0);
+          if (lane == 0) s_rs = rs;
+        }
+        __syncthreads();
+      }
+      if (threadIdx.x == 0) {
+        a.slot_p[row] = s_rs.logp;
+        a.slot_k[row] = s_rs.dlr;
+        if (a.logps_out) a.logps_out[row] = (float)s_rs.logp;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) s_next = claim;
+    __syncthreads();
+    row = s_next;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) gspo_sweep2_kernel(const RowArgs a) {
+  __shared__ RowScalars s_rs;
+  __shared__ long long s_next;
+  if (threadIdx.x == 0) s_next = (long long)atomicAdd(&a.hdr->row_counter2, 1ull);
+  __syncthreads();
+  const int64_t BT = a.B * a.T;
+  const bool zero_masked = !(a.flags & GRPO_SKIP_MASKED_GRAD_ROWS);
+  const uint64_t stream = l2_evict_first();
+  int64_t row = s_next;
+  while (row < BT) {
+    long long claim = 0;
+    if (threadIdx.x == 0) claim = (long long)atomicAdd(&a.hdr->row_counter2, 1ull);
+    const T* x = reinterpret_cast<const T*>(a.policy) + row * a.V;
+    T* grow = reinterpret_cast<T*>(a.grad) + row * a.V;
+    const bool active = a.mask[row] != 0;
+    const int64_t act = active ? a.actions[row] : 0;
+    if (!active || act < 0 || act >= a.V) {
+      if (zero_masked) zero_row<T>(grow, a.V, stream);
+    } else {
+      if (threadIdx.x == 0) {  // the row's scalars from logp and w
+        const double lp = a.slot_p[row], w = a.slot_k[row];
+        RowScalars rs;
+        rs.lse_p = (double)Storage<T>::load1(x + act) - lp;
+        rs.w = w;
+        rs.wneg = (float)(-w);
+        rs.LL = (float)(rs.lse_p * (double)kLog2e);
+        rs.ga = (float)(-w * expm1(lp));
+        rs.q = rs.k = 0.0;
+        rs.logp = lp;
+        rs.dlr = 0.0;
+        rs.precise = a.precise_ok;
+        rs.clip = 0;
+        s_rs = rs;
+      }
+      __syncthreads();
+      const RowScalars rs = s_rs;
+      if (rs.precise)
+        grad_row<T, true>(x, grow, a.V, act, rs, stream, stream, nullptr);
+      else
+        grad_row<T, false>(x, grow, a.V, act, rs, stream, stream, nullptr);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) s_next = claim;
+    __syncthreads();
+    row = s_next;
+  }
+}
+
+template <typename T>
+static cudaError_t launch_gspo_t(const RowArgs& a, int phase, const grpo_profile_t* prof,
+                                 cudaStream_t s) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  int64_t grid = (int64_t)sms * kRowBlocksPerSM;
+  const int64_t rows = a.B * a.T;
+  if (grid > rows) grid = rows;
+  if (grid < 1) return cudaSuccess;
+  if (phase == 1) {
+    if (prof && prof->start) cudaEventRecord((cudaEvent_t)prof->start, s);
+    gspo_sweep1_kernel<T><<<(unsigned)grid, kRowThreads, 0, s>>>(a);
+  } else {
+    gspo_sweep2_kernel<T><<<(unsigned)grid, kRowThreads, 0, s>>>(a);
+  }
+  e = cudaGetLastError();
+  if (phase == 2 && prof && prof->stop) cudaEventRecord((cudaEvent_t)prof->stop, s);
+  return e;
+}
+
+cudaError_t launch_gspo_rows(const RowArgs& a, grpo_dtype_t dt, int phase,
+                             const grpo_profile_t* prof, cudaStream_t s) {
+  switch (dt) {
+    case GRPO_F32: return launch_gspo_t<float>(a, phase, prof, s);
+    case GRPO_BF16: return launch_gspo_t<__nv_bfloat16>(a, phase, prof, s);
+    default: return launch_gspo_t<__half>(a, phase, prof, s);
+  }
 }
 
 template <typename T>

@@ -39,6 +39,7 @@ struct RowScalars {
   float ga;           // gradient at the action element
   int precise;      // bit 0: policy row refined, bit 1: reference row refined
   int clip;         // 0, or the clip that bound: 1 upper, 2 lower, 3 dual
+  double dlr;       // ref_logp - logp
 };
 
 // vector geometry of a row: `head` scalars up to the first 16-byte boundary,
@@ -159,6 +160,7 @@ __device__ __forceinline__ RowScalars finish_fast(const RowArgs& a, float MLp, F
   r.ga = -__fmul_rn(w, emlp);
   r.precise = 0;
   r.clip = t.clip;
+  r.dlr = (double)d;
   if (want_grad && a.precise_ok) {
     // sensitivities of w to the two rows' logsumexp: the KL part's slope
     // (both rows), the policy part's |A| r (policy row), w itself (p_a)
@@ -210,6 +212,7 @@ static __device__ __forceinline__ RowScalars finish_precise(const RowArgs& a, do
   r.ga = (float)(-w * emlp);
   r.precise = 1;
   r.clip = t.clip;
+  r.dlr = d;
   return r;
 }
 

@@ -169,7 +169,12 @@ typedef struct {
                          where r > c.  Only with GRPO_SURROGATE_CLIP. */
   float norm_constant; /* GRPO_FIXED_CONSTANT: the declared constant, finite and
                           > 0; ignored by the other reductions */
-  int32_t _reserved;
+  int32_t ratio_level; /* 0: token ratios r_t.  1: GSPO, one ratio per sequence,
+                          rho_i = exp(mean over its active tokens of logp - old),
+                          used by every token of the sequence in the clipped
+                          surrogate (Relax "REINFORCE++ / REINFORCE++-baseline",
+                          GSPO row; dockyard_rl sequence_level_importance_ratios).
+                          Needs GRPO_SEQUENCE_MEAN and GRPO_SURROGATE_CLIP. */
   const grpo_profile_t *profile; /* host pointer or NULL */
   const grpo_shard_t *shard;     /* host pointer or NULL (the whole batch) */
   unsigned long long *clip_counts; /* device [3] or NULL: overwritten with the

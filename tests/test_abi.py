@@ -123,6 +123,9 @@ def test_fwd_rejects_bad_arguments(lib):
     assert _fwd(lib, p=_params(dual_clip_c=float("nan"))) == 6
     assert _fwd(lib, p=_params(surrogate=1, dual_clip_c=3.0)) == 6  # not with CISPO
     assert _fwd(lib, p=_params(clip_counts=FAKE + 4)) == 4  # misaligned counter array
+    assert _fwd(lib, p=_params(ratio_level=2)) == 6
+    assert _fwd(lib, p=_params(ratio_level=1)) == 6  # GSPO needs the sequence mean
+    assert _fwd(lib, p=_params(ratio_level=1, reduction=1, surrogate=1)) == 6  # not with CISPO
     assert _fwd(lib, dt=1, policy=FAKE + 1) == 4      # bf16 pointer not 2-byte aligned
     assert _fwd(lib, act=FAKE + 4) == 4               # int64 ids
     assert _fwd(lib, ws=FAKE + 16) == 4               # workspace alignment

@@ -44,6 +44,7 @@ OPTIONS = {
     "sequence-mean": dict(reduction="sequence_mean"),
     "fixed-k2-dual": dict(reduction="fixed_constant", norm_constant=40.0, kl="k2",
                           dual_clip_c=1.4),
+    "gspo": dict(reduction="sequence_mean", ratio_level="sequence"),
 }
 
 

@@ -1,5 +1,6 @@
 """Parity of the loss variants -- KL estimators k1 / k2, the dual clip, CISPO,
-the fixed-constant (Dr.GRPO) normaliser -- and of the clip counters, CUDA
+the fixed-constant (Dr.GRPO) normaliser, GSPO's sequence-level ratio -- and
+of the clip counters, CUDA
 library against the oracle, on both boundaries (logits and per-token
 log-probs), with ratios spread wide enough that every clip binds."""
 import numpy as np
@@ -34,13 +35,17 @@ VARIANTS = {
     "k2-dual-seqmean": dict(kl="k2", dual_clip_c=1.25, reduction="sequence_mean"),
     "cispo-k1-fixed": dict(surrogate="cispo", kl="k1", reduction="fixed_constant",
                            norm_constant=7.0),
+    "gspo": dict(ratio_level="sequence", reduction="sequence_mean"),
+    "gspo-k2-dual": dict(ratio_level="sequence", reduction="sequence_mean", kl="k2",
+                         dual_clip_c=1.3),
     "default": dict(),
 }
 _RED = {"token_mean": 0, "sequence_mean": 1, "fixed_constant": 2}
 
 
 def _oracle_kw(v: dict, w) -> dict:
-    kw = {k: v[k] for k in ("kl", "surrogate", "dual_clip_c", "norm_constant") if k in v}
+    kw = {k: v[k] for k in ("kl", "surrogate", "dual_clip_c", "norm_constant", "ratio_level")
+          if k in v}
     kw["reduction"] = _RED[v["reduction"]] if "reduction" in v else w.reduction
     return kw
 
