@@ -306,7 +306,28 @@ def l2_note(w: synth.Workload) -> str:
             f"({LogpsCase.COPIES * per_copy / 1e6:.0f} MB, larger than L2)")
 
 
-def workload_config(w: synth.Workload) -> dict:
+# loss variants a run may time (keyword arguments of the two entry points);
+# "default" is the GRPO loss of the operator page
+VARIANTS = {
+    "default": {},
+    "k1": {"kl": "k1"},
+    "k2": {"kl": "k2"},
+    "dual-clip": {"dual_clip_c": 3.0},
+    "cispo": {"surrogate": "cispo"},
+    "fixed-constant": {"reduction": "fixed_constant"},  # C = B*T, set per workload
+    "gspo": {"ratio_level": "sequence", "reduction": "sequence_mean"},
+}
+
+
+def variant_kwargs(name: str, w: synth.Workload) -> dict:
+    kw = dict(VARIANTS[name])
+    if kw.get("reduction") == "fixed_constant":
+        kw["norm_constant"] = float(w.B * w.T)
+    return kw
+
+
+def workload_config(w: synth.Workload, variant: str = "default",
+                    skip_masked: bool = False) -> dict:
     act = int(w.completion_mask().sum())
     note = l2_note(w)
     cfg = {"workload": f"{w.name}: B={w.B} T={w.T}" + (f" V={w.V} {w.dtype}" if w.V else " logps f32"),
@@ -316,6 +337,12 @@ def workload_config(w: synth.Workload) -> dict:
            "parallelism": "replicas", "l2": note,
            "timing": "device events around the steps, queued behind a head start of "
                      "plain device work so that host call overhead is not timed"}
+    if variant != "default":
+        cfg["variant"] = variant
+        if "reduction" in VARIANTS[variant]:
+            cfg["reduction"] = VARIANTS[variant]["reduction"]
+    if skip_masked:
+        cfg["masked_grad_rows"] = "skipped (GRPO_SKIP_MASKED_GRAD_ROWS)"
     return cfg
 
 
@@ -328,12 +355,18 @@ class LogitsCase:
     launches_per_step = 3  # prep, rows, reduce
     kernel = "rows_kernel (fused sweeps)"
 
-    def __init__(self, w, device):
+    def __init__(self, w, device, variant="default", skip_masked=False):
         import torch
         import grad_row_online_gb300 as g
         self.g, self.w, self.device = g, w, device
         self.inp = device_inputs(w, device)
         self.kw = loss_kwargs(w, self.inp)
+        self.kw.update(variant_kwargs(variant, w))
+        if skip_masked:
+            self.kw["skip_masked_grad_rows"] = True
+        if variant == "gspo":
+            self.launches_per_step = 4  # prep, sweep 1, per-sequence step, sweep 2
+            self.kernel = "gspo_sweep1_kernel + reduce_kernel + gspo_sweep2_kernel"
         self.active = int(self.inp["mask"].sum().item())
         self.grad = torch.empty_like(self.inp["X"])
         self.out3 = torch.empty(3, dtype=torch.float32, device=device)
@@ -380,10 +413,11 @@ class LogpsCase:
     launches_per_step = 2  # prep, logps_kernel
     kernel = "logps_kernel"
 
-    def __init__(self, w, device):
+    def __init__(self, w, device, variant="default", skip_masked=False):
         import torch
         import grad_row_online_gb300 as g
         self.g, self.w, self.device = g, w, device
+        self.vkw = variant_kwargs(variant, w)
         lp, old, ref = w.logps_inputs()
         host = dict(lp=lp, old=old, ref=ref, mask=w.completion_mask(), R=w.rewards())
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
@@ -400,11 +434,12 @@ class LogpsCase:
 
     def _call(self, i, prof=None):
         w = self.w
+        kw = dict(reduction=w.reduction)
+        kw.update(self.vkw)
         self.g.grpo_loss_from_logps(i["lp"], i["old"], i["ref"], i["mask"], i["R"],
                                     samples_per_prompt=w.samples_per_prompt, clip_eps=w.eps_lo,
-                                    clip_eps_hi=w.eps_hi, beta=w.beta, reduction=w.reduction,
-                                    grad=i["grad"], out3=self.out3, workspace=self.wsp,
-                                    profile=prof)
+                                    clip_eps_hi=w.eps_hi, beta=w.beta, grad=i["grad"],
+                                    out3=self.out3, workspace=self.wsp, profile=prof, **kw)
 
     def step(self, k=0, prof=None):
         self._call(self.copies[k % self.COPIES], prof)
@@ -446,7 +481,7 @@ def run_gpu(args, w, ws, rank, local):
     import torch
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    case = (LogpsCase if w.V == 0 else LogitsCase)(w, device)
+    case = (LogpsCase if w.V == 0 else LogitsCase)(w, device, args.variant, args.skip_masked)
     stream = torch.cuda.current_stream(device)
 
     t0 = time.perf_counter()
@@ -512,7 +547,7 @@ def run_gpu(args, w, ws, rank, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype if w.V else "f32",
-        "data": "synthetic", "config": workload_config(w),
+        "data": "synthetic", "config": workload_config(w, args.variant, args.skip_masked),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                      "kernel": case.kernel, "peak_source": f"{peak_kind} hbm_gbs",
@@ -539,6 +574,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--variant", default="default", choices=list(VARIANTS),
+                    help="loss variant to time (default: the operator page's GRPO loss)")
+    ap.add_argument("--skip-masked", action="store_true",
+                    help="leave masked gradient rows untouched (GRPO_SKIP_MASKED_GRAD_ROWS)")
     ap.add_argument("--T", type=int, default=0,
                     help="shorter rows per sequence (lengths scaled alike): small profiling case")
     args = ap.parse_args()
