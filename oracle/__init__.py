@@ -64,6 +64,8 @@ def lib():
         L.oracle_loss_from_logps.argtypes = [i64, i64, vp, vp, vp, vp, vp, dbl, dbl, dbl, dbl,
                                              ci, ci, ci, dbl, dbl, ci, vp, vp, vp, vp, vp]
         L.oracle_grad_rows.argtypes = [vp, ci, i64, i64, vp, vp, vp, ci, vp, vp]
+        L.oracle_lse_partial.argtypes = [vp, ci, i64, i64, i64, i64, vp, vp]
+        L.oracle_lse_merge.argtypes = [i64, i64, vp, vp, vp]
         L.oracle_round_to.argtypes = [vp, i64, ci, vp]
         _lib = L
     return _lib
@@ -150,6 +152,26 @@ def loss_from_logps(logp, ref_logp, old, mask, A, eps_lo, eps_hi, beta,
             "per_seq_policy": per_seq[:B], "per_seq_kl": per_seq[B:2 * B],
             "per_seq_active": per_seq[2 * B:], "w": w, "ratio": ratio,
             "clip_counts": counts}
+
+
+def lse_vocab_parallel(rows, dtype: str, bounds) -> np.ndarray:
+    """The rows' logsumexp from vocabulary slices [bounds[k], bounds[k+1]):
+    a partial normaliser per slice, merged in slice order (the vocab-parallel
+    logprob of the distributed loss)."""
+    rows = _c(rows, _storage_np(dtype))
+    n, V = rows.shape
+    K = len(bounds) - 1
+    M = np.empty((K, n), dtype=np.float64)
+    Z = np.empty((K, n), dtype=np.float64)
+    for k in range(K):
+        mk = np.empty(n, dtype=np.float64)
+        zk = np.empty(n, dtype=np.float64)
+        lib().oracle_lse_partial(_p(rows), DTYPE_CODE[dtype], n, V, int(bounds[k]),
+                                 int(bounds[k + 1]), _p(mk), _p(zk))
+        M[k], Z[k] = mk, zk
+    lse = np.empty(n, dtype=np.float64)
+    lib().oracle_lse_merge(n, K, _p(M), _p(Z), _p(lse))
+    return lse
 
 
 def grad_rows(rows, dtype: str, actions, lse, w, out_dtype: str | None = None):

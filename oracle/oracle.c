@@ -194,6 +194,52 @@ void oracle_log_softmax_rows(const void *rows, int dtype, int64_t nrows, int64_t
   }
 }
 
+/* ------------------------------------------------ vocabulary-parallel rows
+ * RL-Kernel "GRPO Loss", "Tensor and Data Parallel" step 1 (the
+ * vocab-parallel logprob): a rank holding the vocabulary slice [v0, v1)
+ * reduces its part of a row to a partial normaliser (M_k, Z_k), M_k the
+ * slice maximum and Z_k = sum_{v in slice} exp(x_v - M_k); the row's
+ * logsumexp is M + log(sum_k Z_k exp(M_k - M)) with M = max_k M_k (an empty
+ * slice has M_k = -inf and contributes nothing).  Partials are computed per
+ * row for the slice; merge folds K partials per row in slice order. */
+void oracle_lse_partial(const void *rows, int dtype, int64_t nrows, int64_t V, int64_t v0,
+                        int64_t v1, double *M_out, double *Z_out) {
+  for (int64_t r = 0; r < nrows; ++r) {
+    int64_t base = r * V;
+    double M = -INFINITY;
+    for (int64_t v = v0; v < v1; ++v) {
+      double x = or_load(rows, dtype, base + v);
+      if (x > M || isnan(x)) M = x;
+    }
+    double s = 0.0, c = 0.0;
+    if (M != -INFINITY)
+      for (int64_t v = v0; v < v1; ++v) {
+        double t = exp(or_load(rows, dtype, base + v) - M);
+        double u = s + t;
+        if (fabs(s) >= fabs(t))
+          c += (s - u) + t;
+        else
+          c += (t - u) + s;
+        s = u;
+      }
+    M_out[r] = M;
+    Z_out[r] = s + c;
+  }
+}
+
+void oracle_lse_merge(int64_t nrows, int64_t K, const double *M, const double *Z,
+                      double *lse) {
+  for (int64_t r = 0; r < nrows; ++r) {
+    double Mx = -INFINITY;
+    for (int64_t k = 0; k < K; ++k)
+      if (M[k * nrows + r] > Mx) Mx = M[k * nrows + r];
+    double s = 0.0;
+    for (int64_t k = 0; k < K; ++k)
+      if (M[k * nrows + r] != -INFINITY) s += Z[k * nrows + r] * exp(M[k * nrows + r] - Mx);
+    lse[r] = Mx + log(s);
+  }
+}
+
 /* ------------------------------------------------------------ token loss
  * Per active token (mask != 0; masked tokens are never read, [RX] "Notation
  * and mask contract"):

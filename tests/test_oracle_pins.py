@@ -462,3 +462,18 @@ def test_length_weights_table():
     for reduction, key in ((0, "token_mean_total_weight"), (1, "sequence_mean_total_weight")):
         res = oracle.loss_from_logps(logp, None, logp, mask, A, 0.2, 0.2, 0.0, reduction=reduction)
         assert np.allclose(res["w"].sum(1), lw[key], rtol=1e-14)
+
+
+# ----------------------------------------------------------------------------
+# vocabulary-parallel logsumexp: partials per slice, merged in slice order
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("bounds", [[0, 37], [0, 16, 37], [0, 1, 2, 30, 37], [0, 0, 20, 20, 37]])
+def test_vocab_parallel_lse_equals_the_row_lse(bounds):
+    rng = np.random.default_rng(5)
+    x = rng.normal(scale=3.0, size=(6, 37))
+    x[2, 5] += 40.0  # one dominant logit in one slice
+    want = torch.logsumexp(torch.from_numpy(x), -1).numpy()
+    got = oracle.lse_vocab_parallel(x, "f64", bounds)
+    assert np.allclose(got, want, rtol=0, atol=1e-13)
+    direct, _ = oracle.log_softmax_rows(x, "f64")
+    assert np.allclose(got, direct, rtol=0, atol=1e-13)
