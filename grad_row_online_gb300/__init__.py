@@ -23,7 +23,8 @@ from . import _build
 
 __all__ = ["grpo_workspace_size", "grpo_group_adv", "grpo_loss_fwd_bwd", "grpo_loss_fwd_bwd_static",
            "grpo_loss_from_logps", "grpo_count_active", "grpo_loss_finalize", "Shard",
-           "totals_buffer", "SEQ_TOTAL_BYTES",
+           "totals_buffer", "SEQ_TOTAL_BYTES", "grpo_vocab_chunk", "grpo_vocab_partials",
+           "grpo_vocab_loss", "grpo_vocab_grad",
            "grpo_read_device_status", "grpo_status_string", "GrpoError", "library_path",
            "GRPO_ADV_EPS_ADD", "GRPO_SKIP_MASKED_GRAD_ROWS"]
 
@@ -123,6 +124,18 @@ def lib():
         L.grpo_count_active.restype = ctypes.c_int
         L.grpo_loss_finalize.argtypes = [vp, i64, vp, ctypes.POINTER(_Params), vp, vp]
         L.grpo_loss_finalize.restype = ctypes.c_int
+        L.grpo_vocab_chunk.argtypes = []
+        L.grpo_vocab_chunk.restype = sz
+        L.grpo_vocab_partials.argtypes = [vp, vp, ctypes.c_int, i64, i64, i64, i64, vp, vp, vp,
+                                          vp, vp, vp]
+        L.grpo_vocab_partials.restype = ctypes.c_int
+        L.grpo_vocab_loss.argtypes = [vp, vp, i64, vp, i64, vp, vp, vp, i64, i64, vp,
+                                      ctypes.POINTER(_Groups), ctypes.POINTER(_Params), vp, vp, vp,
+                                      vp, vp, vp, sz, vp]
+        L.grpo_vocab_loss.restype = ctypes.c_int
+        L.grpo_vocab_grad.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, vp, vp, vp, vp, u32,
+                                      vp]
+        L.grpo_vocab_grad.restype = ctypes.c_int
         L.grpo_read_device_status.argtypes = [vp, vp]
         L.grpo_read_device_status.restype = ctypes.c_int
         L.grpo_status_string.argtypes = [ctypes.c_int]
@@ -421,6 +434,109 @@ def grpo_loss_finalize(totals: torch.Tensor, global_counts: torch.Tensor, *, bet
     _check(lib().grpo_loss_finalize(_ptr(totals), B, _ptr(global_counts), ctypes.byref(p),
                                     _ptr(out3), _stream(stream)), "grpo_loss_finalize")
     return out3
+
+
+# --------------------------------------------------------------------------
+# vocabulary parallelism (see include/grpo.h): partials -> exchange -> loss ->
+# gradient slices
+def grpo_vocab_chunk() -> int:
+    return int(lib().grpo_vocab_chunk())
+
+
+def grpo_vocab_partials(policy_slice: torch.Tensor, ref_slice: torch.Tensor,
+                        action_ids: torch.Tensor, completion_mask: torch.Tensor, v_begin: int,
+                        stream=None) -> dict:
+    """This rank's partial normalisers: ``part_p`` / ``part_r`` (float32
+    [chunks, B*T, 4] records) and ``action_logits`` ([2, B*T], 0 where the
+    slice does not hold the action)."""
+    if policy_slice.dtype not in _DTYPES:
+        raise ValueError(f"unsupported logits dtype {policy_slice.dtype}")
+    _dev(policy_slice, "policy_slice")
+    _dev(ref_slice, "ref_slice", policy_slice.dtype)
+    B, T, Vk = policy_slice.shape
+    _dev(action_ids, "action_ids", torch.int64)
+    mask = _dev(completion_mask, "completion_mask")
+    if mask.dtype == torch.bool:
+        mask = mask.view(torch.uint8)
+    C = grpo_vocab_chunk()
+    nck = (Vk + C - 1) // C
+    dev = policy_slice.device
+    part_p = torch.empty((nck, B * T, 4), dtype=torch.float32, device=dev)
+    part_r = torch.empty((nck, B * T, 4), dtype=torch.float32, device=dev)
+    act = torch.empty((2, B * T), dtype=torch.float32, device=dev)
+    _check(lib().grpo_vocab_partials(_ptr(policy_slice), _ptr(ref_slice),
+                                     _DTYPES[policy_slice.dtype], B, T, Vk, int(v_begin),
+                                     _ptr(action_ids), _ptr(mask), _ptr(part_p), _ptr(part_r),
+                                     _ptr(act), _stream(stream)), "grpo_vocab_partials")
+    return {"part_p": part_p, "part_r": part_r, "action_logits": act}
+
+
+def grpo_vocab_loss(part_p: torch.Tensor, part_r: torch.Tensor, action_logits: torch.Tensor,
+                    V: int, action_ids: torch.Tensor, old_logps: torch.Tensor,
+                    completion_mask: torch.Tensor, rewards: torch.Tensor, *,
+                    samples_per_prompt: int = 0, group_boundaries=None, clip_eps: float = 0.2,
+                    clip_eps_hi: Optional[float] = None, beta: float = 0.04,
+                    adv_eps: float = 1e-6, eps_add: bool = False, grad_scale: float = 1.0,
+                    reduction="token_mean", want_per_seq: bool = False, want_logps: bool = False,
+                    want_adv: bool = False, workspace: Optional[torch.Tensor] = None,
+                    stream=None, kl: str = "k3", surrogate: str = "clip",
+                    dual_clip_c: Optional[float] = None, norm_constant: Optional[float] = None,
+                    want_clip_counts: bool = False, shard: Optional[Shard] = None,
+                    ratio_level: str = "token") -> dict:
+    """The loss from every slice's partials (concatenated in rank order) and
+    the summed action logits.  Returns ``out3``, ``lse_w`` ([2, B*T] double:
+    logsumexp and dL/dlogp per row, for grpo_vocab_grad) and the optional
+    outputs of grpo_loss_fwd_bwd."""
+    B, T = action_ids.shape
+    dev = action_ids.device
+    for t, n in ((part_p, "part_p"), (part_r, "part_r")):
+        _dev(t, n, torch.float32)
+    _dev(action_logits, "action_logits", torch.float32)
+    _dev(old_logps, "old_logps", torch.float32)
+    _dev(rewards, "rewards", torch.float32)
+    mask = _dev(completion_mask, "completion_mask")
+    if mask.dtype == torch.bool:
+        mask = mask.view(torch.uint8)
+    Bg = rewards.numel() if shard is not None else B
+    g, keep = _groups(Bg, samples_per_prompt, group_boundaries)
+    counts = torch.empty(3, dtype=torch.int64, device=dev) if want_clip_counts else None
+    p, prof = _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction,
+                      GRPO_ADV_EPS_ADD if eps_add else 0, None, kl, surrogate, dual_clip_c,
+                      norm_constant, counts, shard, ratio_level)
+    out3 = torch.empty(3, dtype=torch.float32, device=dev)
+    lse_w = torch.empty((2, B * T), dtype=torch.float64, device=dev)
+    per_seq = torch.empty((3, B), dtype=torch.float32, device=dev) if want_per_seq else None
+    logps = torch.empty((B, T), dtype=torch.float32, device=dev) if want_logps else None
+    adv = torch.empty(B, dtype=torch.float32, device=dev) if want_adv else None
+    ws, need = _workspace(Bg, T, 0, workspace, dev)
+    _check(lib().grpo_vocab_loss(_ptr(part_p), _ptr(part_r), part_p.shape[0], _ptr(action_logits),
+                                 int(V), _ptr(action_ids), _ptr(old_logps), _ptr(mask), B, T,
+                                 _ptr(rewards), ctypes.byref(g), ctypes.byref(p), _ptr(lse_w),
+                                 _ptr(out3), _ptr(per_seq), _ptr(logps), _ptr(adv), _ptr(ws),
+                                 ws.numel(), _stream(stream)), "grpo_vocab_loss")
+    return {"out3": out3, "loss": out3[0], "policy_loss": out3[1], "kl": out3[2],
+            "lse_w": lse_w, "per_seq": per_seq, "logps": logps, "adv": adv,
+            "clip_counts": counts, "workspace": ws}
+
+
+def grpo_vocab_grad(policy_slice: torch.Tensor, action_ids: torch.Tensor,
+                    completion_mask: torch.Tensor, v_begin: int, lse_w: torch.Tensor, *,
+                    grad: Optional[torch.Tensor] = None, skip_masked_grad_rows: bool = False,
+                    stream=None) -> torch.Tensor:
+    """This rank's slice of dL/dlogits ([B, T, Vk], the dtype of the slice)."""
+    _dev(policy_slice, "policy_slice")
+    B, T, Vk = policy_slice.shape
+    mask = _dev(completion_mask, "completion_mask")
+    if mask.dtype == torch.bool:
+        mask = mask.view(torch.uint8)
+    _dev(lse_w, "lse_w", torch.float64)
+    grad = torch.empty_like(policy_slice) if grad is None else _dev(grad, "grad",
+                                                                   policy_slice.dtype)
+    _check(lib().grpo_vocab_grad(_ptr(policy_slice), _DTYPES[policy_slice.dtype], B, T, Vk,
+                                 int(v_begin), _ptr(action_ids), _ptr(mask), _ptr(lse_w),
+                                 _ptr(grad), GRPO_SKIP_MASKED_GRAD_ROWS if skip_masked_grad_rows
+                                 else 0, _stream(stream)), "grpo_vocab_grad")
+    return grad
 
 
 def grpo_read_device_status(workspace: torch.Tensor, stream=None) -> int:

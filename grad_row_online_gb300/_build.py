@@ -9,7 +9,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgrpo_gb300.so")
 SOURCES = ["grpo_api.cu", "grpo_prep.cu", "grpo_rows.cu", "grpo_reduce.cu",
-           "grpo_logps.cu", "grpo_static.cu"]
+           "grpo_logps.cu", "grpo_static.cu", "grpo_vocab.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 FLAGS = [ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 

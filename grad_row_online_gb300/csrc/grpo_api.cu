@@ -267,7 +267,7 @@ extern "C" grpo_status_t grpo_loss_fwd_bwd(
       ReduceArgs rd{completion_mask, L, A + pl.seq_begin, totals, slot_p, slot_k, B, T,
                     params->beta, params->reduction, hdr, NS, out3, per_seq, 1,
                     params->norm_constant, params->clip_counts, pl.shard ? 1 : 0, var, old_logps,
-                    params->grad_scale};
+                    params->grad_scale, 1, nullptr};
       if (launch_reduce(rd, s) != cudaSuccess) return GRPO_ERR_CUDA;
       if (grad_logits && launch_gspo_rows(ra, dt, 2, params->profile, s) != cudaSuccess)
         return GRPO_ERR_CUDA;
@@ -283,7 +283,8 @@ extern "C" grpo_status_t grpo_loss_fwd_bwd(
   ReduceArgs rd{completion_mask, L, A + pl.seq_begin, totals, slot_p, slot_k, B, T,
                 params->beta, params->reduction, hdr, NS, out3, per_seq,
                 var.splits_A() ? 1 : 0, params->norm_constant,
-                params->clip_counts, pl.shard ? 1 : 0, rv, old_logps, params->grad_scale};
+                params->clip_counts, pl.shard ? 1 : 0, rv, old_logps, params->grad_scale, 0,
+                nullptr};
   return cuda_status(launch_reduce(rd, s));
 }
 
@@ -365,6 +366,143 @@ extern "C" grpo_status_t grpo_loss_finalize(const grpo_seq_total_t* totals, int6
   return cuda_status(launch_finalize(reinterpret_cast<const SeqTotal*>(totals), B, global_counts,
                                      params->reduction, params->norm_constant, params->beta,
                                      out3, (cudaStream_t)stream));
+}
+
+extern "C" size_t grpo_vocab_chunk(void) { return (size_t)kVChunk; }
+
+extern "C" grpo_status_t grpo_vocab_partials(const void* policy_slice, const void* ref_slice,
+                                             grpo_dtype_t dt, int64_t B, int64_t T, int64_t Vk,
+                                             int64_t v_begin, const int64_t* action_ids,
+                                             const uint8_t* completion_mask, void* partials_p,
+                                             void* partials_r, float* action_logits,
+                                             void* stream) {
+  if (dt != GRPO_F32 && dt != GRPO_BF16 && dt != GRPO_F16) return GRPO_ERR_DTYPE;
+  if (B < 0 || T < 0 || Vk < 1 || v_begin < 0 || v_begin % kVChunk != 0) return GRPO_ERR_SHAPE;
+  const int64_t rows = B * T;
+  if (rows > 0 && (!policy_slice || !ref_slice || !action_ids || !completion_mask ||
+                   !partials_p || !partials_r || !action_logits))
+    return GRPO_ERR_NULL;
+  const size_t es = elem_size(dt);
+  if (!aligned(policy_slice, es) || !aligned(ref_slice, es) || !aligned(action_ids, 8) ||
+      !aligned(partials_p, 16) || !aligned(partials_r, 16) || !aligned(action_logits, 4))
+    return GRPO_ERR_ALIGN;
+  VocabArgs va{};
+  va.policy = policy_slice;
+  va.ref = ref_slice;
+  va.actions = action_ids;
+  va.mask = completion_mask;
+  va.rows = rows;
+  va.Vk = Vk;
+  va.v_begin = v_begin;
+  va.nck = (Vk + kVChunk - 1) / kVChunk;
+  va.part_p = (float4*)partials_p;
+  va.part_r = (float4*)partials_r;
+  va.act_logits = action_logits;
+  va.precise = dt == GRPO_F32;
+  va.tab = exp_table();
+  return cuda_status(launch_vocab_partials(va, dt, (cudaStream_t)stream));
+}
+
+extern "C" grpo_status_t grpo_vocab_loss(const void* partials_p, const void* partials_r,
+                                         int64_t num_chunks, const float* action_logits,
+                                         int64_t V, const int64_t* action_ids,
+                                         const float* old_logps, const uint8_t* completion_mask,
+                                         int64_t B, int64_t T, const float* rewards,
+                                         const grpo_groups_t* groups, const grpo_params_t* params,
+                                         double* lse_w, float* out3, float* per_seq,
+                                         float* logps_out, float* adv_out, void* ws,
+                                         size_t ws_bytes, void* stream) {
+  if (B < 0 || T < 0 || V < 1) return GRPO_ERR_SHAPE;
+  if (num_chunks != (V + kVChunk - 1) / kVChunk) return GRPO_ERR_SHAPE;
+  if (!params || !groups) return GRPO_ERR_NULL;
+  const int64_t rows = B * T;
+  if (rows > 0 && (!partials_p || !partials_r || !action_logits || !action_ids || !old_logps ||
+                   !completion_mask || !lse_w))
+    return GRPO_ERR_NULL;
+  grpo_status_t st = check_params(params);
+  if (st != GRPO_OK) return st;
+  Placement pl;
+  if ((st = placement_of(params, groups, B, &pl)) != GRPO_OK) return st;
+  if (!out3 && !pl.shard) return GRPO_ERR_NULL;
+  if (pl.Bg > 0 && !rewards) return GRPO_ERR_NULL;
+  int32_t spp;
+  const int64_t* bounds;
+  int64_t G;
+  if ((st = check_groups(groups, pl.Bg, &spp, &bounds, &G)) != GRPO_OK) return st;
+  if (!aligned(partials_p, 16) || !aligned(partials_r, 16) || !aligned(action_logits, 4) ||
+      !aligned(action_ids, 8) || !aligned(old_logps, 4) || !aligned(rewards, 4) ||
+      !aligned(lse_w, 8) || !aligned(out3, 4) || !aligned(per_seq, 4) || !aligned(logps_out, 4) ||
+      !aligned(adv_out, 4))
+    return GRPO_ERR_ALIGN;
+  if ((st = check_ws(ws, ws_bytes, pl.Bg, T)) != GRPO_OK) return st;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  char* w = (char*)ws;
+  const WsLayout lay(pl.Bg, T);
+  WsHeader* hdr = (WsHeader*)w;
+  int32_t* L = (int32_t*)(w + lay.off_L);
+  double* A = (double*)(w + lay.off_A);
+  double* slot_p = (double*)(w + lay.off_slots);
+  double* slot_k = slot_p + rows;
+  const unsigned long long* NS = pl.NS ? pl.NS : &hdr->N;
+  SeqTotal* totals = pl.shard ? pl.totals : (SeqTotal*)(w + lay.off_seq);
+  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return GRPO_ERR_CUDA;
+  PrepArgs pa{rewards, bounds, B, T, G, pl.Bg, pl.seq_begin, &hdr->N, spp, params->adv_eps,
+              (int)(params->flags & GRPO_ADV_EPS_ADD), completion_mask, 1, A, nullptr, adv_out, L,
+              nullptr, hdr};
+  if (launch_prep(pa, s) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (rows > 0) {
+    VocabArgs va{};
+    va.actions = action_ids;
+    va.mask = completion_mask;
+    va.rows = rows;
+    va.nck = num_chunks;
+    va.V = V;
+    va.part_p = (float4*)partials_p;
+    va.part_r = (float4*)partials_r;
+    va.act_logits = (float*)action_logits;
+    va.tab = exp_table();
+    va.slot_p = slot_p;
+    va.slot_k = slot_k;
+    va.lse_w = lse_w;
+    va.logps_out = logps_out;
+    va.hdr = hdr;
+    if (launch_vocab_merge(va, s) != cudaSuccess) return GRPO_ERR_CUDA;
+  }
+  const Variant var = variant_of(params);
+  ReduceArgs rd{completion_mask, L, A + pl.seq_begin, totals, slot_p, slot_k, B, T,
+                params->beta, params->reduction, hdr, NS, out3, per_seq,
+                var.splits_A() ? 1 : 0, params->norm_constant, params->clip_counts,
+                pl.shard ? 1 : 0, var, old_logps, params->grad_scale, rows > 0 ? 1 : 0,
+                rows > 0 ? lse_w + rows : nullptr};
+  return cuda_status(launch_reduce(rd, s));
+}
+
+extern "C" grpo_status_t grpo_vocab_grad(const void* policy_slice, grpo_dtype_t dt, int64_t B,
+                                         int64_t T, int64_t Vk, int64_t v_begin,
+                                         const int64_t* action_ids,
+                                         const uint8_t* completion_mask, const double* lse_w,
+                                         void* grad_slice, uint32_t flags, void* stream) {
+  if (dt != GRPO_F32 && dt != GRPO_BF16 && dt != GRPO_F16) return GRPO_ERR_DTYPE;
+  if (B < 0 || T < 0 || Vk < 1 || v_begin < 0) return GRPO_ERR_SHAPE;
+  if (flags & ~GRPO_SKIP_MASKED_GRAD_ROWS) return GRPO_ERR_PARAM;
+  if (B * T > 0 && (!policy_slice || !action_ids || !completion_mask || !lse_w || !grad_slice))
+    return GRPO_ERR_NULL;
+  const size_t es = elem_size(dt);
+  if (!aligned(policy_slice, es) || !aligned(grad_slice, es) || !aligned(action_ids, 8) ||
+      !aligned(lse_w, 8))
+    return GRPO_ERR_ALIGN;
+  RowArgs ra{};
+  ra.policy = policy_slice;
+  ra.grad = grad_slice;
+  ra.actions = action_ids;
+  ra.mask = completion_mask;
+  ra.B = B;
+  ra.T = T;
+  ra.V = Vk;
+  ra.flags = flags;
+  ra.precise_ok = dt == GRPO_F32;
+  return cuda_status(launch_vocab_grad(ra, dt, v_begin, lse_w, (cudaStream_t)stream));
 }
 
 extern "C" grpo_status_t grpo_read_device_status(const void* ws, void* stream) {

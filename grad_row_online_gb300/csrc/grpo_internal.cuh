@@ -683,11 +683,35 @@ struct ReduceArgs {
   float norm_c;     // GRPO_FIXED_CONSTANT's constant
   unsigned long long* counts_out;  // nullable [3]
   int shard;        // 1: write the totals only (the scalar comes from grpo_loss_finalize)
-  // GSPO (var.seq_ratio): the slots hold logp and d = ref_logp - logp; this
-  // kernel forms rho_i, the per-token terms and w (written over d)
+  // from_slots (GSPO, the vocab-parallel path): the slots hold logp and
+  // d = ref_logp - logp; this kernel forms the ratios (rho_i for GSPO), the
+  // per-token terms and w = dL/dlogp, written to w_out (or over d)
   Variant var;
   const float* old;
   float grad_scale;
+  int from_slots;
+  double* w_out;  // nullable
+};
+
+// The vocabulary-parallel path (grpo_vocab.cu): a rank's slice of every row,
+// [rows, Vk] from vocabulary entry v_begin on, in chunks of kVChunk.
+constexpr int64_t kVChunk = 4096;
+struct VocabArgs {
+  const void* policy;
+  const void* ref;
+  const int64_t* actions;
+  const uint8_t* mask;
+  int64_t rows, Vk, v_begin, nck, V;  // nck: chunks of the slice (partials) or of all slices (merge)
+  float4* part_p;      // [nck][rows] partial normalisers {M, Z.hi, Z.lo, 0}
+  float4* part_r;
+  float* act_logits;   // [2][rows]: policy and reference logit of the action
+  int precise;         // fp32 logits: float-float exponentials
+  ExpTable tab;
+  double* slot_p;      // merge: logp
+  double* slot_k;      // merge: d = ref_logp - logp
+  double* lse_w;       // merge: [rows] policy logsumexp
+  float* logps_out;    // nullable
+  WsHeader* hdr;
 };
 
 struct LogpsArgs {
@@ -720,6 +744,10 @@ cudaError_t launch_rows(const RowArgs& a, grpo_dtype_t dt, const grpo_profile_t*
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t s);
 cudaError_t launch_gspo_rows(const RowArgs& a, grpo_dtype_t dt, int phase,
                              const grpo_profile_t* prof, cudaStream_t s);
+cudaError_t launch_vocab_partials(const VocabArgs& a, grpo_dtype_t dt, cudaStream_t s);
+cudaError_t launch_vocab_merge(const VocabArgs& a, cudaStream_t s);
+cudaError_t launch_vocab_grad(const RowArgs& a, grpo_dtype_t dt, int64_t v_begin,
+                              const double* lse_w, cudaStream_t s);
 cudaError_t launch_logps(const LogpsArgs& a, const grpo_profile_t* prof, cudaStream_t s);
 cudaError_t launch_finalize(const SeqTotal* recs, int64_t B, const unsigned long long* NS,
                             int reduction, float norm_c, float beta, float* out3, cudaStream_t s);

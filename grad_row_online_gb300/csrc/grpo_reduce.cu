@@ -40,26 +40,36 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs
     const int L = a.L[i];
     double v[2] = {0.0, 0.0};
     unsigned nc[3] = {0u, 0u, 0u};
-    if (a.var.seq_ratio) {
-      // GSPO: the slots hold logp and d = ref_logp - logp.  rho_i first (a
-      // fixed-order sum over the sequence), then every token's terms with
-      // rho_i in place of its own ratio, and w = dL/dlogp written over d.
-      double s1[1] = {0.0};
-      for (int64_t t = threadIdx.x; t < a.T; t += blockDim.x)
-        if (m[t]) s1[0] += sp[t] - (double)a.old[i * a.T + t];
-      block_sum<double, 1>(s1, s_d);
-      if (threadIdx.x == 0) s_em = L > 0 ? expm1(s1[0] / (double)L) : 0.0;
-      __syncthreads();
-      const double em = s_em, A = a.A[i];
-      const unsigned long long S = a.NS[1];
-      const double c = L > 0 ? 1.0 / ((double)(S > 0 ? S : 1) * (double)L) : 0.0;
+    if (a.from_slots) {
+      // The slots hold logp and d = ref_logp - logp (GSPO's first sweep, or
+      // the vocab-parallel merge).  GSPO: rho_i first (a fixed-order sum over
+      // the sequence), used by every token in place of its own ratio.  Then
+      // every token's terms in double, and w = dL/dlogp.
+      double em_seq = 0.0;
+      if (a.var.seq_ratio) {
+        double s1[1] = {0.0};
+        for (int64_t t = threadIdx.x; t < a.T; t += blockDim.x)
+          if (m[t]) s1[0] += sp[t] - (double)a.old[i * a.T + t];
+        block_sum<double, 1>(s1, s_d);
+        if (threadIdx.x == 0) s_em = L > 0 ? expm1(s1[0] / (double)L) : 0.0;
+        __syncthreads();
+        em_seq = s_em;
+      }
+      const double A = a.A[i];
+      const unsigned long long N = a.NS[0], S = a.NS[1];
+      const double c = a.reduction == GRPO_TOKEN_MEAN ? 1.0 / (double)(N > 0 ? N : 1)
+                       : a.reduction == GRPO_SEQUENCE_MEAN
+                           ? (L > 0 ? 1.0 / ((double)(S > 0 ? S : 1) * (double)L) : 0.0)
+                           : 1.0 / (double)a.norm_c;
+      double* wo = a.w_out ? a.w_out + i * a.T : sk;
       for (int64_t t = threadIdx.x; t < a.T; t += blockDim.x)
         if (m[t]) {
           const double lp = sp[t], d = sk[t], emd = expm1(d);
+          const double em = a.var.seq_ratio ? em_seq : expm1(lp - (double)a.old[i * a.T + t]);
           const TokEpi<double> te = token_epilogue<double>(em, lp, d, emd, emd - d, true, A, a.var);
           v[0] += te.q;
           v[1] += te.k;
-          sk[t] = (double)a.grad_scale * c * te.g;
+          wo[t] = (double)a.grad_scale * c * te.g;
           if (te.clip == 1) ++nc[0];
           else if (te.clip == 2) ++nc[1];
           else if (te.clip == 3) ++nc[2];
@@ -72,7 +82,7 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs
         }
     }
     block_sum<double, 2>(v, s_d);
-    if (a.var.seq_ratio && a.counts_out) block_sum<unsigned, 3>(nc, s_u);
+    if (a.from_slots && a.counts_out) block_sum<unsigned, 3>(nc, s_u);
     if (threadIdx.x == 0) {
       const double P = a.split_A ? v[0] - a.A[i] * (double)L : v[0];
       put_total(a.seq + i, P, v[1], L);
@@ -81,7 +91,7 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs
         a.per_seq[a.B + i] = (float)v[1];
         a.per_seq[2 * a.B + i] = (float)L;
       }
-      if (a.var.seq_ratio && a.counts_out) add_clip_counts(a.hdr, nc);
+      if (a.from_slots && a.counts_out) add_clip_counts(a.hdr, nc);
       __threadfence();
       const unsigned ticket = atomicAdd(&a.hdr->done_ctas, 1u);
       s_last = ticket == gridDim.x - 1;

@@ -588,6 +588,77 @@ cudaError_t launch_gspo_rows(const RowArgs& a, grpo_dtype_t dt, int phase,
   }
 }
 
+// ------------------------------------------------------- vocab-parallel
+// The gradient of a rank's vocabulary slice [v_begin, v_begin + V) of every
+// row (RowArgs.V is the slice width; policy / grad are [rows, V]) from the
+// row's logsumexp and w = dL/dlogp (lse_w[row], lse_w[rows + row]):
+// dL/dx_v = w (1[v = a] - exp(x_v - lse)); zeros on masked rows.
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) vocab_grad_kernel(
+    const RowArgs a, int64_t v_begin, const double* lse_w) {
+  __shared__ RowScalars s_rs;
+  const int64_t BT = a.B * a.T;
+  const bool zero_masked = !(a.flags & GRPO_SKIP_MASKED_GRAD_ROWS);
+  const uint64_t stream = l2_evict_first();
+  for (int64_t row = blockIdx.x; row < BT; row += gridDim.x) {
+    const T* x = reinterpret_cast<const T*>(a.policy) + row * a.V;
+    T* grow = reinterpret_cast<T*>(a.grad) + row * a.V;
+    const bool active = a.mask[row] != 0;
+    const int64_t act = active ? a.actions[row] - v_begin : -1;  // relative to the slice
+    const double lse = active ? lse_w[row] : 0.0;
+    if (!active || !(lse == lse)) {  // masked, or a row the merge rejected
+      if (zero_masked) zero_row<T>(grow, a.V, stream);
+      continue;
+    }
+    if (threadIdx.x == 0) {
+      const double w = lse_w[BT + row];
+      RowScalars rs;
+      rs.lse_p = lse;
+      rs.w = w;
+      rs.wneg = (float)(-w);
+      rs.LL = (float)(lse * (double)kLog2e);
+      rs.ga = (act >= 0 && act < a.V)
+                  ? (float)(-w * expm1((double)Storage<T>::load1(x + act) - lse))
+                  : 0.f;
+      rs.q = rs.k = rs.logp = rs.dlr = 0.0;
+      rs.precise = a.precise_ok;
+      rs.clip = 0;
+      s_rs = rs;
+    }
+    __syncthreads();
+    const RowScalars rs = s_rs;
+    if (rs.precise)
+      grad_row<T, true>(x, grow, a.V, act, rs, stream, stream, nullptr);
+    else
+      grad_row<T, false>(x, grow, a.V, act, rs, stream, stream, nullptr);
+    __syncthreads();
+  }
+}
+
+template <typename T>
+static cudaError_t launch_vocab_grad_t(const RowArgs& a, int64_t v_begin, const double* lse_w,
+                                       cudaStream_t s) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  int64_t grid = (int64_t)sms * kRowBlocksPerSM;
+  if (grid > a.B * a.T) grid = a.B * a.T;
+  if (grid < 1) return cudaSuccess;
+  vocab_grad_kernel<T><<<(unsigned)grid, kRowThreads, 0, s>>>(a, v_begin, lse_w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_vocab_grad(const RowArgs& a, grpo_dtype_t dt, int64_t v_begin,
+                              const double* lse_w, cudaStream_t s) {
+  switch (dt) {
+    case GRPO_F32: return launch_vocab_grad_t<float>(a, v_begin, lse_w, s);
+    case GRPO_BF16: return launch_vocab_grad_t<__nv_bfloat16>(a, v_begin, lse_w, s);
+    default: return launch_vocab_grad_t<__half>(a, v_begin, lse_w, s);
+  }
+}
+
 template <typename T>
 static cudaError_t launch_t(const RowArgs& a, const grpo_profile_t* prof, cudaStream_t s) {
   int dev = 0, sms = 0;

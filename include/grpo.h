@@ -291,6 +291,59 @@ grpo_status_t grpo_loss_finalize(const grpo_seq_total_t *totals, int64_t B,
                                  const unsigned long long *global_counts,
                                  const grpo_params_t *params, float *out3, void *stream);
 
+/* Vocabulary parallelism (tensor parallelism over V; RL-Kernel "Tensor and
+ * Data Parallel", step 1: "selected logprobs come from VocabParallelLogprobOp,
+ * so ratio and KL inherit cross-TP bitwise equality").  A rank holds the
+ * slice [v_begin, v_begin + Vk) of every policy and reference row, v_begin a
+ * multiple of grpo_vocab_chunk() (every slice but the last spans whole
+ * chunks).  The loss is formed by three calls around one exchange:
+ *   1. grpo_vocab_partials on every rank: one partial normaliser per row and
+ *      per chunk of its slice (the max M_c and sum_v exp(x_v - M_c) as a
+ *      float pair), chunk-major [chunks][B*T] records of 16 bytes, and the
+ *      action's policy / reference logit where the slice holds it (0
+ *      elsewhere).  A chunk's record depends only on the chunk's logits, not
+ *      on the rank or its memory alignment.
+ *   2. the exchange (the caller's collective): every rank's records
+ *      concatenated in rank order (= chunk order), and the action logits
+ *      summed over ranks (exact: one rank holds each);
+ *   3. grpo_vocab_loss on every rank (identical inputs, identical results):
+ *      the chunks folded in order to each row's logsumexp, logp and
+ *      ref_logp, then the loss as grpo_loss_fwd_bwd would form it from them
+ *      (every variant, groups, sharding over sequences); lse_w receives
+ *      [2][B*T] doubles: the policy logsumexp and w = dL/dlogp per row;
+ *   4. grpo_vocab_grad on every rank: its slice of dL/dlogits from lse_w.
+ * Any split at chunk boundaries -- one rank included -- gives the same bits
+ * everywhere.  The fused grpo_loss_fwd_bwd is the faster single-rank path;
+ * the two agree within the stated tolerances, not bit for bit. */
+size_t grpo_vocab_chunk(void);
+
+grpo_status_t grpo_vocab_partials(const void *policy_slice, const void *ref_slice,
+                                  grpo_dtype_t dt, int64_t B, int64_t T, int64_t Vk,
+                                  int64_t v_begin, const int64_t *action_ids,
+                                  const uint8_t *completion_mask, void *partials_p,
+                                  void *partials_r, float *action_logits, void *stream);
+
+/* partials_p / partials_r: [num_chunks][B*T] records of all slices
+ * (num_chunks = ceil(V / grpo_vocab_chunk())); action_logits: [2][B*T]
+ * summed over slices; V: the whole vocabulary (action ids outside [0, V)
+ * set GRPO_ERR_ACTION_RANGE).  Other arguments as for grpo_loss_fwd_bwd. */
+grpo_status_t grpo_vocab_loss(const void *partials_p, const void *partials_r,
+                              int64_t num_chunks, const float *action_logits, int64_t V,
+                              const int64_t *action_ids, const float *old_logps,
+                              const uint8_t *completion_mask, int64_t B, int64_t T,
+                              const float *rewards, const grpo_groups_t *groups,
+                              const grpo_params_t *params, double *lse_w, float *out3,
+                              float *per_seq, float *logps_out, float *adv_out, void *ws,
+                              size_t ws_bytes, void *stream);
+
+/* grad_slice [B,T,Vk] (dtype dt, overwritten): dL/dx_v = w (1[v = a] -
+ * exp(x_v - lse)) over the slice; zeros on masked rows unless flags has
+ * GRPO_SKIP_MASKED_GRAD_ROWS. */
+grpo_status_t grpo_vocab_grad(const void *policy_slice, grpo_dtype_t dt, int64_t B, int64_t T,
+                              int64_t Vk, int64_t v_begin, const int64_t *action_ids,
+                              const uint8_t *completion_mask, const double *lse_w,
+                              void *grad_slice, uint32_t flags, void *stream);
+
 /* Synchronises `stream` and returns the status word the last call on this
  * workspace left (GRPO_OK or an OR of the device-detected bits), or
  * GRPO_ERR_CUDA.  The only entry point that blocks. */

@@ -186,3 +186,36 @@ def test_shard_placement_is_checked(lib):
     assert _fwd(lib, B=4, gr=gr, p=_sharded(0, counts=FAKE + 4), ws_bytes=ws) == 4
     # the workspace must cover the whole batch
     assert _fwd(lib, B=4, gr=gr, p=_sharded(0), ws_bytes=g.grpo_workspace_size(4, 16)) == 7
+
+
+def test_vocab_entry_points_reject_bad_arguments(lib):
+    C = lib.grpo_vocab_chunk()
+    assert C > 0 and C % 64 == 0
+    part = lambda **kw: lib.grpo_vocab_partials(
+        kw.get("pol", FAKE), kw.get("ref", FAKE), kw.get("dt", 1), kw.get("B", 2), kw.get("T", 3),
+        kw.get("Vk", 100), kw.get("v0", 0), kw.get("act", FAKE), kw.get("mask", FAKE),
+        kw.get("pp", FAKE), kw.get("pr", FAKE), kw.get("al", FAKE), None)
+    assert part(dt=9) == 3
+    assert part(v0=C + 1) == 2        # a slice starts on a chunk boundary
+    assert part(Vk=0) == 2
+    assert part(pol=None) == 1
+    assert part(pp=FAKE + 8) == 4
+    assert part(act=FAKE + 4) == 4
+    gr = _groups(8)
+    p = _params()
+    loss = lambda **kw: lib.grpo_vocab_loss(
+        FAKE, FAKE, kw.get("nck", 1), FAKE, kw.get("V", 100), FAKE, FAKE, FAKE, 8, 16, FAKE,
+        ctypes.byref(gr), ctypes.byref(kw.get("p", p)), kw.get("lse", FAKE), FAKE, None, None,
+        None, FAKE, kw.get("ws_bytes", g.grpo_workspace_size(8, 16)), None)
+    assert loss(nck=2) == 2           # chunk count must match V
+    assert loss(lse=None) == 1
+    assert loss(lse=FAKE + 4) == 4
+    assert loss(p=_params(beta=-1.0)) == 6
+    assert loss(ws_bytes=16) == 7
+    grad = lambda **kw: lib.grpo_vocab_grad(FAKE, kw.get("dt", 1), 2, 3, 100, kw.get("v0", 0),
+                                            FAKE, FAKE, kw.get("lse", FAKE), FAKE,
+                                            kw.get("flags", 0), None)
+    assert grad(dt=9) == 3
+    assert grad(v0=-1) == 2
+    assert grad(flags=1) == 6         # only GRPO_SKIP_MASKED_GRAD_ROWS
+    assert grad(lse=None) == 1
