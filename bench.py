@@ -402,6 +402,78 @@ class LogitsCase:
         self.loss_host.copy_(self.out3, non_blocking=True)
 
 
+class VocabCase:
+    """The vocabulary-parallel path on a logits workload, emulated with `tp`
+    slices on one GPU: every slice's partials, the rank-order exchange
+    (a concatenation and a sum, as the collectives would leave them), the
+    loss, every slice's gradient.  Each "rank" holds its own contiguous slice,
+    prepared before the timed region; the timed step is the work of all
+    ranks, done one after the other on the one GPU."""
+
+    kernel = "vocab path: partials + merge + reduce + gradient (whole step)"
+
+    def __init__(self, w, device, variant="default", tp=1):
+        import torch
+        import grad_row_online_gb300 as g
+        self.g, self.w, self.device = g, w, device
+        inp = device_inputs(w, device)
+        C = g.grpo_vocab_chunk()
+        nck = (w.V + C - 1) // C
+        cuts = [min(w.V, C * (nck * r // tp)) for r in range(tp + 1)]
+        self.bounds = [(a, b) for a, b in zip(cuts[:-1], cuts[1:]) if b > a]
+        self.Xs = [inp["X"][:, :, a:b].contiguous() for a, b in self.bounds]
+        self.Ys = [inp["Y"][:, :, a:b].contiguous() for a, b in self.bounds]
+        self.grads = [torch.empty_like(x) for x in self.Xs]
+        del inp["X"], inp["Y"]
+        torch.cuda.empty_cache()
+        self.inp = inp
+        self.kw = loss_kwargs(w, inp)
+        self.kw.update(variant_kwargs(variant, w))
+        self.active = int(inp["mask"].sum().item())
+        self.launches_per_step = 2 * len(self.bounds) + 3  # partials, prep, merge, reduce, grads
+        self.wsp = torch.empty(g.grpo_workspace_size(w.B, w.T), dtype=torch.uint8, device=device)
+        s_in = 2 if w.dtype == "bf16" else 4
+        # policy and ref read once for the partials, policy once more and the
+        # gradient written once for the slices: 4 V s per active row, as the fused path
+        self.alg_bytes = 4.0 * w.V * s_in * self.active
+
+    def step(self, k=0, prof=None):
+        import torch
+        g, i, w = self.g, self.inp, self.w
+        if prof is not None:
+            prof[0].record()
+        parts = [g.grpo_vocab_partials(x, y, i["acts"], i["mask"], a)
+                 for (a, _), x, y in zip(self.bounds, self.Xs, self.Ys)]
+        part_p = torch.cat([p["part_p"] for p in parts])
+        part_r = torch.cat([p["part_r"] for p in parts])
+        act = torch.stack([p["action_logits"] for p in parts]).sum(0)
+        res = g.grpo_vocab_loss(part_p, part_r, act, w.V, i["acts"], i["old"], i["mask"], i["R"],
+                                workspace=self.wsp, **self.kw)
+        for (a, _), x, gr in zip(self.bounds, self.Xs, self.grads):
+            g.grpo_vocab_grad(x, i["acts"], i["mask"], a, res["lse_w"], grad=gr)
+        if prof is not None:
+            prof[1].record()
+        self.out3 = res["out3"]
+
+    def e2e_setup(self):
+        import torch
+        self.host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+                     for t in self.Xs + self.Ys]
+        self.dev_in = [torch.empty_like(t) for t in self.Xs + self.Ys]
+        self.loss_host = torch.empty(3, dtype=torch.float32).pin_memory()
+        rest = sum(self.inp[k].numel() * self.inp[k].element_size()
+                   for k in ("acts", "old", "mask", "R"))
+        return sum(t.numel() * t.element_size() for t in self.host) + rest
+
+    def e2e_step(self):
+        for d, h in zip(self.dev_in, self.host):
+            d.copy_(h, non_blocking=True)
+        n = len(self.Xs)
+        self.Xs, self.Ys = self.dev_in[:n], self.dev_in[n:]
+        self.step()
+        self.loss_host.copy_(self.out3, non_blocking=True)
+
+
 class LogpsCase:
     """grpo_loss_from_logps on the logps-only workload.  One copy of its
     inputs (54 MB) fits in L2, so the timed steps rotate over COPIES copies
@@ -481,7 +553,10 @@ def run_gpu(args, w, ws, rank, local):
     import torch
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    case = (LogpsCase if w.V == 0 else LogitsCase)(w, device, args.variant, args.skip_masked)
+    if args.tp:
+        case = VocabCase(w, device, args.variant, args.tp)
+    else:
+        case = (LogpsCase if w.V == 0 else LogitsCase)(w, device, args.variant, args.skip_masked)
     stream = torch.cuda.current_stream(device)
 
     t0 = time.perf_counter()
@@ -547,7 +622,8 @@ def run_gpu(args, w, ws, rank, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype if w.V else "f32",
-        "data": "synthetic", "config": workload_config(w, args.variant, args.skip_masked),
+        "data": "synthetic", "config": dict(workload_config(w, args.variant, args.skip_masked),
+                                            **({"vocab_slices": args.tp} if args.tp else {})),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                      "kernel": case.kernel, "peak_source": f"{peak_kind} hbm_gbs",
@@ -576,6 +652,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--variant", default="default", choices=list(VARIANTS),
                     help="loss variant to time (default: the operator page's GRPO loss)")
+    ap.add_argument("--tp", type=int, default=0,
+                    help="time the vocabulary-parallel path with this many slices (on one GPU)")
     ap.add_argument("--skip-masked", action="store_true",
                     help="leave masked gradient rows untouched (GRPO_SKIP_MASKED_GRAD_ROWS)")
     ap.add_argument("--T", type=int, default=0,

@@ -12,8 +12,9 @@
 // split at chunk boundaries gives the same bits.
 //
 //   vocab_partials_kernel  one warp per (row, chunk): max, then the sum of
-//                          exp(x - max) as a float pair (a float-float
-//                          exponential for fp32 logits, MUFU 2^x otherwise);
+//                          exp(x - max) (a float-float exponential and
+//                          float-pair sums for fp32 logits; MUFU 2^x and a
+//                          Kahan sum per lane otherwise);
 //                          the action logit where the rank owns it
 //   vocab_merge_kernel     one thread per row: the chunks folded in order,
 //                          logsumexp in double, logp and d = ref_logp - logp
@@ -64,6 +65,7 @@ __device__ void chunk_partial(const T* x, int64_t n, const float* thi, const flo
   nan = __any_sync(0xFFFFFFFFu, nan);
   FF s = {0.f, 0.f};
   if (m != -INFINITY && !nan) {
+    float ks = 0.f, kc = 0.f;  // MUFU path: a Kahan sum per lane
     for (int64_t j = lane; j < nruns; j += 32) {
       float f[R];
       load_run<T>(x, j, n, vec, f);
@@ -74,11 +76,14 @@ __device__ void chunk_partial(const T* x, int64_t n, const float* thi, const flo
           const FF d = two_sum(f[e], -m);
           s = ff_add(s, exp_ff(d.hi, d.lo, thi, tlo, tab));
         } else {
-          const float p = ex2_fast(__fmul_rn(__fsub_rn(f[e], m), kLog2e));
-          s = ff_add(s, FF{p, 0.f});
+          const float y = __fsub_rn(ex2_fast(__fmul_rn(__fsub_rn(f[e], m), kLog2e)), kc);
+          const float t = __fadd_rn(ks, y);
+          kc = __fsub_rn(__fsub_rn(t, ks), y);
+          ks = t;
         }
       }
     }
+    if (!kPrecise) s = two_sum(ks, -kc);
   }
   s = warp_sum_ff2(s);
   Z = FF{__shfl_sync(0xFFFFFFFFu, s.hi, 0), __shfl_sync(0xFFFFFFFFu, s.lo, 0)};
