@@ -5,7 +5,9 @@ contiguous range of whole sequences (ranks in order); the only quantities
 that cross ranks are the integer active-token counts (gathered, so the
 normaliser is exact at every degree) and the per-sequence totals, gathered
 and concatenated in rank order -- an exact byte copy, never an all_reduce,
-whose combine order would follow the collective's topology.
+whose combine order would follow the collective's topology.  A TP rank
+holds a slice of the vocabulary; its chunk records travel the same way
+(gather_vocab_partials).
 
     counts = dp.gather_counts(g.grpo_count_active(mask_local))
     tot = g.totals_buffer(B_local)
@@ -37,25 +39,54 @@ def gather_counts(local_counts: torch.Tensor, group=None) -> torch.Tensor:
     return torch.stack(parts).sum(0)
 
 
-def gather_totals(local_totals: torch.Tensor, group=None) -> torch.Tensor:
-    """Every rank's per-sequence total records (uint8 [B_rank, 32]),
-    concatenated in rank order.  Ranks may own different numbers of
-    sequences: sizes are exchanged first and the records padded to the
+def gather_rows(local: torch.Tensor, group=None) -> torch.Tensor:
+    """Every rank's tensor concatenated along dim 0 in rank order, as an
+    exact copy.  Ranks may hold different numbers of rows (the trailing
+    dims must agree): sizes are exchanged first and the rows padded to the
     largest share for the collective, then trimmed."""
     world = _world(group)
     if world == 1:
-        return local_totals.clone()
-    dev = local_totals.device
-    n = torch.tensor([local_totals.shape[0]], dtype=torch.int64, device=dev)
+        return local.clone()
+    dev = local.device
+    n = torch.tensor([local.shape[0]], dtype=torch.int64, device=dev)
     sizes = [torch.empty_like(n) for _ in range(world)]
     dist.all_gather(sizes, n, group=group)
     sizes = [int(s.item()) for s in sizes]
-    width = local_totals.shape[1]
-    pad = torch.zeros((max(sizes), width), dtype=local_totals.dtype, device=dev)
-    pad[: local_totals.shape[0]] = local_totals
+    pad = torch.zeros((max(sizes),) + tuple(local.shape[1:]), dtype=local.dtype, device=dev)
+    pad[: local.shape[0]] = local
     parts = [torch.empty_like(pad) for _ in range(world)]
     dist.all_gather(parts, pad, group=group)
     return torch.cat([p[:s] for p, s in zip(parts, sizes)])
+
+
+def gather_totals(local_totals: torch.Tensor, group=None) -> torch.Tensor:
+    """Every rank's per-sequence total records (uint8 [B_rank, 32]),
+    concatenated in rank order."""
+    return gather_rows(local_totals, group)
+
+
+def gather_vocab_partials(parts: dict, group=None) -> dict:
+    """The tensor-parallel exchange of grpo_vocab_partials' outputs: the
+    chunk records of every rank concatenated in rank order (= chunk order),
+    and the action logits summed over ranks in rank order (exact: exactly
+    one rank holds each action, the others contribute 0)."""
+    out = {k: gather_rows(parts[k], group) for k in ("part_p", "part_r")}
+    act = parts["action_logits"]
+    if _world(group) == 1:
+        out["action_logits"] = act.clone()
+    else:
+        every = [torch.empty_like(act) for _ in range(_world(group))]
+        dist.all_gather(every, act.contiguous(), group=group)
+        out["action_logits"] = torch.stack(every).sum(0)
+    return out
+
+
+def vocab_shard_bounds(V: int, chunk: int, world: int, rank: int) -> tuple[int, int]:
+    """[begin, end) of the vocabulary for `rank` of `world`: whole chunks, in
+    rank order, as even as possible (the page's vocab_shard_bounds)."""
+    nck = (V + chunk - 1) // chunk
+    a, b = shard_bounds(nck, world, rank)
+    return min(V, a * chunk), min(V, b * chunk)
 
 
 def shard_bounds(num_sequences: int, world: int, rank: int) -> tuple[int, int]:

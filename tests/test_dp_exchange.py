@@ -69,3 +69,55 @@ def test_shard_bounds_partition_in_rank_order(n, world):
         assert b == c and a <= b
     sizes = [b - a for a, b in bounds]
     assert max(sizes) - min(sizes) <= 1
+
+
+def _tp_rank(rank: int, world: int, nck, port: int, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    rows = 5
+    g = torch.Generator().manual_seed(77 + rank)
+    parts = {"part_p": torch.randn(nck[rank], rows, 4, generator=g),
+             "part_r": torch.randn(nck[rank], rows, 4, generator=g),
+             # rank r holds the action of rows r, r + world, ...
+             "action_logits": torch.tensor([[float(10 * j + 1) if j % world == rank else 0.0
+                                             for j in range(rows)]] * 2)}
+    out = dp.gather_vocab_partials(parts)
+    dist.barrier()
+    q.put((rank, out["part_p"].numpy().tobytes(), out["part_r"].shape[0],
+           out["action_logits"].tolist()))
+    dist.destroy_process_group()
+
+
+def test_vocab_partials_exchange():
+    nck = (2, 1, 3)
+    world = len(nck)
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_tp_rank, args=(r, world, nck, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+    got = sorted(q.get(timeout=10) for _ in range(world))
+    want = []
+    for r in range(world):
+        g = torch.Generator().manual_seed(77 + r)
+        want.append(torch.randn(nck[r], 5, 4, generator=g))
+    want = torch.cat(want).numpy().tobytes()
+    for rank, pp, n_r, act in got:
+        assert pp == want and n_r == sum(nck)
+        assert act == [[float(10 * j + 1) for j in range(5)]] * 2
+
+
+@pytest.mark.parametrize("V,world", [(8969, 1), (8969, 2), (8969, 3), (151936, 4), (100, 4)])
+def test_vocab_shard_bounds_are_whole_chunks(V, world):
+    C = 4096
+    b = [dp.vocab_shard_bounds(V, C, world, r) for r in range(world)]
+    assert b[0][0] == 0 and b[-1][1] == V
+    for (x, y), (z, _) in zip(b, b[1:]):
+        assert y == z
+    for x, y in b:
+        assert x == y or x % C == 0  # a nonempty slice starts on a chunk boundary
