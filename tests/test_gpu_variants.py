@@ -199,3 +199,49 @@ def test_variant_parameters_are_checked_on_the_host():
                 dict(reduction="fixed_constant")):
         with pytest.raises(g.GrpoError):
             g.grpo_loss_fwd_bwd(x, x, a, o, m, r, samples_per_prompt=2, **bad)
+
+
+def test_gspo_with_empty_sequences_on_both_boundaries():
+    # sequences with no active token: rho_i undefined, weight 0, excluded from
+    # the sequence mean
+    w = WIDE.with_(len_range=(0, 10), holes=3, reduction=1)
+    case = make_case(w, "f32")
+    assert (case["mask"].sum(1) == 0).sum() >= 3
+    v = dict(ratio_level="sequence", reduction="sequence_mean")
+    exp = oracle.fused(case["X"], case["Y"], "f32", case["acts"], case["old"], case["mask"],
+                       case["R"], case["bounds"], w.eps_lo, w.eps_hi, w.beta, reduction=1,
+                       ratio_level="sequence")
+    res = _run_logits(case, to_device(case), v)
+    out = res["out3"].cpu().numpy().astype(np.float64)
+    for i, k in enumerate(("loss", "policy_loss", "kl")):
+        assert_scalar(out[i], exp[k], k)
+    near = _band(exp, w.eps_lo, w.eps_hi, None)
+    assert_grad_rows(torch_storage(res["grad"])[~near], exp["grad"][~near], "f32")
+    # the same tokens through the logps boundary
+    lp = exp["logp"].astype(np.float32)
+    rf = exp["ref_logp"].astype(np.float32)
+    e2 = oracle.loss_from_logps(lp, rf, case["old"], case["mask"], exp["A"], w.eps_lo, w.eps_hi,
+                                w.beta, reduction=1, ratio_level="sequence")
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    r2 = g.grpo_loss_from_logps(t(lp), t(case["old"]), t(rf), t(case["mask"]), t(case["R"]),
+                                samples_per_prompt=w.samples_per_prompt, clip_eps=w.eps_lo,
+                                clip_eps_hi=w.eps_hi, beta=w.beta, **v)
+    torch.cuda.synchronize()
+    out = r2["out3"].cpu().numpy().astype(np.float64)
+    for i, k in enumerate(("loss", "policy_loss", "kl")):
+        assert_scalar(out[i], e2[k], k)
+
+
+@pytest.mark.parametrize("name", ["k2", "cispo", "gspo", "dual"])
+def test_variants_with_f16_logits(name):
+    v = VARIANTS[name]
+    w = TINY_WIDE
+    case = make_case(w, "f16")
+    exp = oracle.fused(case["X"], case["Y"], "f16", case["acts"], case["old"], case["mask"],
+                       case["R"], case["bounds"], w.eps_lo, w.eps_hi, w.beta, **_oracle_kw(v, w))
+    res = _run_logits(case, to_device(case), v)
+    out = res["out3"].cpu().numpy().astype(np.float64)
+    for i, k in enumerate(("loss", "policy_loss", "kl")):
+        assert_scalar(out[i], exp[k], f"{name} {k}")
+    near = _band(exp, w.eps_lo, w.eps_hi, v.get("dual_clip_c"))
+    assert_grad_rows(torch_storage(res["grad"])[~near], exp["grad"][~near], "f16")

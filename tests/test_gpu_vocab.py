@@ -109,3 +109,63 @@ def test_vocab_parallel_agrees_with_the_fused_path():
     assert np.allclose(a, b, rtol=2e-5, atol=1e-9)
     diff = (tp["grad"].float() - fused["grad"].float()).abs()
     assert diff.max().item() <= 2 * 2 ** -8 * fused["grad"].float().abs().max().item()
+
+
+@pytest.mark.parametrize("V,dtype,widths", [(1000, "f32", [1000]), (2 * C, "bf16", [C, C]),
+                                            (C + 5, "f16", [C, 5])])
+def test_vocab_parallel_edge_vocabularies(V, dtype, widths):
+    # a single partial chunk; whole chunks only; a 5-entry last slice; f16
+    w = WL.with_(V=V, B=8, T=4, len_range=(0, 4))
+    case = make_case(w, dtype)
+    dev = to_device(case)
+    got = _run_with(w, dev, widths)
+    one = _run_with(w, dev, [V])
+    for k in ("out3", "lse_w", "grad"):
+        assert torch.equal(got[k], one[k]), k
+    exp = oracle.fused(case["X"], case["Y"], dtype, case["acts"], case["old"], case["mask"],
+                       case["R"], case["bounds"], w.eps_lo, w.eps_hi, w.beta)
+    out = got["out3"].cpu().numpy().astype(np.float64)
+    for i, k in enumerate(("loss", "policy_loss", "kl")):
+        assert_scalar(out[i], exp[k], k)
+    r = exp["ratio"]
+    near = (np.abs(r - 0.8) <= 1e-6) | (np.abs(r - 1.28) <= 1.3e-6)
+    assert_grad_rows(torch_storage(got["grad"])[~near], exp["grad"][~near], dtype)
+
+
+def _run_with(w, dev, widths):
+    bounds = np.concatenate([[0], np.cumsum(widths)])
+    parts = [g.grpo_vocab_partials(dev["X"][:, :, a:b].contiguous(),
+                                   dev["Y"][:, :, a:b].contiguous(), dev["acts"], dev["mask"],
+                                   int(a)) for a, b in zip(bounds[:-1], bounds[1:])]
+    res = g.grpo_vocab_loss(torch.cat([p["part_p"] for p in parts]),
+                            torch.cat([p["part_r"] for p in parts]),
+                            torch.stack([p["action_logits"] for p in parts]).sum(0), w.V,
+                            dev["acts"], dev["old"], dev["mask"], dev["R"],
+                            samples_per_prompt=w.samples_per_prompt, clip_eps=w.eps_lo,
+                            clip_eps_hi=w.eps_hi, beta=w.beta)
+    res["grad"] = torch.cat([g.grpo_vocab_grad(dev["X"][:, :, a:b].contiguous(), dev["acts"],
+                                               dev["mask"], int(a), res["lse_w"])
+                             for a, b in zip(bounds[:-1], bounds[1:])], dim=2)
+    torch.cuda.synchronize()
+    return res
+
+
+def test_vocab_parallel_masked_rows_and_bad_actions():
+    w = WL.with_(V=3000, B=8, T=4, len_range=(0, 4))
+    case = make_case(w, "bf16")
+    dev = to_device(case)
+    # masked rows are never read: poison their logits
+    m = dev["mask"].bool()
+    dev["X"][~m] = float("nan")
+    dev["Y"][~m] = float("inf")
+    a = _run_with(w, dev, [3000])
+    assert torch.isfinite(a["out3"]).all()
+    assert (a["grad"][~m] == 0).all()
+    # an active token whose action id no slice holds: device status, NaN loss
+    acts = dev["acts"].clone()
+    row = int(m.view(-1).nonzero()[0])
+    acts.view(-1)[row] = w.V + 7
+    dev2 = dict(dev, acts=acts)
+    b = _run_with(w, dev2, [3000])
+    assert torch.isnan(b["out3"]).all()
+    assert g.grpo_read_device_status(b["workspace"]) & 16
