@@ -30,6 +30,8 @@ __all__ = ["grpo_workspace_size", "grpo_group_adv", "grpo_loss_fwd_bwd", "grpo_l
 
 GRPO_ADV_EPS_ADD = 1
 GRPO_SKIP_MASKED_GRAD_ROWS = 2
+GRPO_FLAG_TEST_STALLED_COPY = 0x80000000  # test hook (see include/grpo.h)
+GRPO_ERR_TIMEOUT = 128
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 _REDUCTIONS = {"token_mean": 0, "sequence_mean": 1, "fixed_constant": 2}
 _KL_TYPES = {"k3": 0, "k1": 1, "k2": 2}
@@ -367,9 +369,10 @@ def grpo_loss_from_logps(logps: torch.Tensor, old_logps: torch.Tensor,
                          dual_clip_c: Optional[float] = None,
                          norm_constant: Optional[float] = None,
                          want_clip_counts: bool = False, shard: Optional[Shard] = None,
-                         ratio_level: str = "token") -> dict:
+                         ratio_level: str = "token", extra_flags: int = 0) -> dict:
     """GRPO loss from per-token log-probs; ``grad`` gives dL/dlogp [B,T].
-    Variants, outputs and ``shard`` as in grpo_loss_fwd_bwd."""
+    Variants, outputs and ``shard`` as in grpo_loss_fwd_bwd; ``extra_flags``
+    are raw grpo_params_t flag bits (e.g. GRPO_FLAG_TEST_STALLED_COPY)."""
     _dev(logps, "logps", torch.float32)
     B, T = logps.shape
     _dev(old_logps, "old_logps", torch.float32)
@@ -384,8 +387,8 @@ def grpo_loss_from_logps(logps: torch.Tensor, old_logps: torch.Tensor,
     g, keep = _groups(Bg, samples_per_prompt, group_boundaries)
     counts = torch.empty(3, dtype=torch.int64, device=dev) if want_clip_counts else None
     p, prof = _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction,
-                      GRPO_ADV_EPS_ADD if eps_add else 0, profile, kl, surrogate, dual_clip_c,
-                      norm_constant, counts, shard, ratio_level)
+                      (GRPO_ADV_EPS_ADD if eps_add else 0) | int(extra_flags), profile, kl,
+                      surrogate, dual_clip_c, norm_constant, counts, shard, ratio_level)
     if grad is True:
         grad_t = torch.empty((B, T), dtype=torch.float32, device=dev)
     elif grad is None or grad is False:

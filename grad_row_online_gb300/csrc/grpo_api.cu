@@ -38,7 +38,8 @@ grpo_status_t check_params(const grpo_params_t* p) {
     return GRPO_ERR_PARAM;
   if (p->reduction == GRPO_FIXED_CONSTANT && !(isfinite(p->norm_constant) && p->norm_constant > 0.f))
     return GRPO_ERR_PARAM;
-  if (p->flags & ~(GRPO_ADV_EPS_ADD | GRPO_SKIP_MASKED_GRAD_ROWS)) return GRPO_ERR_PARAM;
+  if (p->flags & ~(GRPO_ADV_EPS_ADD | GRPO_SKIP_MASKED_GRAD_ROWS | GRPO_FLAG_TEST_STALLED_COPY))
+    return GRPO_ERR_PARAM;
   if (p->kl_type != GRPO_KL_K3 && p->kl_type != GRPO_KL_K1 && p->kl_type != GRPO_KL_K2)
     return GRPO_ERR_PARAM;
   if (p->surrogate != GRPO_SURROGATE_CLIP && p->surrogate != GRPO_SURROGATE_CISPO)
@@ -336,7 +337,7 @@ extern "C" grpo_status_t grpo_loss_from_logps(const float* logps, const float* o
                Aff + pl.seq_begin, rng, L, totals, grad_logps, out3,
                per_seq, hdr, B, T, params->clip_eps_lo, params->clip_eps_hi, params->beta,
                params->grad_scale, params->reduction, variant_of(params),
-               params->norm_constant, params->clip_counts, NS, pl.shard ? 1 : 0};
+               params->norm_constant, params->clip_counts, NS, pl.shard ? 1 : 0, params->flags};
   return cuda_status(launch_logps(la, params->profile, s));
 }
 

@@ -736,6 +736,7 @@ struct LogpsArgs {
   unsigned long long* counts_out;  // nullable [3]
   const unsigned long long* NS;    // [2]: N and S of the whole batch
   int shard;     // 1: write the totals only (the scalar comes from grpo_loss_finalize)
+  unsigned flags;  // grpo_params_t.flags
 };
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);

@@ -267,7 +267,8 @@ __device__ __forceinline__ void process_vec(uint32_t mw, const float4& l, const 
 // flight while one is evaluated.
 static constexpr int kChunk = 4 * kLogpsThreads;  // one float4 per thread
 static constexpr int kDepth = 4;
-static constexpr uint32_t kWaitLimit = 1u << 22;  // try_wait rounds before giving up
+static constexpr unsigned long long kWaitNs = 200000000ull;  // 0.2 s per bounded wait
+static constexpr uint32_t kWaitRounds = 1u << 26;  // and never more try_wait rounds than this
 
 struct Stage {
   float4 lp[kChunk / 4];
@@ -306,10 +307,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait for a phase of `bar`; false if it did not complete in time.
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait for a phase of `bar`: false if it did not complete within
+// kWaitNs (read from the global timer every 16 rounds) or kWaitRounds rounds.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 0; i < kWaitRounds; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15u) == 15u && global_ns() - t0 > kWaitNs) return false;
+  }
   return false;
 }
 
@@ -327,6 +337,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
   __shared__ unsigned s_nc[3][kLogpsThreads / 32];
   __shared__ FinalSmem s_fin;
   __shared__ double s_em[1];
+  __shared__ int s_issued;
   __shared__ bool s_last;
   __shared__ __align__(16) Stage s_st[kDepth];
   __shared__ __align__(8) uint64_t s_full[kDepth];
@@ -398,19 +409,24 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
       const int64_t lo = rg.x & ~15, hi = min((int64_t)((rg.y + 15) & ~15), a.T);
       const int nchunks = (int)((hi - lo + kChunk - 1) / kChunk);
       const uint32_t nref = has_ref ? 1u : 0u;
+      // the test hook GRPO_FLAG_TEST_STALLED_COPY: the first chunk of sequence
+      // 0 expects 16 bytes more than its copies deliver, so its wait runs out
+      const uint32_t stall = ((a.flags & GRPO_FLAG_TEST_STALLED_COPY) && b == 0) ? 16u : 0u;
       auto issue = [&](int c) {  // thread 0 only
         const int64_t st = lo + (int64_t)c * kChunk;
         const uint32_t len = (uint32_t)min((int64_t)kChunk, hi - st);
         Stage& S = s_st[c % kDepth];
         uint64_t* bar = &s_full[c % kDepth];
-        mbar_expect_tx(bar, len * (4u * (2u + nref) + 1u));
+        mbar_expect_tx(bar, len * (4u * (2u + nref) + 1u) + (c == 0 ? stall : 0u));
         bulk_g2s(S.lp, a.logps + base + st, 4u * len, bar, pol);
         bulk_g2s(S.od, a.old + base + st, 4u * len, bar, pol);
         if (has_ref) bulk_g2s(S.rf, a.ref + base + st, 4u * len, bar, pol);
         bulk_g2s(S.mk, a.mask + base + st, len, bar, pol);
       };
-      if (threadIdx.x == 0)
+      if (threadIdx.x == 0) {
         for (int c = 0; c < nchunks && c < kDepth; ++c) issue(c);
+        s_issued = nchunks < kDepth ? nchunks : kDepth;
+      }
       // slots outside the widened active range hold no active token
       float4* grow = reinterpret_cast<float4*>(a.grad + base);
       const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -418,18 +434,20 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
         for (int64_t v = threadIdx.x; v < lo / 4; v += kLogpsThreads) grow[v] = z4;
         for (int64_t v = hi / 4 + threadIdx.x; v < a.T / 4; v += kLogpsThreads) grow[v] = z4;
       }
-      bool timed_out = false;
-      for (int c = 0; c < nchunks; ++c) {
+      // A wait that runs out (never expected outside the test hook) is
+      // recorded; the CTA then issues no further copy, still waits for the
+      // copies already issued (bounded), and skips the arithmetic -- the loss
+      // outputs become NaN through the status word.
+      bool stalled = false;
+      __syncthreads();  // s_issued
+      for (int c = 0; c < nchunks && c < s_issued; ++c) {
         const int slot = c % kDepth;
         const int64_t st = lo + (int64_t)c * kChunk;
         const int len = (int)min((int64_t)kChunk, hi - st);
-        bool ready = mbar_wait(&s_full[slot], (uint32_t)(c / kDepth) & 1u);
-        if (!ready) {  // never expected: record it, then give the copy a second chance
-          timed_out = true;
-          ready = mbar_wait(&s_full[slot], (uint32_t)(c / kDepth) & 1u);
-        }
+        const bool ready = mbar_wait(&s_full[slot], (uint32_t)(c / kDepth) & 1u);
+        stalled = __syncthreads_or(!ready) || stalled;  // one decision for the CTA
         const int v = threadIdx.x;
-        if (ready && 4 * v < len) {
+        if (!stalled && 4 * v < len) {
           const Stage& S = s_st[slot];
           float w[4];
           process_vec(S.mk[v], S.lp[v], S.od[v], has_ref ? S.rf[v] : z4, has_ref, f, x, a, acc,
@@ -437,9 +455,13 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
           if (a.grad) grow[st / 4 + v] = make_float4(w[0], w[1], w[2], w[3]);
         }
         __syncthreads();  // the slot is free again
-        if (threadIdx.x == 0 && c + kDepth < nchunks) issue(c + kDepth);
+        if (threadIdx.x == 0 && !stalled && c + kDepth < nchunks) {
+          issue(c + kDepth);
+          s_issued = c + kDepth + 1;
+        }
+        __syncthreads();  // s_issued
       }
-      if (timed_out) atomicOr(&a.hdr->status, (unsigned)GRPO_ERR_TIMEOUT);
+      if (stalled && threadIdx.x == 0) atomicOr(&a.hdr->status, (unsigned)GRPO_ERR_TIMEOUT);
     } else if (vec_ok(a)) {
       const int64_t nv = a.T / 4;
       const uint32_t* mrow = reinterpret_cast<const uint32_t*>(a.mask + base);

@@ -100,6 +100,13 @@ typedef enum {
 #define GRPO_ADV_EPS_ADD 1u          /* divide by std + adv_eps instead of max(std, adv_eps) */
 #define GRPO_SKIP_MASKED_GRAD_ROWS 2u /* leave gradient rows of masked tokens untouched
                                          (caller pre-zeroed them) instead of writing 0 */
+/* Test hook, for the failure-detection tests only: in grpo_loss_from_logps'
+ * staged path (T % 16 == 0, 16-byte aligned arrays) the first asynchronous
+ * copy of sequence 0 is made to under-deliver, so its bounded wait runs out
+ * (after 0.2 s): the call then sets GRPO_ERR_TIMEOUT, the loss outputs are
+ * NaN, the sequence's gradient is not written, and the context stays usable.
+ * Ignored by the other entry points. */
+#define GRPO_FLAG_TEST_STALLED_COPY 0x80000000u
 
 /* Group specification ("Group specification": provide exactly one of
  * samples_per_prompt > 0, or CSR group_boundaries of length num_groups + 1
