@@ -22,6 +22,12 @@
  *                 g_pol = 0 if (A>0, r>1+eps_hi) or (A<0, r<1-eps_lo), else -A r
  *   dL/dx_v     = w (1[v = a] - softmax(x)_v)
  *
+ * That is the default loss; grpo_params_t selects the variants documented
+ * with it (KL estimators k1 / k2, CISPO, the dual clip, the fixed-constant
+ * normaliser, GSPO sequence-level ratios) and the clip counters.  Sequence
+ * sharding (grpo_shard_t) and vocabulary parallelism (grpo_vocab_*) compute
+ * the same loss, bit-identically at every degree.
+ *
  * Conventions shared by every entry point:
  *   - All tensor arguments are DEVICE pointers to row-major contiguous
  *     arrays owned by the caller; the library allocates nothing, keeps no
