@@ -349,6 +349,9 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  // launched as a programmatic dependent of prep: everything above overlaps
+  // prep's tail; prep's outputs (counts, advantages, ranges) are read below
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (b < a.B) {
     SeqCtx x;
@@ -589,12 +592,28 @@ cudaError_t launch_logps(const LogpsArgs& a, const grpo_profile_t* prof, cudaStr
     if (e != cudaSuccess) return e;
     carveout_set.fetch_or(bit, std::memory_order_acq_rel);
   }
-  if (prof && prof->start) cudaEventRecord((cudaEvent_t)prof->start, s);
   const int64_t grid = a.B > 0 ? a.B : 1;
-  logps_kernel<<<(unsigned)grid, kLogpsThreads, 0, s>>>(a);
-  e = cudaGetLastError();
-  if (prof && prof->stop) cudaEventRecord((cudaEvent_t)prof->stop, s);
-  return e;
+  if (prof && (prof->start || prof->stop)) {  // timed alone: an ordinary launch between events
+    if (prof->start) cudaEventRecord((cudaEvent_t)prof->start, s);
+    logps_kernel<<<(unsigned)grid, kLogpsThreads, 0, s>>>(a);
+    e = cudaGetLastError();
+    if (prof->stop) cudaEventRecord((cudaEvent_t)prof->stop, s);
+    return e;
+  }
+  // programmatic dependent launch: the CTAs may start while prep finishes
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kLogpsThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, logps_kernel, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 }  // namespace grpo

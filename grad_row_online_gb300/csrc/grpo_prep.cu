@@ -128,6 +128,10 @@ __device__ void warp_group(const PrepArgs& a, int64_t g, int lane) {
 
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
   __shared__ int s_L[kPrepWarps];
+  // a dependent kernel launched with programmatic stream serialization (the
+  // logps kernel) may start its prologue now; it waits for this grid's
+  // completion (griddepcontrol.wait) before reading anything written here
+  asm volatile("griddepcontrol.launch_dependents;");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t group_ctas = (a.G + kPrepWarps - 1) / kPrepWarps;
   if ((int64_t)blockIdx.x < group_ctas) {
