@@ -11,10 +11,10 @@
 // to warp lanes by their index in the chunk, not by their address), so any
 // split at chunk boundaries gives the same bits.
 //
-//   vocab_partials_kernel  one warp per (row, chunk): max, then the sum of
-//                          exp(x - max) (a float-float exponential and
-//                          float-pair sums for fp32 logits; MUFU 2^x and a
-//                          Kahan sum per lane otherwise);
+//   vocab_partials_kernel  one warp per (row, chunk): the chunk's max and
+//                          sum of exp(x - max) (fp32 logits: two passes with
+//                          a float-float exponential; 16-bit logits: one pass
+//                          of online normalisers with MUFU 2^x);
 //                          the action logit where the rank owns it
 //   vocab_merge_kernel     one thread per row: the chunks folded in order,
 //                          logsumexp in double, logp and d = ref_logp - logp
@@ -42,10 +42,50 @@ __device__ __forceinline__ void load_run(const T* x, int64_t j, int64_t n, bool 
 
 // A chunk's partial normaliser, by one warp: runs of 16 bytes of storage go
 // to lane (run index mod 32), each lane takes its runs in order; a fixed xor
-// tree combines the lanes.  Every lane gets (M, Z).
+// tree combines the lanes.  Every lane gets (M, Z), Z = sum exp(x - M).
+//
+// MUFU path (16-bit logits): one pass, each lane an online normaliser in
+// base 2 (its running max m, mL = fl(m log2e), a Kahan sum of
+// 2^(x log2e - mL)); the lanes' sums rescaled to the chunk's ML = fl(M log2e)
+// and added as float pairs; finally Z = Z_2 2^(ML - M log2e), the residual
+// exponent taken exactly with an FMA.
+template <typename T>
+__device__ void chunk_partial_fast(const T* x, int64_t n, float& M, FF& Z) {
+  constexpr int R = Storage<T>::kVec;
+  const bool vec = ((uintptr_t)x & 15) == 0;
+  const int64_t nruns = (n + R - 1) / R;
+  OnlineLse st;
+  st.init();
+  for (int64_t j = threadIdx.x & 31; j < nruns; j += 32) {
+    float f[R];
+    load_run<T>(x, j, n, vec, f);
+    st.update<R>(f);
+  }
+  const float m = warp_max(st.m);
+  if (m == -INFINITY) {  // an empty chunk contributes nothing
+    M = -INFINITY;
+    Z = FF{0.f, 0.f};
+    return;
+  }
+  const float ML = __fmul_rn(m, kLog2e);
+  const float z = st.m == -INFINITY ? 0.f : __fmul_rn(__fsub_rn(st.s, st.c),
+                                                      ex2_fast(__fsub_rn(st.mL, ML)));
+  const FF s = warp_sum_ff(z);
+  const FF z2 = FF{__shfl_sync(0xFFFFFFFFu, s.hi, 0), __shfl_sync(0xFFFFFFFFu, s.lo, 0)};
+  const float resid = -__fmaf_rn(m, kLog2e, -ML);  // ML - m log2e, exactly
+  Z = ff_scale(z2, ex2_fast(resid));
+  M = m;
+}
+
+// Float-float path (fp32 logits): the chunk's max first, then
+// sum exp(x - M) with the float-float exponential and float-pair sums.
 template <typename T, bool kPrecise>
 __device__ void chunk_partial(const T* x, int64_t n, const float* thi, const float* tlo,
                               const ExpTable& tab, float& M, FF& Z) {
+  if (!kPrecise) {
+    chunk_partial_fast<T>(x, n, M, Z);
+    return;
+  }
   constexpr int R = Storage<T>::kVec;
   const int lane = threadIdx.x & 31;
   const bool vec = ((uintptr_t)x & 15) == 0;
@@ -65,25 +105,16 @@ __device__ void chunk_partial(const T* x, int64_t n, const float* thi, const flo
   nan = __any_sync(0xFFFFFFFFu, nan);
   FF s = {0.f, 0.f};
   if (m != -INFINITY && !nan) {
-    float ks = 0.f, kc = 0.f;  // MUFU path: a Kahan sum per lane
     for (int64_t j = lane; j < nruns; j += 32) {
       float f[R];
       load_run<T>(x, j, n, vec, f);
 #pragma unroll
       for (int e = 0; e < R; ++e) {
         if (f[e] == -INFINITY) continue;
-        if (kPrecise) {
-          const FF d = two_sum(f[e], -m);
-          s = ff_add(s, exp_ff(d.hi, d.lo, thi, tlo, tab));
-        } else {
-          const float y = __fsub_rn(ex2_fast(__fmul_rn(__fsub_rn(f[e], m), kLog2e)), kc);
-          const float t = __fadd_rn(ks, y);
-          kc = __fsub_rn(__fsub_rn(t, ks), y);
-          ks = t;
-        }
+        const FF d = two_sum(f[e], -m);
+        s = ff_add(s, exp_ff(d.hi, d.lo, thi, tlo, tab));
       }
     }
-    if (!kPrecise) s = two_sum(ks, -kc);
   }
   s = warp_sum_ff2(s);
   Z = FF{__shfl_sync(0xFFFFFFFFu, s.hi, 0), __shfl_sync(0xFFFFFFFFu, s.lo, 0)};
