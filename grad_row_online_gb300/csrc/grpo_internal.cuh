@@ -660,6 +660,7 @@ struct RowArgs {
   int reduction;
   unsigned flags;
   int precise_ok;  // fp32 gradient output: rows may take the precise path
+  int tmem_cols;   // tensor-memory columns a row CTA keeps policy vectors in (0: none)
   ExpTable tab;
   Variant var;
   float norm_c;  // GRPO_FIXED_CONSTANT's constant

@@ -93,18 +93,33 @@ __device__ __forceinline__ void lse_row(const T* row, int64_t V, OnlineLse& st, 
 // the same order: equal rows give bit-identical normalisers, so KL is exactly
 // 0 when ref == policy.  Rows of different phases are swept one after the
 // other.
+//
+// With `keep`, the first kPolicySmemVecs policy vectors go to shared memory
+// and, when tmem_vecs > 0 and the row is long enough for every thread to
+// reach them in the unrolled loop, the next tmem_vecs per thread to tensor
+// memory at `tb` (this thread's lane and column base).  Returns the vectors
+// per thread kept in tensor memory (0 or tmem_vecs; block-uniform).
 template <typename T>
-__device__ __forceinline__ void lse_pair(const T* x, const T* y, int64_t V, OnlineLse& sx,
-                                         OnlineLse& sy, uint64_t pol_x, uint64_t pol_y,
-                                         uint4* keep) {
+__device__ __forceinline__ int lse_pair(const T* x, const T* y, int64_t V, OnlineLse& sx,
+                                        OnlineLse& sy, uint64_t pol_x, uint64_t pol_y,
+                                        uint4* keep, uint32_t tb, int tmem_vecs) {
   constexpr int VEC = Storage<T>::kVec;
   const Geom<T> gx(x, V), gy(y, V);
   if (gy.head != gx.head) {
     lse_row<T>(x, V, sx, pol_x, keep);
     lse_row<T>(y, V, sy, pol_y, nullptr);
-    return;
+    return 0;
   }
   const int64_t nsm = keep ? (gx.nvec < kPolicySmemVecs ? gx.nvec : kPolicySmemVecs) : 0;
+  constexpr int U = kPairUnroll;
+  const int tmv =
+      (keep && tmem_vecs > 0 && gx.nvec >= (int64_t)kRowThreads * (kSmemJ + tmem_vecs + U))
+          ? tmem_vecs
+          : 0;
+  // with the tensor-memory slice, the kept vectors are read evict-first: only
+  // the rest of the row is wanted in L2 for sweep 2 (on shorter rows, whose
+  // whole policy slice stays in L2 anyway, the plain policy measured faster)
+  const int64_t nkept = tmv ? nsm + (int64_t)kRowThreads * tmv : 0;
   // head / tail scalars, as one padded vector per thread
   const bool h = (int)threadIdx.x < gx.head;
   const bool t = (int)threadIdx.x < gx.tail;
@@ -125,19 +140,26 @@ __device__ __forceinline__ void lse_pair(const T* x, const T* y, int64_t V, Onli
   }
   const uint4* xv = reinterpret_cast<const uint4*>(x + gx.head);
   const uint4* yv = reinterpret_cast<const uint4*>(y + gx.head);
-  constexpr int U = kPairUnroll;
   const int64_t stride = blockDim.x;
   int64_t k = threadIdx.x;
+  // every thread runs the unrolled loop at least kSmemJ + tmv + 1 steps of
+  // `stride` deep (the length test above), so the tensor-memory stores, whose
+  // condition depends on the step only, are taken by whole warps
   for (; k + (U - 1) * stride < gx.nvec; k += U * stride) {
     uint4 vx[U], vy[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      vx[u] = ld_hint(xv + k + u * stride, pol_x);
+      vx[u] = ld_hint(xv + k + u * stride, k + u * stride < nkept ? pol_y : pol_x);
       vy[u] = ld_hint(yv + k + u * stride, pol_y);
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (k + u * stride < nsm) keep[k + u * stride] = vx[u];
+    for (int u = 0; u < U; ++u) {
+      const int64_t q = k + u * stride;
+      if (q < nsm)
+        keep[q] = vx[u];
+      else if (q < nkept)
+        tmem_st4(tb + 4u * (uint32_t)((q - nsm) / kRowThreads), vx[u]);
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       float f[VEC];
@@ -156,6 +178,8 @@ __device__ __forceinline__ void lse_pair(const T* x, const T* y, int64_t V, Onli
     Storage<T>::unpack(ld_hint(yv + k, pol_y), f);
     sy.update<VEC>(f);
   }
+  if (tmv) tmem_wait_st();  // this thread's stores land before its sweep-2 loads
+  return tmv;
 }
 
 // ------------------------------------------------- precise normaliser sweep
@@ -213,7 +237,8 @@ __device__ double sum_exp_precise(const T* row, int64_t V, float M, const float*
 // element is patched once per vector, outside the element loop.
 template <typename T, bool kPrecise>
 __device__ void grad_row(const T* x, T* g, int64_t V, int64_t act, const RowScalars& rs,
-                         uint64_t pol_in, uint64_t pol_out, const uint4* kept) {
+                         uint64_t pol_in, uint64_t pol_out, const uint4* kept, uint32_t tb = 0,
+                         int tmv = 0) {
   constexpr int VEC = Storage<T>::kVec;
   const bool same_phase = (((uintptr_t)x ^ (uintptr_t)g) & 15) == 0;
   if (!same_phase) {  // differently aligned buffers: element by element
@@ -250,11 +275,13 @@ __device__ void grad_row(const T* x, T* g, int64_t V, int64_t act, const RowScal
     }
     st_hint(gv + q, Storage<T>::pack(f), pol_out);
   };
-  // vectors [0, nsm) were kept in shared memory by sweep 1; the rest, in the
-  // sweep order, from global memory (mostly L2)
+  // vectors [0, nsm) were kept in shared memory by sweep 1, the next tmv per
+  // thread in tensor memory; the rest, in the sweep order, come from global
+  // memory (mostly L2)
   const int64_t nsm = kept ? (n < kPolicySmemVecs ? n : kPolicySmemVecs) : 0;
-  const int64_t ng = n - nsm;
-  auto atg = [&](int64_t k) -> int64_t { return kReverseSweep2 ? n - 1 - k : nsm + k; };
+  const int64_t ntm = (int64_t)kRowThreads * tmv;
+  const int64_t ng = n - nsm - ntm;
+  auto atg = [&](int64_t k) -> int64_t { return kReverseSweep2 ? n - 1 - k : nsm + ntm + k; };
   constexpr int U = kGradUnroll;
   int64_t k = threadIdx.x;
   for (; k + (U - 1) * stride < ng; k += U * stride) {
@@ -265,6 +292,15 @@ __device__ void grad_row(const T* x, T* g, int64_t V, int64_t act, const RowScal
     for (int u = 0; u < U; ++u) emit(v[u], atg(k + u * stride));
   }
   for (; k < ng; k += stride) emit(ld_hint(xv + atg(k), pol_in), atg(k));
+  if (tmv) {
+    __syncwarp();  // the tensor-memory loads are warp-collective
+    for (int j = 0; j < tmv; j += 2) {
+      uint4 v[2];
+      tmem_ld8(tb + 4u * (uint32_t)j, v);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) emit(v[i], nsm + threadIdx.x + (int64_t)kRowThreads * (j + i));
+    }
+  }
   for (int64_t q = threadIdx.x; q < nsm; q += stride) emit(kept[q], q);
 }
 
@@ -291,34 +327,52 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(cons
   __shared__ float s_M[2];
   __shared__ long long s_NS[2];
   __shared__ long long s_next;
+  __shared__ uint32_t s_tmem, s_tb_cols;
+  __shared__ double s_c[2];
+  __shared__ unsigned s_clip[3];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x < 64) {
     s_thi[threadIdx.x] = a.tab.hi[threadIdx.x];
     s_tlo[threadIdx.x] = a.tab.lo[threadIdx.x];
   }
+  // tensor memory for the second kept slice (block-uniform; released below,
+  // after the last row, on every path)
+  const int tcols = a.grad != nullptr ? a.tmem_cols : 0;
+  if (warp == 0) {
+    if (tcols) tmem_alloc(&s_tmem, (uint32_t)tcols);
+    tmem_relinquish();
+  }
+  if (tcols) tmem_fence_before_sync();
   // N = active tokens, S = live sequences of the whole batch (counted by prep,
   // or given by a shard call), read here once
   if (threadIdx.x == 0) {
     s_NS[0] = a.NS[0];
     s_NS[1] = a.NS[1];
     s_next = (long long)atomicAdd(&a.hdr->row_counter, 1ull);
+    s_tb_cols = (uint32_t)(tcols / 2);
   }
   __syncthreads();
-  const long long N = s_NS[0], S = s_NS[1];
-  // token weight: 1/max(N,1) (token mean), 1/(max(S,1) L_i) (sequence mean)
-  // or 1/C (fixed constant)
-  const double c_tok = a.reduction == GRPO_FIXED_CONSTANT ? 1.0 / (double)a.norm_c
-                                                          : 1.0 / (double)(N > 0 ? N : 1);
-  const double inv_S = 1.0 / (double)(S > 0 ? S : 1);
-  unsigned n_clip[3] = {0u, 0u, 0u};  // thread 0: this CTA's clipped rows
+  if (tcols) tmem_fence_after_sync();
+  // thread 0's per-CTA values live in shared memory: every thread holds the
+  // kernel's registers, and the sweeps need them all
+  if (threadIdx.x == 0) {
+    const long long N = s_NS[0], S = s_NS[1];
+    // token weight: 1/max(N,1) (token mean), 1/(max(S,1) L_i) (sequence
+    // mean) or 1/C (fixed constant)
+    s_c[0] = a.reduction == GRPO_FIXED_CONSTANT ? 1.0 / (double)a.norm_c
+                                                : 1.0 / (double)(N > 0 ? N : 1);
+    s_c[1] = 1.0 / (double)(S > 0 ? S : 1);
+    s_clip[0] = s_clip[1] = s_clip[2] = 0u;  // this CTA's clipped rows
+  }
   const int64_t BT = a.B * a.T;
   const bool want_grad = a.grad != nullptr;
   const bool zero_masked = want_grad && !(a.flags & GRPO_SKIP_MASKED_GRAD_ROWS);
-  const uint64_t keep = l2_evict_last(), stream = l2_evict_first();
 
   int64_t row = s_next;
   while (row < BT) {
+    // L2 policies, made per row (one instruction each) rather than held
+    const uint64_t keep = l2_evict_last(), stream = l2_evict_first();
     long long claim = 0;  // the next row, claimed while this one is processed
     if (threadIdx.x == 0) claim = (long long)atomicAdd(&a.hdr->row_counter, 1ull);
     const T* x = reinterpret_cast<const T*>(a.policy) + row * a.V;
@@ -346,15 +400,16 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(cons
         ya = Storage<T>::load1(y + act);
         o = __ldg(a.old + row);
         Ab = a.A[b];
-        c = a.reduction == GRPO_SEQUENCE_MEAN ? inv_S / (double)a.L[b] : c_tok;
+        c = a.reduction == GRPO_SEQUENCE_MEAN ? s_c[1] / (double)a.L[b] : s_c[0];
       }
 
       // sweep 1, the block combine, the fast finish
       OnlineLse sp, sr;
       sp.init();
       sr.init();
-      lse_pair<T>(x, y, a.V, sp, sr, want_grad ? keep : stream, stream,
-                  want_grad ? s_keep : nullptr);
+      const uint32_t tb = tmem_thread_base(s_tmem, s_tb_cols);
+      const int tmv = lse_pair<T>(x, y, a.V, sp, sr, want_grad ? keep : stream, stream,
+                                  want_grad ? s_keep : nullptr, tb, (int)s_tb_cols / 4);
       float Mp, Mr;
       FF Zp = {0.f, 0.f}, Zr = {0.f, 0.f};
       combine_ff(sp, sr, s_f, s_zs, Mp, Mr, Zp, Zr);
@@ -395,16 +450,15 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(cons
         a.slot_p[row] = s_rs.q;
         a.slot_k[row] = s_rs.k;
         if (a.logps_out) a.logps_out[row] = (float)s_rs.logp;
-        if (s_rs.clip == 1) ++n_clip[0];
-        else if (s_rs.clip == 2) ++n_clip[1];
-        else if (s_rs.clip == 3) ++n_clip[2];
+        if (s_rs.clip) ++s_clip[s_rs.clip - 1];
       }
       if (want_grad) {
         const RowScalars rs = s_rs;
+        const uint32_t tb = tmem_thread_base(s_tmem, s_tb_cols);
         if (rs.precise)
-          grad_row<T, true>(x, grow, a.V, act, rs, stream, stream, s_keep);
+          grad_row<T, true>(x, grow, a.V, act, rs, stream, stream, s_keep, tb, tmv);
         else
-          grad_row<T, false>(x, grow, a.V, act, rs, stream, stream, s_keep);
+          grad_row<T, false>(x, grow, a.V, act, rs, stream, stream, s_keep, tb, tmv);
       }
     }
     __syncthreads();  // everyone is done with s_rs / s_next of this row
@@ -412,7 +466,16 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(cons
     __syncthreads();
     row = s_next;
   }
-  if (threadIdx.x == 0) add_clip_counts(a.hdr, n_clip);
+  if (threadIdx.x == 0) {
+    const unsigned n_clip[3] = {s_clip[0], s_clip[1], s_clip[2]};
+    add_clip_counts(a.hdr, n_clip);
+  }
+  if (s_tb_cols) {  // every thread's tensor-memory loads were waited for
+    tmem_fence_before_sync();
+    __syncthreads();
+    tmem_fence_after_sync();
+    if (warp == 0) tmem_dealloc(s_tmem, 2u * s_tb_cols);
+  }
 }
 
 // ------------------------------------------------------------------ GSPO
@@ -472,7 +535,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) gspo_sweep1_kern
       OnlineLse sp, sr;
       sp.init();
       sr.init();
-      lse_pair<T>(x, y, a.V, sp, sr, stream, stream, nullptr);
+      lse_pair<T>(x, y, a.V, sp, sr, stream, stream, nullptr, 0u, 0);
       float Mp, Mr;
       FF Zp = {0.f, 0.f}, Zr = {0.f, 0.f};
       combine_ff(sp, sr, s_f, s_zs, Mp, Mr, Zp, Zr);
@@ -659,6 +722,38 @@ cudaError_t launch_vocab_grad(const RowArgs& a, grpo_dtype_t dt, int64_t v_begin
   }
 }
 
+// CTAs of `kernel` resident per SM, from its registers, shared memory and
+// threads, and the shared-memory carveout (percent) they need.  The occupancy
+// calculator counts a kernel that allocates tensor memory as one CTA per SM;
+// the hardware co-schedules such CTAs up to the other limits (their
+// allocations then have to fit together, which the launcher checks), so the
+// count is taken from the kernel's attributes.
+static cudaError_t resident_ctas(const void* kernel, int threads, int dyn_smem, int dev,
+                                 int* out, int* carveout) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  int regs_sm = 0, smem_sm = 0, thr_sm = 0, blk_sm = 0, smem_res = 0;
+  if ((e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) ||
+      (e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) ||
+      (e = cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev)) ||
+      (e = cudaDeviceGetAttribute(&blk_sm, cudaDevAttrMaxBlocksPerMultiprocessor, dev)) ||
+      (e = cudaDeviceGetAttribute(&smem_res, cudaDevAttrReservedSharedMemoryPerBlock, dev)))
+    return e;
+  const int warps = (threads + 31) / 32;
+  const int regs_warp = (fa.numRegs * 32 + 255) / 256 * 256;  // allocated per warp in 256s
+  int n = regs_sm / (regs_warp * warps > 0 ? regs_warp * warps : 1);
+  const int smem = (int)fa.sharedSizeBytes + dyn_smem + smem_res;
+  if (smem_sm / smem < n) n = smem_sm / smem;
+  if (thr_sm / threads < n) n = thr_sm / threads;
+  if (blk_sm < n) n = blk_sm;
+  *out = n > 0 ? n : 1;
+  const int64_t need = (int64_t)(*out) * smem;
+  int pct = (int)((need * 100 + smem_sm - 1) / smem_sm);
+  *carveout = pct < 100 ? pct : 100;
+  return cudaSuccess;
+}
+
 template <typename T>
 static cudaError_t launch_t(const RowArgs& a, const grpo_profile_t* prof, cudaStream_t s) {
   int dev = 0, sms = 0;
@@ -669,16 +764,27 @@ static cudaError_t launch_t(const RowArgs& a, const grpo_profile_t* prof, cudaSt
   e = cudaFuncSetAttribute(rows_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kPolicySmemBytes);
   if (e != cudaSuccess) return e;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rows_kernel<T>, kRowThreads,
-                                                    kPolicySmemBytes);
+  int per_sm = 0, carveout = 0;
+  e = resident_ctas((const void*)rows_kernel<T>, kRowThreads, kPolicySmemBytes, dev, &per_sm,
+                    &carveout);
   if (e != cudaSuccess) return e;
-  if (per_sm < 1) per_sm = 1;
+  // the shared-memory share of the SM's L1 that those CTAs need, and no more
+  // (the largest carveout measured about 9 % slower on the row kernel)
+  e = cudaFuncSetAttribute(rows_kernel<T>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           carveout);
+  if (e != cudaSuccess) return e;
   int64_t grid = (int64_t)sms * per_sm;
   const int64_t rows = a.B * a.T;
   if (grid > rows) grid = rows;
+  // the resident CTAs of an SM must fit its 512 tensor-memory columns
+  // together, or an allocation would wait for another CTA to exit
+  // (and only rows long enough to reach the tensor-memory slice allocate it)
+  RowArgs ka = a;
+  const bool long_rows =
+      a.V * (int64_t)sizeof(T) >= (int64_t)16 * kRowThreads * (kSmemJ + kTmemVecs + kPairUnroll);
+  ka.tmem_cols = (long_rows && per_sm * kTmemCols <= 512) ? kTmemCols : 0;
   if (prof && prof->start) cudaEventRecord((cudaEvent_t)prof->start, s);
-  rows_kernel<T><<<(unsigned)grid, kRowThreads, kPolicySmemBytes, s>>>(a);
+  rows_kernel<T><<<(unsigned)grid, kRowThreads, kPolicySmemBytes, s>>>(ka);
   e = cudaGetLastError();
   if (prof && prof->stop) cudaEventRecord((cudaEvent_t)prof->stop, s);
   return e;

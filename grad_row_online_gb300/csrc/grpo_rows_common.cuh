@@ -19,6 +19,22 @@ static constexpr bool kReverseSweep2 = true;
 // longest ago, the ones L2 would have lost.
 static constexpr int kPolicySmemBytes = 40 * 1024;
 static constexpr int kPolicySmemVecs = kPolicySmemBytes / 16;
+// Tensor memory as a second kept slice.  Nothing on this path is a
+// contraction, so the SM's 256 KB of tensor memory (128 lanes x 512 columns
+// of 32 bits) is free: each CTA allocates kTmemCols columns (all of it at
+// four CTAs per SM) and keeps there the policy vectors that follow the shared
+// memory slice, kTmemVecs per thread (64 KB per row).  A warp may touch only
+// the 32 lanes of its quadrant (warp index mod 4), so warps w and w + 4 split
+// the columns: thread t of warp w keeps its vectors in lane 32 (w mod 4) + t,
+// columns (w / 4) kTmemCols / 2 + 4 i.  The vectors of a thread are
+// t + kRowThreads j (the sweeps' order); shared memory holds j < kSmemJ,
+// tensor memory kSmemJ <= j < kSmemJ + kTmemVecs.
+static constexpr int kTmemCols = 128;
+static constexpr int kTmemVecs = kTmemCols / 2 / 4;
+static constexpr int kSmemJ = kPolicySmemVecs / kRowThreads;
+static_assert(kPolicySmemVecs % kRowThreads == 0, "the shared slice must end on a sweep step");
+static_assert(kRowThreads == 256, "two warps per tensor-memory lane quadrant");
+static_assert(kTmemVecs % 2 == 0, "tensor memory is read back two vectors at a time");
 // Refinement.  The fast logsumexp of a row has an absolute error below
 // kFastErrBound (the normaliser's relative error, below 2^-19, plus the
 // float-float finish's ~1e-7).  An element of the fp32 gradient stays within
@@ -41,6 +57,57 @@ struct RowScalars {
   int clip;         // 0, or the clip that bound: 1 upper, 2 lower, 3 dual
   double dlr;       // ref_logp - logp
 };
+
+// --------------------------------------------------------- tensor memory
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(d),
+               "r"(ncols)
+               : "memory");
+}
+// A kernel that may allocate tensor memory gets another CTA on an SM only
+// once the resident ones have given up the right to allocate (measured: a
+// CTA that never does runs alone on its SM), so every CTA of such a kernel
+// gives it up at once, whether it allocated or not.
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// this thread's lane and first column in a CTA's allocation `base` whose
+// warps w and w + 4 share a lane quadrant, `half` columns each
+__device__ __forceinline__ uint32_t tmem_thread_base(uint32_t base, uint32_t half) {
+  const uint32_t warp = threadIdx.x >> 5;
+  return base + ((warp & 3u) << 21) + (warp >> 2) * half;
+}
+// one 16-byte vector into 4 columns of this thread's lane (warp-collective)
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint4& v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// two vectors (8 columns) of this thread's lane back, waited for in the same
+// statement so no use of the registers can be scheduled before the data lands
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint4 (&v)[2]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v[0].x), "=r"(v[0].y), "=r"(v[0].z), "=r"(v[0].w), "=r"(v[1].x), "=r"(v[1].y),
+        "=r"(v[1].z), "=r"(v[1].w)
+      : "r"(taddr)
+      : "memory");
+}
 
 // vector geometry of a row: `head` scalars up to the first 16-byte boundary,
 // `nvec` 16-byte vectors, then `tail` scalars
