@@ -17,7 +17,7 @@ static constexpr bool kReverseSweep2 = true;
 // The first kPolicySmemBytes of the policy row are kept in shared memory
 // between the sweeps: with sweep 2 back to front they are the lines read
 // longest ago, the ones L2 would have lost.
-static constexpr int kPolicySmemBytes = 40 * 1024;
+static constexpr int kPolicySmemBytes = 44 * 1024;
 static constexpr int kPolicySmemVecs = kPolicySmemBytes / 16;
 // Tensor memory as a second kept slice.  Nothing on this path is a
 // contraction, so the SM's 256 KB of tensor memory (128 lanes x 512 columns

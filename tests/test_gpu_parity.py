@@ -115,18 +115,18 @@ def test_long_rows(dtype, V):
 
 
 # The row kernel keeps the head of a long policy row on chip between its two
-# sweeps: 2,560 16-byte vectors in shared memory, then 16 per thread (4,096)
-# in tensor memory, when the row has at least 7,424 vectors; the rest is read
+# sweeps: 2,816 16-byte vectors in shared memory, then 16 per thread (4,096)
+# in tensor memory, when the row has at least 7,680 vectors; the rest is read
 # again.  Actions at the edges of each slice, on rows just above and below the
 # length threshold, aligned and not.
-@pytest.mark.parametrize("dtype,V", [("bf16", 90000), ("f32", 40000), ("bf16", 59392),
-                                     ("bf16", 59391), ("f32", 29697), ("f16", 151936)])
+@pytest.mark.parametrize("dtype,V", [("bf16", 90000), ("f32", 40000), ("bf16", 61440),
+                                     ("bf16", 61439), ("f32", 30721), ("f16", 151936)])
 def test_actions_at_kept_slice_edges(dtype, V):
     w = TINY.with_(name=f"edges{V}", B=4, T=3, V=V, seed=400 + V % 89, sigma=2.0,
                    samples_per_prompt=2, mask="full")
     case = make_case(w, dtype)
     per = 4 if dtype == "f32" else 8  # elements per vector
-    e1, e2 = 2560 * per, 6656 * per
+    e1, e2 = 2816 * per, 6912 * per
     acts = np.array([0, e1 - 1, e1, e1 + 1, e2 - 1, e2, e2 + 1, V - 1, e1 + per, e2 - per,
                      (e1 + e2) // 2, V // 2], dtype=np.int64)
     case["acts"] = np.minimum(acts, V - 1).reshape(w.B, w.T)
