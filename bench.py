@@ -483,13 +483,21 @@ class LogpsCase:
     since."""
 
     COPIES = 4
-    launches_per_step = 2  # prep, logps_kernel
-    kernel = "logps_kernel"
+    CTAS_PER_SM = 8  # the logps kernel's residency (128 threads, 27 KB shared memory)
 
     def __init__(self, w, device, variant="default", skip_masked=False):
         import torch
         import grad_row_online_gb300 as g
         self.g, self.w, self.device = g, w, device
+        # one cooperative launch when every sequence's CTA is resident at once,
+        # else the separate advantage / count pass first
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        if w.B <= self.CTAS_PER_SM * sms:
+            self.launches_per_step = 1
+            self.kernel = "logps_kernel (one launch: advantages, counts, loss and gradient)"
+        else:
+            self.launches_per_step = 2
+            self.kernel = "logps_kernel (after prep_kernel)"
         self.vkw = variant_kwargs(variant, w)
         lp, old, ref = w.logps_inputs()
         host = dict(lp=lp, old=old, ref=ref, mask=w.completion_mask(), R=w.rewards())

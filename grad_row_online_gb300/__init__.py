@@ -30,7 +30,12 @@ __all__ = ["grpo_workspace_size", "grpo_group_adv", "grpo_loss_fwd_bwd", "grpo_l
 
 GRPO_ADV_EPS_ADD = 1
 GRPO_SKIP_MASKED_GRAD_ROWS = 2
+GRPO_FLAG_SEPARATE_PREP = 4  # grpo_loss_from_logps: advantages / counts as their own launch
 GRPO_FLAG_TEST_STALLED_COPY = 0x80000000  # test hook (see include/grpo.h)
+GRPO_FLAG_TEST_STALLED_BARRIER = 0x40000000  # test hook (see include/grpo.h)
+GRPO_ERR_ACTION_RANGE = 16  # device-detected status bits (grpo_read_device_status)
+GRPO_ERR_CSR = 32
+GRPO_ERR_NONFINITE_REWARD = 64
 GRPO_ERR_TIMEOUT = 128
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 _REDUCTIONS = {"token_mean": 0, "sequence_mean": 1, "fixed_constant": 2}

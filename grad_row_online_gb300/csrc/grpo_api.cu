@@ -38,7 +38,8 @@ grpo_status_t check_params(const grpo_params_t* p) {
     return GRPO_ERR_PARAM;
   if (p->reduction == GRPO_FIXED_CONSTANT && !(isfinite(p->norm_constant) && p->norm_constant > 0.f))
     return GRPO_ERR_PARAM;
-  if (p->flags & ~(GRPO_ADV_EPS_ADD | GRPO_SKIP_MASKED_GRAD_ROWS | GRPO_FLAG_TEST_STALLED_COPY))
+  if (p->flags & ~(GRPO_ADV_EPS_ADD | GRPO_SKIP_MASKED_GRAD_ROWS | GRPO_FLAG_SEPARATE_PREP |
+                   GRPO_FLAG_TEST_STALLED_COPY | GRPO_FLAG_TEST_STALLED_BARRIER))
     return GRPO_ERR_PARAM;
   if (p->kl_type != GRPO_KL_K3 && p->kl_type != GRPO_KL_K1 && p->kl_type != GRPO_KL_K2)
     return GRPO_ERR_PARAM;
@@ -329,15 +330,27 @@ extern "C" grpo_status_t grpo_loss_from_logps(const float* logps, const float* o
   const unsigned long long* NS = pl.NS ? pl.NS : &hdr->N;
   SeqTotal* totals = pl.shard ? pl.totals : (SeqTotal*)(w + lay.off_seq);
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return GRPO_ERR_CUDA;
-  PrepArgs pa{rewards, bounds, B, T, G, pl.Bg, pl.seq_begin, &hdr->N, spp, params->adv_eps,
-              (int)(params->flags & GRPO_ADV_EPS_ADD), completion_mask, 1, A, Aff, adv_out, L,
-              rng, hdr};
-  if (launch_prep(pa, s) != cudaSuccess) return GRPO_ERR_CUDA;
+  // one cooperative launch when the batch's CTAs fit the GPU at once, else
+  // the separate advantage / count pass first
+  bool fused = false;
+  if (!(params->flags & GRPO_FLAG_SEPARATE_PREP) && B > 0 && T > 0) {
+    int64_t cap = 0;
+    if (logps_fused_capacity(&cap) != cudaSuccess) return GRPO_ERR_CUDA;
+    fused = B <= cap;
+  }
+  if (!fused) {
+    PrepArgs pa{rewards, bounds, B, T, G, pl.Bg, pl.seq_begin, &hdr->N, spp, params->adv_eps,
+                (int)(params->flags & GRPO_ADV_EPS_ADD), completion_mask, 1, A, Aff, adv_out, L,
+                rng, hdr};
+    if (launch_prep(pa, s) != cudaSuccess) return GRPO_ERR_CUDA;
+  }
   LogpsArgs la{logps, old_logps, ref_logps, completion_mask, A + pl.seq_begin,
                Aff + pl.seq_begin, rng, L, totals, grad_logps, out3,
                per_seq, hdr, B, T, params->clip_eps_lo, params->clip_eps_hi, params->beta,
                params->grad_scale, params->reduction, variant_of(params),
-               params->norm_constant, params->clip_counts, NS, pl.shard ? 1 : 0, params->flags};
+               params->norm_constant, params->clip_counts, NS, pl.shard ? 1 : 0, params->flags,
+               fused ? 1 : 0, rewards, bounds, G, pl.Bg, pl.seq_begin, spp, params->adv_eps,
+               (int)(params->flags & GRPO_ADV_EPS_ADD), adv_out};
   return cuda_status(launch_logps(la, params->profile, s));
 }
 

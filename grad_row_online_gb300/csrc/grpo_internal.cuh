@@ -34,6 +34,8 @@ struct WsHeader {
   unsigned long long N;            // active tokens  (prep: integer atomics, exact)
   unsigned long long S;            // live sequences (idem)
   unsigned long long clip[3];      // clipped tokens: upper, lower, dual (integer atomics)
+  unsigned int arrive;             // one-launch logps kernel: CTAs past their counts
+  unsigned int pad;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -506,25 +508,27 @@ __device__ __forceinline__ void put_total(SeqTotal* r, FF P, FF K, int L) {
 // mean adds total / L over live sequences; then one division by N, S or C.
 // The order depends only on the index, so an unsharded call and
 // grpo_loss_finalize over the same records produce the same bits.
-// kind 1 sums in double, kind 2 in float pairs.  A record of another kind,
-// or a nonzero `bad`, gives NaN outputs.  Thread 0 writes out3.
+// kind 1 sums in double, kind 2 in float pairs; each record is read once,
+// and the kind of the whole set is known after the loads (no separate read
+// of the first record ahead of them).  Records of both kinds, of another
+// kind, or a nonzero `bad`, give NaN outputs.  Thread 0 writes out3.
 constexpr int kFinalThreads = 128;
 struct FinalSmem {
   double d[2][kFinalThreads / 32];
   FF f[2][kFinalThreads / 32];
-  int mixed;
+  unsigned kinds;  // bit 0: a kind-1 record, bit 1: kind 2, bit 2: another
 };
 static __device__ __forceinline__ void final_scalar(const SeqTotal* recs, int64_t B, unsigned long long N,
                              unsigned long long S, int reduction, float norm_c, float beta,
                              bool bad, float* out3, FinalSmem& sm) {
   constexpr int kBatch = 4;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int kind = B > 0 ? __ldcg(&recs[0].kind) : kTotalsDouble;
-  if (t == 0) sm.mixed = 0;
+  if (t == 0) sm.kinds = 0u;
   __syncthreads();
   double ud[2] = {0.0, 0.0};
   FF uf[2] = {{0.f, 0.f}, {0.f, 0.f}};
   if (t < kFinalThreads) {
+    unsigned kinds = 0u;
     for (int64_t j0 = t; j0 < B; j0 += kBatch * kFinalThreads) {
       uint4 lo[kBatch], hi[kBatch];
 #pragma unroll
@@ -532,13 +536,14 @@ static __device__ __forceinline__ void final_scalar(const SeqTotal* recs, int64_
         const int64_t j = j0 + (int64_t)k * kFinalThreads;
         const uint4* q = reinterpret_cast<const uint4*>(recs + (j < B ? j : 0));
         lo[k] = j < B ? __ldcg(q) : make_uint4(0u, 0u, 0u, 0u);
-        hi[k] = j < B ? __ldcg(q + 1) : make_uint4(0u, 0u, (unsigned)kind, 0u);
+        hi[k] = j < B ? __ldcg(q + 1) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
         const int L = (int)hi[k].x;
-        if ((int)hi[k].z != kind) sm.mixed = 1;
-        if (kind == kTotalsDouble) {
+        const int rk = (int)hi[k].z;
+        if (rk == kTotalsDouble) {
+          kinds |= 1u;
           double P = __hiloint2double((int)lo[k].y, (int)lo[k].x);
           double K = __hiloint2double((int)lo[k].w, (int)lo[k].z);
           if (reduction == GRPO_SEQUENCE_MEAN) {
@@ -548,7 +553,8 @@ static __device__ __forceinline__ void final_scalar(const SeqTotal* recs, int64_
           }
           ud[0] += P;
           ud[1] += K;
-        } else {
+        } else if (rk == kTotalsFF) {
+          kinds |= 2u;
           FF P = {__uint_as_float(lo[k].x), __uint_as_float(lo[k].y)};
           FF K = {__uint_as_float(lo[k].z), __uint_as_float(lo[k].w)};
           if (reduction == GRPO_SEQUENCE_MEAN) {
@@ -559,9 +565,18 @@ static __device__ __forceinline__ void final_scalar(const SeqTotal* recs, int64_
           }
           uf[0] = ff_add(uf[0], P);
           uf[1] = ff_add(uf[1], K);
+        } else if (j0 + (int64_t)k * kFinalThreads < B) {
+          kinds |= 4u;
         }
       }
     }
+    kinds = __reduce_or_sync(0xFFFFFFFFu, kinds);
+    if (lane == 0 && kinds) atomicOr(&sm.kinds, kinds);
+  }
+  __syncthreads();
+  const unsigned ks = sm.kinds;
+  const int kind = ks == 2u ? kTotalsFF : kTotalsDouble;  // no records: kind 1, zeros
+  if (t < kFinalThreads) {
     if (kind == kTotalsDouble) {
       ud[0] = warp_sum(ud[0]);
       ud[1] = warp_sum(ud[1]);
@@ -612,7 +627,7 @@ static __device__ __forceinline__ void final_scalar(const SeqTotal* recs, int64_
     o1 = ff_float(P);
     o2 = ff_float(K);
   }
-  if (bad || sm.mixed || (kind != kTotalsDouble && kind != kTotalsFF)) o0 = o1 = o2 = NAN;
+  if (bad || (ks & 4u) || ks == 3u) o0 = o1 = o2 = NAN;
   out3[0] = o0;
   out3[1] = o1;
   out3[2] = o2;
@@ -738,9 +753,23 @@ struct LogpsArgs {
   const unsigned long long* NS;    // [2]: N and S of the whole batch
   int shard;     // 1: write the totals only (the scalar comes from grpo_loss_finalize)
   unsigned flags;  // grpo_params_t.flags
+  // One-launch form (fused = 1, a cooperative launch): each CTA scans its own
+  // mask row and forms its own advantage from the groups below (as the
+  // separate pass would), adds its counts to hdr->N / hdr->S and waits at a
+  // grid barrier before any count is read; A, Aff, range and L are unused.
+  int fused;
+  const float* rewards;   // [Bg]
+  const int64_t* bounds;  // NULL -> uniform groups of spp
+  int64_t G, Bg, seq_begin;
+  int32_t spp;
+  float adv_eps;
+  int eps_add;
+  float* adv_out;  // nullable [B]
 };
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
+// sequences the one-launch logps kernel can take (its CTAs all resident)
+cudaError_t logps_fused_capacity(int64_t* cap);
 cudaError_t launch_rows(const RowArgs& a, grpo_dtype_t dt, const grpo_profile_t* prof,
                         cudaStream_t s);
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t s);

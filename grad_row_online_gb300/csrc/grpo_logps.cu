@@ -20,7 +20,7 @@
 // CTA measurably lengthened this kernel.
 #include <atomic>
 
-#include "grpo_internal.cuh"
+#include "grpo_groups.cuh"
 
 namespace grpo {
 
@@ -83,6 +83,7 @@ __device__ __forceinline__ TokEpi<float> tok_terms(float lp, float o, float rf, 
 // so it also forms the token weight c itself.
 struct SeqCtx {
   float A, gc;        // advantage and grad_scale * c, rounded to fp32
+  double Ad;          // the advantage
   int64_t b;          // the sequence
   int L;              // its active tokens
   unsigned long long N, S;
@@ -91,7 +92,7 @@ struct SeqCtx {
 };
 __device__ __noinline__ float w_precise(float lp, float o, float rf, const SeqCtx& x,
                                         const LogpsArgs& a) {
-  const double A = a.A[x.b];
+  const double A = x.Ad;
   const double c = a.reduction == GRPO_TOKEN_MEAN      ? 1.0 / (double)(x.N > 0 ? x.N : 1)
                    : a.reduction == GRPO_SEQUENCE_MEAN ? 1.0 / ((double)(x.S > 0 ? x.S : 1) * (double)x.L)
                                                        : 1.0 / (double)a.norm_c;
@@ -329,7 +330,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ bool staged_ok(const LogpsArgs& a) {
   const uintptr_t m = (uintptr_t)a.logps | (uintptr_t)a.old | (uintptr_t)a.ref |
                       (uintptr_t)a.grad | (uintptr_t)a.mask;
-  return a.range != nullptr && (a.T % 16 == 0) && ((m & 15) == 0);
+  return (a.fused || a.range != nullptr) && (a.T % 16 == 0) && ((m & 15) == 0);
+}
+
+// The grid barrier of the one-launch form, run by thread 0 of every CTA that
+// holds a sequence (a cooperative launch: they are all resident).  Arrival
+// is a release-add after the CTA's count atomics; the wait is an acquire-load
+// loop bounded like the copy waits (false if it ran out).
+__device__ __forceinline__ void grid_arrive(unsigned* c) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(c) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool grid_wait(const unsigned* c, unsigned expected) {
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 0; i < kWaitRounds; ++i) {
+    if (ld_acquire(c) >= expected) return true;
+    if ((i & 15u) == 15u && global_ns() - t0 > kWaitNs) return false;
+  }
+  return false;
 }
 
 __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs a) {
@@ -341,6 +368,11 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
   __shared__ bool s_last;
   __shared__ __align__(16) Stage s_st[kDepth];
   __shared__ __align__(8) uint64_t s_full[kDepth];
+  __shared__ int s_scan[3][kLogpsThreads / 32];
+  __shared__ double s_adv;
+  __shared__ int s_L;
+  __shared__ int2 s_rg;
+  __shared__ unsigned long long s_NS[2];
   const int64_t b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t pol = l2_evict_first();  // every input byte is read once
@@ -351,40 +383,134 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
   __syncthreads();
   // launched as a programmatic dependent of prep: everything above overlaps
   // prep's tail; prep's outputs (counts, advantages, ranges) are read below
+  // (in the one-launch form there is no prep and this returns at once)
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (b < a.B) {
     SeqCtx x;
     x.b = b;
-    x.N = a.NS[0];
-    x.S = a.NS[1];
-    x.L = a.L[b];
-    const float2 Ab = a.Aff[b];
-    x.A = Ab.x;
-    // grad_scale * c in fp32: c = 1/max(N,1), 1/(max(S,1) L_b) or 1/C; the
-    // products and quotient are rounded in fp32, well inside the gradient's
-    // rounding allowance
-    const float den =
-        a.reduction == GRPO_TOKEN_MEAN      ? __ull2float_rn(x.N > 0 ? x.N : 1)
-        : a.reduction == GRPO_SEQUENCE_MEAN ? __fmul_rn(__ull2float_rn(x.S > 0 ? x.S : 1), (float)x.L)
-                                            : a.norm_c;
-    x.gc = x.L > 0 ? __fdiv_rn(a.grad_scale, den) : 0.f;
-    const bool has_ref = a.ref != nullptr;
-    FastCtx f;
-    f.on = a.var.is_default();
-    f.clip_kind = x.A > 0.f ? 1 : (x.A < 0.f ? 2 : 0);
-    const float sgn = x.A > 0.f ? 1.f : -1.f;
-    f.s2 = f2(sgn);
-    f.neg_absA2 = f2(-fabsf(x.A));
-    f.negA2 = f2(-x.A);
-    f.gc2 = f2(x.gc);
-    f.neg_beta2 = f2(-a.beta);
-    f.lim = x.A > 0.f ? a.eps_hi : a.eps_lo;
-    {
-      const float gm = x.gc > 0.f ? __fdiv_rn(kWPrecise, x.gc) : INFINITY;
-      f.g2_max = __fmul_rn(gm, gm);
-    }
     const int64_t base = b * a.T;
+    const bool has_ref = a.ref != nullptr;
+    const bool staged = staged_ok(a);
+    // the staged path's chunks cover the active range widened to 16-slot
+    // boundaries, [lo, hi)
+    int64_t lo = 0, hi = 0;
+    int nchunks = 0;
+    auto geometry = [&](int2 rg) {
+      lo = rg.x & ~15;
+      hi = min((int64_t)((rg.y + 15) & ~15), a.T);
+      nchunks = staged ? (int)((hi - lo + kChunk - 1) / kChunk) : 0;
+    };
+    const uint32_t nref = has_ref ? 1u : 0u;
+    // the test hook GRPO_FLAG_TEST_STALLED_COPY: the first chunk of sequence
+    // 0 expects 16 bytes more than its copies deliver, so its wait runs out
+    const uint32_t stall = ((a.flags & GRPO_FLAG_TEST_STALLED_COPY) && b == 0) ? 16u : 0u;
+    auto issue = [&](int c) {  // one thread
+      const int64_t st = lo + (int64_t)c * kChunk;
+      const uint32_t len = (uint32_t)min((int64_t)kChunk, hi - st);
+      Stage& S = s_st[c % kDepth];
+      uint64_t* bar = &s_full[c % kDepth];
+      mbar_expect_tx(bar, len * (4u * (2u + nref) + 1u) + (c == 0 ? stall : 0u));
+      bulk_g2s(S.lp, a.logps + base + st, 4u * len, bar, pol);
+      bulk_g2s(S.od, a.old + base + st, 4u * len, bar, pol);
+      if (has_ref) bulk_g2s(S.rf, a.ref + base + st, 4u * len, bar, pol);
+      bulk_g2s(S.mk, a.mask + base + st, len, bar, pol);
+    };
+    auto first_copies = [&]() {  // one thread
+      for (int c = 0; c < nchunks && c < kDepth; ++c) issue(c);
+      s_issued = nchunks < kDepth ? nchunks : kDepth;
+    };
+    // slots outside the widened active range hold no active token
+    float4* grow = reinterpret_cast<float4*>(a.grad + base);
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto zero_outside = [&](int t, int nt) {
+      if (!staged || !a.grad) return;
+      for (int64_t v = t; v < lo / 4; v += nt) grow[v] = z4;
+      for (int64_t v = hi / 4 + t; v < a.T / 4; v += nt) grow[v] = z4;
+    };
+
+    float2 Ab;
+    if (a.fused) {
+      // Warp 0 forms this sequence's advantage from its group (fp64: the
+      // longest chain here) while warps 1-3 scan the mask row, add the
+      // counts, arrive at the grid barrier, start the copies and zero the
+      // slots outside the active range.
+      if (warp == 0) {
+        const int64_t gb = a.seq_begin + b;
+        const int64_t g = a.bounds ? warp_find_group(a.bounds, a.G, gb, lane) : gb / a.spp;
+        int64_t glo, ghi;
+        group_bounds(a.bounds, a.spp, a.G, a.Bg, g, glo, ghi);
+        const GroupStats gs = warp_group_stats(a.rewards, glo, ghi, a.adv_eps, a.eps_add, lane);
+        if (lane == 0) {
+          const double Ai = group_adv(gs, __ldg(a.rewards + gb));
+          s_adv = Ai;
+          if (a.adv_out) a.adv_out[b] = (float)Ai;
+        }
+      } else {
+        // warp 1 + p scans piece p of three (a multiple of 16 slots each);
+        // the integer counts combine exactly, each warp forming the same
+        // range from the three records
+        constexpr int kScanWarps = kLogpsThreads / 32 - 1;
+        const int p = warp - 1;
+        const int64_t q = (a.T + 16 * kScanWarps - 1) / (16 * kScanWarps) * 16;
+        const int64_t t0 = min((int64_t)p * q, a.T), t1 = min(t0 + q, a.T);
+        const SeqScan sc = warp_scan(a.mask + base + t0, t1 - t0, lane);
+        if (lane == 0) {
+          s_scan[0][p] = sc.count;
+          s_scan[1][p] = sc.count ? (int)t0 + sc.first : 0x7FFFFFFF;
+          s_scan[2][p] = sc.count ? (int)t0 + sc.last : -1;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kScanWarps) : "memory");
+        int L = 0, first = 0x7FFFFFFF, last = -1;
+#pragma unroll
+        for (int k = 0; k < kScanWarps; ++k) {
+          L += s_scan[0][k];
+          first = min(first, s_scan[1][k]);
+          last = max(last, s_scan[2][k]);
+        }
+        const int2 rg = L > 0 ? make_int2(first, last + 1) : make_int2(0, 0);
+        geometry(rg);
+        if (threadIdx.x == 32) {
+          s_L = L;
+          s_rg = rg;
+          if (!a.shard) {  // a shard call is given the batch's counts
+            if (L) atomicAdd(&a.hdr->N, (unsigned long long)L);
+            if (L) atomicAdd(&a.hdr->S, 1ull);
+            grid_arrive(&a.hdr->arrive);
+          }
+          if (staged) first_copies();
+        }
+        zero_outside((int)threadIdx.x - 32, kLogpsThreads - 32);
+        if (warp == kScanWarps) {
+          // every group is checked once over the grid, as the separate pass
+          // does: its boundaries, and its rewards for non-finite values
+          for (int64_t g = blockIdx.x; g < a.G; g += gridDim.x) {
+            int64_t glo, ghi;
+            const bool ok = group_bounds(a.bounds, a.spp, a.G, a.Bg, g, glo, ghi);
+            int nf = 0;
+            for (int64_t i = glo + lane; i < ghi; i += 32) nf += !isfinite(__ldg(a.rewards + i));
+            nf = warp_sum(nf);
+            if (lane == 0 && !ok) atomicOr(&a.hdr->status, (unsigned)GRPO_ERR_CSR);
+            if (lane == 0 && nf) atomicOr(&a.hdr->status, (unsigned)GRPO_ERR_NONFINITE_REWARD);
+          }
+        }
+      }
+      __syncthreads();
+      x.L = s_L;
+      if (warp == 0) geometry(s_rg);
+      x.Ad = s_adv;
+      const float hi32 = (float)x.Ad;
+      Ab = make_float2(hi32, (float)(x.Ad - (double)hi32));
+    } else {
+      x.L = a.L[b];
+      geometry(a.range ? a.range[b] : make_int2(0, (int)a.T));
+      if (staged && threadIdx.x == 0) first_copies();
+      zero_outside((int)threadIdx.x, kLogpsThreads);
+      x.Ad = a.A[b];
+      Ab = a.Aff[b];
+    }
+    x.A = Ab.x;
+
     x.em_seq = 0.f;
     x.em_seq_d = 0.0;
     if (a.var.seq_ratio) {
@@ -406,37 +532,49 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
       x.em_seq_d = s_em[0];
       x.em_seq = (float)x.em_seq_d;
     }
+
+    // the batch counts: complete once every CTA has passed the barrier (the
+    // test hook GRPO_FLAG_TEST_STALLED_BARRIER makes CTA 0 wait for one CTA
+    // more than there are, so its wait runs out)
+    if (threadIdx.x == 0) {
+      if (a.fused && !a.shard) {
+        const unsigned extra = ((a.flags & GRPO_FLAG_TEST_STALLED_BARRIER) && b == 0) ? 1u : 0u;
+        if (!grid_wait(&a.hdr->arrive, (unsigned)a.B + extra))
+          atomicOr(&a.hdr->status, (unsigned)GRPO_ERR_TIMEOUT);
+        s_NS[0] = ld_acquire(a.NS);
+        s_NS[1] = ld_acquire(a.NS + 1);
+      } else {
+        s_NS[0] = a.NS[0];
+        s_NS[1] = a.NS[1];
+      }
+    }
+    __syncthreads();
+    x.N = s_NS[0];
+    x.S = s_NS[1];
+    // grad_scale * c in fp32: c = 1/max(N,1), 1/(max(S,1) L_b) or 1/C; the
+    // products and quotient are rounded in fp32, well inside the gradient's
+    // rounding allowance
+    const float den =
+        a.reduction == GRPO_TOKEN_MEAN      ? __ull2float_rn(x.N > 0 ? x.N : 1)
+        : a.reduction == GRPO_SEQUENCE_MEAN ? __fmul_rn(__ull2float_rn(x.S > 0 ? x.S : 1), (float)x.L)
+                                            : a.norm_c;
+    x.gc = x.L > 0 ? __fdiv_rn(a.grad_scale, den) : 0.f;
+    FastCtx f;
+    f.on = a.var.is_default();
+    f.clip_kind = x.A > 0.f ? 1 : (x.A < 0.f ? 2 : 0);
+    const float sgn = x.A > 0.f ? 1.f : -1.f;
+    f.s2 = f2(sgn);
+    f.neg_absA2 = f2(-fabsf(x.A));
+    f.negA2 = f2(-x.A);
+    f.gc2 = f2(x.gc);
+    f.neg_beta2 = f2(-a.beta);
+    f.lim = x.A > 0.f ? a.eps_hi : a.eps_lo;
+    {
+      const float gm = x.gc > 0.f ? __fdiv_rn(kWPrecise, x.gc) : INFINITY;
+      f.g2_max = __fmul_rn(gm, gm);
+    }
     Acc acc;
-    if (staged_ok(a)) {
-      const int2 rg = a.range[b];
-      const int64_t lo = rg.x & ~15, hi = min((int64_t)((rg.y + 15) & ~15), a.T);
-      const int nchunks = (int)((hi - lo + kChunk - 1) / kChunk);
-      const uint32_t nref = has_ref ? 1u : 0u;
-      // the test hook GRPO_FLAG_TEST_STALLED_COPY: the first chunk of sequence
-      // 0 expects 16 bytes more than its copies deliver, so its wait runs out
-      const uint32_t stall = ((a.flags & GRPO_FLAG_TEST_STALLED_COPY) && b == 0) ? 16u : 0u;
-      auto issue = [&](int c) {  // thread 0 only
-        const int64_t st = lo + (int64_t)c * kChunk;
-        const uint32_t len = (uint32_t)min((int64_t)kChunk, hi - st);
-        Stage& S = s_st[c % kDepth];
-        uint64_t* bar = &s_full[c % kDepth];
-        mbar_expect_tx(bar, len * (4u * (2u + nref) + 1u) + (c == 0 ? stall : 0u));
-        bulk_g2s(S.lp, a.logps + base + st, 4u * len, bar, pol);
-        bulk_g2s(S.od, a.old + base + st, 4u * len, bar, pol);
-        if (has_ref) bulk_g2s(S.rf, a.ref + base + st, 4u * len, bar, pol);
-        bulk_g2s(S.mk, a.mask + base + st, len, bar, pol);
-      };
-      if (threadIdx.x == 0) {
-        for (int c = 0; c < nchunks && c < kDepth; ++c) issue(c);
-        s_issued = nchunks < kDepth ? nchunks : kDepth;
-      }
-      // slots outside the widened active range hold no active token
-      float4* grow = reinterpret_cast<float4*>(a.grad + base);
-      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (a.grad) {
-        for (int64_t v = threadIdx.x; v < lo / 4; v += kLogpsThreads) grow[v] = z4;
-        for (int64_t v = hi / 4 + threadIdx.x; v < a.T / 4; v += kLogpsThreads) grow[v] = z4;
-      }
+    if (staged) {
       // A wait that runs out (never expected outside the test hook) is
       // recorded; the CTA then issues no further copy, still waits for the
       // copies already issued (bounded), and skips the arithmetic -- the loss
@@ -574,46 +712,76 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
 
   // the scalar over the B sequence records, in index order
   const bool bad = ((volatile unsigned*)&a.hdr->status)[0] != 0u;
-  final_scalar(a.seq, a.B, a.B > 0 ? a.NS[0] : 0ull, a.B > 0 ? a.NS[1] : 0ull, a.reduction,
+  final_scalar(a.seq, a.B, a.B > 0 ? s_NS[0] : 0ull, a.B > 0 ? s_NS[1] : 0ull, a.reduction,
                a.norm_c, a.beta, bad, a.out3, s_fin);
 }
 
-cudaError_t launch_logps(const LogpsArgs& a, const grpo_profile_t* prof, cudaStream_t s) {
-  // eight 27 KB CTAs per SM need the largest shared-memory carveout; the
-  // attribute is set once per device (setting it again costs host time)
+// eight 27 KB CTAs per SM need the largest shared-memory carveout; the
+// attribute, and the resident-CTA count it gives, are taken once per device
+// (setting or querying them again costs host time)
+static constexpr int kMaxDevices = 64;
+static std::atomic<long long> g_capacity[kMaxDevices];  // 0: not yet known
+
+static cudaError_t prepare_device(int dev, int64_t* cap) {
+  const int d = dev & (kMaxDevices - 1);
+  long long c = g_capacity[d].load(std::memory_order_acquire);
+  if (c == 0) {
+    cudaError_t e = cudaFuncSetAttribute(logps_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0, sms = 0, coop = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, logps_kernel, kLogpsThreads,
+                                                           0)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess)
+      return e;
+    c = coop ? (long long)per_sm * sms : 0;
+    g_capacity[d].store(c > 0 ? c : -1, std::memory_order_release);  // -1: none
+  }
+  *cap = c > 0 ? c : 0;
+  return cudaSuccess;
+}
+
+cudaError_t logps_fused_capacity(int64_t* cap) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  static std::atomic<unsigned long long> carveout_set{0};
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(carveout_set.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(logps_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    carveout_set.fetch_or(bit, std::memory_order_acq_rel);
-  }
+  return prepare_device(dev, cap);
+}
+
+cudaError_t launch_logps(const LogpsArgs& a, const grpo_profile_t* prof, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int64_t cap = 0;
+  if ((e = prepare_device(dev, &cap)) != cudaSuccess) return e;
   const int64_t grid = a.B > 0 ? a.B : 1;
-  if (prof && (prof->start || prof->stop)) {  // timed alone: an ordinary launch between events
-    if (prof->start) cudaEventRecord((cudaEvent_t)prof->start, s);
-    logps_kernel<<<(unsigned)grid, kLogpsThreads, 0, s>>>(a);
-    e = cudaGetLastError();
-    if (prof->stop) cudaEventRecord((cudaEvent_t)prof->stop, s);
-    return e;
-  }
-  // programmatic dependent launch: the CTAs may start while prep finishes
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kLogpsThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 0;
+  if (a.fused) {
+    // every CTA resident at once: the grid barrier's precondition
+    if (grid > cap) return cudaErrorCooperativeLaunchTooLarge;
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.numAttrs = 1;
+  } else if (!(prof && (prof->start || prof->stop))) {
+    // programmatic dependent launch: the CTAs may start while prep finishes
+    // (a launch timed alone between events is an ordinary one)
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 1;
+  }
+  if (prof && prof->start) cudaEventRecord((cudaEvent_t)prof->start, s);
   e = cudaLaunchKernelEx(&cfg, logps_kernel, a);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (prof && prof->stop) cudaEventRecord((cudaEvent_t)prof->stop, s);
+  return e;
 }
 
 }  // namespace grpo

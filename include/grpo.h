@@ -72,7 +72,8 @@ typedef enum {
   GRPO_ERR_ACTION_RANGE = 16,    /* active token with action id outside [0, V) */
   GRPO_ERR_CSR = 32,             /* boundaries not 0 = g_0 < g_1 < ... < g_G = B */
   GRPO_ERR_NONFINITE_REWARD = 64, /* a reward is NaN or infinite */
-  GRPO_ERR_TIMEOUT = 128          /* a bounded wait on an asynchronous copy ran out */
+  GRPO_ERR_TIMEOUT = 128          /* a bounded wait (an asynchronous copy, the grid
+                                     barrier of the one-launch logps kernel) ran out */
 } grpo_status_t;
 
 typedef enum { GRPO_F32 = 0, GRPO_BF16 = 1, GRPO_F16 = 2 } grpo_dtype_t;
@@ -106,6 +107,14 @@ typedef enum {
 #define GRPO_ADV_EPS_ADD 1u          /* divide by std + adv_eps instead of max(std, adv_eps) */
 #define GRPO_SKIP_MASKED_GRAD_ROWS 2u /* leave gradient rows of masked tokens untouched
                                          (caller pre-zeroed them) instead of writing 0 */
+/* grpo_loss_from_logps: run the advantage / active-count pass as its own
+ * launch before the per-sequence kernel.  By default, when every sequence's
+ * CTA fits on the GPU at once (B up to 8 per SM: 1,216 on GB300), the pass is
+ * folded into that kernel, launched cooperatively: each CTA scans its own
+ * mask row and forms its own advantage, and the CTAs meet at a grid barrier
+ * (bounded like every wait: GRPO_ERR_TIMEOUT) before the counts N and S are
+ * read.  Both forms give the same bits.  Ignored by the other entry points. */
+#define GRPO_FLAG_SEPARATE_PREP 4u
 /* Test hook, for the failure-detection tests only: in grpo_loss_from_logps'
  * staged path (T % 16 == 0, 16-byte aligned arrays) the first asynchronous
  * copy of sequence 0 is made to under-deliver, so its bounded wait runs out
@@ -113,6 +122,12 @@ typedef enum {
  * NaN, the sequence's gradient is not written, and the context stays usable.
  * Ignored by the other entry points. */
 #define GRPO_FLAG_TEST_STALLED_COPY 0x80000000u
+/* Test hook, for the failure-detection tests only: in grpo_loss_from_logps'
+ * one-launch form, the CTA of sequence 0 waits at the grid barrier for one
+ * CTA more than there are, so its bounded wait runs out (after 0.2 s): the
+ * call sets GRPO_ERR_TIMEOUT and the loss outputs are NaN; the context stays
+ * usable.  Ignored elsewhere (and with GRPO_FLAG_SEPARATE_PREP). */
+#define GRPO_FLAG_TEST_STALLED_BARRIER 0x40000000u
 
 /* Group specification ("Group specification": provide exactly one of
  * samples_per_prompt > 0, or CSR group_boundaries of length num_groups + 1
@@ -173,7 +188,7 @@ typedef struct {
   float adv_eps;      /* > 0, 1e-6 on the pages */
   float grad_scale;   /* finite; multiplies every gradient (1 = dL/dlogits) */
   int32_t reduction;  /* grpo_reduction_t */
-  uint32_t flags;     /* GRPO_ADV_EPS_ADD | GRPO_SKIP_MASKED_GRAD_ROWS */
+  uint32_t flags;     /* GRPO_ADV_EPS_ADD | GRPO_SKIP_MASKED_GRAD_ROWS | GRPO_FLAG_SEPARATE_PREP */
   int32_t kl_type;    /* grpo_kl_t */
   int32_t surrogate;  /* grpo_surrogate_t */
   float dual_clip_c;  /* 0: off.  > 1: dual clip ("ratio_clip_c", a lower bound

@@ -1,0 +1,152 @@
+"""The logps path in one launch: when every sequence's CTA fits on the GPU at
+once, grpo_loss_from_logps runs a single cooperative kernel whose CTAs scan
+their own mask rows, form their own advantages and meet at a grid barrier
+before reading the batch counts N and S.  Against the separate advantage /
+count pass (GRPO_FLAG_SEPARATE_PREP) it must give the same bits for every
+output -- loss outputs, gradient, per-sequence totals, advantages, clip
+counts -- on the staged, register and scalar row paths, uniform and CSR
+groups, every reduction and the loss variants.  Batches too large for one
+wave take the separate pass by themselves; device-detected errors are still
+reported; a barrier wait that runs out is reported and leaves the context
+usable."""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import grad_row_online_gb300 as g
+import oracle
+import synth
+from workload_inputs import assert_scalar
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import os
+    import __graft_entry__
+    if not os.path.exists(g.library_path()):
+        __graft_entry__.build()
+
+
+BASE = synth.WORKLOADS["logps"].with_(name="onelaunch", B=48, T=64, len_range=(0, 64),
+                                      samples_per_prompt=8, old_sigma=0.3, ref_logp_sigma=0.1)
+CSR = BASE.with_(name="onelaunch_csr", samples_per_prompt=0, csr_size_range=(1, 9),
+                 reward="normal")
+
+
+def _tensors(w):
+    lp, old, ref = w.logps_inputs()
+    host = dict(lp=lp, old=old, ref=ref, mask=w.completion_mask(), R=w.rewards())
+    t = {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in host.items()}
+    t["bounds"] = (torch.from_numpy(w.group_boundaries()).cuda()
+                   if not w.samples_per_prompt else None)
+    return t
+
+
+def _call(w, t, flags=0, **kw):
+    args = dict(clip_eps=w.eps_lo, clip_eps_hi=w.eps_hi, beta=w.beta, want_per_seq=True,
+                want_adv=True, want_clip_counts=True, extra_flags=flags)
+    if w.samples_per_prompt:
+        args["samples_per_prompt"] = w.samples_per_prompt
+    else:
+        args["group_boundaries"] = t["bounds"]
+    args.update(kw)
+    res = g.grpo_loss_from_logps(t["lp"], t["old"], t["ref"], t["mask"], t["R"], **args)
+    torch.cuda.synchronize()
+    return res
+
+
+OUTS = ("out3", "grad", "per_seq", "adv", "clip_counts")
+OPTIONS = {
+    "token-mean": dict(),
+    "sequence-mean": dict(reduction="sequence_mean"),
+    "fixed-k2-dual": dict(reduction="fixed_constant", norm_constant=50.0, kl="k2",
+                          dual_clip_c=1.4),
+    "cispo-k1": dict(surrogate="cispo", kl="k1"),
+    "gspo": dict(reduction="sequence_mean", ratio_level="sequence"),
+}
+
+
+@pytest.mark.parametrize("opt", list(OPTIONS))
+@pytest.mark.parametrize("T", [64, 100, 37])  # staged, register and scalar row paths
+@pytest.mark.parametrize("w", [BASE, CSR], ids=["uniform", "csr"])
+def test_one_launch_equals_the_separate_pass(w, T, opt):
+    w = w.with_(T=T, len_range=(0, T))
+    t = _tensors(w)
+    one = _call(w, t, **OPTIONS[opt])
+    two = _call(w, t, flags=g.GRPO_FLAG_SEPARATE_PREP, **OPTIONS[opt])
+    assert g.grpo_read_device_status(one["workspace"]) == 0
+    for k in OUTS:
+        assert torch.equal(one[k], two[k]), k
+
+
+def test_one_launch_parity_with_the_oracle():
+    w = CSR.with_(reduction=1)
+    t = _tensors(w)
+    res = _call(w, t, reduction="sequence_mean")
+    lp, old, ref = w.logps_inputs()
+    A = oracle.group_advantages(w.rewards(), w.group_boundaries())
+    assert np.array_equal(res["adv"].cpu().numpy(), A.astype(np.float32))
+    exp = oracle.loss_from_logps(lp, ref, old, w.completion_mask(), A, w.eps_lo, w.eps_hi, w.beta,
+                                 reduction=1)
+    out = res["out3"].cpu().numpy().astype(np.float64)
+    for i, k in enumerate(("loss", "policy_loss", "kl")):
+        assert_scalar(out[i], exp[k], k)
+
+
+def test_a_batch_larger_than_one_wave_takes_the_separate_pass():
+    # 1,304 sequences: more CTAs than GB300 holds at once (8 per SM x 152)
+    w = BASE.with_(name="onelaunch_big", B=1304, T=32, len_range=(0, 32))
+    t = _tensors(w)
+    one = _call(w, t)
+    two = _call(w, t, flags=g.GRPO_FLAG_SEPARATE_PREP)
+    for k in OUTS:
+        assert torch.equal(one[k], two[k]), k
+    lp, old, ref = w.logps_inputs()
+    A = oracle.group_advantages(w.rewards(), w.group_boundaries())
+    exp = oracle.loss_from_logps(lp, ref, old, w.completion_mask(), A, w.eps_lo, w.eps_hi, w.beta)
+    out = one["out3"].cpu().numpy().astype(np.float64)
+    for i, k in enumerate(("loss", "policy_loss", "kl")):
+        assert_scalar(out[i], exp[k], k)
+
+
+def test_device_errors_in_one_launch():
+    w = BASE
+    t = _tensors(w)
+    R = t["R"].clone()
+    R[13] = float("nan")
+    res = _call(w, dict(t, R=R))
+    assert g.grpo_read_device_status(res["workspace"]) == g.GRPO_ERR_NONFINITE_REWARD
+    assert torch.isnan(res["out3"]).all()
+    # a CSR whose groups do not end at B (checked over the grid, group by group)
+    wc = CSR
+    tc = _tensors(wc)
+    bad = tc["bounds"].clone()
+    bad[-1] = wc.B - 1
+    res = _call(wc, dict(tc, bounds=bad))
+    assert g.grpo_read_device_status(res["workspace"]) == g.GRPO_ERR_CSR
+    assert torch.isnan(res["out3"]).all()
+    res = _call(wc, tc, workspace=res["workspace"])
+    assert g.grpo_read_device_status(res["workspace"]) == 0
+
+
+def test_a_stalled_barrier_times_out_and_the_context_survives():
+    w = BASE
+    t = _tensors(w)
+    t0 = time.time()
+    bad = _call(w, t, flags=g.GRPO_FLAG_TEST_STALLED_BARRIER)
+    status = g.grpo_read_device_status(bad["workspace"])
+    assert status == g.GRPO_ERR_TIMEOUT
+    assert torch.isnan(bad["out3"]).all()
+    assert time.time() - t0 < 30.0
+    good = _call(w, t, workspace=bad["workspace"])
+    assert g.grpo_read_device_status(good["workspace"]) == 0
+    ref = _call(w, t, flags=g.GRPO_FLAG_SEPARATE_PREP)
+    for k in OUTS:
+        assert torch.equal(good[k], ref[k]), k
