@@ -266,7 +266,8 @@ __device__ __forceinline__ void process_vec(uint32_t mw, const float4& l, const 
 // in chunks of kChunk tokens (logps, old, ref and the mask bytes: four
 // cp.async.bulk copies completing on one mbarrier); kDepth chunks are in
 // flight while one is evaluated.
-static constexpr int kChunk = 4 * kLogpsThreads;  // one float4 per thread
+static constexpr int kChunkVecs = 1;  // float4 vectors per thread per chunk
+static constexpr int kChunk = 4 * kLogpsThreads * kChunkVecs;
 static constexpr int kDepth = 4;
 static constexpr unsigned long long kWaitNs = 200000000ull;  // 0.2 s per bounded wait
 static constexpr uint32_t kWaitRounds = 1u << 26;  // and never more try_wait rounds than this
@@ -364,7 +365,6 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
   __shared__ unsigned s_nc[3][kLogpsThreads / 32];
   __shared__ FinalSmem s_fin;
   __shared__ double s_em[1];
-  __shared__ int s_issued;
   __shared__ bool s_last;
   __shared__ __align__(16) Stage s_st[kDepth];
   __shared__ __align__(8) uint64_t s_full[kDepth];
@@ -418,7 +418,6 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
     };
     auto first_copies = [&]() {  // one thread
       for (int c = 0; c < nchunks && c < kDepth; ++c) issue(c);
-      s_issued = nchunks < kDepth ? nchunks : kDepth;
     };
     // slots outside the widened active range hold no active token
     float4* grow = reinterpret_cast<float4*>(a.grad + base);
@@ -579,28 +578,35 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
       // recorded; the CTA then issues no further copy, still waits for the
       // copies already issued (bounded), and skips the arithmetic -- the loss
       // outputs become NaN through the status word.
+      // One CTA-wide barrier per chunk: past it, every thread is done with
+      // chunk c - 1, whose slot is then refilled with chunk c - 1 + kDepth.
+      // Every thread counts the chunks issued so far (the decisions are the
+      // same everywhere: `stalled` is taken CTA-wide).
       bool stalled = false;
-      __syncthreads();  // s_issued
-      for (int c = 0; c < nchunks && c < s_issued; ++c) {
+      int issued = nchunks < kDepth ? nchunks : kDepth;
+      for (int c = 0; c < issued; ++c) {
         const int slot = c % kDepth;
         const int64_t st = lo + (int64_t)c * kChunk;
         const int len = (int)min((int64_t)kChunk, hi - st);
         const bool ready = mbar_wait(&s_full[slot], (uint32_t)(c / kDepth) & 1u);
         stalled = __syncthreads_or(!ready) || stalled;  // one decision for the CTA
-        const int v = threadIdx.x;
-        if (!stalled && 4 * v < len) {
+        if (!stalled && c >= 1 && c - 1 + kDepth < nchunks) {
+          if (threadIdx.x == 0) issue(c - 1 + kDepth);
+          issued = c + kDepth;
+        }
+        if (!stalled) {
           const Stage& S = s_st[slot];
-          float w[4];
-          process_vec(S.mk[v], S.lp[v], S.od[v], has_ref ? S.rf[v] : z4, has_ref, f, x, a, acc,
-                      w);
-          if (a.grad) grow[st / 4 + v] = make_float4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+          for (int u = 0; u < kChunkVecs; ++u) {
+            const int v = threadIdx.x + u * kLogpsThreads;
+            if (4 * v < len) {
+              float w[4];
+              process_vec(S.mk[v], S.lp[v], S.od[v], has_ref ? S.rf[v] : z4, has_ref, f, x, a,
+                          acc, w);
+              if (a.grad) grow[st / 4 + v] = make_float4(w[0], w[1], w[2], w[3]);
+            }
+          }
         }
-        __syncthreads();  // the slot is free again
-        if (threadIdx.x == 0 && !stalled && c + kDepth < nchunks) {
-          issue(c + kDepth);
-          s_issued = c + kDepth + 1;
-        }
-        __syncthreads();  // s_issued
       }
       if (stalled && threadIdx.x == 0) atomicOr(&a.hdr->status, (unsigned)GRPO_ERR_TIMEOUT);
     } else if (vec_ok(a)) {
