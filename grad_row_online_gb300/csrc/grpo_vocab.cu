@@ -49,18 +49,8 @@ __device__ __forceinline__ void load_run(const T* x, int64_t j, int64_t n, bool 
 // 2^(x log2e - mL)); the lanes' sums rescaled to the chunk's ML = fl(M log2e)
 // and added as float pairs; finally Z = Z_2 2^(ML - M log2e), the residual
 // exponent taken exactly with an FMA.
-template <typename T>
-__device__ void chunk_partial_fast(const T* x, int64_t n, float& M, FF& Z) {
-  constexpr int R = Storage<T>::kVec;
-  const bool vec = ((uintptr_t)x & 15) == 0;
-  const int64_t nruns = (n + R - 1) / R;
-  OnlineLse st;
-  st.init();
-  for (int64_t j = threadIdx.x & 31; j < nruns; j += 32) {
-    float f[R];
-    load_run<T>(x, j, n, vec, f);
-    st.update<R>(f);
-  }
+// The lanes' online normalisers of one chunk reduced to the chunk's (M, Z).
+__device__ __forceinline__ void finish_partial(const OnlineLse& st, float& M, FF& Z) {
   const float m = warp_max(st.m);
   if (m == -INFINITY) {  // an empty chunk contributes nothing
     M = -INFINITY;
@@ -77,15 +67,55 @@ __device__ void chunk_partial_fast(const T* x, int64_t n, float& M, FF& Z) {
   M = m;
 }
 
+// The MUFU path over the same chunk of the policy (x) and reference (y)
+// rows at once, kRunsAhead runs of each in flight per lane: the loads run
+// ahead of the updates, and each row's normaliser still takes its runs in
+// index order, so (M, Z) are the bits one row alone would give.
+static constexpr int kRunsAhead = 4;
+template <typename T>
+__device__ void chunk_pair_fast(const T* x, const T* y, int64_t n, float& Mx, FF& Zx, float& My,
+                                FF& Zy) {
+  constexpr int R = Storage<T>::kVec;
+  const int lane = threadIdx.x & 31;
+  const bool vec = (((uintptr_t)x | (uintptr_t)y) & 15) == 0;
+  const int64_t nruns = (n + R - 1) / R;
+  const int64_t nfull = vec ? n / R : 0;  // runs read as whole vectors
+  OnlineLse sx, sy;
+  sx.init();
+  sy.init();
+  int64_t j = lane;
+  for (; j + 32 * (kRunsAhead - 1) < nfull; j += 32 * kRunsAhead) {
+    uint4 vx[kRunsAhead], vy[kRunsAhead];
+#pragma unroll
+    for (int u = 0; u < kRunsAhead; ++u) {
+      vx[u] = __ldg(reinterpret_cast<const uint4*>(x) + j + 32 * u);
+      vy[u] = __ldg(reinterpret_cast<const uint4*>(y) + j + 32 * u);
+    }
+#pragma unroll
+    for (int u = 0; u < kRunsAhead; ++u) {
+      float f[R];
+      Storage<T>::unpack(vx[u], f);
+      sx.update<R>(f);
+      Storage<T>::unpack(vy[u], f);
+      sy.update<R>(f);
+    }
+  }
+  for (; j < nruns; j += 32) {
+    float f[R];
+    load_run<T>(x, j, n, vec, f);
+    sx.update<R>(f);
+    load_run<T>(y, j, n, vec, f);
+    sy.update<R>(f);
+  }
+  finish_partial(sx, Mx, Zx);
+  finish_partial(sy, My, Zy);
+}
+
 // Float-float path (fp32 logits): the chunk's max first, then
 // sum exp(x - M) with the float-float exponential and float-pair sums.
-template <typename T, bool kPrecise>
+template <typename T>
 __device__ void chunk_partial(const T* x, int64_t n, const float* thi, const float* tlo,
                               const ExpTable& tab, float& M, FF& Z) {
-  if (!kPrecise) {
-    chunk_partial_fast<T>(x, n, M, Z);
-    return;
-  }
   constexpr int R = Storage<T>::kVec;
   const int lane = threadIdx.x & 31;
   const bool vec = ((uintptr_t)x & 15) == 0;
@@ -139,13 +169,19 @@ __global__ void __launch_bounds__(32 * kVocabWarps) vocab_partials_kernel(const 
     if (!a.mask[row]) continue;
     const int64_t e0 = c * kVChunk;
     const int64_t n = (a.Vk - e0) < kVChunk ? (a.Vk - e0) : kVChunk;
-    for (int which = 0; which < 2; ++which) {
-      const T* x = reinterpret_cast<const T*>(which ? a.ref : a.policy) + row * a.Vk + e0;
-      float M;
-      FF Z;
-      chunk_partial<T, kPrecise>(x, n, s_thi, s_tlo, a.tab, M, Z);
-      if (lane == 0)
-        (which ? a.part_r : a.part_p)[c * rows + row] = make_float4(M, Z.hi, Z.lo, 0.f);
+    const T* xp = reinterpret_cast<const T*>(a.policy) + row * a.Vk + e0;
+    const T* xr = reinterpret_cast<const T*>(a.ref) + row * a.Vk + e0;
+    float Mp, Mr;
+    FF Zp, Zr;
+    if (kPrecise) {
+      chunk_partial<T>(xp, n, s_thi, s_tlo, a.tab, Mp, Zp);
+      chunk_partial<T>(xr, n, s_thi, s_tlo, a.tab, Mr, Zr);
+    } else {
+      chunk_pair_fast<T>(xp, xr, n, Mp, Zp, Mr, Zr);
+    }
+    if (lane == 0) {
+      a.part_p[c * rows + row] = make_float4(Mp, Zp.hi, Zp.lo, 0.f);
+      a.part_r[c * rows + row] = make_float4(Mr, Zr.hi, Zr.lo, 0.f);
     }
     if (c == 0 && lane == 0) {  // the action logit, where this slice holds it
       const int64_t act = a.actions[row] - a.v_begin;
@@ -231,8 +267,14 @@ static cudaError_t launch_partials_t(const VocabArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
+  // one wave of resident CTAs, each warp striding over the items
+  const void* kern = a.precise ? (const void*)vocab_partials_kernel<T, true>
+                               : (const void*)vocab_partials_kernel<T, false>;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * kVocabWarps, 0);
+  if (e != cudaSuccess) return e;
   const int64_t items = a.rows * a.nck;
-  int64_t grid = (int64_t)sms * 8;
+  int64_t grid = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
   const int64_t need = (items + kVocabWarps - 1) / kVocabWarps;
   if (grid > need) grid = need;
   if (grid < 1) return cudaSuccess;
