@@ -83,10 +83,12 @@ def _sharded_logits(dev, w, sizes, opts):
                 totals=all_totals, clips=torch.stack(clips).sum(0), counts=global_counts)
 
 
+# V = 70001: rows long enough for the row kernel's tensor-memory slice
+@pytest.mark.parametrize("V", [3001, 70001])
 @pytest.mark.parametrize("opt", list(OPTIONS))
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_logits_shards_are_bitwise_identical(dtype, opt):
-    w = BATCH
+def test_logits_shards_are_bitwise_identical(dtype, opt, V):
+    w = BATCH.with_(V=V)
     case = make_case(w, dtype)
     dev = to_device(case)
     opts = OPTIONS[opt]
