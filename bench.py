@@ -189,6 +189,26 @@ def oracle_threads() -> int:
     return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform)."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
 # ---------------------------------------------------------------------------
 def dist_setup():
     import torch
@@ -270,7 +290,7 @@ def cpu_baseline(w: synth.Workload, budget_s: float = 12.0) -> dict:
         if el > budget_s or passes >= 10000:
             break
     return {"value": n / el, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
-            "sample": f"{what}; {passes} passes, {el:.1f} s"}
+            "cpu_model": cpu_model(), "sample": f"{what}; {passes} passes, {el:.1f} s"}
 
 
 def run_reference(args, w, ws, rank):
@@ -292,7 +312,7 @@ def run_reference(args, w, ws, rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(w),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_threads(),
-                             "kind": "oracle", "sample": what},
+                             "kind": "oracle", "cpu_model": cpu_model(), "sample": what},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -350,6 +370,18 @@ def workload_config(w: synth.Workload, variant: str = "default",
 # ---------------------------------------------------------------------------
 # the two boundaries under test
 # ---------------------------------------------------------------------------
+def logits_side_bytes(w, active: int, s_in: int, skip_masked: bool) -> dict:
+    """The roofline's secondary figures for a logits workload: the strict
+    lower bound (the policy read once, as if each row stayed on chip:
+    3 V s_in per active token) and the side streams outside the algorithmic
+    bytes (action id, behaviour log-prob and mask per token; the zero fill of
+    the masked rows' gradient unless they are skipped)."""
+    masked = w.B * w.T - active
+    return {"strict_bytes_per_launch": 3.0 * w.V * s_in * active,
+            "side_bytes_per_launch": 13.0 * active + (0.0 if skip_masked else
+                                                      float(w.V * s_in * masked))}
+
+
 class LogitsCase:
     """grpo_loss_fwd_bwd on a logits workload (inputs larger than L2)."""
 
@@ -375,6 +407,8 @@ class LogitsCase:
         s_in = 2 if w.dtype == "bf16" else 4
         # policy read twice, ref once, grad written once, per active row
         self.alg_bytes = 4.0 * w.V * s_in * self.active
+        self.extra_bytes = logits_side_bytes(w, self.active, s_in, False)
+        self.extra_bytes = logits_side_bytes(w, self.active, s_in, skip_masked)
 
     def step(self, k=0, prof=None):
         i = self.inp
@@ -512,6 +546,7 @@ class LogpsCase:
         self.wsp = torch.empty(g.grpo_workspace_size(w.B, w.T), dtype=torch.uint8, device=device)
         # logp / old / ref of active tokens, the mask, dL/dlogp of every slot
         self.alg_bytes = 12.0 * self.active + 5.0 * w.B * w.T
+        self.extra_bytes = {}
 
     def _call(self, i, prof=None):
         w = self.w
@@ -644,7 +679,9 @@ def run_gpu(args, w, ws, rank, local):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                      "kernel": case.kernel, "peak_source": f"{peak_kind} hbm_gbs",
-                     "bytes_per_launch": case.alg_bytes, "avg_launch_ms": kern_avg_s * 1e3},
+                     "bytes_per_launch": case.alg_bytes, "avg_launch_ms": kern_avg_s * 1e3,
+                     **({"strict_frac": case.extra_bytes["strict_bytes_per_launch"] / kern_avg_s
+                         / 1e9 / peak, **case.extra_bytes} if case.extra_bytes else {})},
         "step_gbs_algorithmic": case.alg_bytes / (ms_per_step / 1e3) / 1e9,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": 12, "steps": e2e_steps},
