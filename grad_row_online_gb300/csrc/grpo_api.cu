@@ -93,6 +93,9 @@ grpo_status_t check_groups(const grpo_groups_t* g, int64_t B, int32_t* spp,
   return GRPO_OK;
 }
 
+// Slots per sequence: positions and counts within a sequence are 32-bit.
+static constexpr int64_t kMaxT = (int64_t)1 << 30;
+
 grpo_status_t check_ws(const void* ws, size_t ws_bytes, int64_t B, int64_t T) {
   if (!ws) return GRPO_ERR_NULL;
   if (!aligned(ws, 256)) return GRPO_ERR_ALIGN;
@@ -193,7 +196,7 @@ extern "C" grpo_status_t grpo_loss_fwd_bwd(
     const grpo_params_t* params, void* grad_logits, float* out3, float* per_seq,
     float* logps_out, float* adv_out, void* ws, size_t ws_bytes, void* stream) {
   if (dt != GRPO_F32 && dt != GRPO_BF16 && dt != GRPO_F16) return GRPO_ERR_DTYPE;
-  if (B < 0 || T < 0 || V < 1) return GRPO_ERR_SHAPE;
+  if (B < 0 || T < 0 || T > kMaxT || V < 1) return GRPO_ERR_SHAPE;
   if (!params || !groups) return GRPO_ERR_NULL;
   const bool any_rows = B > 0 && T > 0;
   if (any_rows && (!policy_logits || !ref_logits || !action_ids || !old_logps ||
@@ -298,7 +301,7 @@ extern "C" grpo_status_t grpo_loss_from_logps(const float* logps, const float* o
                                               const grpo_params_t* params, float* grad_logps,
                                               float* out3, float* per_seq, float* adv_out,
                                               void* ws, size_t ws_bytes, void* stream) {
-  if (B < 0 || T < 0) return GRPO_ERR_SHAPE;
+  if (B < 0 || T < 0 || T > kMaxT) return GRPO_ERR_SHAPE;
   if (!params || !groups) return GRPO_ERR_NULL;
   grpo_status_t st = check_params(params);
   if (st != GRPO_OK) return st;
@@ -356,7 +359,7 @@ extern "C" grpo_status_t grpo_loss_from_logps(const float* logps, const float* o
 
 extern "C" grpo_status_t grpo_count_active(const uint8_t* completion_mask, int64_t B, int64_t T,
                                            unsigned long long* counts_out, void* stream) {
-  if (B < 0 || T < 0) return GRPO_ERR_SHAPE;
+  if (B < 0 || T < 0 || T > kMaxT) return GRPO_ERR_SHAPE;
   if (!counts_out || (B > 0 && T > 0 && !completion_mask)) return GRPO_ERR_NULL;
   if (!aligned(counts_out, 8)) return GRPO_ERR_ALIGN;
   cudaStream_t s = (cudaStream_t)stream;
@@ -391,7 +394,8 @@ extern "C" grpo_status_t grpo_vocab_partials(const void* policy_slice, const voi
                                              void* partials_r, float* action_logits,
                                              void* stream) {
   if (dt != GRPO_F32 && dt != GRPO_BF16 && dt != GRPO_F16) return GRPO_ERR_DTYPE;
-  if (B < 0 || T < 0 || Vk < 1 || v_begin < 0 || v_begin % kVChunk != 0) return GRPO_ERR_SHAPE;
+  if (B < 0 || T < 0 || T > kMaxT || Vk < 1 || v_begin < 0 || v_begin % kVChunk != 0)
+    return GRPO_ERR_SHAPE;
   const int64_t rows = B * T;
   if (rows > 0 && (!policy_slice || !ref_slice || !action_ids || !completion_mask ||
                    !partials_p || !partials_r || !action_logits))
@@ -426,7 +430,7 @@ extern "C" grpo_status_t grpo_vocab_loss(const void* partials_p, const void* par
                                          double* lse_w, float* out3, float* per_seq,
                                          float* logps_out, float* adv_out, void* ws,
                                          size_t ws_bytes, void* stream) {
-  if (B < 0 || T < 0 || V < 1) return GRPO_ERR_SHAPE;
+  if (B < 0 || T < 0 || T > kMaxT || V < 1) return GRPO_ERR_SHAPE;
   if (num_chunks != (V + kVChunk - 1) / kVChunk) return GRPO_ERR_SHAPE;
   if (!params || !groups) return GRPO_ERR_NULL;
   const int64_t rows = B * T;
@@ -498,7 +502,7 @@ extern "C" grpo_status_t grpo_vocab_grad(const void* policy_slice, grpo_dtype_t 
                                          const uint8_t* completion_mask, const double* lse_w,
                                          void* grad_slice, uint32_t flags, void* stream) {
   if (dt != GRPO_F32 && dt != GRPO_BF16 && dt != GRPO_F16) return GRPO_ERR_DTYPE;
-  if (B < 0 || T < 0 || Vk < 1 || v_begin < 0) return GRPO_ERR_SHAPE;
+  if (B < 0 || T < 0 || T > kMaxT || Vk < 1 || v_begin < 0) return GRPO_ERR_SHAPE;
   if (flags & ~GRPO_SKIP_MASKED_GRAD_ROWS) return GRPO_ERR_PARAM;
   if (B * T > 0 && (!policy_slice || !action_ids || !completion_mask || !lse_w || !grad_slice))
     return GRPO_ERR_NULL;

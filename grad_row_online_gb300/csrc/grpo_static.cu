@@ -57,7 +57,7 @@ extern "C" grpo_status_t grpo_loss_fwd_bwd_static(
     const grpo_params_t* params, void* grad_logits, float* out3, float* per_seq,
     float* logps_out, float* adv_out, void* stream) {
   // sizes beyond the fixed scratch are rejected before anything else runs
-  if (B < 0 || T < 0) return GRPO_ERR_SHAPE;
+  if (B < 0 || T < 0 || T > ((int64_t)1 << 30)) return GRPO_ERR_SHAPE;
   if (grpo_workspace_size(B, T, 0) > kStaticScratchBytes) return GRPO_ERR_WORKSPACE;
   void* ws = nullptr;
   const grpo_status_t st = scratch_for_current_device(&ws);

@@ -60,7 +60,7 @@ extern "C" {
 typedef enum {
   GRPO_OK = 0,
   GRPO_ERR_NULL = 1,       /* a required pointer is NULL */
-  GRPO_ERR_SHAPE = 2,      /* negative sizes, V < 1, B not a multiple of spp, ... */
+  GRPO_ERR_SHAPE = 2,      /* negative sizes, T > 2^30, V < 1, B not a multiple of spp, ... */
   GRPO_ERR_DTYPE = 3,      /* unknown grpo_dtype_t */
   GRPO_ERR_ALIGN = 4,      /* a pointer is not aligned to its element size, or
                               the workspace is not 256-byte aligned */

@@ -93,6 +93,7 @@ def test_fwd_rejects_bad_arguments(lib):
     assert _fwd(lib, dt=7) == 3                       # dtype
     assert _fwd(lib, V=0) == 2                        # V < 1
     assert _fwd(lib, B=-1) == 2
+    assert _fwd(lib, T=(1 << 30) + 1) == 2            # positions within a sequence are 32-bit
     assert _fwd(lib, policy=None) == 1                # null input
     assert _fwd(lib, out3=None) == 1
     assert _fwd(lib, ws=None) == 1
@@ -142,6 +143,8 @@ def test_logps_and_adv_reject_bad_arguments(lib):
              None, None, FAKE, 10, None) == 7
     assert L(FAKE + 2, FAKE, FAKE, FAKE, 8, 16, FAKE, ctypes.byref(gr), ctypes.byref(p), None,
              FAKE, None, None, FAKE, ws, None) == 4
+    assert L(FAKE, FAKE, FAKE, FAKE, 8, (1 << 30) + 1, FAKE, ctypes.byref(gr), ctypes.byref(p),
+             None, FAKE, None, None, FAKE, ws, None) == 2  # T > 2^30
     A = lib.grpo_group_adv
     assert A(FAKE, ctypes.byref(gr), ctypes.c_float(0.0), 0, FAKE, FAKE, ws, None) == 6
     assert A(FAKE, ctypes.byref(gr), ctypes.c_float(1e-6), 4, FAKE, FAKE, ws, None) == 6
@@ -153,6 +156,7 @@ def test_logps_and_adv_reject_bad_arguments(lib):
 def test_shard_entry_points_reject_bad_arguments(lib):
     # grpo_count_active / grpo_loss_finalize host checks
     assert lib.grpo_count_active(FAKE, -1, 4, FAKE, None) == 2
+    assert lib.grpo_count_active(FAKE, 2, (1 << 30) + 1, FAKE, None) == 2
     assert lib.grpo_count_active(FAKE, 2, 4, None, None) == 1
     assert lib.grpo_count_active(None, 2, 4, FAKE, None) == 1
     assert lib.grpo_count_active(FAKE, 2, 4, FAKE + 4, None) == 4
