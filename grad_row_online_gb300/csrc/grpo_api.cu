@@ -341,12 +341,10 @@ extern "C" grpo_status_t grpo_loss_from_logps(const float* logps, const float* o
     if (logps_fused_capacity(&cap) != cudaSuccess) return GRPO_ERR_CUDA;
     fused = B <= cap;
   }
-  if (!fused) {
-    PrepArgs pa{rewards, bounds, B, T, G, pl.Bg, pl.seq_begin, &hdr->N, spp, params->adv_eps,
-                (int)(params->flags & GRPO_ADV_EPS_ADD), completion_mask, 1, A, Aff, adv_out, L,
-                rng, hdr};
-    if (launch_prep(pa, s) != cudaSuccess) return GRPO_ERR_CUDA;
-  }
+  PrepArgs pa{rewards, bounds, B, T, G, pl.Bg, pl.seq_begin, &hdr->N, spp, params->adv_eps,
+              (int)(params->flags & GRPO_ADV_EPS_ADD), completion_mask, 1, A, Aff, adv_out, L,
+              rng, hdr};
+  if (!fused && launch_prep(pa, s) != cudaSuccess) return GRPO_ERR_CUDA;
   LogpsArgs la{logps, old_logps, ref_logps, completion_mask, A + pl.seq_begin,
                Aff + pl.seq_begin, rng, L, totals, grad_logps, out3,
                per_seq, hdr, B, T, params->clip_eps_lo, params->clip_eps_hi, params->beta,
@@ -354,7 +352,16 @@ extern "C" grpo_status_t grpo_loss_from_logps(const float* logps, const float* o
                params->norm_constant, params->clip_counts, NS, pl.shard ? 1 : 0, params->flags,
                fused ? 1 : 0, rewards, bounds, G, pl.Bg, pl.seq_begin, spp, params->adv_eps,
                (int)(params->flags & GRPO_ADV_EPS_ADD), adv_out};
-  return cuda_status(launch_logps(la, params->profile, s));
+  cudaError_t e = launch_logps(la, params->profile, s);
+  if (fused && e == cudaErrorCooperativeLaunchTooLarge) {
+    // fewer SMs than the device has (a partitioned device, say): the two
+    // launches instead, which give the same bits
+    (void)cudaGetLastError();
+    if (launch_prep(pa, s) != cudaSuccess) return GRPO_ERR_CUDA;
+    la.fused = 0;
+    e = launch_logps(la, params->profile, s);
+  }
+  return cuda_status(e);
 }
 
 extern "C" grpo_status_t grpo_count_active(const uint8_t* completion_mask, int64_t B, int64_t T,
