@@ -407,7 +407,6 @@ class LogitsCase:
         s_in = 2 if w.dtype == "bf16" else 4
         # policy read twice, ref once, grad written once, per active row
         self.alg_bytes = 4.0 * w.V * s_in * self.active
-        self.extra_bytes = logits_side_bytes(w, self.active, s_in, False)
         self.extra_bytes = logits_side_bytes(w, self.active, s_in, skip_masked)
 
     def step(self, k=0, prof=None):
@@ -471,6 +470,7 @@ class VocabCase:
         # policy and ref read once for the partials, policy once more and the
         # gradient written once for the slices: 4 V s per active row, as the fused path
         self.alg_bytes = 4.0 * w.V * s_in * self.active
+        self.extra_bytes = logits_side_bytes(w, self.active, s_in, False)
 
     def step(self, k=0, prof=None):
         import torch

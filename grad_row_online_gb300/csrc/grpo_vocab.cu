@@ -23,7 +23,7 @@
 
 namespace grpo {
 
-static constexpr int kVocabWarps = 8;
+static constexpr int kVocabWarps = 4;  // measured: 8 warps per CTA 4 % slower
 static constexpr int kMergeThreads = 256;
 
 // The elements of run j (16 bytes of storage) of a chunk, -inf beyond n.
