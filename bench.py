@@ -42,6 +42,8 @@ CSRC = os.path.join(ROOT, "grad_row_online_gb300", "csrc")
 PROFILES = {
     "large_vocab": ("rows_kernel_large_vocab.md",
                     ("grpo_rows.cu", "grpo_rows_common.cuh", "grpo_internal.cuh")),
+    "fused": ("rows_kernel_fused.md",
+              ("grpo_rows.cu", "grpo_rows_common.cuh", "grpo_internal.cuh")),
     "logps": ("logps_kernel_logps.md", ("grpo_logps.cu", "grpo_internal.cuh")),
 }
 
@@ -712,12 +714,18 @@ def main():
                     help="leave masked gradient rows untouched (GRPO_SKIP_MASKED_GRAD_ROWS)")
     ap.add_argument("--T", type=int, default=0,
                     help="shorter rows per sequence (lengths scaled alike): small profiling case")
+    ap.add_argument("--B", type=int, default=0,
+                    help="fewer sequences (the same length mix): small profiling case")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     w = synth.WORKLOADS[args.workload]
     if args.T:
         lo, hi = w.len_range
         w = w.with_(name=w.name, T=args.T, len_range=(max(1, lo * args.T // w.T), hi * args.T // w.T))
+    if args.B:
+        assert not w.samples_per_prompt or args.B % w.samples_per_prompt == 0, \
+            "B must be a multiple of samples_per_prompt"
+        w = w.with_(name=w.name, B=args.B, holes=w.holes * args.B // w.B)
 
     ws, rank, local = dist_setup()
     if args.impl == "reference":
