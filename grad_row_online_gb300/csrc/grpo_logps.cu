@@ -516,8 +516,33 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
       // GSPO: rho_i = exp(mean over the active tokens of logp - old), before
       // any token's term (Kahan sums per thread, float pairs across the CTA)
       float ss = 0.f, sc = 0.f;
-      for (int64_t t = threadIdx.x; t < a.T; t += blockDim.x)
-        if (a.mask[base + t]) kahan(ss, sc, __fsub_rn(a.logps[base + t], a.old[base + t]));
+      if (vec_ok(a)) {
+        // 4-slot vectors of the widened active range, two per thread in
+        // flight, read whole (masked slots are loaded but never used)
+        const uint32_t* mrow = reinterpret_cast<const uint32_t*>(a.mask + base);
+        const float4* lrow = reinterpret_cast<const float4*>(a.logps + base);
+        const float4* orow = reinterpret_cast<const float4*>(a.old + base);
+        auto add4 = [&](uint32_t mw, const float4& l, const float4& o) {
+          const float d[4] = {__fsub_rn(l.x, o.x), __fsub_rn(l.y, o.y), __fsub_rn(l.z, o.z),
+                              __fsub_rn(l.w, o.w)};
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if ((mw >> (8 * j)) & 0xFFu) kahan(ss, sc, d[j]);
+        };
+        const int64_t v1 = hi / 4;
+        int64_t v = lo / 4 + threadIdx.x;
+        for (; v + kLogpsThreads < v1; v += 2 * kLogpsThreads) {
+          const uint32_t m0 = __ldg(mrow + v), m1 = __ldg(mrow + v + kLogpsThreads);
+          const float4 l0 = __ldg(lrow + v), l1 = __ldg(lrow + v + kLogpsThreads);
+          const float4 o0 = __ldg(orow + v), o1 = __ldg(orow + v + kLogpsThreads);
+          add4(m0, l0, o0);
+          add4(m1, l1, o1);
+        }
+        if (v < v1) add4(__ldg(mrow + v), __ldg(lrow + v), __ldg(orow + v));
+      } else {
+        for (int64_t t = threadIdx.x; t < a.T; t += blockDim.x)
+          if (a.mask[base + t]) kahan(ss, sc, __fsub_rn(a.logps[base + t], a.old[base + t]));
+      }
       const FF wsum = warp_sum_ff2(FF{ss, -sc});
       if (lane == 0) s_ff[0][warp] = wsum;
       __syncthreads();
