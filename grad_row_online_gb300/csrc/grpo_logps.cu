@@ -213,6 +213,69 @@ __device__ __forceinline__ bool vec_fast(const float4& l4, const float4& o4, con
   return __fadd_rn(d2.x, d2.y) < 0.25f && __fadd_rn(g2.x, g2.y) <= f.g2_max;
 }
 
+// One vector of four active slots on the fast path for the other loss
+// variants (k1 / k2 KL, the dual clip, CISPO, GSPO's sequence ratio): the
+// same packed polynomials give e^(logp - old) - 1 (GSPO: the sequence's
+// rho - 1 instead), e^d - 1 and k3, then each token takes the variant's
+// epilogue in fp32, unrolled.  Same range checks as vec_fast (|d| < 1/2 for
+// every argument taken from the polynomial, every |w| <= kWPrecise); the
+// clip counts are returned, to be added only when the vector passes.
+__device__ __forceinline__ bool vec_fast_variant(const float4& l4, const float4& o4,
+                                                 const float4& r4, bool has_ref,
+                                                 const SeqCtx& x, const LogpsArgs& a,
+                                                 float (&w)[4], float& vq, float& vk,
+                                                 unsigned (&nc)[3]) {
+  const float lp[4] = {l4.x, l4.y, l4.z, l4.w};
+  float em[4], d[4], emd[4], k3[4];
+  float2 d2 = f2(0.f);
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const float2 l2 = p ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
+    float2 e2 = f2(x.em_seq);
+    if (!a.var.seq_ratio) {
+      const float2 o2 = p ? make_float2(o4.z, o4.w) : make_float2(o4.x, o4.y);
+      const float2 dp = __ffma2_rn(o2, f2(-1.f), l2);  // logp - old
+      const float2 Qp = Q_poly2(dp), ddp = __fmul2_rn(dp, dp);
+      e2 = __ffma2_rn(ddp, Qp, dp);
+      d2 = __fadd2_rn(d2, ddp);
+    }
+    float2 dr = f2(0.f), k2 = f2(0.f), er = f2(0.f);
+    if (has_ref) {
+      const float2 r2 = p ? make_float2(r4.z, r4.w) : make_float2(r4.x, r4.y);
+      dr = __ffma2_rn(l2, f2(-1.f), r2);  // ref - logp
+      const float2 Qr = Q_poly2(dr), ddr = __fmul2_rn(dr, dr);
+      k2 = __fmul2_rn(ddr, Qr);
+      er = __ffma2_rn(ddr, Qr, dr);
+      d2 = __fadd2_rn(d2, ddr);
+    }
+    em[2 * p] = e2.x;
+    em[2 * p + 1] = e2.y;
+    d[2 * p] = dr.x;
+    d[2 * p + 1] = dr.y;
+    emd[2 * p] = er.x;
+    emd[2 * p + 1] = er.y;
+    k3[2 * p] = k2.x;
+    k3[2 * p + 1] = k2.y;
+  }
+  vq = 0.f;
+  vk = 0.f;
+  nc[0] = nc[1] = nc[2] = 0u;
+  bool small = true;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const TokEpi<float> t = token_epilogue<float>(em[j], lp[j], d[j], emd[j], k3[j], has_ref,
+                                                  x.A, a.var);
+    vq = __fadd_rn(vq, t.q);
+    vk = __fadd_rn(vk, t.k);
+    nc[0] += t.clip == 1;
+    nc[1] += t.clip == 2;
+    nc[2] += t.clip == 3;
+    w[j] = __fmul_rn(x.gc, t.g);
+    small = small && fabsf(w[j]) <= kWPrecise;
+  }
+  return __fadd_rn(d2.x, d2.y) < 0.25f && small;
+}
+
 // Every byte of a mask word nonzero.
 __device__ __forceinline__ bool all_active(uint32_t mw) {
   return ((((mw & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | mw) & 0x80808080u) == 0x80808080u;
@@ -244,6 +307,7 @@ __device__ __forceinline__ void vec_general(uint32_t mw, const float4& l4, const
 // One vector of four slots: its gradient, and its q / k sums into the
 // thread's Kahan pairs.  Fully active vectors take the fast path when their
 // range check passes; everything else the general path.
+template <bool kDefault>
 __device__ __forceinline__ void process_vec(uint32_t mw, const float4& l, const float4& o,
                                             const float4& r, bool has_ref, const FastCtx& f,
                                             const SeqCtx& x, const LogpsArgs& a, Acc& acc,
@@ -252,8 +316,14 @@ __device__ __forceinline__ void process_vec(uint32_t mw, const float4& l, const 
   if (mw == 0u) return;
   float vq, vk;
   int nclip;
+  unsigned nc[3];
   if (f.on && all_active(mw) && vec_fast(l, o, r, has_ref, f, w, vq, vk, nclip)) {
     acc.count(f.clip_kind, (unsigned)nclip);
+  } else if (!kDefault && all_active(mw) &&
+             vec_fast_variant(l, o, r, has_ref, x, a, w, vq, vk, nc)) {
+    acc.nc[0] += nc[0];
+    acc.nc[1] += nc[1];
+    acc.nc[2] += nc[2];
   } else {
     vec_general(mw, l, o, r, x, a, w, vq, vk, acc);
   }
@@ -360,6 +430,10 @@ __device__ __forceinline__ bool grid_wait(const unsigned* c, unsigned expected) 
   return false;
 }
 
+// kDefault: the call's loss is the default variant (clipped surrogate, k3);
+// each form is its own instantiation, so that the other's fast path does not
+// cost it registers.
+template <bool kDefault>
 __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs a) {
   __shared__ FF s_ff[2][kLogpsThreads / 32];
   __shared__ unsigned s_nc[3][kLogpsThreads / 32];
@@ -584,7 +658,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
                                             : a.norm_c;
     x.gc = x.L > 0 ? __fdiv_rn(a.grad_scale, den) : 0.f;
     FastCtx f;
-    f.on = a.var.is_default();
+    f.on = kDefault && a.var.is_default();
     f.clip_kind = x.A > 0.f ? 1 : (x.A < 0.f ? 2 : 0);
     const float sgn = x.A > 0.f ? 1.f : -1.f;
     f.s2 = f2(sgn);
@@ -626,7 +700,8 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
             const int v = threadIdx.x + u * kLogpsThreads;
             if (4 * v < len) {
               float w[4];
-              process_vec(S.mk[v], S.lp[v], S.od[v], has_ref ? S.rf[v] : z4, has_ref, f, x, a,
+              process_vec<kDefault>(S.mk[v], S.lp[v], S.od[v], has_ref ? S.rf[v] : z4, has_ref,
+                                    f, x, a,
                           acc, w);
               if (a.grad) grow[st / 4 + v] = make_float4(w[0], w[1], w[2], w[3]);
             }
@@ -665,7 +740,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
         }
         const uint32_t m2 = v + 2 * kS < nv ? __ldg(mrow + v + 2 * kS) : 0u;
         float w[4];
-        process_vec(m0, l0, o0, r0, has_ref, f, x, a, acc, w);
+        process_vec<kDefault>(m0, l0, o0, r0, has_ref, f, x, a, acc, w);
         if (a.grad) grow[v] = make_float4(w[0], w[1], w[2], w[3]);
         m0 = m1;
         m1 = m2;
@@ -757,11 +832,15 @@ static cudaError_t prepare_device(int dev, int64_t* cap) {
   const int d = dev & (kMaxDevices - 1);
   long long c = g_capacity[d].load(std::memory_order_acquire);
   if (c == 0) {
-    cudaError_t e = cudaFuncSetAttribute(logps_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+    cudaError_t e = cudaFuncSetAttribute(logps_kernel<true>,
+                                         cudaFuncAttributePreferredSharedMemoryCarveout,
                                          (int)cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(logps_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int per_sm = 0, sms = 0, coop = 0;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, logps_kernel, kLogpsThreads,
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, logps_kernel<true>, kLogpsThreads,
                                                            0)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess)
@@ -809,7 +888,8 @@ cudaError_t launch_logps(const LogpsArgs& a, const grpo_profile_t* prof, cudaStr
     cfg.numAttrs = 1;
   }
   if (prof && prof->start) cudaEventRecord((cudaEvent_t)prof->start, s);
-  e = cudaLaunchKernelEx(&cfg, logps_kernel, a);
+  e = a.var.is_default() ? cudaLaunchKernelEx(&cfg, logps_kernel<true>, a)
+                         : cudaLaunchKernelEx(&cfg, logps_kernel<false>, a);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (prof && prof->stop) cudaEventRecord((cudaEvent_t)prof->stop, s);
   return e;
