@@ -189,6 +189,34 @@ def test_logps_default_counts_on_the_fast_path():
         assert_scalar(out[i], exp[k], k)
 
 
+@pytest.mark.parametrize("name", list(VARIANTS))
+def test_logps_variants_on_the_fast_path(name):
+    # small log ratios: every fully active 4-token vector passes the fast
+    # path's range check, so the variants' packed path carries the tokens
+    v = VARIANTS[name]
+    w = LOGPS_WIDE.with_(B=64, T=512, len_range=(384, 512), old_sigma=0.15,
+                         ref_logp_sigma=0.05, beta=0.04)
+    lp, old, ref, mask, R = _logps_inputs(w)
+    A = oracle.group_advantages(R, w.group_boundaries())
+    exp = oracle.loss_from_logps(lp, ref, old, mask, A, w.eps_lo, w.eps_hi, w.beta,
+                                 **_oracle_kw(v, w))
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    args = dict(samples_per_prompt=w.samples_per_prompt, clip_eps=w.eps_lo, clip_eps_hi=w.eps_hi,
+                beta=w.beta, reduction=w.reduction, want_per_seq=True, want_clip_counts=True)
+    args.update(v)
+    res = g.grpo_loss_from_logps(t(lp), t(old), t(ref), t(mask), t(R), **args)
+    torch.cuda.synchronize()
+    out = res["out3"].cpu().numpy().astype(np.float64)
+    for i, k in enumerate(("loss", "policy_loss", "kl")):
+        assert_scalar(out[i], exp[k], f"{name} {k}")
+    near = _band(exp, w.eps_lo, w.eps_hi, v.get("dual_clip_c"))
+    _check_counts(res["clip_counts"], exp, near)
+    want = exp["w"].astype(np.float32)
+    got = res["grad"].cpu().numpy()
+    ok = np.abs(got.astype(np.float64) - want) <= np.spacing(np.abs(want)) + 1e-9
+    assert np.all(ok | near), np.argwhere(~(ok | near))[:5]
+
+
 def test_variant_parameters_are_checked_on_the_host():
     x = torch.zeros((2, 1, 4), device="cuda")
     a = torch.zeros((2, 1), dtype=torch.int64, device="cuda")
