@@ -129,10 +129,10 @@ typedef enum {
  * usable.  Ignored elsewhere (and with GRPO_FLAG_SEPARATE_PREP). */
 #define GRPO_FLAG_TEST_STALLED_BARRIER 0x40000000u
 
-/* Group specification ("Group specification": provide exactly one of
- * samples_per_prompt > 0, or CSR group_boundaries of length num_groups + 1
- * with boundaries[0] = 0, boundaries[num_groups] = num_seqs and strictly
- * increasing entries, e.g. {0, 8, 16, 24}). */
+/* Group specification (RL-Kernel "GRPO Loss", "Group specification"): give
+ * either samples_per_prompt > 0 or CSR group_boundaries of length
+ * num_groups + 1 with boundaries[0] = 0, boundaries[num_groups] = num_seqs
+ * and strictly increasing entries, e.g. {0, 8, 16, 24}; not both. */
 typedef struct {
   int64_t num_seqs;                /* B */
   int32_t samples_per_prompt;      /* > 0: uniform groups of this size, B % spp == 0 */
@@ -166,8 +166,9 @@ typedef struct {
  * keeps its own slice), while the token arguments (logits or log-probs,
  * action_ids, old_logps, completion_mask, gradients, per_seq, adv_out)
  * cover only the shard's B sequences, starting at sequence seq_begin of the
- * batch.  The token weights use the whole batch's counts; only per-sequence
- * totals cross a rank boundary.  Whatever the partition, every gradient,
+ * batch.  The token weights use the whole batch's counts; besides the
+ * counts, the per-sequence totals are all that ranks exchange.  Whatever the
+ * partition, every gradient,
  * per-sequence total and loss output is bit-identical to the unsharded
  * call's. */
 typedef struct {
@@ -261,8 +262,8 @@ grpo_status_t grpo_loss_fwd_bwd(const void *policy_logits, const void *ref_logit
 
 /* The same loss when the per-token log-probs are already known (grpo.cpp
  * README "CUDA": the selected-token GRPO loss; RL-Kernel "Tensor and Data
- * Parallel": by the time the objective sees a logprob the vocabulary is
- * reduced).
+ * Parallel": the objective only ever receives log-probs, the vocabulary
+ * already reduced away).
  *   logps, old_logps : [B,T] f32.   ref_logps : [B,T] f32, NULL iff beta == 0.
  *   completion_mask  : [B,T] uint8.  rewards : [B] f32.
  *   grad_logps (nullable) : [B,T] f32, receives dL/dlogp (0 on masked tokens).
@@ -301,9 +302,9 @@ grpo_status_t grpo_loss_fwd_bwd_static(const void *policy_logits, const void *re
 /* Sequence sharding ("Tensor and Data Parallel", steps 2-6).  A rank that
  * owns B sequences of T slots counts them: counts_out (device [2]) receives
  * N = sum of active tokens and S = sequences with at least one, as exact
- * integers; the whole batch's counts are the sums over ranks.  The paper's
- * normaliser "divides by a global active-token count, gathered as integers
- * so it is exact at every degree". */
+ * integers; the whole batch's counts are the sums over ranks.  (The page's
+ * normaliser uses the batch-wide active-token count, exchanged as integers,
+ * which makes it the same at any number of ranks.) */
 grpo_status_t grpo_count_active(const uint8_t *completion_mask, int64_t B, int64_t T,
                                 unsigned long long *counts_out, void *stream);
 
@@ -313,15 +314,16 @@ grpo_status_t grpo_count_active(const uint8_t *completion_mask, int64_t B, int64
  * (device [2], as in grpo_shard_t) and the same params (reduction,
  * norm_constant, beta).  out3 = {loss, policy_loss, kl}, computed by the
  * same code, in the same order, as an unsharded call; so the result is
- * bit-identical to it ("all_reduce is excluded on purpose": the sum runs
- * in declared sequence order). */
+ * bit-identical to it (the page rules out an all-reduce for this sum: it
+ * runs over the sequences in their declared order). */
 grpo_status_t grpo_loss_finalize(const grpo_seq_total_t *totals, int64_t B,
                                  const unsigned long long *global_counts,
                                  const grpo_params_t *params, float *out3, void *stream);
 
 /* Vocabulary parallelism (tensor parallelism over V; RL-Kernel "Tensor and
- * Data Parallel", step 1: "selected logprobs come from VocabParallelLogprobOp,
- * so ratio and KL inherit cross-TP bitwise equality").  A rank holds the
+ * Data Parallel", step 1: the selected log-probs come from a vocab-parallel
+ * log-prob, so the ratio and KL are bitwise the same at every tensor-parallel
+ * degree).  A rank holds the
  * slice [v_begin, v_begin + Vk) of every policy and reference row, v_begin a
  * multiple of grpo_vocab_chunk() (every slice but the last spans whole
  * chunks).  The loss is formed by three calls around one exchange:
