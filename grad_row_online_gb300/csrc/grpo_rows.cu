@@ -7,9 +7,9 @@
 //   sweep 1   one streaming read of the policy and reference rows, both in
 //             flight together, each reduced to (max, sum exp) by a per-thread
 //             online normaliser and a fixed-order block combine in float-float
-//             arithmetic (RL-Kernel "GRPO Loss" intro: logits -> ratio / KL via
-//             online softmax; grpo.cpp README "CUDA": carry the row maximum and
-//             normaliser together);
+//             arithmetic (RL-Kernel "GRPO Loss" intro: the ratio and KL come
+//             from logits through an online softmax; grpo.cpp README "CUDA":
+//             carry the row maximum and normaliser together);
 //   finish    one thread, fp32 / float-float: logp, ref_logp, ratio, clipped
 //             surrogate, k3 KL, token weight and w = dL/dlogp (RL-Kernel
 //             "Accuracy"; dockyard_rl "One loss, many algorithms",

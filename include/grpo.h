@@ -80,7 +80,7 @@ typedef enum { GRPO_F32 = 0, GRPO_BF16 = 1, GRPO_F16 = 2 } grpo_dtype_t;
 
 /* Normaliser ("Normalizer semantics"): the global active-token count, the
  * per-sequence count then the mean over live sequences, or a declared
- * constant (the Dr.GRPO form, independent of the mask). */
+ * constant (the Dr.GRPO form: the divisor does not depend on the mask). */
 typedef enum {
   GRPO_TOKEN_MEAN = 0,
   GRPO_SEQUENCE_MEAN = 1,

@@ -265,8 +265,8 @@ void oracle_lse_merge(int64_t nrows, int64_t K, const double *M, const double *Z
  *   kl_type 1, k1 (the log ratio):  k = logp - ref = -d,  g_kl = 1
  *   kl_type 2, k2:                  k = (logp - ref)^2 / 2 = d^2 / 2,
  *                                   g_kl = logp - ref = -d
- *   dual clip c > 1 (A < 0 only; "a lower bound on negative-advantage
- *     terms"):  p = -max(min(r A, clip(r) A), c A), which for A < 0 is
+ *   dual clip c > 1 (A < 0 only: a floor under the objective of tokens
+ *     with negative advantage):  p = -max(min(r A, clip(r) A), c A), which for A < 0 is
  *     -A min(max(r, 1 - eps_lo), c); g_pol is also 0 where r > c.
  *   surrogate 1, CISPO:  p = -A sg(clip(r)) logp, so g_pol = -A clip(r)
  *     (the clipped weight sits behind a stop-gradient; every token keeps a
