@@ -372,6 +372,14 @@ def workload_config(w: synth.Workload, variant: str = "default",
 # ---------------------------------------------------------------------------
 # the two boundaries under test
 # ---------------------------------------------------------------------------
+def active_runs(mask) -> list:
+    """[begin, end) ranges of consecutive active slots of a [B, T] host mask,
+    over the flattened rows (a run may continue into the next sequence)."""
+    flat = (np.asarray(mask).reshape(-1) != 0).astype(np.int8)
+    edges = np.diff(np.concatenate([[0], flat, [0]]))
+    return list(zip(np.flatnonzero(edges == 1).tolist(), np.flatnonzero(edges == -1).tolist()))
+
+
 def logits_side_bytes(w, active: int, s_in: int, skip_masked: bool) -> dict:
     """The roofline's secondary figures for a logits workload: the strict
     lower bound (the policy read once, as if each row stayed on chip:
@@ -417,6 +425,9 @@ class LogitsCase:
                                  grad=self.grad, out3=self.out3, workspace=self.wsp, profile=prof,
                                  **self.kw)
 
+    e2e_copy = ("the logits rows the call reads (runs of active tokens, found from the host "
+                "mask inside each step: masked rows are never read), the other inputs whole")
+
     def e2e_setup(self):
         import torch
         self.host = {}
@@ -427,12 +438,21 @@ class LogitsCase:
         self.dev_in["bounds"] = self.inp["bounds"]
         self.kw_e = loss_kwargs(self.w, self.dev_in)
         self.loss_host = torch.empty(3, dtype=torch.float32).pin_memory()
-        return sum(v.numel() * v.element_size() for k, v in self.host.items() if k != "bounds")
+        self.mask_host = self.host["mask"].numpy()
+        rows = sum(e - b for b, e in active_runs(self.mask_host))
+        row_bytes = self.w.V * self.host["X"].element_size()
+        return 2 * rows * row_bytes + sum(self.host[k].numel() * self.host[k].element_size()
+                                          for k in ("acts", "old", "mask", "R"))
 
     def e2e_step(self):
-        d = self.dev_in
-        for k in ("X", "Y", "acts", "old", "mask", "R"):
-            d[k].copy_(self.host[k], non_blocking=True)
+        d, h, V = self.dev_in, self.host, self.w.V
+        xd, yd = d["X"].view(-1, V), d["Y"].view(-1, V)
+        xh, yh = h["X"].view(-1, V), h["Y"].view(-1, V)
+        for b, e in active_runs(self.mask_host):
+            xd[b:e].copy_(xh[b:e], non_blocking=True)
+            yd[b:e].copy_(yh[b:e], non_blocking=True)
+        for k in ("acts", "old", "mask", "R"):
+            d[k].copy_(h[k], non_blocking=True)
         self.g.grpo_loss_fwd_bwd(d["X"], d["Y"], d["acts"], d["old"], d["mask"], d["R"],
                                  grad=self.grad, out3=self.out3, workspace=self.wsp, **self.kw_e)
         self.loss_host.copy_(self.out3, non_blocking=True)
@@ -494,19 +514,20 @@ class VocabCase:
 
     def e2e_setup(self):
         import torch
+        self.small = ("acts", "old", "mask", "R")
         self.host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
-                     for t in self.Xs + self.Ys]
+                     for t in self.Xs + self.Ys + [self.inp[k] for k in self.small]]
         self.dev_in = [torch.empty_like(t) for t in self.Xs + self.Ys]
+        self.dev_small = {k: torch.empty_like(self.inp[k]) for k in self.small}
         self.loss_host = torch.empty(3, dtype=torch.float32).pin_memory()
-        rest = sum(self.inp[k].numel() * self.inp[k].element_size()
-                   for k in ("acts", "old", "mask", "R"))
-        return sum(t.numel() * t.element_size() for t in self.host) + rest
+        return sum(t.numel() * t.element_size() for t in self.host)
 
     def e2e_step(self):
-        for d, h in zip(self.dev_in, self.host):
-            d.copy_(h, non_blocking=True)
         n = len(self.Xs)
+        for d, h in zip(self.dev_in + [self.dev_small[k] for k in self.small], self.host):
+            d.copy_(h, non_blocking=True)
         self.Xs, self.Ys = self.dev_in[:n], self.dev_in[n:]
+        self.inp = dict(self.inp, **self.dev_small)
         self.step()
         self.loss_host.copy_(self.out3, non_blocking=True)
 
@@ -652,6 +673,7 @@ def run_gpu(args, w, ws, rank, local):
 
     # ---- end to end: pinned host inputs -> device -> loss -> host ----
     e2e_steps = min(args.e2e_steps, args.steps)
+    resident_out3 = case.out3.clone()  # the loss of the device-resident steps
     h2d = case.e2e_setup()
     case.e2e_step()
     torch.cuda.synchronize(device)
@@ -665,6 +687,8 @@ def run_gpu(args, w, ws, rank, local):
     torch.cuda.synchronize(device)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, device)
     e2e_value = aggregate_value(case.active, e2e_steps, ws, e2e_ms)
+    if not torch.equal(case.out3, resident_out3):  # the same inputs, copied in
+        raise RuntimeError("the end-to-end steps' loss differs from the device-resident steps'")
 
     if rank != 0:
         barrier(ws)
@@ -686,7 +710,8 @@ def run_gpu(args, w, ws, rank, local):
                          / 1e9 / peak, **case.extra_bytes} if case.extra_bytes else {})},
         "step_gbs_algorithmic": case.alg_bytes / (ms_per_step / 1e3) / 1e9,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": 12, "steps": e2e_steps},
+                "d2h_bytes_per_step": 12, "steps": e2e_steps,
+                **({"copies": case.e2e_copy} if getattr(case, "e2e_copy", None) else {})},
         "gpu_launches": case.launches_per_step * args.steps,
         "clocks": clk,
     }
