@@ -512,20 +512,33 @@ class VocabCase:
             prof[1].record()
         self.out3 = res["out3"]
 
+    e2e_copy = LogitsCase.e2e_copy
+
     def e2e_setup(self):
         import torch
         self.small = ("acts", "old", "mask", "R")
         self.host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
-                     for t in self.Xs + self.Ys + [self.inp[k] for k in self.small]]
+                     for t in self.Xs + self.Ys]
+        self.host_small = {k: torch.empty(self.inp[k].shape, dtype=self.inp[k].dtype,
+                                          pin_memory=True).copy_(self.inp[k])
+                           for k in self.small}
         self.dev_in = [torch.empty_like(t) for t in self.Xs + self.Ys]
         self.dev_small = {k: torch.empty_like(self.inp[k]) for k in self.small}
         self.loss_host = torch.empty(3, dtype=torch.float32).pin_memory()
-        return sum(t.numel() * t.element_size() for t in self.host)
+        self.mask_host = self.host_small["mask"].numpy()
+        rows = sum(e - b for b, e in active_runs(self.mask_host))
+        return (rows * sum(t.shape[-1] * t.element_size() for t in self.host)
+                + sum(t.numel() * t.element_size() for t in self.host_small.values()))
 
     def e2e_step(self):
         n = len(self.Xs)
-        for d, h in zip(self.dev_in + [self.dev_small[k] for k in self.small], self.host):
-            d.copy_(h, non_blocking=True)
+        runs = active_runs(self.mask_host)
+        for d, h in zip(self.dev_in, self.host):  # every slice: the rows the calls read
+            dv, hv = d.view(-1, d.shape[-1]), h.view(-1, h.shape[-1])
+            for b, e in runs:
+                dv[b:e].copy_(hv[b:e], non_blocking=True)
+        for k in self.small:
+            self.dev_small[k].copy_(self.host_small[k], non_blocking=True)
         self.Xs, self.Ys = self.dev_in[:n], self.dev_in[n:]
         self.inp = dict(self.inp, **self.dev_small)
         self.step()
