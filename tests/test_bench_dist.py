@@ -41,3 +41,21 @@ def test_two_rank_harness_on_gloo():
     for rank, slowest, value in got:
         assert slowest == 15.0  # both ranks see the slower rank's time
         assert value == pytest.approx(1000 * 4 * 2 / 0.015)  # two replicas' tokens / max time
+
+
+def test_active_runs_cover_exactly_the_active_slots():
+    # the end-to-end step copies these runs of logits rows; together they must
+    # be exactly the active slots, in order, without overlap
+    import numpy as np
+    import bench
+    rng = np.random.default_rng(5)
+    for B, T, p in [(4, 7, 0.5), (16, 64, 0.9), (3, 5, 0.0), (3, 5, 1.0), (1, 1, 1.0)]:
+        mask = (rng.random((B, T)) < p).astype(np.uint8) * rng.integers(1, 255, (B, T))
+        runs = bench.active_runs(mask.astype(np.uint8))
+        cover = np.zeros(B * T, dtype=bool)
+        last = -1
+        for b, e in runs:
+            assert last < b < e <= B * T  # ordered, nonempty, separated
+            cover[b:e] = True
+            last = e
+        assert np.array_equal(cover, mask.reshape(-1) != 0)
