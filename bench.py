@@ -436,7 +436,10 @@ class LogitsCase:
             self.host[k].copy_(v)
         self.dev_in = {k: torch.empty_like(v) for k, v in self.inp.items()}
         self.dev_in["bounds"] = self.inp["bounds"]
-        self.kw_e = loss_kwargs(self.w, self.dev_in)
+        # the same call as the resident steps (variant, masked-row mode), on the copied inputs
+        self.kw_e = dict(self.kw)
+        if "group_boundaries" in self.kw_e:
+            self.kw_e["group_boundaries"] = self.dev_in["bounds"]
         self.loss_host = torch.empty(3, dtype=torch.float32).pin_memory()
         self.mask_host = self.host["mask"].numpy()
         rows = sum(e - b for b, e in active_runs(self.mask_host))

@@ -316,7 +316,12 @@ __device__ void zero_row(T* g, int64_t V, uint64_t pol) {
 }
 
 // ------------------------------------------------------------------ kernel
-template <typename T>
+// kTmem: the instantiation that may keep the tensor-memory slice.  16-bit
+// rows too short to reach it take the other one, which holds no
+// tensor-memory code at all (a kernel that may allocate tensor memory
+// measured 1.3 % slower on the 64 KB rows of the fused workload, where the
+// slice is never used).
+template <typename T, bool kTmem>
 __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(const RowArgs a) {
   extern __shared__ __align__(16) uint4 s_keep[];  // kPolicySmemVecs vectors
   __shared__ float s_f[64];
@@ -338,8 +343,8 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(cons
   }
   // tensor memory for the second kept slice (block-uniform; released below,
   // after the last row, on every path)
-  const int tcols = a.grad != nullptr ? a.tmem_cols : 0;
-  if (warp == 0) {
+  const int tcols = kTmem && a.grad != nullptr ? a.tmem_cols : 0;
+  if (kTmem && warp == 0) {
     if (tcols) tmem_alloc(&s_tmem, (uint32_t)tcols);
     tmem_relinquish();
   }
@@ -409,7 +414,8 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(cons
       sr.init();
       const uint32_t tb = tmem_thread_base(s_tmem, s_tb_cols);
       const int tmv = lse_pair<T>(x, y, a.V, sp, sr, want_grad ? keep : stream, stream,
-                                  want_grad ? s_keep : nullptr, tb, (int)s_tb_cols / 4);
+                                  want_grad ? s_keep : nullptr, tb,
+                                  kTmem ? (int)s_tb_cols / 4 : 0);
       float Mp, Mr;
       FF Zp = {0.f, 0.f}, Zr = {0.f, 0.f};
       combine_ff(sp, sr, s_f, s_zs, Mp, Mr, Zp, Zr);
@@ -470,7 +476,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(cons
     const unsigned n_clip[3] = {s_clip[0], s_clip[1], s_clip[2]};
     add_clip_counts(a.hdr, n_clip);
   }
-  if (s_tb_cols) {  // every thread's tensor-memory loads were waited for
+  if (kTmem && s_tb_cols) {  // every thread's tensor-memory loads were waited for
     tmem_fence_before_sync();
     __syncthreads();
     tmem_fence_after_sync();
@@ -754,23 +760,24 @@ static cudaError_t resident_ctas(const void* kernel, int threads, int dyn_smem, 
   return cudaSuccess;
 }
 
-template <typename T>
-static cudaError_t launch_t(const RowArgs& a, const grpo_profile_t* prof, cudaStream_t s) {
+template <typename T, bool kTmem>
+static cudaError_t launch_rows_kernel(const RowArgs& a, int tmem_cols, const grpo_profile_t* prof,
+                                      cudaStream_t s) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
-  e = cudaFuncSetAttribute(rows_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(rows_kernel<T, kTmem>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kPolicySmemBytes);
   if (e != cudaSuccess) return e;
   int per_sm = 0, carveout = 0;
-  e = resident_ctas((const void*)rows_kernel<T>, kRowThreads, kPolicySmemBytes, dev, &per_sm,
-                    &carveout);
+  e = resident_ctas((const void*)rows_kernel<T, kTmem>, kRowThreads, kPolicySmemBytes, dev,
+                    &per_sm, &carveout);
   if (e != cudaSuccess) return e;
   // the shared-memory share of the SM's L1 that those CTAs need, and no more
   // (the largest carveout measured about 9 % slower on the row kernel)
-  e = cudaFuncSetAttribute(rows_kernel<T>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(rows_kernel<T, kTmem>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            carveout);
   if (e != cudaSuccess) return e;
   int64_t grid = (int64_t)sms * per_sm;
@@ -778,16 +785,29 @@ static cudaError_t launch_t(const RowArgs& a, const grpo_profile_t* prof, cudaSt
   if (grid > rows) grid = rows;
   // the resident CTAs of an SM must fit its 512 tensor-memory columns
   // together, or an allocation would wait for another CTA to exit
-  // (and only rows long enough to reach the tensor-memory slice allocate it)
   RowArgs ka = a;
-  const bool long_rows =
-      a.V * (int64_t)sizeof(T) >= (int64_t)16 * kRowThreads * (kSmemJ + kTmemVecs + kPairUnroll);
-  ka.tmem_cols = (long_rows && per_sm * kTmemCols <= 512) ? kTmemCols : 0;
+  ka.tmem_cols = (kTmem && per_sm * tmem_cols <= 512) ? tmem_cols : 0;
   if (prof && prof->start) cudaEventRecord((cudaEvent_t)prof->start, s);
-  rows_kernel<T><<<(unsigned)grid, kRowThreads, kPolicySmemBytes, s>>>(ka);
+  rows_kernel<T, kTmem><<<(unsigned)grid, kRowThreads, kPolicySmemBytes, s>>>(ka);
   e = cudaGetLastError();
   if (prof && prof->stop) cudaEventRecord((cudaEvent_t)prof->stop, s);
   return e;
+}
+
+template <typename T>
+static cudaError_t launch_t(const RowArgs& a, const grpo_profile_t* prof, cudaStream_t s) {
+  // only rows long enough to reach the tensor-memory slice (and only calls
+  // that write a gradient) take the instantiation that allocates it
+  const bool long_rows =
+      a.V * (int64_t)sizeof(T) >= (int64_t)16 * kRowThreads * (kSmemJ + kTmemVecs + kPairUnroll);
+  const bool slice = long_rows && a.grad != nullptr;
+  if constexpr (sizeof(T) == 4) {
+    // fp32 rows keep one instantiation (the plain one spilled registers)
+    return launch_rows_kernel<T, true>(a, slice ? kTmemCols : 0, prof, s);
+  } else {
+    if (slice) return launch_rows_kernel<T, true>(a, kTmemCols, prof, s);
+    return launch_rows_kernel<T, false>(a, 0, prof, s);
+  }
 }
 
 cudaError_t launch_rows(const RowArgs& a, grpo_dtype_t dt, const grpo_profile_t* prof,
