@@ -45,7 +45,25 @@ PROFILES = {
     "fused": ("rows_kernel_fused.md",
               ("grpo_rows.cu", "grpo_rows_common.cuh", "grpo_internal.cuh")),
     "logps": ("logps_kernel_logps.md", ("grpo_logps.cu", "grpo_internal.cuh")),
+    "large_vocab/gspo": ("gspo_kernels_large_vocab.md",
+                         ("grpo_rows.cu", "grpo_rows_common.cuh", "grpo_internal.cuh",
+                          "grpo_reduce.cu")),
 }
+
+
+def profile_key(w, variant: str = "default", skip_masked: bool = False, tp: int = 0) -> str:
+    """The committed profile a bench line's traffic comes from.  On the logits
+    path the loss variants run the same row kernel and move the same bytes,
+    except GSPO (two passes); the masked-row mode and the vocabulary-parallel
+    path move other bytes; the logps path's variants run another kernel
+    instantiation."""
+    if tp:
+        return f"{w.name}/tp{tp}"
+    if skip_masked:
+        return f"{w.name}/skip_masked"
+    if variant == "gspo" or (w.V == 0 and variant != "default"):
+        return f"{w.name}/{variant}"
+    return w.name
 
 
 def source_hash(files) -> str:
@@ -66,7 +84,7 @@ def profiled_traffic(workload: str):
         return None
     text = open(path).read()
     src = re.search(r"kernel_source_sha:\s*(\w+)", text)
-    wl = re.search(r"workload:\s*(\w+)", text)
+    wl = re.search(r"workload:\s*([\w/]+)", text)
     tb = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     if not (src and wl and tb) or src.group(1) != source_hash(files) or wl.group(1) != workload:
         return None
@@ -719,7 +737,9 @@ def run_gpu(args, w, ws, rank, local):
         "data": "synthetic", "config": dict(workload_config(w, args.variant, args.skip_masked),
                                             **({"vocab_slices": args.tp} if args.tp else {})),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": profiled_traffic(w.name),
+                     "frac": achieved / peak,
+                     "traffic": profiled_traffic(profile_key(w, args.variant,
+                                                             args.skip_masked, args.tp)),
                      "kernel": case.kernel, "peak_source": f"{peak_kind} hbm_gbs",
                      "bytes_per_launch": case.alg_bytes, "avg_launch_ms": kern_avg_s * 1e3,
                      **({"strict_frac": case.extra_bytes["strict_bytes_per_launch"] / kern_avg_s
