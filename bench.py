@@ -83,9 +83,9 @@ def profiled_traffic(workload: str):
     if not os.path.exists(path):
         return None
     text = open(path).read()
-    src = re.search(r"kernel_source_sha:\s*(\w+)", text)
-    wl = re.search(r"workload:\s*([\w/]+)", text)
-    tb = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    src = re.search(r"^kernel_source_sha:\s*(\w+)", text, re.M)
+    wl = re.search(r"^workload:\s*([\w/]+)", text, re.M)
+    tb = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
     if not (src and wl and tb) or src.group(1) != source_hash(files) or wl.group(1) != workload:
         return None
     return float(tb.group(1))
