@@ -59,3 +59,23 @@ def test_active_runs_cover_exactly_the_active_slots():
             cover[b:e] = True
             last = e
         assert np.array_equal(cover, mask.reshape(-1) != 0)
+
+
+def test_committed_profiles_name_their_own_key():
+    # every profile bench.py may take a traffic figure from exists and names
+    # the key it is filed under; masked-row and vocabulary-parallel lines never
+    # borrow the fused path's figure
+    import os
+    import re
+    import bench
+    import synth
+    for key, (name, files) in bench.PROFILES.items():
+        text = open(os.path.join(bench.ROOT, "profiles", name)).read()
+        assert re.search(r"^workload:\s*([\w/]+)", text, re.M).group(1) == key
+        assert re.search(r"^traffic_bytes_per_launch:\s*[0-9.eE+]+", text, re.M)
+        assert re.search(r"^kernel_source_sha:\s*\w+", text, re.M)
+    w = synth.WORKLOADS["large_vocab"]
+    assert bench.profile_key(w, skip_masked=True) not in bench.PROFILES
+    assert bench.profile_key(w, tp=2) not in bench.PROFILES
+    assert bench.profile_key(w, "k2") == "large_vocab"
+    assert bench.profile_key(synth.WORKLOADS["logps"], "k2") not in bench.PROFILES
