@@ -119,20 +119,6 @@ template <> struct Storage<__half> {
   __device__ static void store1(__half* p, float f) { *p = __float2half_rn(f); }
 };
 
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ void st_stream(void* p, const uint4& v) {
-  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
 // L2 eviction-priority policies (createpolicy) and loads / stores that carry
 // them: rows that will be read again are kept (evict_last), rows read or
 // written for the last time go first (evict_first).
@@ -360,17 +346,6 @@ __device__ __forceinline__ void block_sum(T (&v)[K], T* scratch) {
     T x = lane < nw ? scratch[k * 32 + lane] : T(0);
     v[k] = warp_sum(x);
   }
-}
-
-__device__ __forceinline__ float block_max(float v, float* scratch) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nw = (blockDim.x + 31) >> 5;
-  v = warp_max(v);
-  __syncthreads();
-  if (lane == 0) scratch[warp] = v;
-  __syncthreads();
-  float x = lane < nw ? scratch[lane] : -INFINITY;
-  return warp_max(x);
 }
 
 // ----------------------------------------------------------------------------

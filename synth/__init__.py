@@ -271,15 +271,6 @@ class Workload:
         return out
 
 
-def host_array_to_torch(a: np.ndarray, dtype: str):
-    """numpy host array (float32, or uint16 holding bf16 bits) -> torch CPU tensor."""
-    import torch
-    t = torch.from_numpy(np.ascontiguousarray(a))
-    if dtype == "bf16":
-        return t.view(torch.bfloat16)
-    return t
-
-
 # The five workloads of the fused GRPO loss benchmark.
 WORKLOADS = {
     # 2 prompts x 4 samples, T=16, V=64, fp32 logits ~N(0,1)

@@ -39,9 +39,3 @@ def _ensure_built():
 
 
 _ensure_built()
-
-
-@pytest.fixture(scope="session")
-def cuda_available():
-    import torch
-    return torch.cuda.is_available()
