@@ -372,6 +372,7 @@ def workload_config(w: synth.Workload, variant: str = "default",
     note = l2_note(w)
     cfg = {"workload": f"{w.name}: B={w.B} T={w.T}" + (f" V={w.V} {w.dtype}" if w.V else " logps f32"),
            "B": w.B, "T": w.T, "V": w.V or None, "active_tokens": act,
+           "storage_dtype": w.dtype if w.V else "f32",
            "samples_per_prompt": w.samples_per_prompt or None,
            "reduction": ["token_mean", "sequence_mean"][w.reduction],
            "parallelism": "replicas", "l2": note,
@@ -733,7 +734,9 @@ def run_gpu(args, w, ws, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype if w.V else "f32",
+        # the arithmetic type of the path (fp32 with float-pair and fp64 steps; the
+        # logits' storage type is in config["storage_dtype"])
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": dict(workload_config(w, args.variant, args.skip_masked),
                                             **({"vocab_slices": args.tp} if args.tp else {})),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
