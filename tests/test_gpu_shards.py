@@ -115,7 +115,7 @@ LOGPS = synth.WORKLOADS["logps"].with_(name="logps_shards", B=12, T=64, len_rang
                                       beta=0.1)
 
 
-def _sharded_logps(t, w, sizes, opts):
+def _sharded_logps(t, w, sizes, opts, flags=0):
     parts = _bounds(sizes)
     counts = [g.grpo_count_active(t["mask"][a:b]) for a, b in parts]
     global_counts = torch.stack(counts).sum(0)
@@ -125,7 +125,8 @@ def _sharded_logps(t, w, sizes, opts):
         res = g.grpo_loss_from_logps(t["lp"][a:b], t["old"][a:b], t["ref"][a:b], t["mask"][a:b],
                                      t["R"], samples_per_prompt=w.samples_per_prompt,
                                      clip_eps=w.eps_lo, clip_eps_hi=w.eps_hi, beta=w.beta,
-                                     shard=g.Shard(a, global_counts, tot), **opts)
+                                     shard=g.Shard(a, global_counts, tot), extra_flags=flags,
+                                     **opts)
         grads.append(res["grad"])
         totals.append(tot)
     all_totals = torch.cat(totals)
@@ -155,6 +156,10 @@ def test_logps_shards_are_bitwise_identical(T, opt):
         got = _sharded_logps(t, w, sizes, opts)
         for k in ("out3", "grad", "totals"):
             assert torch.equal(got[k], ref_run[k]), (name, k)
+    # the shards' advantages and counts from the separate pass: the same bits
+    got = _sharded_logps(t, w, PARTITIONS["straddle"], opts, flags=g.GRPO_FLAG_SEPARATE_PREP)
+    for k in ("out3", "grad", "totals"):
+        assert torch.equal(got[k], ref_run[k]), ("separate pass", k)
 
 
 def test_count_active_matches_the_mask():
