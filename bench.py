@@ -91,6 +91,11 @@ def profiled_traffic(workload: str):
     return float(tb.group(1))
 
 
+# GB300's nominal HBM3e bandwidth (~8 TB/s); the roofline fraction is taken
+# against the measured copy rate, and against this figure beside it
+NOMINAL_HBM_GBS = 8000.0
+
+
 def measured_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -444,8 +449,11 @@ class LogitsCase:
                                  grad=self.grad, out3=self.out3, workspace=self.wsp, profile=prof,
                                  **self.kw)
 
-    e2e_copy = ("the logits rows the call reads (runs of active tokens, found from the host "
-                "mask inside each step: masked rows are never read), the other inputs whole")
+    e2e_copy = ("in: the logits rows the call reads (runs of active tokens, found from the "
+                "host mask inside each step: masked rows are never read), the other inputs "
+                "whole; out: the loss outputs and the gradient rows of the active tokens into a "
+                "pinned host gradient buffer (the masked rows' gradient is zero by contract: "
+                "the host buffer is zeroed once before the timed steps)")
 
     def e2e_setup(self):
         import torch
@@ -461,16 +469,36 @@ class LogitsCase:
             self.kw_e["group_boundaries"] = self.dev_in["bounds"]
         self.loss_host = torch.empty(3, dtype=torch.float32).pin_memory()
         self.mask_host = self.host["mask"].numpy()
-        rows = sum(e - b for b, e in active_runs(self.mask_host))
+        self.runs = active_runs(self.mask_host)
+        self.grad_host = torch.zeros(self.grad.shape, dtype=self.grad.dtype, pin_memory=True)
+        rows = sum(e - b for b, e in self.runs)
         row_bytes = self.w.V * self.host["X"].element_size()
-        return 2 * rows * row_bytes + sum(self.host[k].numel() * self.host[k].element_size()
-                                          for k in ("acts", "old", "mask", "R"))
+        h2d = 2 * rows * row_bytes + sum(self.host[k].numel() * self.host[k].element_size()
+                                         for k in ("acts", "old", "mask", "R"))
+        return h2d, rows * row_bytes + 12
+
+    def e2e_check(self):
+        """The host gradient's active rows equal the device gradient's (sampled
+        rows), and its masked rows are still zero."""
+        import torch
+        V = self.w.V
+        act = np.flatnonzero(self.mask_host.reshape(-1))
+        rng = np.random.default_rng(1)
+        pick = np.unique(np.concatenate([act[:4], act[-4:], rng.choice(act, min(64, len(act)),
+                                                                      replace=False)]))
+        dev_rows = self.grad.view(-1, V)[torch.as_tensor(pick, device=self.grad.device)].cpu()
+        if not torch.equal(dev_rows, self.grad_host.view(-1, V)[torch.as_tensor(pick)]):
+            raise RuntimeError("the end-to-end gradient rows differ from the device's")
+        masked = np.flatnonzero(self.mask_host.reshape(-1) == 0)
+        if len(masked) and bool(self.grad_host.view(-1, V)[torch.as_tensor(masked[:64])].any()):
+            raise RuntimeError("masked rows of the host gradient are not zero")
 
     def e2e_step(self):
         d, h, V = self.dev_in, self.host, self.w.V
         xd, yd = d["X"].view(-1, V), d["Y"].view(-1, V)
         xh, yh = h["X"].view(-1, V), h["Y"].view(-1, V)
-        for b, e in active_runs(self.mask_host):
+        runs = active_runs(self.mask_host)
+        for b, e in runs:
             xd[b:e].copy_(xh[b:e], non_blocking=True)
             yd[b:e].copy_(yh[b:e], non_blocking=True)
         for k in ("acts", "old", "mask", "R"):
@@ -478,6 +506,9 @@ class LogitsCase:
         self.g.grpo_loss_fwd_bwd(d["X"], d["Y"], d["acts"], d["old"], d["mask"], d["R"],
                                  grad=self.grad, out3=self.out3, workspace=self.wsp, **self.kw_e)
         self.loss_host.copy_(self.out3, non_blocking=True)
+        gd, gh = self.grad.view(-1, V), self.grad_host.view(-1, V)
+        for b, e in runs:
+            gh[b:e].copy_(gd[b:e], non_blocking=True)
 
 
 class VocabCase:
@@ -534,7 +565,9 @@ class VocabCase:
             prof[1].record()
         self.out3 = res["out3"]
 
-    e2e_copy = LogitsCase.e2e_copy
+    e2e_copy = ("in: every slice's logits rows the calls read (runs of active tokens), the "
+                "other inputs whole; out: the loss outputs and every slice's gradient rows of the "
+                "active tokens into pinned host buffers (masked rows are zero by contract)")
 
     def e2e_setup(self):
         import torch
@@ -548,9 +581,20 @@ class VocabCase:
         self.dev_small = {k: torch.empty_like(self.inp[k]) for k in self.small}
         self.loss_host = torch.empty(3, dtype=torch.float32).pin_memory()
         self.mask_host = self.host_small["mask"].numpy()
+        self.grads_host = [torch.zeros(t.shape, dtype=t.dtype, pin_memory=True)
+                           for t in self.grads]
         rows = sum(e - b for b, e in active_runs(self.mask_host))
-        return (rows * sum(t.shape[-1] * t.element_size() for t in self.host)
-                + sum(t.numel() * t.element_size() for t in self.host_small.values()))
+        h2d = (rows * sum(t.shape[-1] * t.element_size() for t in self.host)
+               + sum(t.numel() * t.element_size() for t in self.host_small.values()))
+        return h2d, rows * sum(t.shape[-1] * t.element_size() for t in self.grads) + 12
+
+    def e2e_check(self):
+        import torch
+        act = np.flatnonzero(self.mask_host.reshape(-1))[:64]
+        for gd, gh in zip(self.grads, self.grads_host):
+            a = gd.view(-1, gd.shape[-1])[torch.as_tensor(act, device=gd.device)].cpu()
+            if not torch.equal(a, gh.view(-1, gh.shape[-1])[torch.as_tensor(act)]):
+                raise RuntimeError("the end-to-end gradient rows differ from the device's")
 
     def e2e_step(self):
         n = len(self.Xs)
@@ -565,6 +609,10 @@ class VocabCase:
         self.inp = dict(self.inp, **self.dev_small)
         self.step()
         self.loss_host.copy_(self.out3, non_blocking=True)
+        for gd, gh in zip(self.grads, self.grads_host):  # every slice's active gradient rows
+            dv, hv = gd.view(-1, gd.shape[-1]), gh.view(-1, gh.shape[-1])
+            for b, e in runs:
+                hv[b:e].copy_(dv[b:e], non_blocking=True)
 
 
 class LogpsCase:
@@ -628,13 +676,24 @@ class LogpsCase:
             self.host[k].copy_(v)
         self.dev_in = {k: torch.empty_like(v) for k, v in self.inp.items()}
         self.loss_host = torch.empty(3, dtype=torch.float32).pin_memory()
-        return sum(v.numel() * v.element_size() for v in self.host.values())
+        self.grad_host = torch.empty(self.grad.shape, dtype=torch.float32, pin_memory=True)
+        return (sum(v.numel() * v.element_size() for v in self.host.values()),
+                self.grad_host.numel() * 4 + 12)
+
+    e2e_copy = ("in: every input whole; out: the loss outputs and dL/dlogp of every slot "
+                "into pinned host memory")
 
     def e2e_step(self):
         for k in self.host:
             self.dev_in[k].copy_(self.host[k], non_blocking=True)
         self._call(self.dev_in)
         self.loss_host.copy_(self.out3, non_blocking=True)
+        self.grad_host.copy_(self.dev_in["grad"], non_blocking=True)
+
+    def e2e_check(self):
+        import torch
+        if not torch.equal(self.grad_host, self.inp["grad"].cpu()):
+            raise RuntimeError("the end-to-end dL/dlogp differs from the device-resident steps'")
 
 
 def head_start(device, seconds: float):
@@ -696,12 +755,22 @@ def run_gpu(args, w, ws, rank, local):
     hs = head_start(device, 2.0 * host_per_step * args.steps + 1e-3)
     for k in range(args.steps):
         case.step(k, kev[k])
+    # and once more with an event between consecutive steps: the spread of
+    # the step times (the headline stays the event-free first pass)
+    sev = [ev() for _ in range(args.steps + 1)]
+    torch.cuda.synchronize(device)
+    hs = head_start(device, 2.0 * host_per_step * args.steps + 1e-3)
+    sev[0].record(stream)
+    for k in range(args.steps):
+        case.step(k)
+        sev[k + 1].record(stream)
     torch.cuda.synchronize(device)
     barrier(ws)
     clk = clocks.stop() if rank == 0 else None
     del hs
     elapsed_ms = e_start.elapsed_time(e_stop)
     kernel_ms = [a.elapsed_time(b) for a, b in kev]
+    step_ms = [a.elapsed_time(b) for a, b in zip(sev[:-1], sev[1:])]
     elapsed_ms = max_over_ranks(elapsed_ms, ws, device)
     ms_per_step = elapsed_ms / args.steps
     value = aggregate_value(case.active, args.steps, ws, elapsed_ms)
@@ -709,7 +778,7 @@ def run_gpu(args, w, ws, rank, local):
     # ---- end to end: pinned host inputs -> device -> loss -> host ----
     e2e_steps = min(args.e2e_steps, args.steps)
     resident_out3 = case.out3.clone()  # the loss of the device-resident steps
-    h2d = case.e2e_setup()
+    h2d, d2h = case.e2e_setup()
     case.e2e_step()
     torch.cuda.synchronize(device)
     barrier(ws)
@@ -724,6 +793,9 @@ def run_gpu(args, w, ws, rank, local):
     e2e_value = aggregate_value(case.active, e2e_steps, ws, e2e_ms)
     if not torch.equal(case.out3, resident_out3):  # the same inputs, copied in
         raise RuntimeError("the end-to-end steps' loss differs from the device-resident steps'")
+    if not torch.equal(case.loss_host, resident_out3.cpu()):
+        raise RuntimeError("the loss read back to the host differs from the device's")
+    case.e2e_check()
 
     if rank != 0:
         barrier(ws)
@@ -739,8 +811,13 @@ def run_gpu(args, w, ws, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": dict(workload_config(w, args.variant, args.skip_masked),
                                             **({"vocab_slices": args.tp} if args.tp else {})),
+        "median_ms": statistics.median(step_ms), "min_ms": min(step_ms),
+        "max_ms": max(step_ms),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
+                     "nominal_peak": NOMINAL_HBM_GBS, "frac_vs_nominal": achieved / NOMINAL_HBM_GBS,
+                     "launch_ms": {"median": statistics.median(kernel_ms),
+                                   "min": min(kernel_ms), "max": max(kernel_ms)},
                      "traffic": profiled_traffic(profile_key(w, args.variant,
                                                              args.skip_masked, args.tp)),
                      "kernel": case.kernel, "peak_source": f"{peak_kind} hbm_gbs",
@@ -749,7 +826,7 @@ def run_gpu(args, w, ws, rank, local):
                          / 1e9 / peak, **case.extra_bytes} if case.extra_bytes else {})},
         "step_gbs_algorithmic": case.alg_bytes / (ms_per_step / 1e3) / 1e9,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": 12, "steps": e2e_steps,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 **({"copies": case.e2e_copy} if getattr(case, "e2e_copy", None) else {})},
         "gpu_launches": case.launches_per_step * args.steps,
         "clocks": clk,

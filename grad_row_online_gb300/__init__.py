@@ -240,6 +240,35 @@ def _check(code: int, what: str):
         raise GrpoError(code, what)
 
 
+def _check_logits_call(policy_logits, ref_logits, action_ids, old_logps, completion_mask,
+                       rewards, sharded: bool):
+    """Device, dtype, layout and shape checks shared by the logits entry
+    points; returns (B, T, V, mask as uint8)."""
+    if not isinstance(policy_logits, torch.Tensor) or policy_logits.dtype not in _DTYPES:
+        raise ValueError(f"unsupported logits dtype {getattr(policy_logits, 'dtype', None)}")
+    _dev(policy_logits, "policy_logits")
+    _dev(ref_logits, "ref_logits", policy_logits.dtype)
+    if policy_logits.dim() != 3 or ref_logits.shape != policy_logits.shape:
+        raise ValueError("policy_logits and ref_logits must both be [B, T, V]")
+    B, T, V = policy_logits.shape
+    _dev(action_ids, "action_ids", torch.int64)
+    _dev(old_logps, "old_logps", torch.float32)
+    _dev(rewards, "rewards", torch.float32)
+    mask = _dev(completion_mask, "completion_mask")
+    if mask.dtype == torch.bool:
+        mask = mask.view(torch.uint8)
+    elif mask.dtype != torch.uint8:
+        raise ValueError("completion_mask must be bool or uint8")
+    if action_ids.shape != (B, T) or old_logps.shape != (B, T) or mask.shape != (B, T):
+        raise ValueError("action_ids, old_logps and completion_mask must be [B, T]")
+    if not sharded and rewards.shape != (B,):
+        raise ValueError("rewards must be [B]")
+    devs = {t.device for t in (ref_logits, action_ids, old_logps, rewards, mask)}
+    if devs != {policy_logits.device}:
+        raise ValueError("every tensor must be on the device of policy_logits")
+    return B, T, V, mask
+
+
 # --------------------------------------------------------------------------
 def grpo_group_adv(rewards: torch.Tensor, *, samples_per_prompt: int = 0, group_boundaries=None,
                    adv_eps: float = 1e-6, eps_add: bool = False, out: Optional[torch.Tensor] = None,
@@ -285,25 +314,8 @@ def grpo_loss_fwd_bwd(policy_logits: torch.Tensor, ref_logits: torch.Tensor,
     upper bound, at the lower bound, by the dual clip).  With ``shard``
     (see ``Shard``) ``rewards`` and the groups span the whole batch, the
     token tensors the shard's sequences, and ``out3`` is not written."""
-    if policy_logits.dtype not in _DTYPES:
-        raise ValueError(f"unsupported logits dtype {policy_logits.dtype}")
-    _dev(policy_logits, "policy_logits")
-    _dev(ref_logits, "ref_logits", policy_logits.dtype)
-    if policy_logits.dim() != 3 or ref_logits.shape != policy_logits.shape:
-        raise ValueError("policy_logits and ref_logits must both be [B, T, V]")
-    B, T, V = policy_logits.shape
-    _dev(action_ids, "action_ids", torch.int64)
-    _dev(old_logps, "old_logps", torch.float32)
-    _dev(rewards, "rewards", torch.float32)
-    mask = _dev(completion_mask, "completion_mask")
-    if mask.dtype == torch.bool:
-        mask = mask.view(torch.uint8)
-    elif mask.dtype != torch.uint8:
-        raise ValueError("completion_mask must be bool or uint8")
-    if action_ids.shape != (B, T) or old_logps.shape != (B, T) or mask.shape != (B, T):
-        raise ValueError("action_ids, old_logps and completion_mask must be [B, T]")
-    if shard is None and rewards.shape != (B,):
-        raise ValueError("rewards must be [B]")
+    B, T, V, mask = _check_logits_call(policy_logits, ref_logits, action_ids, old_logps,
+                                       completion_mask, rewards, shard is not None)
     dev = policy_logits.device
     g, keep = _groups(rewards.numel() if shard is not None else B, samples_per_prompt,
                       group_boundaries)
@@ -348,10 +360,24 @@ def grpo_loss_fwd_bwd_static(policy_logits: torch.Tensor, ref_logits: torch.Tens
     """grpo_loss_fwd_bwd with the library's fixed scratch memory instead of a
     workspace, for callers that cannot allocate device memory at the call
     (e.g. inside CUDA graph capture).  Every output is caller-provided:
-    `out3` ([3] f32) and, optionally, `grad` (like policy_logits).  Returns
+    `out3` ([3] f32) and, optionally, `grad` (like policy_logits);
+    `group_boundaries`, if given, must already be an int64 device tensor.
+    The arguments are checked as in grpo_loss_fwd_bwd (ValueError).  Returns
     the status code (0 = ok); nothing is allocated by this call."""
-    B, T, V = policy_logits.shape
-    mask = completion_mask.view(torch.uint8) if completion_mask.dtype == torch.bool else completion_mask
+    B, T, V, mask = _check_logits_call(policy_logits, ref_logits, action_ids, old_logps,
+                                       completion_mask, rewards, False)
+    if out3 is None:
+        raise ValueError("out3 ([3] float32 on the device) is required")
+    _dev(out3, "out3", torch.float32)
+    if out3.shape != (3,) or out3.device != policy_logits.device:
+        raise ValueError("out3 must be [3] on the device of policy_logits")
+    if grad is not None:
+        _dev(grad, "grad", policy_logits.dtype)
+        if grad.shape != policy_logits.shape or grad.device != policy_logits.device:
+            raise ValueError("grad must have the shape and device of policy_logits")
+    if group_boundaries is not None and not isinstance(group_boundaries, torch.Tensor):
+        raise ValueError("group_boundaries must be an int64 device tensor here (a list would "
+                         "need an allocation and a host-to-device copy)")
     g, keep = _groups(B, samples_per_prompt, group_boundaries)
     p, prof = _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction,
                       GRPO_ADV_EPS_ADD if eps_add else 0, None)

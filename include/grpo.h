@@ -285,12 +285,15 @@ grpo_status_t grpo_loss_from_logps(const float *logps, const float *old_logps,
  * device image, present on every GPU that loads the library until the
  * process exits.  Sizes whose grpo_workspace_size(B, T, 0) exceeds 4.5 MiB
  * are rejected with GRPO_ERR_WORKSPACE (any B <= 8192 with B*T <= 262144
- * fits).  No device memory is allocated.
- * The first call on a device looks the array's device address up (once per
- * device, with that device current); make that first call before any stream
- * capture.  All calls share the array: calls whose GPU work may overlap
- * (other streams or threads without ordering between them) race on it and
- * must be serialised by the caller. */
+ * fits); in a shard call (grpo_params_t.shard) the limit applies to the
+ * whole batch, grpo_workspace_size(groups->num_seqs, T, 0).  No device
+ * memory is allocated.
+ * The first call in a device's context looks the array's device address up
+ * (with that device current) and keeps it for that context; make that first
+ * call before any stream capture, and again after anything that replaces
+ * the context (cudaDeviceReset).  All calls share the array: calls whose GPU
+ * work may overlap (other streams or threads without ordering between them)
+ * race on it and must be serialised by the caller. */
 grpo_status_t grpo_loss_fwd_bwd_static(const void *policy_logits, const void *ref_logits,
                                        grpo_dtype_t dt, int64_t B, int64_t T, int64_t V,
                                        const int64_t *action_ids, const float *old_logps,

@@ -174,9 +174,10 @@ def lse_vocab_parallel(rows, dtype: str, bounds) -> np.ndarray:
     return lse
 
 
-def grad_rows(rows, dtype: str, actions, lse, w, out_dtype: str | None = None):
+def grad_rows(rows, dtype: str, actions, lse, w, out_dtype: str | None = None,
+              want_f64: bool = True):
     """dL/dlogits for the given rows.  Returns (rounded storage array,
-    unrounded float64 array)."""
+    unrounded float64 array, or None when want_f64 is False)."""
     out_dtype = out_dtype or dtype
     rows = _c(rows, _storage_np(dtype))
     n, V = rows.shape
@@ -184,7 +185,7 @@ def grad_rows(rows, dtype: str, actions, lse, w, out_dtype: str | None = None):
     l = _c(lse, np.float64)
     wd = _c(w, np.float64)
     out = np.empty((n, V), dtype=_storage_np(out_dtype))
-    f64 = np.empty((n, V), dtype=np.float64)
+    f64 = np.empty((n, V), dtype=np.float64) if want_f64 else None
     lib().oracle_grad_rows(_p(rows), DTYPE_CODE[dtype], n, V, _p(a), _p(l), _p(wd),
                            DTYPE_CODE[out_dtype], _p(out), _p(f64))
     return out, f64

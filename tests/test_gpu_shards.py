@@ -4,14 +4,19 @@ emulated as K "ranks" on one GPU, each with its own workspace -- gives
 bit-identical gradients, per-sequence totals and loss outputs to the
 unsharded call, for every K, with advantage groups straddling shards.  The
 exchange is what the page describes: the active-token counts gathered as
-integers, the per-sequence totals concatenated in shard order."""
+integers, the per-sequence totals concatenated in shard order.  The same
+page's claim is also that this common result is the loss: every partition's
+loss outputs, per-sequence totals, clip counts and gradients are compared
+with the oracle as well."""
 import numpy as np
 import pytest
 import torch
 
 import grad_row_online_gb300 as g
+import oracle
 import synth
-from workload_inputs import make_case, to_device
+from workload_inputs import (assert_grad_rows, assert_scalar, make_case, to_device,
+                             torch_storage)
 
 pytestmark = pytest.mark.gpu
 
@@ -46,6 +51,54 @@ OPTIONS = {
                           dual_clip_c=1.4),
     "gspo": dict(reduction="sequence_mean", ratio_level="sequence"),
 }
+
+
+_RED = {"token_mean": oracle.TOKEN_MEAN, "sequence_mean": oracle.SEQUENCE_MEAN,
+        "fixed_constant": oracle.FIXED_CONSTANT}
+
+
+def _oracle_kw(opts: dict) -> dict:
+    kw = {k: opts[k] for k in ("kl", "dual_clip_c", "norm_constant", "ratio_level") if k in opts}
+    kw["reduction"] = _RED[opts.get("reduction", "token_mean")]
+    return kw
+
+
+def _near_clip(exp, w, opts, band=1e-6):
+    """Tokens whose oracle ratio is within `band` (relative) of a clip bound:
+    either branch's gradient is a correct reading there."""
+    r = exp["ratio"]
+    near = np.zeros(r.shape, bool)
+    for b in (1.0 - float(np.float32(w.eps_lo)), 1.0 + float(np.float32(w.eps_hi)),
+              float(np.float32(opts["dual_clip_c"])) if opts.get("dual_clip_c") else None):
+        if b is not None:
+            near |= np.abs(r - b) <= band * b
+    return near
+
+
+def _check_against_oracle(got, exp, near, what, dtype=None):
+    """One partition's results against the oracle: the loss outputs (1e-5
+    relative), per-sequence totals, clip counts (tokens at a clip kink may
+    count either way) and every gradient element (1 ulp + 1e-9; logits
+    gradients of dtype `dtype`, else the f32 dL/dlogp)."""
+    out = got["out3"].cpu().numpy().astype(np.float64)
+    for i, k in enumerate(("loss", "policy_loss", "kl")):
+        assert_scalar(out[i], exp[k], f"{what} {k}")
+    if got.get("per_seq") is not None:
+        ps = got["per_seq"].cpu().numpy().astype(np.float64)
+        assert np.allclose(ps[0], exp["per_seq_policy"], rtol=1e-5, atol=1e-6), what
+        assert np.allclose(ps[1], exp["per_seq_kl"], rtol=1e-5, atol=1e-7), what
+        assert np.array_equal(ps[2], exp["per_seq_active"]), what
+    if got.get("clips") is not None:
+        c = got["clips"].cpu().numpy()
+        assert np.all(np.abs(c - exp["clip_counts"]) <= near.sum()), (what, c, exp["clip_counts"])
+    if dtype is not None:
+        assert_grad_rows(torch_storage(got["grad"])[~near], exp["grad"][~near], dtype,
+                         what=f"{what} grad")
+    else:
+        want = exp["w"].astype(np.float32)
+        gw = got["grad"].cpu().numpy()
+        ok = np.abs(gw.astype(np.float64) - want) <= np.spacing(np.abs(want)) + 1e-9
+        assert np.all(ok | near), (what, np.argwhere(~(ok | near))[:5])
 
 
 def _bounds(sizes):
@@ -104,10 +157,14 @@ def test_logits_shards_are_bitwise_identical(dtype, opt, V):
     assert torch.equal(ref["per_seq"], whole["per_seq"])
     assert torch.equal(ref["clips"], whole["clip_counts"])
     assert int(ref["counts"][0]) == int(case["mask"].sum())
+    exp = oracle.fused(case["X"], case["Y"], dtype, case["acts"], case["old"], case["mask"],
+                       case["R"], case["bounds"], w.eps_lo, w.eps_hi, w.beta, **_oracle_kw(opts))
+    near = _near_clip(exp, w, opts)
     for name, sizes in PARTITIONS.items():
         got = _sharded_logits(dev, w, sizes, opts)
         for k in ("out3", "grad", "per_seq", "totals", "clips", "counts"):
             assert torch.equal(got[k], ref[k]), (name, k)
+        _check_against_oracle(got, exp, near, f"{dtype} {opt} V={V} {name}", dtype)
 
 
 LOGPS = synth.WORKLOADS["logps"].with_(name="logps_shards", B=12, T=64, len_range=(0, 64),
@@ -119,22 +176,26 @@ def _sharded_logps(t, w, sizes, opts, flags=0):
     parts = _bounds(sizes)
     counts = [g.grpo_count_active(t["mask"][a:b]) for a, b in parts]
     global_counts = torch.stack(counts).sum(0)
-    grads, totals = [], []
+    grads, totals, per_seq, clips = [], [], [], []
     for a, b in parts:
         tot = g.totals_buffer(b - a)
         res = g.grpo_loss_from_logps(t["lp"][a:b], t["old"][a:b], t["ref"][a:b], t["mask"][a:b],
                                      t["R"], samples_per_prompt=w.samples_per_prompt,
                                      clip_eps=w.eps_lo, clip_eps_hi=w.eps_hi, beta=w.beta,
+                                     want_per_seq=True, want_clip_counts=True,
                                      shard=g.Shard(a, global_counts, tot), extra_flags=flags,
                                      **opts)
         grads.append(res["grad"])
         totals.append(tot)
+        per_seq.append(res["per_seq"])
+        clips.append(res["clip_counts"])
     all_totals = torch.cat(totals)
     out3 = g.grpo_loss_finalize(all_totals, global_counts, beta=w.beta,
                                 reduction=opts.get("reduction", "token_mean"),
                                 norm_constant=opts.get("norm_constant"))
     torch.cuda.synchronize()
-    return dict(out3=out3, grad=torch.cat(grads), totals=all_totals)
+    return dict(out3=out3, grad=torch.cat(grads), totals=all_totals,
+                per_seq=torch.cat(per_seq, dim=1), clips=torch.stack(clips).sum(0))
 
 
 @pytest.mark.parametrize("opt", list(OPTIONS))
@@ -152,13 +213,18 @@ def test_logps_shards_are_bitwise_identical(T, opt):
     ref_run = _sharded_logps(t, w, PARTITIONS["1"], opts)
     assert torch.equal(ref_run["out3"], whole["out3"])
     assert torch.equal(ref_run["grad"], whole["grad"])
+    A = oracle.group_advantages(host["R"], w.group_boundaries())
+    exp = oracle.loss_from_logps(lp, ref, old, host["mask"], A, w.eps_lo, w.eps_hi, w.beta,
+                                 **_oracle_kw(opts))
+    near = _near_clip(exp, w, opts)
     for name, sizes in PARTITIONS.items():
         got = _sharded_logps(t, w, sizes, opts)
-        for k in ("out3", "grad", "totals"):
+        for k in ("out3", "grad", "totals", "per_seq", "clips"):
             assert torch.equal(got[k], ref_run[k]), (name, k)
+        _check_against_oracle(got, exp, near, f"logps T={T} {opt} {name}")
     # the shards' advantages and counts from the separate pass: the same bits
     got = _sharded_logps(t, w, PARTITIONS["straddle"], opts, flags=g.GRPO_FLAG_SEPARATE_PREP)
-    for k in ("out3", "grad", "totals"):
+    for k in ("out3", "grad", "totals", "per_seq", "clips"):
         assert torch.equal(got[k], ref_run[k]), ("separate pass", k)
 
 
@@ -189,3 +255,6 @@ def test_dp_helper_single_rank_matches_the_plain_call():
     torch.cuda.synchronize()
     assert torch.equal(res["out3"], whole["out3"])
     assert torch.equal(res["grad"], whole["grad"])
+    exp = oracle.fused(case["X"], case["Y"], "bf16", case["acts"], case["old"], case["mask"],
+                       case["R"], case["bounds"], w.eps_lo, w.eps_hi, w.beta)
+    _check_against_oracle(res, exp, _near_clip(exp, w, {}), "dp helper", "bf16")

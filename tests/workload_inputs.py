@@ -28,8 +28,21 @@ def ulp(x: np.ndarray, dtype: str) -> np.ndarray:
     prec, emin = (8, -126) if dtype == "bf16" else (11, -14)
     with np.errstate(divide="ignore"):
         e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
-    e = np.maximum(e, emin)
+    # zero: the spacing of the subnormals, as for every value below 2^emin
+    e = np.where(a > 0, np.maximum(e, emin), emin)
     return np.ldexp(1.0, (e - (prec - 1)).astype(np.int64))
+
+
+_PREC = {"f32": (24, -126), "bf16": (8, -126), "f16": (11, -14)}
+
+
+def ulp_device(o: torch.Tensor, dtype: str) -> torch.Tensor:
+    """ulp() on the device: o holds float64 values exactly representable in
+    the storage dtype."""
+    prec, emin = _PREC[dtype]
+    _, e = torch.frexp(o.abs())  # |o| = m 2^e, m in [1/2, 1): floor(log2|o|) = e - 1
+    e = torch.where(o != 0, torch.clamp(e - 1, min=emin), torch.full_like(e, emin))
+    return torch.ldexp(torch.ones_like(o), (e - (prec - 1)).to(o.dtype))
 
 
 def storage_to_f64(a: np.ndarray, dtype: str) -> np.ndarray:
@@ -122,6 +135,40 @@ def assert_grad_rows(got: np.ndarray, want: np.ndarray, dtype: str, what: str = 
         raise AssertionError(f"{what}: {bad.sum()} elements out of tolerance, e.g. "
                              + ", ".join(f"{tuple(i)} gpu={g[tuple(i)]:.9g} oracle={o[tuple(i)]:.9g}"
                                          for i in idx))
+
+
+def assert_grad_rows_streamed(w: synth.Workload, X: torch.Tensor, grad: torch.Tensor,
+                              exp: dict, rows: np.ndarray, chunk: int = 256) -> int:
+    """Every element of the gradient rows `rows` (flat row indices) against
+    the oracle, |gpu - oracle_rounded| <= ulp_dtype(oracle_rounded) + 1e-9,
+    in chunks: the policy rows are copied to the host for the oracle, whose
+    rounded rows go back to the device for the comparison.  Returns the
+    number of elements checked."""
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[w.dtype]
+    Xf, Gf = X.view(-1, w.V), grad.view(-1, w.V)
+    wflat = exp["w"].reshape(-1)
+    n = 0
+    for i in range(0, len(rows), chunk):
+        r = rows[i:i + chunk]
+        idx = torch.as_tensor(r, device=X.device)
+        xs = torch_storage(Xf[idx])
+        want, _ = oracle.grad_rows(xs, w.dtype, exp["acts"][r], exp["lse"][r], wflat[r],
+                                   want_f64=False)
+        wt = torch.from_numpy(want).to(X.device)
+        if w.dtype != "f32":
+            wt = wt.view(tdt)
+        o = wt.to(torch.float64)
+        g = Gf[idx].to(torch.float64)
+        bad = (g - o).abs() > ulp_device(o, w.dtype) + 1e-9
+        if bool(bad.any()):
+            k = torch.nonzero(bad)[:5].cpu().numpy()
+            raise AssertionError(
+                f"{w.name} grad: {int(bad.sum())} elements out of tolerance in rows "
+                f"{r[0]}..{r[-1]}, e.g. " + ", ".join(
+                    f"row {r[a]} col {b} gpu={float(g[a, b]):.9g} oracle={float(o[a, b]):.9g}"
+                    for a, b in k))
+        n += len(r) * w.V
+    return n
 
 
 # ---------------------------------------------------------------------------
