@@ -332,7 +332,6 @@ extern "C" grpo_status_t grpo_loss_from_logps(const float* logps, const float* o
   int2* rng = (int2*)(w + lay.off_rng);
   const unsigned long long* NS = pl.NS ? pl.NS : &hdr->N;
   SeqTotal* totals = pl.shard ? pl.totals : (SeqTotal*)(w + lay.off_seq);
-  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return GRPO_ERR_CUDA;
   // one cooperative launch when the batch's CTAs fit the GPU at once, else
   // the separate advantage / count pass first
   bool fused = false;
@@ -341,6 +340,7 @@ extern "C" grpo_status_t grpo_loss_from_logps(const float* logps, const float* o
     if (logps_fused_capacity(&cap) != cudaSuccess) return GRPO_ERR_CUDA;
     fused = B <= cap;
   }
+  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return GRPO_ERR_CUDA;
   PrepArgs pa{rewards, bounds, B, T, G, pl.Bg, pl.seq_begin, &hdr->N, spp, params->adv_eps,
               (int)(params->flags & GRPO_ADV_EPS_ADD), completion_mask, 1, A, Aff, adv_out, L,
               rng, hdr};

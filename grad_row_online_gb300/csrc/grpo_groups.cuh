@@ -42,15 +42,25 @@ __device__ __forceinline__ SeqScan warp_scan(const uint8_t* m, int64_t T, int la
     if (m[t]) { ++s.count; s.first = min(s.first, (int)t); s.last = max(s.last, (int)t); }
   for (int64_t t = tail0 + lane; t < T; t += 32)
     if (m[t]) { ++s.count; s.first = min(s.first, (int)t); s.last = max(s.last, (int)t); }
+  // rounds of kScanBatch 16-byte words per lane, all loaded before any is
+  // scanned: a piece of up to 2 KB per warp costs one memory round trip
+  constexpr int kScanBatch = 4;
   const uint4* mv = reinterpret_cast<const uint4*>(m + head);
-#pragma unroll 8
-  for (int64_t k = lane; k < nvec; k += 32) {
-    const uint4 v = __ldg(mv + k);
-    const int pos = (int)(head + 16 * k);
-    scan_word(v.x, pos, s);
-    scan_word(v.y, pos + 4, s);
-    scan_word(v.z, pos + 8, s);
-    scan_word(v.w, pos + 12, s);
+  for (int64_t k0 = lane; k0 < nvec; k0 += 32 * kScanBatch) {
+    uint4 v[kScanBatch];
+#pragma unroll
+    for (int u = 0; u < kScanBatch; ++u) {
+      const int64_t k = k0 + 32 * u;
+      v[u] = k < nvec ? __ldg(mv + k) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kScanBatch; ++u) {
+      const int pos = (int)(head + 16 * (k0 + 32 * u));
+      scan_word(v[u].x, pos, s);
+      scan_word(v[u].y, pos + 4, s);
+      scan_word(v[u].z, pos + 8, s);
+      scan_word(v[u].w, pos + 12, s);
+    }
   }
   s.count = warp_sum(s.count);
   s.first = __reduce_min_sync(0xFFFFFFFFu, s.first);
@@ -100,49 +110,82 @@ __device__ __forceinline__ int64_t warp_find_group(const int64_t* bounds, int64_
   return g0;
 }
 
-// One group's statistics, by one warp: every sum runs over the lanes'
-// strided elements in index order and then a fixed xor tree, in double.
+// One group's statistics, by one warp, in float-pair arithmetic (about 46
+// significant bits: the double-precision units of GB300 are a small
+// fraction of its fp32 rate, and a dozen dependent double operations with
+// divisions and a square root held the one-launch logps kernel for
+// microseconds).  Every sum runs over the lanes' strided elements in index
+// order, then the fixed xor tree; lane 0's result is broadcast, so every
+// lane holds the same statistics.
 struct GroupStats {
-  double mean, den;
+  FF mean, den;
   bool degenerate;  // max == min: every advantage of the group is 0
   int nonfinite;    // non-finite rewards in the group
 };
+__device__ __forceinline__ FF ff_mul(FF a, FF b) {
+  const float p = __fmul_rn(a.hi, b.hi);
+  const float e = __fmaf_rn(a.hi, b.hi, -p);
+  return fast_two_sum(p, __fadd_rn(e, __fmaf_rn(a.hi, b.lo, __fmul_rn(a.lo, b.hi))));
+}
+// sqrt of a non-negative float pair: the fp32 root, then one Newton
+// correction from the exact residual a - s^2.
+__device__ __forceinline__ FF ff_sqrt(FF a) {
+  if (!(a.hi > 0.f)) return {0.f, 0.f};
+  const float s = __fsqrt_rn(a.hi);
+  const float p = __fmul_rn(s, s);
+  const float e = __fmaf_rn(s, s, -p);
+  const float r = __fadd_rn(__fsub_rn(__fsub_rn(a.hi, p), e), a.lo);
+  return fast_two_sum(s, __fdiv_rn(r, __fmul_rn(2.f, s)));
+}
+__device__ __forceinline__ FF ff_bcast0(FF v) {
+  return {__shfl_sync(0xFFFFFFFFu, v.hi, 0), __shfl_sync(0xFFFFFFFFu, v.lo, 0)};
+}
 __device__ __forceinline__ GroupStats warp_group_stats(const float* rewards, int64_t lo,
                                                        int64_t hi, float adv_eps, int eps_add,
                                                        int lane) {
   const int64_t n = hi - lo;
-  double sum = 0.0;
+  FF sum = {0.f, 0.f};
   int nonfinite = 0;
   float mx = -INFINITY, mn = INFINITY;
   for (int64_t i = lo + lane; i < hi; i += 32) {
     const float r = __ldg(rewards + i);
     nonfinite += !isfinite(r);
-    sum += (double)r;
+    sum = ff_add(sum, FF{r, 0.f});
     mx = fmaxf(mx, r);
     mn = fminf(mn, r);
   }
-  sum = warp_sum(sum);
+  sum = ff_bcast0(warp_sum_ff2(sum));
   GroupStats g;
   g.nonfinite = warp_sum(nonfinite);
   mx = warp_max(mx);
   mn = -warp_max(-mn);
-  g.mean = n > 0 ? sum / (double)n : 0.0;
+  const FF nf = ff_from_u64((unsigned long long)(n > 0 ? n : 1));
+  g.mean = n > 0 ? ff_div(sum, nf) : FF{0.f, 0.f};
 
-  double ss = 0.0;  // population variance
+  FF ss = {0.f, 0.f};  // population variance
   for (int64_t i = lo + lane; i < hi; i += 32) {
-    const double d = (double)__ldg(rewards + i) - g.mean;
-    ss += d * d;
+    const FF d = ff_add(FF{__ldg(rewards + i), 0.f}, ff_neg(g.mean));
+    ss = ff_add(ss, ff_mul(d, d));
   }
-  ss = warp_sum(ss);
-  const double sd = n > 0 ? sqrt(ss / (double)n) : 0.0;
-  const double eps = (double)adv_eps;
-  g.den = eps_add ? sd + eps : (sd > eps ? sd : eps);
+  ss = ff_bcast0(warp_sum_ff2(ss));
+  const FF sd = n > 0 ? ff_sqrt(ff_div(ss, nf)) : FF{0.f, 0.f};
+  const FF eps = {adv_eps, 0.f};
+  if (eps_add) {
+    g.den = ff_add(sd, eps);
+  } else {  // max(sd, eps)
+    const bool above = sd.hi > adv_eps || (sd.hi == adv_eps && sd.lo > 0.f);
+    g.den = above ? sd : eps;
+  }
   g.degenerate = !(mx > mn);
   return g;
 }
 
+// The advantage of a reward r of the group, as a double (the float pair's
+// exact sum).
 __device__ __forceinline__ double group_adv(const GroupStats& g, float r) {
-  return g.degenerate ? 0.0 : ((double)r - g.mean) / g.den;
+  if (g.degenerate) return 0.0;
+  const FF a = ff_div(ff_add(FF{r, 0.f}, ff_neg(g.mean)), g.den);
+  return (double)a.hi + (double)a.lo;
 }
 
 }  // namespace grpo

@@ -34,8 +34,10 @@ struct WsHeader {
   unsigned long long N;            // active tokens  (prep: integer atomics, exact)
   unsigned long long S;            // live sequences (idem)
   unsigned long long clip[3];      // clipped tokens: upper, lower, dual (integer atomics)
-  unsigned int arrive;             // one-launch logps kernel: CTAs past their counts
-  unsigned int pad;
+  // one-launch logps kernel: the grid barrier and the batch counts in one
+  // word, so that one relaxed atomic per CTA carries both (bits 52-63: CTAs
+  // arrived, 41-51: live sequences S, 0-40: active tokens N)
+  unsigned long long arrive;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -477,7 +479,7 @@ __device__ __forceinline__ void put_total(SeqTotal* r, FF P, FF K, int L) {
 // The final scalar from B records, by the first kFinalThreads threads of a
 // CTA (every thread of the CTA calls it: it holds __syncthreads).  Each
 // thread takes records j = t, t + 128, ... in index order (loads batched
-// four at a time, from L2: the records may come from other CTAs of the
+// kBatch at a time, from L2: the records may come from other CTAs of the
 // same launch), then a fixed xor tree per warp and the four warps in index
 // order.  The token mean and the fixed constant add the totals; the sequence
 // mean adds total / L over live sequences; then one division by N, S or C.
@@ -493,6 +495,40 @@ struct FinalSmem {
   FF f[2][kFinalThreads / 32];
   unsigned kinds;  // bit 0: a kind-1 record, bit 1: kind 2, bit 2: another
 };
+// One float-pair record's contribution (the sequence mean divides by L and
+// skips empty sequences: false), shared by both final forms.
+__device__ __forceinline__ bool ff_record(const uint4& lo, int L, int reduction, FF& P, FF& K) {
+  P = {__uint_as_float(lo.x), __uint_as_float(lo.y)};
+  K = {__uint_as_float(lo.z), __uint_as_float(lo.w)};
+  if (reduction == GRPO_SEQUENCE_MEAN) {
+    if (L == 0) return false;
+    const FF Lf = {(float)L, 0.f};
+    P = ff_div(P, Lf);
+    K = ff_div(K, Lf);
+  }
+  return true;
+}
+// The float-pair outputs from the warps' partial sums (thread 0).
+__device__ __forceinline__ void ff_final_outputs(const FinalSmem& sm, unsigned long long N,
+                                                 unsigned long long S, int reduction,
+                                                 float norm_c, float beta, float& o0, float& o1,
+                                                 float& o2) {
+  FF P = sm.f[0][0], K = sm.f[1][0];
+#pragma unroll
+  for (int k = 1; k < kFinalThreads / 32; ++k) {
+    P = ff_add(P, sm.f[0][k]);
+    K = ff_add(K, sm.f[1][k]);
+  }
+  const FF den = reduction == GRPO_FIXED_CONSTANT
+                     ? FF{norm_c, 0.f}
+                     : ff_from_u64(reduction == GRPO_TOKEN_MEAN ? (N > 0 ? N : 1) : (S > 0 ? S : 1));
+  P = ff_div(P, den);
+  K = ff_div(K, den);
+  o0 = ff_float(ff_add(P, ff_scale(K, beta)));
+  o1 = ff_float(P);
+  o2 = ff_float(K);
+}
+
 static __device__ __forceinline__ void final_scalar(const SeqTotal* recs, int64_t B, unsigned long long N,
                              unsigned long long S, int reduction, float norm_c, float beta,
                              bool bad, float* out3, FinalSmem& sm) {
@@ -505,18 +541,22 @@ static __device__ __forceinline__ void final_scalar(const SeqTotal* recs, int64_
   if (t < kFinalThreads) {
     unsigned kinds = 0u;
     for (int64_t j0 = t; j0 < B; j0 += kBatch * kFinalThreads) {
-      uint4 lo[kBatch], hi[kBatch];
+      // per record: the four totals words, the count and the kind
+      uint4 lo[kBatch];
+      unsigned Lk[kBatch], kk[kBatch];
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
         const int64_t j = j0 + (int64_t)k * kFinalThreads;
         const uint4* q = reinterpret_cast<const uint4*>(recs + (j < B ? j : 0));
+        const unsigned* h = reinterpret_cast<const unsigned*>(q + 1);
         lo[k] = j < B ? __ldcg(q) : make_uint4(0u, 0u, 0u, 0u);
-        hi[k] = j < B ? __ldcg(q + 1) : make_uint4(0u, 0u, 0u, 0u);
+        Lk[k] = j < B ? __ldcg(h) : 0u;
+        kk[k] = j < B ? __ldcg(h + 2) : 0u;
       }
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
-        const int L = (int)hi[k].x;
-        const int rk = (int)hi[k].z;
+        const int L = (int)Lk[k];
+        const int rk = (int)kk[k];
         if (rk == kTotalsDouble) {
           kinds |= 1u;
           double P = __hiloint2double((int)lo[k].y, (int)lo[k].x);
@@ -530,14 +570,8 @@ static __device__ __forceinline__ void final_scalar(const SeqTotal* recs, int64_
           ud[1] += K;
         } else if (rk == kTotalsFF) {
           kinds |= 2u;
-          FF P = {__uint_as_float(lo[k].x), __uint_as_float(lo[k].y)};
-          FF K = {__uint_as_float(lo[k].z), __uint_as_float(lo[k].w)};
-          if (reduction == GRPO_SEQUENCE_MEAN) {
-            if (L == 0) continue;
-            const FF Lf = {(float)L, 0.f};
-            P = ff_div(P, Lf);
-            K = ff_div(K, Lf);
-          }
+          FF P, K;
+          if (!ff_record(lo[k], L, reduction, P, K)) continue;
           uf[0] = ff_add(uf[0], P);
           uf[1] = ff_add(uf[1], K);
         } else if (j0 + (int64_t)k * kFinalThreads < B) {
@@ -587,22 +621,56 @@ static __device__ __forceinline__ void final_scalar(const SeqTotal* recs, int64_
     o1 = (float)P;
     o2 = (float)K;
   } else {
-    FF P = sm.f[0][0], K = sm.f[1][0];
-#pragma unroll
-    for (int k = 1; k < kFinalThreads / 32; ++k) {
-      P = ff_add(P, sm.f[0][k]);
-      K = ff_add(K, sm.f[1][k]);
-    }
-    const FF den = reduction == GRPO_FIXED_CONSTANT
-                       ? FF{norm_c, 0.f}
-                       : ff_from_u64(reduction == GRPO_TOKEN_MEAN ? (N > 0 ? N : 1) : (S > 0 ? S : 1));
-    P = ff_div(P, den);
-    K = ff_div(K, den);
-    o0 = ff_float(ff_add(P, ff_scale(K, beta)));
-    o1 = ff_float(P);
-    o2 = ff_float(K);
+    ff_final_outputs(sm, N, S, reduction, norm_c, beta, o0, o1, o2);
   }
   if (bad || (ks & 4u) || ks == 3u) o0 = o1 = o2 = NAN;
+  out3[0] = o0;
+  out3[1] = o1;
+  out3[2] = o2;
+}
+
+// final_scalar for B records all known to be float pairs (written by the
+// calling launch): the same order and arithmetic, hence the same bits, with
+// kBatch records per thread in flight at once.
+template <int kBatch>
+static __device__ __forceinline__ void final_scalar_ff(const SeqTotal* recs, int64_t B,
+                                                       unsigned long long N, unsigned long long S,
+                                                       int reduction, float norm_c, float beta,
+                                                       bool bad, float* out3, FinalSmem& sm) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  FF uf[2] = {{0.f, 0.f}, {0.f, 0.f}};
+  if (t < kFinalThreads) {
+    for (int64_t j0 = t; j0 < B; j0 += kBatch * kFinalThreads) {
+      uint4 lo[kBatch];
+      unsigned Lk[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int64_t j = j0 + (int64_t)k * kFinalThreads;
+        const uint4* q = reinterpret_cast<const uint4*>(recs + (j < B ? j : 0));
+        lo[k] = j < B ? __ldcg(q) : make_uint4(0u, 0u, 0u, 0u);
+        Lk[k] = j < B ? __ldcg(reinterpret_cast<const unsigned*>(q + 1)) : 0u;
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        if (j0 + (int64_t)k * kFinalThreads >= B) continue;
+        FF P, K;
+        if (!ff_record(lo[k], (int)Lk[k], reduction, P, K)) continue;
+        uf[0] = ff_add(uf[0], P);
+        uf[1] = ff_add(uf[1], K);
+      }
+    }
+    uf[0] = warp_sum_ff2(uf[0]);
+    uf[1] = warp_sum_ff2(uf[1]);
+    if (lane == 0) {
+      sm.f[0][warp] = uf[0];
+      sm.f[1][warp] = uf[1];
+    }
+  }
+  __syncthreads();
+  if (t != 0) return;
+  float o0, o1, o2;
+  ff_final_outputs(sm, N, S, reduction, norm_c, beta, o0, o1, o2);
+  if (bad) o0 = o1 = o2 = NAN;
   out3[0] = o0;
   out3[1] = o1;
   out3[2] = o2;
@@ -730,8 +798,9 @@ struct LogpsArgs {
   unsigned flags;  // grpo_params_t.flags
   // One-launch form (fused = 1, a cooperative launch): each CTA scans its own
   // mask row and forms its own advantage from the groups below (as the
-  // separate pass would), adds its counts to hdr->N / hdr->S and waits at a
-  // grid barrier before any count is read; A, Aff, range and L are unused.
+  // separate pass would), adds its counts to hdr->arrive and waits at the
+  // grid barrier that word also is before any count is read; A, Aff, range
+  // and L are unused.
   int fused;
   const float* rewards;   // [Bg]
   const int64_t* bounds;  // NULL -> uniform groups of spp

@@ -289,19 +289,27 @@ __device__ __forceinline__ void vec_general(uint32_t mw, const float4& l4, const
   const float lp[4] = {l4.x, l4.y, l4.z, l4.w};
   const float od[4] = {o4.x, o4.y, o4.z, o4.w};
   const float rf[4] = {r4.x, r4.y, r4.z, r4.w};
+  // the token loop is kept rolled (code size); its arrays, indexed by the
+  // loop counter, live in local memory, so the gradients go through wt and
+  // reach w (which the fast path keeps in registers) by constant indices
+  float wt[4];
   vq = 0.f;
   vk = 0.f;
 #pragma unroll 1
   for (int j = 0; j < 4; ++j) {
-    w[j] = 0.f;
+    wt[j] = 0.f;
     if ((mw >> (8 * j)) & 0xFFu) {
       const TokEpi<float> t = tok_terms(lp[j], od[j], rf[j], x.A, a, x.em_seq);
       vq = __fadd_rn(vq, t.q);
       vk = __fadd_rn(vk, t.k);
       acc.count(t.clip);
-      w[j] = token_w(lp[j], od[j], rf[j], t, x, a);
+      wt[j] = token_w(lp[j], od[j], rf[j], t, x, a);
     }
   }
+  w[0] = wt[0];
+  w[1] = wt[1];
+  w[2] = wt[2];
+  w[3] = wt[3];
 }
 
 // One vector of four slots: its gradient, and its q / k sums into the
@@ -332,10 +340,13 @@ __device__ __forceinline__ void process_vec(uint32_t mw, const float4& l, const 
 }
 
 // ---- staging through shared memory with bulk asynchronous copies ----
-// The active range of the sequence, widened to 16-token boundaries, moves
-// in chunks of kChunk tokens (logps, old, ref and the mask bytes: four
-// cp.async.bulk copies completing on one mbarrier); kDepth chunks are in
-// flight while one is evaluated.
+// A sequence's row is cut into chunks of kChunk tokens from slot 0; the
+// chunks that hold its active tokens move through shared memory (logps,
+// old, ref and the mask bytes: four cp.async.bulk copies completing on one
+// mbarrier), kDepth of them in flight while one is evaluated.  (Requesting
+// chunks before the mask scan, or prefetching the whole active range into
+// L2 once it is known, measured slower: the flood of requests delays the
+// mask scan and the grid barrier behind it.)
 static constexpr int kChunkVecs = 1;  // float4 vectors per thread per chunk
 static constexpr int kChunk = 4 * kLogpsThreads * kChunkVecs;
 static constexpr int kDepth = 4;
@@ -404,27 +415,36 @@ __device__ __forceinline__ bool staged_ok(const LogpsArgs& a) {
   return (a.fused || a.range != nullptr) && (a.T % 16 == 0) && ((m & 15) == 0);
 }
 
-// The grid barrier of the one-launch form, run by thread 0 of every CTA that
-// holds a sequence (a cooperative launch: they are all resident).  Arrival
-// is a release-add after the CTA's count atomics; the wait is an acquire-load
-// loop bounded like the copy waits (false if it ran out).
-__device__ __forceinline__ void grid_arrive(unsigned* c) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(c) : "memory");
+// The grid barrier of the one-launch form (a cooperative launch: every CTA
+// that holds a sequence is resident).  A CTA arrives with one relaxed 64-bit
+// add of (1 << 52) + ([L > 0] << 41) + L to the header's word: the word is
+// the barrier and the batch counts at once, so no other data crosses CTAs
+// and no memory fence is needed (under a saturated memory system a fence
+// costs microseconds).  B <= 4095 CTAs, S <= B < 2^11 and N <= B T < 2^41
+// fit their fields.  The wait polls the word, bounded like the copy waits
+// (false if it ran out).
+static constexpr int kArriveShift = 52, kLiveShift = 41;
+__device__ __forceinline__ void grid_arrive(unsigned long long* c, int L) {
+  const unsigned long long v =
+      (1ull << kArriveShift) + ((unsigned long long)(L > 0) << kLiveShift) + (unsigned long long)L;
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(c), "l"(v) : "memory");
 }
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
-__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p) {
+__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long* p) {
   unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ bool grid_wait(const unsigned* c, unsigned expected) {
+__device__ __forceinline__ bool grid_wait(const unsigned long long* c, unsigned expected,
+                                          unsigned long long& word) {
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 0; i < kWaitRounds; ++i) {
-    if (ld_acquire(c) >= expected) return true;
+    word = ld_relaxed(c);
+    if ((unsigned)(word >> kArriveShift) >= expected) return true;
     if ((i & 15u) == 15u && global_ns() - t0 > kWaitNs) return false;
   }
   return false;
@@ -444,12 +464,32 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
   __shared__ __align__(8) uint64_t s_full[kDepth];
   __shared__ int s_scan[3][kLogpsThreads / 32];
   __shared__ double s_adv;
+  __shared__ float2 s_aff;
   __shared__ int s_L;
   __shared__ int2 s_rg;
   __shared__ unsigned long long s_NS[2];
   const int64_t b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t pol = l2_evict_first();  // every input byte is read once
+  const int64_t base = b * a.T;
+  const bool has_ref = a.ref != nullptr;
+  const bool staged = staged_ok(a);
+  const uint32_t nref = has_ref ? 1u : 0u;
+  // the test hook GRPO_FLAG_TEST_STALLED_COPY: the first copy of sequence 0
+  // expects 16 bytes more than it delivers, so its wait runs out
+  const uint32_t stall = ((a.flags & GRPO_FLAG_TEST_STALLED_COPY) && b == 0) ? 16u : 0u;
+  // chunk c of the row into the stage of the k-th chunk taken (one thread)
+  auto issue = [&](int c, int k) {
+    const int64_t st = (int64_t)c * kChunk;
+    const uint32_t len = (uint32_t)min((int64_t)kChunk, a.T - st);
+    Stage& S = s_st[k % kDepth];
+    uint64_t* bar = &s_full[k % kDepth];
+    mbar_expect_tx(bar, len * (4u * (2u + nref) + 1u) + (k == 0 ? stall : 0u));
+    bulk_g2s(S.lp, a.logps + base + st, 4u * len, bar, pol);
+    bulk_g2s(S.od, a.old + base + st, 4u * len, bar, pol);
+    if (has_ref) bulk_g2s(S.rf, a.ref + base + st, 4u * len, bar, pol);
+    bulk_g2s(S.mk, a.mask + base + st, len, bar, pol);
+  };
   if (threadIdx.x == 0) {
     for (int d = 0; d < kDepth; ++d) mbar_init(&s_full[d], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -463,51 +503,34 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
   if (b < a.B) {
     SeqCtx x;
     x.b = b;
-    const int64_t base = b * a.T;
-    const bool has_ref = a.ref != nullptr;
-    const bool staged = staged_ok(a);
-    // the staged path's chunks cover the active range widened to 16-slot
-    // boundaries, [lo, hi)
-    int64_t lo = 0, hi = 0;
-    int nchunks = 0;
+    // The staged path takes the chunks [c_lo, c_hi) that hold active tokens,
+    // the k-th of them (chunk c_lo + k) in stage k % kDepth; the gradient
+    // slots outside them are zero-stored.
+    int c_lo = 0, c_hi = 0, nlive = 0;
     auto geometry = [&](int2 rg) {
-      lo = rg.x & ~15;
-      hi = min((int64_t)((rg.y + 15) & ~15), a.T);
-      nchunks = staged ? (int)((hi - lo + kChunk - 1) / kChunk) : 0;
-    };
-    const uint32_t nref = has_ref ? 1u : 0u;
-    // the test hook GRPO_FLAG_TEST_STALLED_COPY: the first chunk of sequence
-    // 0 expects 16 bytes more than its copies deliver, so its wait runs out
-    const uint32_t stall = ((a.flags & GRPO_FLAG_TEST_STALLED_COPY) && b == 0) ? 16u : 0u;
-    auto issue = [&](int c) {  // one thread
-      const int64_t st = lo + (int64_t)c * kChunk;
-      const uint32_t len = (uint32_t)min((int64_t)kChunk, hi - st);
-      Stage& S = s_st[c % kDepth];
-      uint64_t* bar = &s_full[c % kDepth];
-      mbar_expect_tx(bar, len * (4u * (2u + nref) + 1u) + (c == 0 ? stall : 0u));
-      bulk_g2s(S.lp, a.logps + base + st, 4u * len, bar, pol);
-      bulk_g2s(S.od, a.old + base + st, 4u * len, bar, pol);
-      if (has_ref) bulk_g2s(S.rf, a.ref + base + st, 4u * len, bar, pol);
-      bulk_g2s(S.mk, a.mask + base + st, len, bar, pol);
+      c_lo = rg.y > rg.x ? rg.x / kChunk : 0;
+      c_hi = rg.y > rg.x ? (rg.y + kChunk - 1) / kChunk : 0;
+      if (!staged) c_lo = c_hi = 0;
+      nlive = c_hi - c_lo;
     };
     auto first_copies = [&]() {  // one thread
-      for (int c = 0; c < nchunks && c < kDepth; ++c) issue(c);
+      for (int k = 0; k < nlive && k < kDepth; ++k) issue(c_lo + k, k);
     };
-    // slots outside the widened active range hold no active token
+    // slots outside the evaluated chunks hold no active token
     float4* grow = reinterpret_cast<float4*>(a.grad + base);
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
     auto zero_outside = [&](int t, int nt) {
       if (!staged || !a.grad) return;
-      for (int64_t v = t; v < lo / 4; v += nt) grow[v] = z4;
-      for (int64_t v = hi / 4 + t; v < a.T / 4; v += nt) grow[v] = z4;
+      const int64_t v_lo = (int64_t)c_lo * (kChunk / 4);
+      const int64_t v_hi = min((int64_t)c_hi * (kChunk / 4), a.T / 4);
+      for (int64_t v = t; v < v_lo; v += nt) grow[v] = z4;
+      for (int64_t v = v_hi + t; v < a.T / 4; v += nt) grow[v] = z4;
     };
-
-    float2 Ab;
     if (a.fused) {
-      // Warp 0 forms this sequence's advantage from its group (fp64: the
-      // longest chain here) while warps 1-3 scan the mask row, add the
-      // counts, arrive at the grid barrier, start the copies and zero the
-      // slots outside the active range.
+      // warp 0 forms this sequence's advantage from its group while warps 1-3
+      // scan the mask row, arrive at the grid barrier with the counts,
+      // request the first chunks and zero the slots outside the evaluated
+      // chunks
       if (warp == 0) {
         const int64_t gb = a.seq_begin + b;
         const int64_t g = a.bounds ? warp_find_group(a.bounds, a.G, gb, lane) : gb / a.spp;
@@ -516,8 +539,10 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
         const GroupStats gs = warp_group_stats(a.rewards, glo, ghi, a.adv_eps, a.eps_add, lane);
         if (lane == 0) {
           const double Ai = group_adv(gs, __ldg(a.rewards + gb));
+          const float hi32 = (float)Ai;
           s_adv = Ai;
-          if (a.adv_out) a.adv_out[b] = (float)Ai;
+          s_aff = make_float2(hi32, (float)(Ai - (double)hi32));
+          if (a.adv_out) a.adv_out[b] = hi32;
         }
       } else {
         // warp 1 + p scans piece p of three (a multiple of 16 slots each);
@@ -546,13 +571,9 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
         if (threadIdx.x == 32) {
           s_L = L;
           s_rg = rg;
-          if (!a.shard) {  // a shard call is given the batch's counts
-            if (L) atomicAdd(&a.hdr->N, (unsigned long long)L);
-            if (L) atomicAdd(&a.hdr->S, 1ull);
-            grid_arrive(&a.hdr->arrive);
-          }
-          if (staged) first_copies();
+          if (!a.shard) grid_arrive(&a.hdr->arrive, L);  // a shard call is given the batch's counts
         }
+        if (threadIdx.x == 64 && staged) first_copies();
         zero_outside((int)threadIdx.x - 32, kLogpsThreads - 32);
         if (warp == kScanWarps) {
           // every group is checked once over the grid, as the separate pass
@@ -571,18 +592,12 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
       __syncthreads();
       x.L = s_L;
       if (warp == 0) geometry(s_rg);
-      x.Ad = s_adv;
-      const float hi32 = (float)x.Ad;
-      Ab = make_float2(hi32, (float)(x.Ad - (double)hi32));
     } else {
       x.L = a.L[b];
       geometry(a.range ? a.range[b] : make_int2(0, (int)a.T));
       if (staged && threadIdx.x == 0) first_copies();
       zero_outside((int)threadIdx.x, kLogpsThreads);
-      x.Ad = a.A[b];
-      Ab = a.Aff[b];
     }
-    x.A = Ab.x;
 
     x.em_seq = 0.f;
     x.em_seq_d = 0.0;
@@ -591,8 +606,9 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
       // any token's term (Kahan sums per thread, float pairs across the CTA)
       float ss = 0.f, sc = 0.f;
       if (vec_ok(a)) {
-        // 4-slot vectors of the widened active range, two per thread in
-        // flight, read whole (masked slots are loaded but never used)
+        // 4-slot vectors of the evaluated chunks (the whole row off the
+        // staged path), two per thread in flight, read whole (masked slots
+        // are loaded but never used)
         const uint32_t* mrow = reinterpret_cast<const uint32_t*>(a.mask + base);
         const float4* lrow = reinterpret_cast<const float4*>(a.logps + base);
         const float4* orow = reinterpret_cast<const float4*>(a.old + base);
@@ -603,8 +619,8 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
           for (int j = 0; j < 4; ++j)
             if ((mw >> (8 * j)) & 0xFFu) kahan(ss, sc, d[j]);
         };
-        const int64_t v1 = hi / 4;
-        int64_t v = lo / 4 + threadIdx.x;
+        const int64_t v1 = staged ? min((int64_t)c_hi * (kChunk / 4), a.T / 4) : a.T / 4;
+        int64_t v = (staged ? (int64_t)c_lo * (kChunk / 4) : 0) + threadIdx.x;
         for (; v + kLogpsThreads < v1; v += 2 * kLogpsThreads) {
           const uint32_t m0 = __ldg(mrow + v), m1 = __ldg(mrow + v + kLogpsThreads);
           const float4 l0 = __ldg(lrow + v), l1 = __ldg(lrow + v + kLogpsThreads);
@@ -631,24 +647,33 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
       x.em_seq = (float)x.em_seq_d;
     }
 
-    // the batch counts: complete once every CTA has passed the barrier (the
-    // test hook GRPO_FLAG_TEST_STALLED_BARRIER makes CTA 0 wait for one CTA
-    // more than there are, so its wait runs out)
+    // the batch counts: complete once every CTA has arrived (the test hook
+    // GRPO_FLAG_TEST_STALLED_BARRIER makes CTA 0 wait for one arrival more
+    // than there are, so its wait runs out)
     if (threadIdx.x == 0) {
       if (a.fused && !a.shard) {
         const unsigned extra = ((a.flags & GRPO_FLAG_TEST_STALLED_BARRIER) && b == 0) ? 1u : 0u;
-        if (!grid_wait(&a.hdr->arrive, (unsigned)a.B + extra))
+        unsigned long long word = 0ull;
+        if (!grid_wait(&a.hdr->arrive, (unsigned)a.B + extra, word))
           atomicOr(&a.hdr->status, (unsigned)GRPO_ERR_TIMEOUT);
-        s_NS[0] = ld_acquire(a.NS);
-        s_NS[1] = ld_acquire(a.NS + 1);
+        s_NS[0] = word & ((1ull << kLiveShift) - 1ull);
+        s_NS[1] = (word >> kLiveShift) & ((1ull << (kArriveShift - kLiveShift)) - 1ull);
+      } else if (a.fused) {
+        s_NS[0] = a.NS[0];
+        s_NS[1] = a.NS[1];
       } else {
         s_NS[0] = a.NS[0];
         s_NS[1] = a.NS[1];
+        s_adv = a.A[b];
+        s_aff = a.Aff[b];
       }
     }
     __syncthreads();
     x.N = s_NS[0];
     x.S = s_NS[1];
+    x.Ad = s_adv;
+    const float2 Ab = s_aff;
+    x.A = Ab.x;
     // grad_scale * c in fp32: c = 1/max(N,1), 1/(max(S,1) L_b) or 1/C; the
     // products and quotient are rounded in fp32, well inside the gradient's
     // rounding allowance
@@ -678,20 +703,22 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
       // copies already issued (bounded), and skips the arithmetic -- the loss
       // outputs become NaN through the status word.
       // One CTA-wide barrier per chunk: past it, every thread is done with
-      // chunk c - 1, whose slot is then refilled with chunk c - 1 + kDepth.
-      // Every thread counts the chunks issued so far (the decisions are the
-      // same everywhere: `stalled` is taken CTA-wide).
+      // the (k-1)-th chunk, whose stage is then refilled with the
+      // (k-1+kDepth)-th.  Every thread counts the chunks requested so far (the
+      // decisions are the same everywhere: `stalled` is taken CTA-wide).
       bool stalled = false;
-      int issued = nchunks < kDepth ? nchunks : kDepth;
-      for (int c = 0; c < issued; ++c) {
-        const int slot = c % kDepth;
-        const int64_t st = lo + (int64_t)c * kChunk;
-        const int len = (int)min((int64_t)kChunk, hi - st);
-        const bool ready = mbar_wait(&s_full[slot], (uint32_t)(c / kDepth) & 1u);
+      int issued = nlive < kDepth ? nlive : kDepth;
+      for (int k = 0; k < issued; ++k) {
+        const int slot = k % kDepth;
+        const int64_t st = (int64_t)(c_lo + k) * kChunk;
+        const int len = (int)min((int64_t)kChunk, a.T - st);
+        // warp 0 waits for the copies (the other warps sleep in the CTA
+        // barrier, leaving the issue slots to the warps still computing)
+        const bool ready = warp != 0 || mbar_wait(&s_full[slot], (uint32_t)(k / kDepth) & 1u);
         stalled = __syncthreads_or(!ready) || stalled;  // one decision for the CTA
-        if (!stalled && c >= 1 && c - 1 + kDepth < nchunks) {
-          if (threadIdx.x == 0) issue(c - 1 + kDepth);
-          issued = c + kDepth;
+        if (!stalled && k >= 1 && k - 1 + kDepth < nlive) {
+          if (threadIdx.x == 0) issue(c_lo + k - 1 + kDepth, k - 1 + kDepth);
+          issued = k + kDepth;
         }
         if (!stalled) {
           const Stage& S = s_st[slot];
@@ -701,8 +728,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
             if (4 * v < len) {
               float w[4];
               process_vec<kDefault>(S.mk[v], S.lp[v], S.od[v], has_ref ? S.rf[v] : z4, has_ref,
-                                    f, x, a,
-                          acc, w);
+                                    f, x, a, acc, w);
               if (a.grad) grow[st / 4 + v] = make_float4(w[0], w[1], w[2], w[3]);
             }
           }
@@ -803,22 +829,22 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
         }
         add_clip_counts(a.hdr, n);
       }
-      __threadfence();
-      s_last = atomicAdd(&a.hdr->done_ctas, 1u) == gridDim.x - 1;
+      // the ticket: a release (this thread wrote the record and added the
+      // clip counts) and, for the CTA that takes the last one, an acquire
+      s_last = atom_add_acq_rel(&a.hdr->done_ctas, 1u) == gridDim.x - 1;
     }
   } else if (threadIdx.x == 0) {
     s_last = true;  // B == 0: a single CTA writes the zero loss
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   if (threadIdx.x == 0 && a.counts_out)  // every CTA added its counts before its ticket
     for (int j = 0; j < 3; ++j) a.counts_out[j] = __ldcg(&a.hdr->clip[j]);
   if (a.shard) return;  // the scalar comes from grpo_loss_finalize over all shards' totals
 
   // the scalar over the B sequence records, in index order
   const bool bad = ((volatile unsigned*)&a.hdr->status)[0] != 0u;
-  final_scalar(a.seq, a.B, a.B > 0 ? s_NS[0] : 0ull, a.B > 0 ? s_NS[1] : 0ull, a.reduction,
+  final_scalar_ff<4>(a.seq, a.B, a.B > 0 ? s_NS[0] : 0ull, a.B > 0 ? s_NS[1] : 0ull, a.reduction,
                a.norm_c, a.beta, bad, a.out3, s_fin);
 }
 
@@ -846,6 +872,7 @@ static cudaError_t prepare_device(int dev, int64_t* cap) {
         (e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess)
       return e;
     c = coop ? (long long)per_sm * sms : 0;
+    if (c > (1ll << (64 - kArriveShift)) - 1) c = (1ll << (64 - kArriveShift)) - 1;  // the arrival field
     g_capacity[d].store(c > 0 ? c : -1, std::memory_order_release);  // -1: none
   }
   *cap = c > 0 ? c : 0;
