@@ -623,7 +623,7 @@ class LogpsCase:
     since."""
 
     COPIES = 4
-    CTAS_PER_SM = 8  # the logps kernel's residency (128 threads, 27 KB shared memory)
+    CTAS_PER_SM = 7  # the logps kernel's residency (128 threads of 72 registers, 27 KB shared memory)
 
     def __init__(self, w, device, variant="default", skip_masked=False):
         import torch

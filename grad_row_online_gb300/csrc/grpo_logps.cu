@@ -454,7 +454,7 @@ __device__ __forceinline__ bool grid_wait(const unsigned long long* c, unsigned 
 // each form is its own instantiation, so that the other's fast path does not
 // cost it registers.
 template <bool kDefault>
-__global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs a) {
+__global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs a) {
   __shared__ FF s_ff[2][kLogpsThreads / 32];
   __shared__ unsigned s_nc[3][kLogpsThreads / 32];
   __shared__ FinalSmem s_fin;
@@ -848,7 +848,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 8) logps_kernel(const LogpsArgs
                a.norm_c, a.beta, bad, a.out3, s_fin);
 }
 
-// eight 27 KB CTAs per SM need the largest shared-memory carveout; the
+// seven 27 KB CTAs per SM need the largest shared-memory carveout; the
 // attribute, and the resident-CTA count it gives, are taken once per device
 // (setting or querying them again costs host time)
 static constexpr int kMaxDevices = 64;

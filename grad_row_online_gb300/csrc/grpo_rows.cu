@@ -494,7 +494,11 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) rows_kernel(cons
 //   (reduce)            rho_i, the per-token terms and w into the slots;
 //   gspo_sweep2_kernel  sweep 2 of every row from (logp, w): the gradient,
 //                       zeros on masked rows.
-// Rows are claimed from two device counters, as in rows_kernel.
+// Rows are claimed from two device counters, as in rows_kernel: sweep 1 from
+// the first row on, reading the policy rows evict-last, sweep 2 from the last
+// row back, so that its first rows are the ones L2 still holds from sweep 1
+// (the second read of the policy is the method's own: rho_i needs every
+// token of the sequence before any gradient of it).
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) gspo_sweep1_kernel(const RowArgs a) {
   __shared__ float s_f[64];
@@ -513,7 +517,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) gspo_sweep1_kern
   __syncthreads();
   const int64_t BT = a.B * a.T;
   const bool refine = a.precise_ok && a.grad != nullptr;
-  const uint64_t stream = l2_evict_first();
+  const uint64_t stream = l2_evict_first(), keep = l2_evict_last();
   int64_t row = s_next;
   while (row < BT) {
     long long claim = 0;
@@ -541,7 +545,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) gspo_sweep1_kern
       OnlineLse sp, sr;
       sp.init();
       sr.init();
-      lse_pair<T>(x, y, a.V, sp, sr, stream, stream, nullptr, 0u, 0);
+      lse_pair<T>(x, y, a.V, sp, sr, keep, stream, nullptr, 0u, 0);
       float Mp, Mr;
       FF Zp = {0.f, 0.f}, Zr = {0.f, 0.f};
       combine_ff(sp, sr, s_f, s_zs, Mp, Mr, Zp, Zr);
@@ -585,8 +589,9 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) gspo_sweep2_kern
   const int64_t BT = a.B * a.T;
   const bool zero_masked = !(a.flags & GRPO_SKIP_MASKED_GRAD_ROWS);
   const uint64_t stream = l2_evict_first();
-  int64_t row = s_next;
-  while (row < BT) {
+  int64_t k = s_next;  // claims count from the last row back
+  while (k < BT) {
+    const int64_t row = BT - 1 - k;
     long long claim = 0;
     if (threadIdx.x == 0) claim = (long long)atomicAdd(&a.hdr->row_counter2, 1ull);
     const T* x = reinterpret_cast<const T*>(a.policy) + row * a.V;
@@ -621,7 +626,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) gspo_sweep2_kern
     __syncthreads();
     if (threadIdx.x == 0) s_next = claim;
     __syncthreads();
-    row = s_next;
+    k = s_next;
   }
 }
 

@@ -109,7 +109,7 @@ typedef enum {
                                          (caller pre-zeroed them) instead of writing 0 */
 /* grpo_loss_from_logps: run the advantage / active-count pass as its own
  * launch before the per-sequence kernel.  By default, when every sequence's
- * CTA fits on the GPU at once (B up to 8 per SM: 1,216 on GB300), the pass is
+ * CTA fits on the GPU at once (B up to 7 per SM: 1,064 on GB300), the pass is
  * folded into that kernel, launched cooperatively: each CTA scans its own
  * mask row and forms its own advantage, and the CTAs meet at a grid barrier
  * (bounded like every wait: GRPO_ERR_TIMEOUT) before the counts N and S are
