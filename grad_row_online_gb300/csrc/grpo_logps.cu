@@ -110,6 +110,16 @@ __device__ __forceinline__ void kahan(float& s, float& c, float x) {
   c = __fsub_rn(__fsub_rn(t, s), y);
   s = t;
 }
+// Two Kahan sums side by side on packed fp32x2 (the policy and KL terms):
+// the same IEEE operations as two calls of kahan(), a - b formed as
+// fma(b, -1, a) (one rounding, as a subtraction).
+__device__ __forceinline__ void kahan2(float2& s, float2& c, float2 x) {
+  const float2 m1 = make_float2(-1.f, -1.f);
+  const float2 y = __ffma2_rn(c, m1, x);
+  const float2 t = __fadd2_rn(s, y);
+  c = __ffma2_rn(y, m1, __ffma2_rn(s, m1, t));
+  s = t;
+}
 
 __device__ __forceinline__ bool vec_ok(const LogpsArgs& a) {
   const uintptr_t m = (uintptr_t)a.logps | (uintptr_t)a.old | (uintptr_t)a.ref | (uintptr_t)a.grad;
@@ -119,7 +129,7 @@ __device__ __forceinline__ bool vec_ok(const LogpsArgs& a) {
 // Per-thread sums: q and k each as a Kahan pair.  A vector's four active
 // tokens are added in fp32 first and enter the Kahan sum once.
 struct Acc {
-  float sq = 0.f, cq = 0.f, sk = 0.f, ck = 0.f;
+  float2 s = {0.f, 0.f}, c = {0.f, 0.f};  // Kahan sums of (q, k) and their compensations
   unsigned nc[3] = {0u, 0u, 0u};  // clipped tokens: upper, lower, dual
   // (constant indices only, so the counters stay in registers)
   __device__ __forceinline__ void count(int clip, unsigned n = 1u) {
@@ -165,6 +175,7 @@ __device__ __forceinline__ float2 Q_poly2(float2 d) {
 
 // Two active tokens on the fast path (every operation but the clip on
 // packed fp32x2).  Accumulates q and k, and the sums behind the range check.
+template <bool kCount>
 __device__ __forceinline__ float2 pair_fast(float2 lp, float2 od, float2 rf, bool has_ref,
                                             const FastCtx& f, float2& vq, float2& vk,
                                             float2& d2sum, float2& g2sum, int& nclip) {
@@ -182,7 +193,7 @@ __device__ __forceinline__ float2 pair_fast(float2 lp, float2 od, float2 rf, boo
   const bool cx = se.x > f.lim, cy = se.y > f.lim;
   gp.x = cx ? 0.f : gp.x;
   gp.y = cy ? 0.f : gp.y;
-  nclip += (int)cx + (int)cy;
+  if (kCount) nclip += (int)cx + (int)cy;
   const float2 g = __ffma2_rn(f.neg_beta2, emr, gp);
   vq = __fadd2_rn(vq, q);
   vk = __fadd2_rn(vk, k);
@@ -195,15 +206,16 @@ __device__ __forceinline__ float2 pair_fast(float2 lp, float2 od, float2 rf, boo
 // token needs the general path: a log ratio outside |d| < 1/2 (caught by
 // the vector's sum of d^2 reaching 1/4), or a gradient above kWPrecise
 // (caught by its sum of g^2); NaNs fail the check too.
+template <bool kCount>
 __device__ __forceinline__ bool vec_fast(const float4& l4, const float4& o4, const float4& r4,
                                          bool has_ref, const FastCtx& f, float (&w)[4],
                                          float& vq, float& vk, int& nclip) {
   float2 sq = f2(0.f), sk = f2(0.f), d2 = f2(0.f), g2 = f2(0.f);
   nclip = 0;
-  const float2 w01 = pair_fast(make_float2(l4.x, l4.y), make_float2(o4.x, o4.y),
-                               make_float2(r4.x, r4.y), has_ref, f, sq, sk, d2, g2, nclip);
-  const float2 w23 = pair_fast(make_float2(l4.z, l4.w), make_float2(o4.z, o4.w),
-                               make_float2(r4.z, r4.w), has_ref, f, sq, sk, d2, g2, nclip);
+  const float2 w01 = pair_fast<kCount>(make_float2(l4.x, l4.y), make_float2(o4.x, o4.y),
+                                       make_float2(r4.x, r4.y), has_ref, f, sq, sk, d2, g2, nclip);
+  const float2 w23 = pair_fast<kCount>(make_float2(l4.z, l4.w), make_float2(o4.z, o4.w),
+                                       make_float2(r4.z, r4.w), has_ref, f, sq, sk, d2, g2, nclip);
   w[0] = w01.x;
   w[1] = w01.y;
   w[2] = w23.x;
@@ -315,7 +327,7 @@ __device__ __forceinline__ void vec_general(uint32_t mw, const float4& l4, const
 // One vector of four slots: its gradient, and its q / k sums into the
 // thread's Kahan pairs.  Fully active vectors take the fast path when their
 // range check passes; everything else the general path.
-template <bool kDefault>
+template <bool kDefault, bool kCount>
 __device__ __forceinline__ void process_vec(uint32_t mw, const float4& l, const float4& o,
                                             const float4& r, bool has_ref, const FastCtx& f,
                                             const SeqCtx& x, const LogpsArgs& a, Acc& acc,
@@ -325,8 +337,8 @@ __device__ __forceinline__ void process_vec(uint32_t mw, const float4& l, const 
   float vq, vk;
   int nclip;
   unsigned nc[3];
-  if (f.on && all_active(mw) && vec_fast(l, o, r, has_ref, f, w, vq, vk, nclip)) {
-    acc.count(f.clip_kind, (unsigned)nclip);
+  if (f.on && all_active(mw) && vec_fast<kCount>(l, o, r, has_ref, f, w, vq, vk, nclip)) {
+    if (kCount) acc.count(f.clip_kind, (unsigned)nclip);
   } else if (!kDefault && all_active(mw) &&
              vec_fast_variant(l, o, r, has_ref, x, a, w, vq, vk, nc)) {
     acc.nc[0] += nc[0];
@@ -335,8 +347,7 @@ __device__ __forceinline__ void process_vec(uint32_t mw, const float4& l, const 
   } else {
     vec_general(mw, l, o, r, x, a, w, vq, vk, acc);
   }
-  kahan(acc.sq, acc.cq, vq);
-  kahan(acc.sk, acc.ck, vk);
+  kahan2(acc.s, acc.c, make_float2(vq, vk));
 }
 
 // ---- staging through shared memory with bulk asynchronous copies ----
@@ -451,9 +462,10 @@ __device__ __forceinline__ bool grid_wait(const unsigned long long* c, unsigned 
 }
 
 // kDefault: the call's loss is the default variant (clipped surrogate, k3);
-// each form is its own instantiation, so that the other's fast path does not
-// cost it registers.
-template <bool kDefault>
+// kCount: the call wants the clip counters.  Each form is its own
+// instantiation, so that the other's fast path does not cost it registers
+// or instructions.
+template <bool kDefault, bool kCount>
 __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs a) {
   __shared__ FF s_ff[2][kLogpsThreads / 32];
   __shared__ unsigned s_nc[3][kLogpsThreads / 32];
@@ -727,7 +739,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
             const int v = threadIdx.x + u * kLogpsThreads;
             if (4 * v < len) {
               float w[4];
-              process_vec<kDefault>(S.mk[v], S.lp[v], S.od[v], has_ref ? S.rf[v] : z4, has_ref,
+              process_vec<kDefault, kCount>(S.mk[v], S.lp[v], S.od[v], has_ref ? S.rf[v] : z4, has_ref,
                                     f, x, a, acc, w);
               if (a.grad) grow[st / 4 + v] = make_float4(w[0], w[1], w[2], w[3]);
             }
@@ -766,7 +778,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
         }
         const uint32_t m2 = v + 2 * kS < nv ? __ldg(mrow + v + 2 * kS) : 0u;
         float w[4];
-        process_vec<kDefault>(m0, l0, o0, r0, has_ref, f, x, a, acc, w);
+        process_vec<kDefault, kCount>(m0, l0, o0, r0, has_ref, f, x, a, acc, w);
         if (a.grad) grow[v] = make_float4(w[0], w[1], w[2], w[3]);
         m0 = m1;
         m1 = m2;
@@ -781,8 +793,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
           const float lp = a.logps[base + t], o = a.old[base + t];
           const float rf = a.ref ? a.ref[base + t] : 0.f;
           const TokEpi<float> tt = tok_terms(lp, o, rf, x.A, a, x.em_seq);
-          kahan(acc.sq, acc.cq, tt.q);
-          kahan(acc.sk, acc.ck, tt.k);
+          kahan2(acc.s, acc.c, make_float2(tt.q, tt.k));
           acc.count(tt.clip);
           w = token_w(lp, o, rf, tt, x, a);
         }
@@ -791,7 +802,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
     }
     // the sequence's totals as float pairs: threads' Kahan sums, a fixed
     // xor tree per warp, warps in index order
-    FF fq = warp_sum_ff2(FF{acc.sq, -acc.cq}), fk = warp_sum_ff2(FF{acc.sk, -acc.ck});
+    FF fq = warp_sum_ff2(FF{acc.s.x, -acc.c.x}), fk = warp_sum_ff2(FF{acc.s.y, -acc.c.y});
     unsigned nc[3] = {0u, 0u, 0u};
     if (a.counts_out) {
 #pragma unroll
@@ -858,15 +869,15 @@ static cudaError_t prepare_device(int dev, int64_t* cap) {
   const int d = dev & (kMaxDevices - 1);
   long long c = g_capacity[d].load(std::memory_order_acquire);
   if (c == 0) {
-    cudaError_t e = cudaFuncSetAttribute(logps_kernel<true>,
-                                         cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         (int)cudaSharedmemCarveoutMaxShared);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(logps_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                               (int)cudaSharedmemCarveoutMaxShared);
+    cudaError_t e = cudaSuccess;
+    for (auto k : {logps_kernel<true, false>, logps_kernel<true, true>, logps_kernel<false, false>,
+                   logps_kernel<false, true>})
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int per_sm = 0, sms = 0, coop = 0;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, logps_kernel<true>, kLogpsThreads,
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, logps_kernel<true, false>, kLogpsThreads,
                                                            0)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess)
@@ -915,8 +926,12 @@ cudaError_t launch_logps(const LogpsArgs& a, const grpo_profile_t* prof, cudaStr
     cfg.numAttrs = 1;
   }
   if (prof && prof->start) cudaEventRecord((cudaEvent_t)prof->start, s);
-  e = a.var.is_default() ? cudaLaunchKernelEx(&cfg, logps_kernel<true>, a)
-                         : cudaLaunchKernelEx(&cfg, logps_kernel<false>, a);
+  const bool count = a.counts_out != nullptr;
+  e = a.var.is_default()
+          ? (count ? cudaLaunchKernelEx(&cfg, logps_kernel<true, true>, a)
+                   : cudaLaunchKernelEx(&cfg, logps_kernel<true, false>, a))
+          : (count ? cudaLaunchKernelEx(&cfg, logps_kernel<false, true>, a)
+                   : cudaLaunchKernelEx(&cfg, logps_kernel<false, false>, a));
   if (e == cudaSuccess) e = cudaGetLastError();
   if (prof && prof->stop) cudaEventRecord((cudaEvent_t)prof->stop, s);
   return e;
