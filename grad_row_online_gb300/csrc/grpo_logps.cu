@@ -456,6 +456,7 @@ __device__ __forceinline__ bool grid_wait(const unsigned long long* c, unsigned 
   for (uint32_t i = 0; i < kWaitRounds; ++i) {
     word = ld_relaxed(c);
     if ((unsigned)(word >> kArriveShift) >= expected) return true;
+    __nanosleep(100);  // fewer polls of the one word every CTA adds to
     if ((i & 15u) == 15u && global_ns() - t0 > kWaitNs) return false;
   }
   return false;
@@ -855,7 +856,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
 
   // the scalar over the B sequence records, in index order
   const bool bad = ((volatile unsigned*)&a.hdr->status)[0] != 0u;
-  final_scalar_ff<4>(a.seq, a.B, a.B > 0 ? s_NS[0] : 0ull, a.B > 0 ? s_NS[1] : 0ull, a.reduction,
+  final_scalar_ff<8>(a.seq, a.B, a.B > 0 ? s_NS[0] : 0ull, a.B > 0 ? s_NS[1] : 0ull, a.reduction,
                a.norm_c, a.beta, bad, a.out3, s_fin);
 }
 
