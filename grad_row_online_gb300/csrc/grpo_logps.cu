@@ -491,10 +491,14 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
   // the test hook GRPO_FLAG_TEST_STALLED_COPY: the first copy of sequence 0
   // expects 16 bytes more than it delivers, so its wait runs out
   const uint32_t stall = ((a.flags & GRPO_FLAG_TEST_STALLED_COPY) && b == 0) ? 16u : 0u;
-  // chunk c of the row into the stage of the k-th chunk taken (one thread)
+  // the staged path's active range ends at slot hi16 (the last active slot + 1,
+  // rounded up to 16 slots)
+  int hi16 = 0;  // slots within a sequence are 32-bit (T <= 2^30)
+  // chunk c of the row, up to hi16, into the stage of the k-th chunk taken
+  // (one thread)
   auto issue = [&](int c, int k) {
     const int64_t st = (int64_t)c * kChunk;
-    const uint32_t len = (uint32_t)min((int64_t)kChunk, a.T - st);
+    const uint32_t len = (uint32_t)min((int64_t)kChunk, (int64_t)hi16 - st);
     Stage& S = s_st[k % kDepth];
     uint64_t* bar = &s_full[k % kDepth];
     mbar_expect_tx(bar, len * (4u * (2u + nref) + 1u) + (k == 0 ? stall : 0u));
@@ -516,14 +520,16 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
   if (b < a.B) {
     SeqCtx x;
     x.b = b;
-    // The staged path takes the chunks [c_lo, c_hi) that hold active tokens,
-    // the k-th of them (chunk c_lo + k) in stage k % kDepth; the gradient
-    // slots outside them are zero-stored.
+    // The staged path takes the chunks [c_lo, c_hi) that hold active tokens
+    // (the last one only up to hi16), the k-th of them (chunk c_lo + k) in
+    // stage k % kDepth; the gradient slots outside [c_lo kChunk, hi16) are
+    // zero-stored.
     int c_lo = 0, c_hi = 0, nlive = 0;
     auto geometry = [&](int2 rg) {
       c_lo = rg.y > rg.x ? rg.x / kChunk : 0;
       c_hi = rg.y > rg.x ? (rg.y + kChunk - 1) / kChunk : 0;
-      if (!staged) c_lo = c_hi = 0;
+      hi16 = rg.y > rg.x ? (int)min((int64_t)((rg.y + 15) & ~15), a.T) : 0;
+      if (!staged) c_lo = c_hi = 0, hi16 = 0;
       nlive = c_hi - c_lo;
     };
     auto first_copies = [&]() {  // one thread
@@ -535,7 +541,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
     auto zero_outside = [&](int t, int nt) {
       if (!staged || !a.grad) return;
       const int64_t v_lo = (int64_t)c_lo * (kChunk / 4);
-      const int64_t v_hi = min((int64_t)c_hi * (kChunk / 4), a.T / 4);
+      const int64_t v_hi = hi16 / 4;
       for (int64_t v = t; v < v_lo; v += nt) grow[v] = z4;
       for (int64_t v = v_hi + t; v < a.T / 4; v += nt) grow[v] = z4;
     };
@@ -632,7 +638,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
           for (int j = 0; j < 4; ++j)
             if ((mw >> (8 * j)) & 0xFFu) kahan(ss, sc, d[j]);
         };
-        const int64_t v1 = staged ? min((int64_t)c_hi * (kChunk / 4), a.T / 4) : a.T / 4;
+        const int64_t v1 = staged ? hi16 / 4 : a.T / 4;
         int64_t v = (staged ? (int64_t)c_lo * (kChunk / 4) : 0) + threadIdx.x;
         for (; v + kLogpsThreads < v1; v += 2 * kLogpsThreads) {
           const uint32_t m0 = __ldg(mrow + v), m1 = __ldg(mrow + v + kLogpsThreads);
@@ -724,7 +730,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
       for (int k = 0; k < issued; ++k) {
         const int slot = k % kDepth;
         const int64_t st = (int64_t)(c_lo + k) * kChunk;
-        const int len = (int)min((int64_t)kChunk, a.T - st);
+        const int len = min(kChunk, hi16 - (c_lo + k) * kChunk);
         // warp 0 waits for the copies (the other warps sleep in the CTA
         // barrier, leaving the issue slots to the warps still computing)
         const bool ready = warp != 0 || mbar_wait(&s_full[slot], (uint32_t)(k / kDepth) & 1u);
