@@ -390,6 +390,9 @@ def workload_config(w: synth.Workload, variant: str = "default",
             cfg["reduction"] = VARIANTS[variant]["reduction"]
     if skip_masked:
         cfg["masked_grad_rows"] = "skipped (GRPO_SKIP_MASKED_GRAD_ROWS)"
+    if not w.V:
+        cfg["workspace"] = ("one workspace for every step; calls after the first skip the "
+                            "header reset (GRPO_FLAG_WORKSPACE_CLEAN)")
     return cfg
 
 
@@ -650,6 +653,7 @@ class LogpsCase:
         self.active = int(self.inp["mask"].sum().item())
         self.out3 = torch.empty(3, dtype=torch.float32, device=device)
         self.wsp = torch.empty(g.grpo_workspace_size(w.B, w.T), dtype=torch.uint8, device=device)
+        self.ws_clean = False  # the first call resets the header
         # logp / old / ref of active tokens, the mask, dL/dlogp of every slot
         self.alg_bytes = 12.0 * self.active + 5.0 * w.B * w.T
         self.extra_bytes = {}
@@ -658,10 +662,14 @@ class LogpsCase:
         w = self.w
         kw = dict(reduction=w.reduction)
         kw.update(self.vkw)
+        # one workspace for every step: each call leaves its header clean, so
+        # every call after the first skips the reset (GRPO_FLAG_WORKSPACE_CLEAN)
         self.g.grpo_loss_from_logps(i["lp"], i["old"], i["ref"], i["mask"], i["R"],
                                     samples_per_prompt=w.samples_per_prompt, clip_eps=w.eps_lo,
                                     clip_eps_hi=w.eps_hi, beta=w.beta, grad=i["grad"],
-                                    out3=self.out3, workspace=self.wsp, profile=prof, **kw)
+                                    out3=self.out3, workspace=self.wsp, profile=prof,
+                                    workspace_clean=self.ws_clean, **kw)
+        self.ws_clean = True
 
     def step(self, k=0, prof=None):
         self._call(self.copies[k % self.COPIES], prof)

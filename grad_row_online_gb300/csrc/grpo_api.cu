@@ -39,7 +39,8 @@ grpo_status_t check_params(const grpo_params_t* p) {
   if (p->reduction == GRPO_FIXED_CONSTANT && !(isfinite(p->norm_constant) && p->norm_constant > 0.f))
     return GRPO_ERR_PARAM;
   if (p->flags & ~(GRPO_ADV_EPS_ADD | GRPO_SKIP_MASKED_GRAD_ROWS | GRPO_FLAG_SEPARATE_PREP |
-                   GRPO_FLAG_TEST_STALLED_COPY | GRPO_FLAG_TEST_STALLED_BARRIER))
+                   GRPO_FLAG_WORKSPACE_CLEAN | GRPO_FLAG_TEST_STALLED_COPY |
+                   GRPO_FLAG_TEST_STALLED_BARRIER))
     return GRPO_ERR_PARAM;
   if (p->kl_type != GRPO_KL_K3 && p->kl_type != GRPO_KL_K1 && p->kl_type != GRPO_KL_K2)
     return GRPO_ERR_PARAM;
@@ -340,7 +341,11 @@ extern "C" grpo_status_t grpo_loss_from_logps(const float* logps, const float* o
     if (logps_fused_capacity(&cap) != cudaSuccess) return GRPO_ERR_CUDA;
     fused = B <= cap;
   }
-  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return GRPO_ERR_CUDA;
+  // the logps kernel's last CTA leaves the header clean; the caller may
+  // state that it still is (GRPO_FLAG_WORKSPACE_CLEAN)
+  if (!(params->flags & GRPO_FLAG_WORKSPACE_CLEAN) &&
+      cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess)
+    return GRPO_ERR_CUDA;
   PrepArgs pa{rewards, bounds, B, T, G, pl.Bg, pl.seq_begin, &hdr->N, spp, params->adv_eps,
               (int)(params->flags & GRPO_ADV_EPS_ADD), completion_mask, 1, A, Aff, adv_out, L,
               rng, hdr};
@@ -532,12 +537,12 @@ extern "C" grpo_status_t grpo_vocab_grad(const void* policy_slice, grpo_dtype_t 
 
 extern "C" grpo_status_t grpo_read_device_status(const void* ws, void* stream) {
   if (!ws) return GRPO_ERR_NULL;
-  unsigned int h = 0;
+  WsHeader h;
   cudaStream_t s = (cudaStream_t)stream;
   if (cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return GRPO_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return GRPO_ERR_CUDA;
-  return (grpo_status_t)h;
+  return (grpo_status_t)(h.status | h.last_status);
 }
 
 extern "C" const char* grpo_status_string(grpo_status_t status) {

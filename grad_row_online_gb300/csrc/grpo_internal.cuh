@@ -38,7 +38,13 @@ struct WsHeader {
   // word, so that one relaxed atomic per CTA carries both (bits 52-63: CTAs
   // arrived, 41-51: live sequences S, 0-40: active tokens N)
   unsigned long long arrive;
+  // grpo_loss_from_logps: the status bits of the call, moved here by its
+  // last CTA, which also zeroes every counter above (the header is then
+  // clean for the next call)
+  unsigned int last_status;
+  unsigned int pad_;
 };
+static_assert(sizeof(WsHeader) <= 256, "the header region is 256 bytes");
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 

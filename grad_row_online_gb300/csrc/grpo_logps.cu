@@ -358,9 +358,9 @@ __device__ __forceinline__ void process_vec(uint32_t mw, const float4& l, const 
 // chunks before the mask scan, or prefetching the whole active range into
 // L2 once it is known, measured slower: the flood of requests delays the
 // mask scan and the grid barrier behind it.)
-static constexpr int kChunkVecs = 1;  // float4 vectors per thread per chunk
+static constexpr int kChunkVecs = 2;  // float4 vectors per thread per chunk
 static constexpr int kChunk = 4 * kLogpsThreads * kChunkVecs;
-static constexpr int kDepth = 4;
+static constexpr int kDepth = 2;
 static constexpr unsigned long long kWaitNs = 200000000ull;  // 0.2 s per bounded wait
 static constexpr uint32_t kWaitRounds = 1u << 26;  // and never more try_wait rounds than this
 
@@ -858,12 +858,26 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
   if (!s_last) return;
   if (threadIdx.x == 0 && a.counts_out)  // every CTA added its counts before its ticket
     for (int j = 0; j < 3; ++j) a.counts_out[j] = __ldcg(&a.hdr->clip[j]);
-  if (a.shard) return;  // the scalar comes from grpo_loss_finalize over all shards' totals
-
-  // the scalar over the B sequence records, in index order
-  const bool bad = ((volatile unsigned*)&a.hdr->status)[0] != 0u;
-  final_scalar_ff<8>(a.seq, a.B, a.B > 0 ? s_NS[0] : 0ull, a.B > 0 ? s_NS[1] : 0ull, a.reduction,
-               a.norm_c, a.beta, bad, a.out3, s_fin);
+  // the status of the call (every CTA set its bits before its ticket)
+  const unsigned status = ((volatile unsigned*)&a.hdr->status)[0];
+  if (!a.shard) {  // a shard's scalar comes from grpo_loss_finalize over all shards' totals
+    // the scalar over the B sequence records, in index order
+    final_scalar_ff<8>(a.seq, a.B, a.B > 0 ? s_NS[0] : 0ull, a.B > 0 ? s_NS[1] : 0ull,
+                       a.reduction, a.norm_c, a.beta, status != 0u, a.out3, s_fin);
+  }
+  // every other CTA has taken its ticket, so nothing reads the counters any
+  // more: leave the header clean for the next call (GRPO_FLAG_WORKSPACE_CLEAN),
+  // the status bits moved to last_status
+  if (threadIdx.x == 0) {
+    WsHeader* h = a.hdr;
+    h->last_status = status;
+    h->status = 0u;
+    h->done_ctas = 0u;
+    h->N = 0ull;
+    h->S = 0ull;
+    h->clip[0] = h->clip[1] = h->clip[2] = 0ull;
+    h->arrive = 0ull;
+  }
 }
 
 // seven 27 KB CTAs per SM need the largest shared-memory carveout; the

@@ -150,3 +150,62 @@ def test_a_stalled_barrier_times_out_and_the_context_survives():
     ref = _call(w, t, flags=g.GRPO_FLAG_SEPARATE_PREP)
     for k in OUTS:
         assert torch.equal(good[k], ref[k]), k
+
+
+@pytest.mark.parametrize("flags", [0, g.GRPO_FLAG_SEPARATE_PREP], ids=["one-launch", "two-launch"])
+def test_clean_workspace_calls_give_the_same_bits(flags):
+    # every call leaves the header clean, so a loop of calls on one workspace
+    # may skip its reset (GRPO_FLAG_WORKSPACE_CLEAN): same bits as a fresh
+    # workspace, for every option, on both forms, after errors and timeouts
+    ws = torch.empty(g.grpo_workspace_size(CSR.B, 100, 0), dtype=torch.uint8, device="cuda")
+    _call(BASE, _tensors(BASE), flags=flags, workspace=ws)  # leaves it clean
+    for w in (BASE, CSR):
+        for T in (64, 100):
+            wt = w.with_(T=T, len_range=(0, T))
+            t = _tensors(wt)
+            for opt in OPTIONS.values():
+                got = _call(wt, t, flags=flags, workspace=ws, workspace_clean=True, **opt)
+                assert g.grpo_read_device_status(ws) == 0
+                want = _call(wt, t, flags=flags, **opt)
+                for k in OUTS:
+                    assert torch.equal(got[k], want[k]), k
+    # a device-detected error is reported by its own call, and the next clean
+    # call is clean
+    t = _tensors(BASE)
+    R = t["R"].clone()
+    R[5] = float("inf")
+    bad = _call(BASE, dict(t, R=R), flags=flags, workspace=ws, workspace_clean=True)
+    assert g.grpo_read_device_status(ws) == g.GRPO_ERR_NONFINITE_REWARD
+    assert torch.isnan(bad["out3"]).all()
+    good = _call(BASE, t, flags=flags, workspace=ws, workspace_clean=True)
+    assert g.grpo_read_device_status(ws) == 0
+    want = _call(BASE, t, flags=flags)
+    for k in OUTS:
+        assert torch.equal(good[k], want[k]), k
+    if flags == 0:
+        # a barrier wait that runs out still leaves the header clean
+        bad = _call(BASE, t, flags=g.GRPO_FLAG_TEST_STALLED_BARRIER, workspace=ws,
+                    workspace_clean=True)
+        assert g.grpo_read_device_status(ws) == g.GRPO_ERR_TIMEOUT
+        good = _call(BASE, t, workspace=ws, workspace_clean=True)
+        assert g.grpo_read_device_status(ws) == 0
+        for k in OUTS:
+            assert torch.equal(good[k], want[k]), k
+
+
+def test_clean_workspace_shard_calls():
+    w = BASE
+    t = _tensors(w)
+    mask = w.completion_mask()
+    counts = torch.tensor([int(mask.sum()), int((mask.sum(1) > 0).sum())], dtype=torch.int64,
+                          device="cuda")
+    ws = torch.zeros(g.grpo_workspace_size(w.B, w.T, 0), dtype=torch.uint8, device="cuda")
+    outs = []
+    for clean in (False, True, True):
+        tot = g.totals_buffer(w.B)
+        r = _call(w, t, shard=g.Shard(0, counts, tot), workspace=ws, workspace_clean=clean,
+                  want_per_seq=False)
+        outs.append((tot, r["grad"], r["clip_counts"]))
+    for o in outs[1:]:
+        for a, b in zip(o, outs[0]):
+            assert torch.equal(a, b)
