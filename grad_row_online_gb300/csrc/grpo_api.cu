@@ -356,7 +356,8 @@ extern "C" grpo_status_t grpo_loss_from_logps(const float* logps, const float* o
                params->grad_scale, params->reduction, variant_of(params),
                params->norm_constant, params->clip_counts, NS, pl.shard ? 1 : 0, params->flags,
                fused ? 1 : 0, rewards, bounds, G, pl.Bg, pl.seq_begin, spp, params->adv_eps,
-               (int)(params->flags & GRPO_ADV_EPS_ADD), adv_out};
+               (int)(params->flags & GRPO_ADV_EPS_ADD), adv_out,
+               (uint32_t*)(w + lay.off_slots)};
   cudaError_t e = launch_logps(la, params->profile, s);
   if (fused && e == cudaErrorCooperativeLaunchTooLarge) {
     // fewer SMs than the device has (a partitioned device, say): the two

@@ -815,6 +815,9 @@ struct LogpsArgs {
   float adv_eps;
   int eps_add;
   float* adv_out;  // nullable [B]
+  // the workspace's token-slot area (16 bytes per slot, unused by this
+  // path's sums): each sequence's vectors left to the general path
+  uint32_t* defer;
 };
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);

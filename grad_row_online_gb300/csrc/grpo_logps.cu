@@ -90,18 +90,32 @@ struct SeqCtx {
   float em_seq;       // GSPO: rho_i - 1 (fp32 and double)
   double em_seq_d;
 };
-__device__ __noinline__ float w_precise(float lp, float o, float rf, const SeqCtx& x,
-                                        const LogpsArgs& a) {
-  const double A = x.Ad;
-  const double c = a.reduction == GRPO_TOKEN_MEAN      ? 1.0 / (double)(x.N > 0 ? x.N : 1)
-                   : a.reduction == GRPO_SEQUENCE_MEAN ? 1.0 / ((double)(x.S > 0 ? x.S : 1) * (double)x.L)
-                                                       : 1.0 / (double)a.norm_c;
-  const double em = a.var.seq_ratio ? x.em_seq_d : expm1((double)lp - (double)o);
-  const double d = a.ref ? (double)rf - (double)lp : 0.0;
+// The sequence's constants the precise path needs, in shared memory (set
+// once per CTA before the token loop): the rare call then takes three
+// floats, and neither a per-thread struct nor the kernel's arguments need an
+// address (either would give the kernel a stack frame).
+struct PreciseCtx {
+  double A, em_seq;  // the advantage; GSPO: rho_i - 1
+  unsigned long long N, S;
+  int L, reduction;
+  float norm_c, grad_scale;
+  Variant var;
+  bool has_ref;
+};
+__shared__ PreciseCtx g_pc;
+__device__ __noinline__ float w_precise(float lp, float o, float rf) {
+  const PreciseCtx& p = g_pc;
+  // the token weight c: 1/max(N,1), 1/(max(S,1) L) or 1/C
+  const double c = p.reduction == GRPO_TOKEN_MEAN ? 1.0 / (double)(p.N > 0 ? p.N : 1)
+                   : p.reduction == GRPO_SEQUENCE_MEAN
+                       ? 1.0 / ((double)(p.S > 0 ? p.S : 1) * (double)p.L)
+                       : 1.0 / (double)p.norm_c;
+  const double em = p.var.seq_ratio ? p.em_seq : expm1((double)lp - (double)o);
+  const double d = p.has_ref ? (double)rf - (double)lp : 0.0;
   const double emd = expm1(d);
   const TokEpi<double> t =
-      token_epilogue<double>(em, (double)lp, d, emd, emd - d, a.ref != nullptr, A, a.var);
-  return (float)((double)a.grad_scale * c * t.g);
+      token_epilogue<double>(em, (double)lp, d, emd, emd - d, p.has_ref, p.A, p.var);
+  return (float)((double)p.grad_scale * c * t.g);
 }
 
 __device__ __forceinline__ void kahan(float& s, float& c, float x) {
@@ -142,7 +156,7 @@ struct Acc {
 __device__ __forceinline__ float token_w(float lp, float o, float rf, const TokEpi<float>& t,
                                          const SeqCtx& x, const LogpsArgs& a) {
   float w = __fmul_rn(x.gc, t.g);
-  if (fabsf(w) > kWPrecise) w = w_precise(lp, o, rf, x, a);
+  if (fabsf(w) > kWPrecise) w = w_precise(lp, o, rf);
   return w;
 }
 
@@ -208,7 +222,7 @@ __device__ __forceinline__ float2 pair_fast(float2 lp, float2 od, float2 rf, boo
 // (caught by its sum of g^2); NaNs fail the check too.
 template <bool kCount>
 __device__ __forceinline__ bool vec_fast(const float4& l4, const float4& o4, const float4& r4,
-                                         bool has_ref, const FastCtx& f, float (&w)[4],
+                                         bool has_ref, const FastCtx& f, float4& w,
                                          float& vq, float& vk, int& nclip) {
   float2 sq = f2(0.f), sk = f2(0.f), d2 = f2(0.f), g2 = f2(0.f);
   nclip = 0;
@@ -216,10 +230,7 @@ __device__ __forceinline__ bool vec_fast(const float4& l4, const float4& o4, con
                                        make_float2(r4.x, r4.y), has_ref, f, sq, sk, d2, g2, nclip);
   const float2 w23 = pair_fast<kCount>(make_float2(l4.z, l4.w), make_float2(o4.z, o4.w),
                                        make_float2(r4.z, r4.w), has_ref, f, sq, sk, d2, g2, nclip);
-  w[0] = w01.x;
-  w[1] = w01.y;
-  w[2] = w23.x;
-  w[3] = w23.y;
+  w = make_float4(w01.x, w01.y, w23.x, w23.y);
   vq = __fadd_rn(sq.x, sq.y);
   vk = __fadd_rn(sk.x, sk.y);
   return __fadd_rn(d2.x, d2.y) < 0.25f && __fadd_rn(g2.x, g2.y) <= f.g2_max;
@@ -235,7 +246,7 @@ __device__ __forceinline__ bool vec_fast(const float4& l4, const float4& o4, con
 __device__ __forceinline__ bool vec_fast_variant(const float4& l4, const float4& o4,
                                                  const float4& r4, bool has_ref,
                                                  const SeqCtx& x, const LogpsArgs& a,
-                                                 float (&w)[4], float& vq, float& vk,
+                                                 float4& w, float& vq, float& vk,
                                                  unsigned (&nc)[3]) {
   const float lp[4] = {l4.x, l4.y, l4.z, l4.w};
   float em[4], d[4], emd[4], k3[4];
@@ -273,6 +284,7 @@ __device__ __forceinline__ bool vec_fast_variant(const float4& l4, const float4&
   vk = 0.f;
   nc[0] = nc[1] = nc[2] = 0u;
   bool small = true;
+  float wj[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const TokEpi<float> t = token_epilogue<float>(em[j], lp[j], d[j], emd[j], k3[j], has_ref,
@@ -282,9 +294,10 @@ __device__ __forceinline__ bool vec_fast_variant(const float4& l4, const float4&
     nc[0] += t.clip == 1;
     nc[1] += t.clip == 2;
     nc[2] += t.clip == 3;
-    w[j] = __fmul_rn(x.gc, t.g);
-    small = small && fabsf(w[j]) <= kWPrecise;
+    wj[j] = __fmul_rn(x.gc, t.g);
+    small = small && fabsf(wj[j]) <= kWPrecise;
   }
+  w = make_float4(wj[0], wj[1], wj[2], wj[3]);
   return __fadd_rn(d2.x, d2.y) < 0.25f && small;
 }
 
@@ -296,44 +309,46 @@ __device__ __forceinline__ bool all_active(uint32_t mw) {
 // The same vector on the general path, token by token.
 __device__ __forceinline__ void vec_general(uint32_t mw, const float4& l4, const float4& o4,
                                             const float4& r4, const SeqCtx& x,
-                                            const LogpsArgs& a, float (&w)[4], float& vq,
+                                            const LogpsArgs& a, float4& w, float& vq,
                                             float& vk, Acc& acc) {
-  const float lp[4] = {l4.x, l4.y, l4.z, l4.w};
-  const float od[4] = {o4.x, o4.y, o4.z, o4.w};
-  const float rf[4] = {r4.x, r4.y, r4.z, r4.w};
-  // the token loop is kept rolled (code size); its arrays, indexed by the
-  // loop counter, live in local memory, so the gradients go through wt and
-  // reach w (which the fast path keeps in registers) by constant indices
-  float wt[4];
+  // the token loop is kept rolled (code size); its operands and results are
+  // picked by selects on the loop counter, so nothing goes to local memory
+  float w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f;
   vq = 0.f;
   vk = 0.f;
 #pragma unroll 1
   for (int j = 0; j < 4; ++j) {
-    wt[j] = 0.f;
     if ((mw >> (8 * j)) & 0xFFu) {
-      const TokEpi<float> t = tok_terms(lp[j], od[j], rf[j], x.A, a, x.em_seq);
+      const float lp = j == 0 ? l4.x : j == 1 ? l4.y : j == 2 ? l4.z : l4.w;
+      const float od = j == 0 ? o4.x : j == 1 ? o4.y : j == 2 ? o4.z : o4.w;
+      const float rf = j == 0 ? r4.x : j == 1 ? r4.y : j == 2 ? r4.z : r4.w;
+      const TokEpi<float> t = tok_terms(lp, od, rf, x.A, a, x.em_seq);
       vq = __fadd_rn(vq, t.q);
       vk = __fadd_rn(vk, t.k);
       acc.count(t.clip);
-      wt[j] = token_w(lp[j], od[j], rf[j], t, x, a);
+      const float wj = token_w(lp, od, rf, t, x, a);
+      w0 = j == 0 ? wj : w0;
+      w1 = j == 1 ? wj : w1;
+      w2 = j == 2 ? wj : w2;
+      w3 = j == 3 ? wj : w3;
     }
   }
-  w[0] = wt[0];
-  w[1] = wt[1];
-  w[2] = wt[2];
-  w[3] = wt[3];
+  w = make_float4(w0, w1, w2, w3);
 }
 
-// One vector of four slots: its gradient, and its q / k sums into the
-// thread's Kahan pairs.  Fully active vectors take the fast path when their
-// range check passes; everything else the general path.
+// One vector of four slots in the token loop: its gradient, and its q / k
+// sums into the thread's Kahan pairs, when the vector is fully active and a
+// fast path's range check passes (or fully masked: zeros).  Returns false
+// for every other vector, which the thread records and evaluates on the
+// general path after the loop (deferred_list): the loop then holds no general
+// path code, no call and no double arithmetic.
 template <bool kDefault, bool kCount>
-__device__ __forceinline__ void process_vec(uint32_t mw, const float4& l, const float4& o,
+__device__ __forceinline__ bool process_vec(uint32_t mw, const float4& l, const float4& o,
                                             const float4& r, bool has_ref, const FastCtx& f,
                                             const SeqCtx& x, const LogpsArgs& a, Acc& acc,
-                                            float (&w)[4]) {
-  w[0] = w[1] = w[2] = w[3] = 0.f;
-  if (mw == 0u) return;
+                                            float4& w) {
+  w = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (mw == 0u) return true;
   float vq, vk;
   int nclip;
   unsigned nc[3];
@@ -344,10 +359,25 @@ __device__ __forceinline__ void process_vec(uint32_t mw, const float4& l, const 
     acc.nc[0] += nc[0];
     acc.nc[1] += nc[1];
     acc.nc[2] += nc[2];
+  } else if (kDefault) {
+    return false;
   } else {
     vec_general(mw, l, o, r, x, a, w, vq, vk, acc);
   }
   kahan2(acc.s, acc.c, make_float2(vq, vk));
+  return true;
+}
+
+// The vectors a thread leaves to the general path, in the order it met them:
+// entry k of thread t at list[t * m + k], m = ceil(vectors of the row / 128)
+// (the most any thread meets), in the workspace's token-slot area of the
+// sequence (16 bytes per slot; at most T / 4 + 127 entries are used, below
+// its 4 T words).  Each thread reads back only its own entries.
+// (Only the count lives in a register through the loop; the address is
+// formed from the kernel's arguments when a vector is recorded.)
+__device__ __forceinline__ uint32_t* deferred_list(const LogpsArgs& a, int64_t b) {
+  const int64_t m = (a.T / 4 + kLogpsThreads - 1) / kLogpsThreads;
+  return a.defer + b * 4 * a.T + (int64_t)threadIdx.x * m;
 }
 
 // ---- staging through shared memory with bulk asynchronous copies ----
@@ -686,6 +716,8 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
         s_adv = a.A[b];
         s_aff = a.Aff[b];
       }
+      g_pc = PreciseCtx{s_adv, x.em_seq_d, s_NS[0], s_NS[1], x.L, a.reduction, a.norm_c,
+                        a.grad_scale, a.var, has_ref};
     }
     __syncthreads();
     x.N = s_NS[0];
@@ -716,6 +748,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
       f.g2_max = __fmul_rn(gm, gm);
     }
     Acc acc;
+    int n_def = 0;  // vectors this thread left to the general path
     if (staged) {
       // A wait that runs out (never expected outside the test hook) is
       // recorded; the CTA then issues no further copy, still waits for the
@@ -745,10 +778,13 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
           for (int u = 0; u < kChunkVecs; ++u) {
             const int v = threadIdx.x + u * kLogpsThreads;
             if (4 * v < len) {
-              float w[4];
-              process_vec<kDefault, kCount>(S.mk[v], S.lp[v], S.od[v], has_ref ? S.rf[v] : z4, has_ref,
-                                    f, x, a, acc, w);
-              if (a.grad) grow[st / 4 + v] = make_float4(w[0], w[1], w[2], w[3]);
+              float4 w;
+              if (process_vec<kDefault, kCount>(S.mk[v], S.lp[v], S.od[v],
+                                                has_ref ? S.rf[v] : z4, has_ref, f, x, a, acc, w)) {
+                if (a.grad) grow[st / 4 + v] = w;
+              } else {
+                deferred_list(a, b)[n_def++] = (uint32_t)(st / 4 + v);
+              }
             }
           }
         }
@@ -784,9 +820,12 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
           if (a.ref) r1 = __ldg(rrow + v + kS);
         }
         const uint32_t m2 = v + 2 * kS < nv ? __ldg(mrow + v + 2 * kS) : 0u;
-        float w[4];
-        process_vec<kDefault, kCount>(m0, l0, o0, r0, has_ref, f, x, a, acc, w);
-        if (a.grad) grow[v] = make_float4(w[0], w[1], w[2], w[3]);
+        float4 w;
+        if (process_vec<kDefault, kCount>(m0, l0, o0, r0, has_ref, f, x, a, acc, w)) {
+          if (a.grad) grow[v] = w;
+        } else {
+          deferred_list(a, b)[n_def++] = (uint32_t)v;
+        }
         m0 = m1;
         m1 = m2;
         l0 = l1;
@@ -794,6 +833,8 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
         r0 = r1;
       }
     } else {
+      // the scalar loop (rows that break the vector paths' rules): every
+      // token on the general path
       for (int64_t t = threadIdx.x; t < a.T; t += blockDim.x) {
         float w = 0.f;
         if (a.mask[base + t]) {
@@ -806,6 +847,20 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
         }
         if (a.grad) a.grad[base + t] = w;
       }
+    }
+    // the vectors this thread left to the general path, in the order it met
+    // them (vector paths only: both need vec_ok's alignment)
+    for (int k = 0; k < n_def; ++k) {
+      const int64_t v = deferred_list(a, b)[k];
+      const uint32_t mw = __ldg(reinterpret_cast<const uint32_t*>(a.mask + base) + v);
+      const float4 l4 = __ldg(reinterpret_cast<const float4*>(a.logps + base) + v);
+      const float4 o4 = __ldg(reinterpret_cast<const float4*>(a.old + base) + v);
+      const float4 r4 = has_ref ? __ldg(reinterpret_cast<const float4*>(a.ref + base) + v) : z4;
+      float vq, vk;
+      float4 w;
+      vec_general(mw, l4, o4, r4, x, a, w, vq, vk, acc);
+      kahan2(acc.s, acc.c, make_float2(vq, vk));
+      if (a.grad) reinterpret_cast<float4*>(a.grad + base)[v] = w;
     }
     // the sequence's totals as float pairs: threads' Kahan sums, a fixed
     // xor tree per warp, warps in index order
