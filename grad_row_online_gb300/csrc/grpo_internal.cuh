@@ -24,7 +24,9 @@ namespace grpo {
 //   seq      SeqTotal[B]      per-sequence totals (the records of
 //                             grpo_seq_total_t: double totals on the logits
 //                             path, float pairs on the logps path)
-//   slots    double[2 B T]    per-token policy / KL terms (logits path)
+//   slots    double[2 B T]    per-token policy / KL terms (logits path); the
+//                             logps path's per-thread lists of vectors left
+//                             to its general path
 // ----------------------------------------------------------------------------
 struct WsHeader {
   unsigned int status;             // device-detected error bits

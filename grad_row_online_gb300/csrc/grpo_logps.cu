@@ -337,11 +337,13 @@ __device__ __forceinline__ void vec_general(uint32_t mw, const float4& l4, const
 }
 
 // One vector of four slots in the token loop: its gradient, and its q / k
-// sums into the thread's Kahan pairs, when the vector is fully active and a
-// fast path's range check passes (or fully masked: zeros).  Returns false
-// for every other vector, which the thread records and evaluates on the
-// general path after the loop (deferred_list): the loop then holds no general
-// path code, no call and no double arithmetic.
+// sums into the thread's Kahan pairs.  Fully active vectors take a fast path
+// when its range check passes; fully masked ones give zeros.  Any other
+// vector: the default-loss instantiation returns false, and the thread
+// records it and evaluates it on the general path after the loop
+// (deferred_list), so that loop holds no general-path code, call or double
+// arithmetic; the variants' instantiation (whose loop measured faster with
+// it) takes the general path in place.
 template <bool kDefault, bool kCount>
 __device__ __forceinline__ bool process_vec(uint32_t mw, const float4& l, const float4& o,
                                             const float4& r, bool has_ref, const FastCtx& f,
