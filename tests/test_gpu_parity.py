@@ -357,8 +357,10 @@ def _mask_pattern(B, T, pattern, seed):
 @pytest.mark.parametrize("T", [2064, 100])
 @pytest.mark.parametrize("pattern", ["random", "suffix", "single"])
 def test_logps_mask_patterns(T, pattern):
-    # T=2064: rows staged through shared memory in five chunks (the ring of
-    # four wraps, the last chunk is partial); T=100: the register path
+    # T=2064: rows staged through shared memory in three 1,024-token chunks
+    # (the ring of two wraps, the last chunk is partial); T=100: the register
+    # path.  The random mask leaves most vectors partly active: those go to the
+    # general path after the token loop, several per thread.
     w = LOGPS_SMALL.with_(B=16, T=T)
     c = _logps_case(w)
     c["mask"] = _mask_pattern(w.B, w.T, pattern, seed=T)
@@ -371,3 +373,16 @@ def test_logps_large_weights_take_the_precise_path():
     w = LOGPS_SMALL.with_(B=8, T=4, len_range=(0, 2))
     c = _logps_case(w)
     _logps_check(w, c, _logps_run(w, c))
+
+
+@pytest.mark.parametrize("flags", [0, g.GRPO_FLAG_SEPARATE_PREP], ids=["one-launch", "two-launch"])
+def test_logps_every_vector_on_the_general_path(flags):
+    # log ratios ~N(0, 2): nearly every vector fails the fast path's range
+    # check, so each thread evaluates its whole share of the row (eight vectors
+    # at T=4096) after the token loop, from its list in the workspace
+    w = LOGPS_SMALL.with_(name="logps_general", B=8, T=4096, len_range=(3000, 4096),
+                          old_sigma=2.0, ref_logp_sigma=1.0)
+    c = _logps_case(w)
+    for reduction in (0, 1):
+        _logps_check(w, c, _logps_run(w, c, reduction=reduction, extra_flags=flags),
+                     reduction=reduction)
