@@ -658,8 +658,8 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
       float ss = 0.f, sc = 0.f;
       if (vec_ok(a)) {
         // 4-slot vectors of the evaluated chunks (the whole row off the
-        // staged path), two per thread in flight, read whole (masked slots
-        // are loaded but never used)
+        // staged path), four per thread in flight, read whole (masked slots
+        // are loaded but never used); each thread adds its vectors in order
         const uint32_t* mrow = reinterpret_cast<const uint32_t*>(a.mask + base);
         const float4* lrow = reinterpret_cast<const float4*>(a.logps + base);
         const float4* orow = reinterpret_cast<const float4*>(a.old + base);
@@ -672,14 +672,20 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
         };
         const int64_t v1 = staged ? hi16 / 4 : a.T / 4;
         int64_t v = (staged ? (int64_t)c_lo * (kChunk / 4) : 0) + threadIdx.x;
-        for (; v + kLogpsThreads < v1; v += 2 * kLogpsThreads) {
-          const uint32_t m0 = __ldg(mrow + v), m1 = __ldg(mrow + v + kLogpsThreads);
-          const float4 l0 = __ldg(lrow + v), l1 = __ldg(lrow + v + kLogpsThreads);
-          const float4 o0 = __ldg(orow + v), o1 = __ldg(orow + v + kLogpsThreads);
-          add4(m0, l0, o0);
-          add4(m1, l1, o1);
+        constexpr int kPre = 4;  // vectors per thread in flight
+        for (; v < v1; v += kPre * kLogpsThreads) {
+          uint32_t m[kPre];
+          float4 l[kPre], o[kPre];
+#pragma unroll
+          for (int u = 0; u < kPre; ++u) {
+            const int64_t vu = v + u * kLogpsThreads;
+            m[u] = vu < v1 ? __ldg(mrow + vu) : 0u;
+            l[u] = vu < v1 ? __ldg(lrow + vu) : make_float4(0.f, 0.f, 0.f, 0.f);
+            o[u] = vu < v1 ? __ldg(orow + vu) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int u = 0; u < kPre; ++u) add4(m[u], l[u], o[u]);
         }
-        if (v < v1) add4(__ldg(mrow + v), __ldg(lrow + v), __ldg(orow + v));
       } else {
         for (int64_t t = threadIdx.x; t < a.T; t += blockDim.x)
           if (a.mask[base + t]) kahan(ss, sc, __fsub_rn(a.logps[base + t], a.old[base + t]));
