@@ -654,6 +654,7 @@ class LogpsCase:
         self.out3 = torch.empty(3, dtype=torch.float32, device=device)
         self.wsp = torch.empty(g.grpo_workspace_size(w.B, w.T), dtype=torch.uint8, device=device)
         self.ws_clean = False  # the first call resets the header
+        self.overlap_launch = False  # --overlap-launch: GRPO_FLAG_OVERLAP_LAUNCH
         # logp / old / ref of active tokens, the mask, dL/dlogp of every slot
         self.alg_bytes = 12.0 * self.active + 5.0 * w.B * w.T
         self.extra_bytes = {}
@@ -668,7 +669,8 @@ class LogpsCase:
                                     samples_per_prompt=w.samples_per_prompt, clip_eps=w.eps_lo,
                                     clip_eps_hi=w.eps_hi, beta=w.beta, grad=i["grad"],
                                     out3=self.out3, workspace=self.wsp, profile=prof,
-                                    workspace_clean=self.ws_clean, **kw)
+                                    workspace_clean=self.ws_clean,
+                                    overlap_launch=self.overlap_launch, **kw)
         self.ws_clean = True
 
     def step(self, k=0, prof=None):
@@ -726,6 +728,10 @@ def run_gpu(args, w, ws, rank, local):
         case = VocabCase(w, device, args.variant, args.tp)
     else:
         case = (LogpsCase if w.V == 0 else LogitsCase)(w, device, args.variant, args.skip_masked)
+    if args.overlap_launch:
+        if not isinstance(case, LogpsCase):
+            raise SystemExit("--overlap-launch applies to the logps workloads")
+        case.overlap_launch = True
     stream = torch.cuda.current_stream(device)
 
     t0 = time.perf_counter()
@@ -818,6 +824,9 @@ def run_gpu(args, w, ws, rank, local):
         # logits' storage type is in config["storage_dtype"])
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": dict(workload_config(w, args.variant, args.skip_masked),
+                                            **({"launch": "GRPO_FLAG_OVERLAP_LAUNCH: dispatched "
+                                                "while the previous step ends, not "
+                                                "cooperative"} if args.overlap_launch else {}),
                                             **({"vocab_slices": args.tp} if args.tp else {})),
         "median_ms": statistics.median(step_ms), "min_ms": min(step_ms),
         "max_ms": max(step_ms),
@@ -859,6 +868,8 @@ def main():
                     help="loss variant to time (default: the operator page's GRPO loss)")
     ap.add_argument("--tp", type=int, default=0,
                     help="time the vocabulary-parallel path with this many slices (on one GPU)")
+    ap.add_argument("--overlap-launch", action="store_true",
+                    help="logps workloads: GRPO_FLAG_OVERLAP_LAUNCH (nothing else runs on the GPU)")
     ap.add_argument("--skip-masked", action="store_true",
                     help="leave masked gradient rows untouched (GRPO_SKIP_MASKED_GRAD_ROWS)")
     ap.add_argument("--T", type=int, default=0,

@@ -32,6 +32,7 @@ GRPO_ADV_EPS_ADD = 1
 GRPO_SKIP_MASKED_GRAD_ROWS = 2
 GRPO_FLAG_SEPARATE_PREP = 4  # grpo_loss_from_logps: advantages / counts as their own launch
 GRPO_FLAG_WORKSPACE_CLEAN = 8  # grpo_loss_from_logps: the header is clean, skip its reset
+GRPO_FLAG_OVERLAP_LAUNCH = 16  # grpo_loss_from_logps: dispatch while the previous kernel ends
 GRPO_FLAG_TEST_STALLED_COPY = 0x80000000  # test hook (see include/grpo.h)
 GRPO_FLAG_TEST_STALLED_BARRIER = 0x40000000  # test hook (see include/grpo.h)
 GRPO_ERR_ACTION_RANGE = 16  # device-detected status bits (grpo_read_device_status)
@@ -402,13 +403,17 @@ def grpo_loss_from_logps(logps: torch.Tensor, old_logps: torch.Tensor,
                          norm_constant: Optional[float] = None,
                          want_clip_counts: bool = False, shard: Optional[Shard] = None,
                          ratio_level: str = "token", workspace_clean: bool = False,
-                         extra_flags: int = 0) -> dict:
+                         overlap_launch: bool = False, extra_flags: int = 0) -> dict:
     """GRPO loss from per-token log-probs; ``grad`` gives dL/dlogp [B,T].
     Variants, outputs and ``shard`` as in grpo_loss_fwd_bwd.
     ``workspace_clean``: the given ``workspace`` was last used by a
     grpo_loss_from_logps call that succeeded (or was zeroed), so its header
     is clean and the call skips resetting it (GRPO_FLAG_WORKSPACE_CLEAN; a
-    workspace allocated here is never clean).  ``extra_flags``
+    workspace allocated here is never clean).  ``overlap_launch``: the
+    one-launch form is dispatched while the previous kernel on the stream
+    ends instead of cooperatively; the caller states that no other kernel
+    holds SMs for long meanwhile (GRPO_FLAG_OVERLAP_LAUNCH, include/grpo.h).
+    ``extra_flags``
     are raw grpo_params_t flag bits (e.g. GRPO_FLAG_TEST_STALLED_COPY)."""
     _dev(logps, "logps", torch.float32)
     B, T = logps.shape
@@ -426,7 +431,8 @@ def grpo_loss_from_logps(logps: torch.Tensor, old_logps: torch.Tensor,
     p, prof = _params(clip_eps, clip_eps_hi, beta, adv_eps, grad_scale, reduction,
                       (GRPO_ADV_EPS_ADD if eps_add else 0)
                       | (GRPO_FLAG_WORKSPACE_CLEAN if workspace_clean and workspace is not None
-                         else 0) | int(extra_flags), profile, kl,
+                         else 0) | (GRPO_FLAG_OVERLAP_LAUNCH if overlap_launch else 0)
+                      | int(extra_flags), profile, kl,
                       surrogate, dual_clip_c, norm_constant, counts, shard, ratio_level)
     if grad is True:
         grad_t = torch.empty((B, T), dtype=torch.float32, device=dev)

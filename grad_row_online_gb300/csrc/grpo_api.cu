@@ -39,7 +39,7 @@ grpo_status_t check_params(const grpo_params_t* p) {
   if (p->reduction == GRPO_FIXED_CONSTANT && !(isfinite(p->norm_constant) && p->norm_constant > 0.f))
     return GRPO_ERR_PARAM;
   if (p->flags & ~(GRPO_ADV_EPS_ADD | GRPO_SKIP_MASKED_GRAD_ROWS | GRPO_FLAG_SEPARATE_PREP |
-                   GRPO_FLAG_WORKSPACE_CLEAN | GRPO_FLAG_TEST_STALLED_COPY |
+                   GRPO_FLAG_WORKSPACE_CLEAN | GRPO_FLAG_OVERLAP_LAUNCH | GRPO_FLAG_TEST_STALLED_COPY |
                    GRPO_FLAG_TEST_STALLED_BARRIER))
     return GRPO_ERR_PARAM;
   if (p->kl_type != GRPO_KL_K3 && p->kl_type != GRPO_KL_K1 && p->kl_type != GRPO_KL_K2)

@@ -999,8 +999,14 @@ cudaError_t launch_logps(const LogpsArgs& a, const grpo_profile_t* prof, cudaStr
   if (a.fused) {
     // every CTA resident at once: the grid barrier's precondition
     if (grid > cap) return cudaErrorCooperativeLaunchTooLarge;
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    if (a.flags & GRPO_FLAG_OVERLAP_LAUNCH) {
+      // the caller vouches for residency (include/grpo.h); dispatch early
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+    } else {
+      attr[0].id = cudaLaunchAttributeCooperative;
+      attr[0].val.cooperative = 1;
+    }
     cfg.numAttrs = 1;
   } else if (!(prof && (prof->start || prof->stop))) {
     // programmatic dependent launch: the CTAs may start while prep finishes

@@ -124,6 +124,18 @@ typedef enum {
  * log-probs step after step on one workspace.  Ignored by the other entry
  * points, which always reset the header (and leave it in use). */
 #define GRPO_FLAG_WORKSPACE_CLEAN 8u
+/* grpo_loss_from_logps' one-launch form: launch the kernel as a programmatic
+ * dependent of the kernel before it on the stream, so that its CTAs are
+ * dispatched while that kernel's last CTAs still run (they wait for it to
+ * complete before touching memory), instead of as a cooperative launch, which
+ * would rule that out (about 2 us per call on GB300).  The kernel's grid
+ * barrier still needs every CTA of the batch resident at once, which only the
+ * cooperative launch guarantees: with this flag the caller states that no
+ * other kernel holds SMs for long while the call runs (nothing running on
+ * other streams, say).  If that does not hold, the barrier's bounded wait runs
+ * out (0.2 s) and the call reports GRPO_ERR_TIMEOUT with NaN loss outputs.
+ * Ignored by the other entry points and by the two-launch form. */
+#define GRPO_FLAG_OVERLAP_LAUNCH 16u
 /* Test hook, for the failure-detection tests only: in grpo_loss_from_logps'
  * staged path (T % 16 == 0, 16-byte aligned arrays) the first asynchronous
  * copy of sequence 0 is made to under-deliver, so its bounded wait runs out

@@ -112,7 +112,7 @@ def test_fwd_rejects_bad_arguments(lib):
     assert _fwd(lib, p=_params(adv_eps=0.0)) == 6
     assert _fwd(lib, p=_params(grad_scale=float("inf"))) == 6
     assert _fwd(lib, p=_params(reduction=3)) == 6
-    assert _fwd(lib, p=_params(flags=16)) == 6
+    assert _fwd(lib, p=_params(flags=64)) == 6
     # loss variants
     assert _fwd(lib, p=_params(reduction=2)) == 6  # fixed constant without a constant
     assert _fwd(lib, p=_params(reduction=2, norm_constant=-1.0)) == 6

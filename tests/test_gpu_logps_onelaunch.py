@@ -209,3 +209,31 @@ def test_clean_workspace_shard_calls():
     for o in outs[1:]:
         for a, b in zip(o, outs[0]):
             assert torch.equal(a, b)
+
+
+def test_overlap_launch_gives_the_same_bits():
+    # GRPO_FLAG_OVERLAP_LAUNCH: the one-launch kernel dispatched while the
+    # previous kernel on the stream ends (nothing else runs on this GPU in the
+    # test, so every CTA becomes resident); back-to-back calls on one
+    # workspace give the cooperative launch's bits
+    ws = torch.empty(g.grpo_workspace_size(CSR.B, 100, 0), dtype=torch.uint8, device="cuda")
+    for w in (BASE, CSR):
+        for T in (64, 100):
+            wt = w.with_(T=T, len_range=(0, T))
+            t = _tensors(wt)
+            for opt in OPTIONS.values():
+                want = _call(wt, t, **opt)
+                args = dict(clip_eps=wt.eps_lo, clip_eps_hi=wt.eps_hi, beta=wt.beta,
+                            want_per_seq=True, want_adv=True, want_clip_counts=True,
+                            workspace=ws, overlap_launch=True, **opt)
+                if wt.samples_per_prompt:
+                    args["samples_per_prompt"] = wt.samples_per_prompt
+                else:
+                    args["group_boundaries"] = t["bounds"]
+                outs = [g.grpo_loss_from_logps(t["lp"], t["old"], t["ref"], t["mask"], t["R"],
+                                               workspace_clean=k > 0, **args) for k in range(3)]
+                torch.cuda.synchronize()
+                assert g.grpo_read_device_status(ws) == 0
+                for got in outs:
+                    for k in OUTS:
+                        assert torch.equal(got[k], want[k]), k
