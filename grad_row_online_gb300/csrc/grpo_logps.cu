@@ -6,13 +6,16 @@
 // Parallel" for the two nested reductions (token slots -> sequence totals ->
 // scalar).
 //
-// One kernel, after prep has counted the active tokens (L_i, N and S in the
-// workspace): one CTA per sequence evaluates each active token's policy and
-// KL terms once, writes dL/dlogp for every slot (0 on masked ones) and forms
-// the sequence's totals in a fixed order; the CTA that finishes last (an
-// atomic ticket that nobody waits on) forms the scalar from the B totals in
-// index order.  The whole cost is one pass over logps / old_logps /
-// ref_logps / mask plus the gradient write.
+// One CTA per sequence evaluates each active token's policy and KL terms
+// once, writes dL/dlogp for every slot (0 on masked ones) and forms the
+// sequence's totals in a fixed order; the CTA that finishes last (an atomic
+// ticket that nobody waits on) forms the scalar from the B totals in index
+// order.  When every sequence's CTA fits on the GPU at once the kernel is one
+// cooperative launch that also does the advantage / count pass: each CTA
+// scans its own mask row and forms its own advantage, and the CTAs meet at a
+// grid barrier for the batch counts N and S; otherwise (or on request) that
+// pass runs first as its own kernel.  The whole cost is one pass over logps /
+// old_logps / ref_logps / mask plus the gradient write.
 //
 // Arithmetic: fp32 per token, Kahan sums per thread, float pairs (two_sum)
 // for every sum above that.  No fp64 on the common path: GB300's fp64 pipe
