@@ -304,6 +304,47 @@ __device__ __forceinline__ bool vec_fast_variant(const float4& l4, const float4&
   return __fadd_rn(d2.x, d2.y) < 0.25f && small;
 }
 
+enum : int { kModeDefault = 0, kModeVariant = 1, kModeGspo = 2 };
+
+// GSPO with the clipped surrogate and k3: every token of the sequence shares
+// the ratio rho_i, so its policy term q, policy gradient and clip are the
+// sequence's constants (token_epilogue at r - 1 = rho_i - 1, once per CTA);
+// per token only the KL term and its gradient remain: k3 and e^d - 1 from
+// the packed polynomial, g = g_pol - beta (e^d - 1).
+struct GspoCtx {
+  bool on;
+  float q;        // the policy term of every token
+  int clip;       // its clip (counted per token, as the general path does)
+  float2 gpol2, neg_beta2, gc2;
+};
+__device__ __forceinline__ bool vec_fast_gspo(const float4& l4, const float4& r4, bool has_ref,
+                                              const GspoCtx& gs, float4& w, float& vq,
+                                              float& vk) {
+  float2 d2 = f2(0.f);
+  float k[4];
+  float2 wv[2];
+  bool small = true;
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const float2 l2 = p ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
+    const float2 r2 = p ? make_float2(r4.z, r4.w) : make_float2(r4.x, r4.y);
+    const float2 dr = has_ref ? __ffma2_rn(l2, f2(-1.f), r2) : f2(0.f);  // ref - logp
+    const float2 Qr = Q_poly2(dr), ddr = __fmul2_rn(dr, dr);
+    const float2 kk = __fmul2_rn(ddr, Qr);        // k3
+    const float2 emr = __ffma2_rn(ddr, Qr, dr);   // e^(ref-logp) - 1
+    d2 = __fadd2_rn(d2, ddr);
+    wv[p] = __fmul2_rn(gs.gc2, __ffma2_rn(gs.neg_beta2, emr, gs.gpol2));
+    small = small && fabsf(wv[p].x) <= kWPrecise && fabsf(wv[p].y) <= kWPrecise;
+    k[2 * p] = kk.x;
+    k[2 * p + 1] = kk.y;
+  }
+  w = make_float4(wv[0].x, wv[0].y, wv[1].x, wv[1].y);
+  // the four tokens' terms added in token order, as the general path adds them
+  vq = __fadd_rn(__fadd_rn(__fadd_rn(gs.q, gs.q), gs.q), gs.q);
+  vk = __fadd_rn(__fadd_rn(__fadd_rn(k[0], k[1]), k[2]), k[3]);
+  return __fadd_rn(d2.x, d2.y) < 0.25f && small;
+}
+
 // Every byte of a mask word nonzero.
 __device__ __forceinline__ bool all_active(uint32_t mw) {
   return ((((mw & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | mw) & 0x80808080u) == 0x80808080u;
@@ -347,24 +388,27 @@ __device__ __forceinline__ void vec_general(uint32_t mw, const float4& l4, const
 // (deferred_list), so that loop holds no general-path code, call or double
 // arithmetic; the variants' instantiation (whose loop measured faster with
 // it) takes the general path in place.
-template <bool kDefault, bool kCount>
+template <int kMode, bool kCount>
 __device__ __forceinline__ bool process_vec(uint32_t mw, const float4& l, const float4& o,
                                             const float4& r, bool has_ref, const FastCtx& f,
-                                            const SeqCtx& x, const LogpsArgs& a, Acc& acc,
-                                            float4& w) {
+                                            const GspoCtx& gs, const SeqCtx& x,
+                                            const LogpsArgs& a, Acc& acc, float4& w) {
   w = make_float4(0.f, 0.f, 0.f, 0.f);
   if (mw == 0u) return true;
   float vq, vk;
   int nclip;
   unsigned nc[3];
-  if (f.on && all_active(mw) && vec_fast<kCount>(l, o, r, has_ref, f, w, vq, vk, nclip)) {
+  if (kMode == kModeDefault && all_active(mw) &&
+      vec_fast<kCount>(l, o, r, has_ref, f, w, vq, vk, nclip)) {
     if (kCount) acc.count(f.clip_kind, (unsigned)nclip);
-  } else if (!kDefault && all_active(mw) &&
+  } else if (kMode == kModeGspo && all_active(mw) && vec_fast_gspo(l, r, has_ref, gs, w, vq, vk)) {
+    if (gs.clip) acc.count(gs.clip, 4u);
+  } else if (kMode == kModeVariant && all_active(mw) &&
              vec_fast_variant(l, o, r, has_ref, x, a, w, vq, vk, nc)) {
     acc.nc[0] += nc[0];
     acc.nc[1] += nc[1];
     acc.nc[2] += nc[2];
-  } else if (kDefault) {
+  } else if (kMode != kModeVariant) {
     return false;
   } else {
     vec_general(mw, l, o, r, x, a, w, vq, vk, acc);
@@ -497,11 +541,12 @@ __device__ __forceinline__ bool grid_wait(const unsigned long long* c, unsigned 
   return false;
 }
 
-// kDefault: the call's loss is the default variant (clipped surrogate, k3);
-// kCount: the call wants the clip counters.  Each form is its own
-// instantiation, so that the other's fast path does not cost it registers
-// or instructions.
-template <bool kDefault, bool kCount>
+// kMode: the call's loss is the default variant (clipped surrogate, k3:
+// kModeDefault), GSPO with the clipped surrogate and k3 (kModeGspo), or any
+// other variant (kModeVariant); kCount: the call wants the clip counters.
+// Each form is its own instantiation, so that another's fast path does not
+// cost it registers or instructions.
+template <int kMode, bool kCount>
 __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs a) {
   __shared__ FF s_ff[2][kLogpsThreads / 32];
   __shared__ unsigned s_nc[3][kLogpsThreads / 32];
@@ -523,6 +568,9 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
   const bool has_ref = a.ref != nullptr;
   const bool staged = staged_ok(a);
   const uint32_t nref = has_ref ? 1u : 0u;
+  // GSPO's tokens use the sequence's ratio, so the token loop needs no
+  // behaviour log-probs (its pre-pass reads them); its stages skip them
+  const uint32_t nold = a.var.seq_ratio ? 0u : 1u;
   // the test hook GRPO_FLAG_TEST_STALLED_COPY: the first copy of sequence 0
   // expects 16 bytes more than it delivers, so its wait runs out
   const uint32_t stall = ((a.flags & GRPO_FLAG_TEST_STALLED_COPY) && b == 0) ? 16u : 0u;
@@ -536,9 +584,9 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
     const uint32_t len = (uint32_t)min((int64_t)kChunk, (int64_t)hi16 - st);
     Stage& S = s_st[k % kDepth];
     uint64_t* bar = &s_full[k % kDepth];
-    mbar_expect_tx(bar, len * (4u * (2u + nref) + 1u) + (k == 0 ? stall : 0u));
+    mbar_expect_tx(bar, len * (4u * (1u + nold + nref) + 1u) + (k == 0 ? stall : 0u));
     bulk_g2s(S.lp, a.logps + base + st, 4u * len, bar, pol);
-    bulk_g2s(S.od, a.old + base + st, 4u * len, bar, pol);
+    if (nold) bulk_g2s(S.od, a.old + base + st, 4u * len, bar, pol);
     if (has_ref) bulk_g2s(S.rf, a.ref + base + st, 4u * len, bar, pol);
     bulk_g2s(S.mk, a.mask + base + st, len, bar, pol);
   };
@@ -745,7 +793,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
                                             : a.norm_c;
     x.gc = x.L > 0 ? __fdiv_rn(a.grad_scale, den) : 0.f;
     FastCtx f;
-    f.on = kDefault && a.var.is_default();
+    f.on = kMode == kModeDefault;
     f.clip_kind = x.A > 0.f ? 1 : (x.A < 0.f ? 2 : 0);
     const float sgn = x.A > 0.f ? 1.f : -1.f;
     f.s2 = f2(sgn);
@@ -757,6 +805,18 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
     {
       const float gm = x.gc > 0.f ? __fdiv_rn(kWPrecise, x.gc) : INFINITY;
       f.g2_max = __fmul_rn(gm, gm);
+    }
+    GspoCtx gs;
+    gs.on = kMode == kModeGspo;
+    {
+      // the policy part at the sequence's ratio (no KL part: has_ref false)
+      const TokEpi<float> t0 = token_epilogue<float>(x.em_seq, 0.f, 0.f, 0.f, 0.f, false, x.A,
+                                                     a.var);
+      gs.q = t0.q;
+      gs.clip = t0.clip;
+      gs.gpol2 = f2(t0.g);
+      gs.neg_beta2 = f2(-a.beta);
+      gs.gc2 = f2(x.gc);
     }
     Acc acc;
     int n_def = 0;  // vectors this thread left to the general path
@@ -790,8 +850,9 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
             const int v = threadIdx.x + u * kLogpsThreads;
             if (4 * v < len) {
               float4 w;
-              if (process_vec<kDefault, kCount>(S.mk[v], S.lp[v], S.od[v],
-                                                has_ref ? S.rf[v] : z4, has_ref, f, x, a, acc, w)) {
+              if (process_vec<kMode, kCount>(S.mk[v], S.lp[v], S.od[v],
+                                                has_ref ? S.rf[v] : z4, has_ref, f, gs, x, a,
+                                                acc, w)) {
                 if (a.grad) grow[st / 4 + v] = w;
               } else {
                 deferred_list(a, b)[n_def++] = (uint32_t)(st / 4 + v);
@@ -832,7 +893,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
         }
         const uint32_t m2 = v + 2 * kS < nv ? __ldg(mrow + v + 2 * kS) : 0u;
         float4 w;
-        if (process_vec<kDefault, kCount>(m0, l0, o0, r0, has_ref, f, x, a, acc, w)) {
+        if (process_vec<kMode, kCount>(m0, l0, o0, r0, has_ref, f, gs, x, a, acc, w)) {
           if (a.grad) grow[v] = w;
         } else {
           deferred_list(a, b)[n_def++] = (uint32_t)v;
@@ -957,14 +1018,15 @@ static cudaError_t prepare_device(int dev, int64_t* cap) {
   long long c = g_capacity[d].load(std::memory_order_acquire);
   if (c == 0) {
     cudaError_t e = cudaSuccess;
-    for (auto k : {logps_kernel<true, false>, logps_kernel<true, true>, logps_kernel<false, false>,
-                   logps_kernel<false, true>})
+    for (auto k : {logps_kernel<kModeDefault, false>, logps_kernel<kModeDefault, true>,
+                   logps_kernel<kModeVariant, false>, logps_kernel<kModeVariant, true>,
+                   logps_kernel<kModeGspo, false>, logps_kernel<kModeGspo, true>})
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int per_sm = 0, sms = 0, coop = 0;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, logps_kernel<true, false>, kLogpsThreads,
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, logps_kernel<kModeDefault, false>, kLogpsThreads,
                                                            0)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess)
@@ -1020,11 +1082,17 @@ cudaError_t launch_logps(const LogpsArgs& a, const grpo_profile_t* prof, cudaStr
   }
   if (prof && prof->start) cudaEventRecord((cudaEvent_t)prof->start, s);
   const bool count = a.counts_out != nullptr;
-  e = a.var.is_default()
-          ? (count ? cudaLaunchKernelEx(&cfg, logps_kernel<true, true>, a)
-                   : cudaLaunchKernelEx(&cfg, logps_kernel<true, false>, a))
-          : (count ? cudaLaunchKernelEx(&cfg, logps_kernel<false, true>, a)
-                   : cudaLaunchKernelEx(&cfg, logps_kernel<false, false>, a));
+  const bool gspo = a.var.seq_ratio && a.var.kl_type == GRPO_KL_K3 &&
+                    a.var.surrogate == GRPO_SURROGATE_CLIP;
+  if (a.var.is_default())
+    e = count ? cudaLaunchKernelEx(&cfg, logps_kernel<kModeDefault, true>, a)
+              : cudaLaunchKernelEx(&cfg, logps_kernel<kModeDefault, false>, a);
+  else if (gspo)
+    e = count ? cudaLaunchKernelEx(&cfg, logps_kernel<kModeGspo, true>, a)
+              : cudaLaunchKernelEx(&cfg, logps_kernel<kModeGspo, false>, a);
+  else
+    e = count ? cudaLaunchKernelEx(&cfg, logps_kernel<kModeVariant, true>, a)
+              : cudaLaunchKernelEx(&cfg, logps_kernel<kModeVariant, false>, a);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (prof && prof->stop) cudaEventRecord((cudaEvent_t)prof->stop, s);
   return e;
