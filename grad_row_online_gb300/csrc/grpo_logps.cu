@@ -171,7 +171,7 @@ __device__ __forceinline__ float token_w(float lp, float o, float rf, const TokE
 struct FastCtx {
   bool on;     // the call's loss is the default variant (clipped surrogate, k3)
   int clip_kind;  // how a clipped token counts: 1 upper (A > 0), 2 lower (A < 0), 0 not
-  float2 s2, neg_absA2, negA2, gc2, neg_beta2;
+  float2 s2, neg_absA2, negA2, gc2, neg_beta2, beta2;
   float lim;
   float g2_max;  // (kWPrecise / gc)^2: a vector whose sum of g^2 stays below
                  // it has every |w| <= kWPrecise
@@ -192,7 +192,11 @@ __device__ __forceinline__ float2 Q_poly2(float2 d) {
 
 // Two active tokens on the fast path (every operation but the clip on
 // packed fp32x2).  Accumulates q and k, and the sums behind the range check.
-template <bool kCount>
+// kKL: the KL estimator, 0 k3 (the default; k = e^d - d - 1 from the
+// polynomial, its gradient -(e^d - 1)), 1 k1 (k = -d, gradient 1), 2 k2
+// (k = d^2 / 2, gradient -d); d = ref_logp - logp, and only k3 puts d under
+// the polynomial's range check.
+template <bool kCount, int kKL>
 __device__ __forceinline__ float2 pair_fast(float2 lp, float2 od, float2 rf, bool has_ref,
                                             const FastCtx& f, float2& vq, float2& vk,
                                             float2& d2sum, float2& g2sum, int& nclip) {
@@ -200,9 +204,17 @@ __device__ __forceinline__ float2 pair_fast(float2 lp, float2 od, float2 rf, boo
   const float2 Qp = Q_poly2(dp), ddp = __fmul2_rn(dp, dp);
   const float2 em = __ffma2_rn(ddp, Qp, dp);       // r - 1
   const float2 dr = has_ref ? __ffma2_rn(lp, f2(-1.f), rf) : f2(0.f);  // ref - logp
-  const float2 Qr = Q_poly2(dr), ddr = __fmul2_rn(dr, dr);
-  const float2 k = __fmul2_rn(ddr, Qr);            // k3
-  const float2 emr = __ffma2_rn(ddr, Qr, dr);      // e^(ref-logp) - 1
+  float2 k, ddr = f2(0.f), emr = f2(0.f);
+  if (kKL == 0) {
+    const float2 Qr = Q_poly2(dr);
+    ddr = __fmul2_rn(dr, dr);
+    k = __fmul2_rn(ddr, Qr);                       // k3
+    emr = __ffma2_rn(ddr, Qr, dr);                 // e^(ref-logp) - 1
+  } else if (kKL == 1) {
+    k = __fmul2_rn(dr, f2(-1.f));                  // k1 = -d
+  } else {
+    k = __fmul2_rn(__fmul2_rn(dr, dr), f2(0.5f));  // k2 = d^2 / 2
+  }
   const float2 se = __fmul2_rn(f.s2, em);
   const float2 mn = make_float2(fminf(se.x, f.lim), fminf(se.y, f.lim));
   const float2 q = __fmul2_rn(f.neg_absA2, mn);
@@ -211,10 +223,12 @@ __device__ __forceinline__ float2 pair_fast(float2 lp, float2 od, float2 rf, boo
   gp.x = cx ? 0.f : gp.x;
   gp.y = cy ? 0.f : gp.y;
   if (kCount) nclip += (int)cx + (int)cy;
-  const float2 g = __ffma2_rn(f.neg_beta2, emr, gp);
+  const float2 g = kKL == 0 ? __ffma2_rn(f.neg_beta2, emr, gp)
+                 : kKL == 1 ? __fadd2_rn(gp, f.beta2)
+                            : __ffma2_rn(f.neg_beta2, dr, gp);
   vq = __fadd2_rn(vq, q);
   vk = __fadd2_rn(vk, k);
-  d2sum = __fadd2_rn(d2sum, __fadd2_rn(ddp, ddr));
+  d2sum = __fadd2_rn(d2sum, kKL == 0 ? __fadd2_rn(ddp, ddr) : ddp);
   g2sum = __ffma2_rn(g, g, g2sum);
   return __fmul2_rn(f.gc2, g);
 }
@@ -223,15 +237,15 @@ __device__ __forceinline__ float2 pair_fast(float2 lp, float2 od, float2 rf, boo
 // token needs the general path: a log ratio outside |d| < 1/2 (caught by
 // the vector's sum of d^2 reaching 1/4), or a gradient above kWPrecise
 // (caught by its sum of g^2); NaNs fail the check too.
-template <bool kCount>
+template <bool kCount, int kKL>
 __device__ __forceinline__ bool vec_fast(const float4& l4, const float4& o4, const float4& r4,
                                          bool has_ref, const FastCtx& f, float4& w,
                                          float& vq, float& vk, int& nclip) {
   float2 sq = f2(0.f), sk = f2(0.f), d2 = f2(0.f), g2 = f2(0.f);
   nclip = 0;
-  const float2 w01 = pair_fast<kCount>(make_float2(l4.x, l4.y), make_float2(o4.x, o4.y),
+  const float2 w01 = pair_fast<kCount, kKL>(make_float2(l4.x, l4.y), make_float2(o4.x, o4.y),
                                        make_float2(r4.x, r4.y), has_ref, f, sq, sk, d2, g2, nclip);
-  const float2 w23 = pair_fast<kCount>(make_float2(l4.z, l4.w), make_float2(o4.z, o4.w),
+  const float2 w23 = pair_fast<kCount, kKL>(make_float2(l4.z, l4.w), make_float2(o4.z, o4.w),
                                        make_float2(r4.z, r4.w), has_ref, f, sq, sk, d2, g2, nclip);
   w = make_float4(w01.x, w01.y, w23.x, w23.y);
   vq = __fadd_rn(sq.x, sq.y);
@@ -304,7 +318,15 @@ __device__ __forceinline__ bool vec_fast_variant(const float4& l4, const float4&
   return __fadd_rn(d2.x, d2.y) < 0.25f && small;
 }
 
-enum : int { kModeDefault = 0, kModeVariant = 1, kModeGspo = 2 };
+enum : int { kModeDefault = 0, kModeVariant = 1, kModeGspo = 2, kModeK1 = 3, kModeK2 = 4 };
+// The clipped surrogate without the dual clip or sequence ratios, with the KL
+// estimator of the mode: the packed fast path of vec_fast.
+__host__ __device__ constexpr int mode_kl(int mode) {
+  return mode == kModeK1 ? 1 : (mode == kModeK2 ? 2 : 0);
+}
+__host__ __device__ constexpr bool mode_packed(int mode) {
+  return mode == kModeDefault || mode == kModeK1 || mode == kModeK2;
+}
 
 // GSPO with the clipped surrogate and k3: every token of the sequence shares
 // the ratio rho_i, so its policy term q, policy gradient and clip are the
@@ -398,8 +420,8 @@ __device__ __forceinline__ bool process_vec(uint32_t mw, const float4& l, const 
   float vq, vk;
   int nclip;
   unsigned nc[3];
-  if (kMode == kModeDefault && all_active(mw) &&
-      vec_fast<kCount>(l, o, r, has_ref, f, w, vq, vk, nclip)) {
+  if (mode_packed(kMode) && all_active(mw) &&
+      vec_fast<kCount, mode_kl(kMode)>(l, o, r, has_ref, f, w, vq, vk, nclip)) {
     if (kCount) acc.count(f.clip_kind, (unsigned)nclip);
   } else if (kMode == kModeGspo && all_active(mw) && vec_fast_gspo(l, r, has_ref, gs, w, vq, vk)) {
     if (gs.clip) acc.count(gs.clip, 4u);
@@ -542,8 +564,10 @@ __device__ __forceinline__ bool grid_wait(const unsigned long long* c, unsigned 
 }
 
 // kMode: the call's loss is the default variant (clipped surrogate, k3:
-// kModeDefault), GSPO with the clipped surrogate and k3 (kModeGspo), or any
-// other variant (kModeVariant); kCount: the call wants the clip counters.
+// kModeDefault), the clipped surrogate with k1 or k2 (kModeK1, kModeK2: the
+// same packed path with the other KL term), GSPO with the clipped surrogate
+// and k3 (kModeGspo), or any other variant (kModeVariant); kCount: the call
+// wants the clip counters.
 // Each form is its own instantiation, so that another's fast path does not
 // cost it registers or instructions.
 template <int kMode, bool kCount>
@@ -793,7 +817,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
                                             : a.norm_c;
     x.gc = x.L > 0 ? __fdiv_rn(a.grad_scale, den) : 0.f;
     FastCtx f;
-    f.on = kMode == kModeDefault;
+    f.on = mode_packed(kMode);
     f.clip_kind = x.A > 0.f ? 1 : (x.A < 0.f ? 2 : 0);
     const float sgn = x.A > 0.f ? 1.f : -1.f;
     f.s2 = f2(sgn);
@@ -801,6 +825,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
     f.negA2 = f2(-x.A);
     f.gc2 = f2(x.gc);
     f.neg_beta2 = f2(-a.beta);
+    f.beta2 = f2(a.beta);
     f.lim = x.A > 0.f ? a.eps_hi : a.eps_lo;
     {
       const float gm = x.gc > 0.f ? __fdiv_rn(kWPrecise, x.gc) : INFINITY;
@@ -1020,7 +1045,9 @@ static cudaError_t prepare_device(int dev, int64_t* cap) {
     cudaError_t e = cudaSuccess;
     for (auto k : {logps_kernel<kModeDefault, false>, logps_kernel<kModeDefault, true>,
                    logps_kernel<kModeVariant, false>, logps_kernel<kModeVariant, true>,
-                   logps_kernel<kModeGspo, false>, logps_kernel<kModeGspo, true>})
+                   logps_kernel<kModeGspo, false>, logps_kernel<kModeGspo, true>,
+                   logps_kernel<kModeK1, false>, logps_kernel<kModeK1, true>,
+                   logps_kernel<kModeK2, false>, logps_kernel<kModeK2, true>})
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
@@ -1084,9 +1111,17 @@ cudaError_t launch_logps(const LogpsArgs& a, const grpo_profile_t* prof, cudaStr
   const bool count = a.counts_out != nullptr;
   const bool gspo = a.var.seq_ratio && a.var.kl_type == GRPO_KL_K3 &&
                     a.var.surrogate == GRPO_SURROGATE_CLIP;
+  const bool plain_clip = a.var.surrogate == GRPO_SURROGATE_CLIP && a.var.dual_c == 0.f &&
+                          !a.var.seq_ratio;
   if (a.var.is_default())
     e = count ? cudaLaunchKernelEx(&cfg, logps_kernel<kModeDefault, true>, a)
               : cudaLaunchKernelEx(&cfg, logps_kernel<kModeDefault, false>, a);
+  else if (plain_clip && a.var.kl_type == GRPO_KL_K1)
+    e = count ? cudaLaunchKernelEx(&cfg, logps_kernel<kModeK1, true>, a)
+              : cudaLaunchKernelEx(&cfg, logps_kernel<kModeK1, false>, a);
+  else if (plain_clip && a.var.kl_type == GRPO_KL_K2)
+    e = count ? cudaLaunchKernelEx(&cfg, logps_kernel<kModeK2, true>, a)
+              : cudaLaunchKernelEx(&cfg, logps_kernel<kModeK2, false>, a);
   else if (gspo)
     e = count ? cudaLaunchKernelEx(&cfg, logps_kernel<kModeGspo, true>, a)
               : cudaLaunchKernelEx(&cfg, logps_kernel<kModeGspo, false>, a);
