@@ -66,10 +66,34 @@ def profile_key(w, variant: str = "default", skip_masked: bool = False, tp: int 
     return w.name
 
 
+_TOKENS = re.compile(r'"(?:\\.|[^"\\\n])*"|\'(?:\\.|[^\'\\\n])*\'|//[^\n]*|/\*.*?\*/', re.S)
+
+
+def _code_only(text: str) -> str:
+    """The source with its comments removed and every run of blanks outside
+    string and character literals made one space (the literals kept as they
+    are)."""
+    out, code, pos = [], [], 0
+    for m in _TOKENS.finditer(text):
+        code.append(text[pos:m.start()])
+        if m.group(0)[0] in "\"'":
+            out.append(re.sub(r"\s+", " ", "".join(code)))
+            out.append(m.group(0))
+            code = []
+        else:
+            code.append(" ")
+        pos = m.end()
+    code.append(text[pos:])
+    out.append(re.sub(r"\s+", " ", "".join(code)))
+    return "".join(out).strip()
+
+
 def source_hash(files) -> str:
+    """Hash of the code of the kernel sources (comments and layout do not
+    count), the key under which a profile's traffic figure stays valid."""
     h = hashlib.sha256()
     for f in files:
-        h.update(open(os.path.join(CSRC, f), "rb").read())
+        h.update(_code_only(open(os.path.join(CSRC, f)).read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -173,6 +173,7 @@ struct FastCtx {
   int clip_kind;  // how a clipped token counts: 1 upper (A > 0), 2 lower (A < 0), 0 not
   float2 s2, neg_absA2, negA2, gc2, neg_beta2, beta2;
   float lim;
+  float lo, hi;  // CISPO: the bounds on r - 1, -eps_lo and eps_hi
   float g2_max;  // (kWPrecise / gc)^2: a vector whose sum of g^2 stays below
                  // it has every |w| <= kWPrecise
 };
@@ -231,6 +232,50 @@ __device__ __forceinline__ float2 pair_fast(float2 lp, float2 od, float2 rf, boo
   d2sum = __fadd2_rn(d2sum, kKL == 0 ? __fadd2_rn(ddp, ddr) : ddp);
   g2sum = __ffma2_rn(g, g, g2sum);
   return __fmul2_rn(f.gc2, g);
+}
+
+// CISPO with k3 on two active tokens (packed fp32x2 but for the clip): the
+// weight clip(r) behind the stop-gradient gives p = -A clip(r) logp and the
+// policy gradient -A clip(r); every token keeps it.
+template <bool kCount>
+__device__ __forceinline__ float2 pair_cispo(float2 lp, float2 od, float2 rf, bool has_ref,
+                                             const FastCtx& f, float2& vq, float2& vk,
+                                             float2& d2sum, float2& g2sum, int (&nclip)[2]) {
+  const float2 dp = __ffma2_rn(od, f2(-1.f), lp);  // logp - old
+  const float2 Qp = Q_poly2(dp), ddp = __fmul2_rn(dp, dp);
+  const float2 em = __ffma2_rn(ddp, Qp, dp);       // r - 1
+  const float2 dr = has_ref ? __ffma2_rn(lp, f2(-1.f), rf) : f2(0.f);  // ref - logp
+  const float2 Qr = Q_poly2(dr), ddr = __fmul2_rn(dr, dr);
+  const float2 k = __fmul2_rn(ddr, Qr);            // k3
+  const float2 emr = __ffma2_rn(ddr, Qr, dr);      // e^(ref-logp) - 1
+  const float2 emc = make_float2(fminf(fmaxf(em.x, f.lo), f.hi), fminf(fmaxf(em.y, f.lo), f.hi));
+  const float2 gp = __fmul2_rn(f.negA2, __fadd2_rn(f2(1.f), emc));  // -A clip(r)
+  const float2 q = __fmul2_rn(gp, lp);
+  if (kCount) {
+    nclip[0] += (int)(em.x > f.hi) + (int)(em.y > f.hi);
+    nclip[1] += (int)(em.x < f.lo) + (int)(em.y < f.lo);
+  }
+  const float2 g = __ffma2_rn(f.neg_beta2, emr, gp);
+  vq = __fadd2_rn(vq, q);
+  vk = __fadd2_rn(vk, k);
+  d2sum = __fadd2_rn(d2sum, __fadd2_rn(ddp, ddr));
+  g2sum = __ffma2_rn(g, g, g2sum);
+  return __fmul2_rn(f.gc2, g);
+}
+template <bool kCount>
+__device__ __forceinline__ bool vec_cispo(const float4& l4, const float4& o4, const float4& r4,
+                                          bool has_ref, const FastCtx& f, float4& w, float& vq,
+                                          float& vk, int (&nclip)[2]) {
+  float2 sq = f2(0.f), sk = f2(0.f), d2 = f2(0.f), g2 = f2(0.f);
+  nclip[0] = nclip[1] = 0;
+  const float2 w01 = pair_cispo<kCount>(make_float2(l4.x, l4.y), make_float2(o4.x, o4.y),
+                                        make_float2(r4.x, r4.y), has_ref, f, sq, sk, d2, g2, nclip);
+  const float2 w23 = pair_cispo<kCount>(make_float2(l4.z, l4.w), make_float2(o4.z, o4.w),
+                                        make_float2(r4.z, r4.w), has_ref, f, sq, sk, d2, g2, nclip);
+  w = make_float4(w01.x, w01.y, w23.x, w23.y);
+  vq = __fadd_rn(sq.x, sq.y);
+  vk = __fadd_rn(sk.x, sk.y);
+  return __fadd_rn(d2.x, d2.y) < 0.25f && __fadd_rn(g2.x, g2.y) <= f.g2_max;
 }
 
 // One vector of four active slots on the fast path.  Returns false when a
@@ -318,7 +363,8 @@ __device__ __forceinline__ bool vec_fast_variant(const float4& l4, const float4&
   return __fadd_rn(d2.x, d2.y) < 0.25f && small;
 }
 
-enum : int { kModeDefault = 0, kModeVariant = 1, kModeGspo = 2, kModeK1 = 3, kModeK2 = 4 };
+enum : int { kModeDefault = 0, kModeVariant = 1, kModeGspo = 2, kModeK1 = 3, kModeK2 = 4,
+             kModeCispo = 5 };
 // The clipped surrogate without the dual clip or sequence ratios, with the KL
 // estimator of the mode: the packed fast path of vec_fast.
 __host__ __device__ constexpr int mode_kl(int mode) {
@@ -327,6 +373,8 @@ __host__ __device__ constexpr int mode_kl(int mode) {
 __host__ __device__ constexpr bool mode_packed(int mode) {
   return mode == kModeDefault || mode == kModeK1 || mode == kModeK2;
 }
+// Modes whose general-path vectors wait for the end of the token loop.
+__host__ __device__ constexpr bool mode_defers(int mode) { return mode != kModeVariant; }
 
 // GSPO with the clipped surrogate and k3: every token of the sequence shares
 // the ratio rho_i, so its policy term q, policy gradient and clip are the
@@ -405,11 +453,12 @@ __device__ __forceinline__ void vec_general(uint32_t mw, const float4& l4, const
 // One vector of four slots in the token loop: its gradient, and its q / k
 // sums into the thread's Kahan pairs.  Fully active vectors take a fast path
 // when its range check passes; fully masked ones give zeros.  Any other
-// vector: the default-loss instantiation returns false, and the thread
-// records it and evaluates it on the general path after the loop
-// (deferred_list), so that loop holds no general-path code, call or double
-// arithmetic; the variants' instantiation (whose loop measured faster with
-// it) takes the general path in place.
+// vector: an instantiation with a packed path of its own (every mode but
+// kModeVariant) returns false, and the thread records it and evaluates it on
+// the general path after the loop (deferred_list), so that loop holds no
+// general-path code, call or double arithmetic; the shared variants'
+// instantiation (whose loop measured faster with it) takes the general path
+// in place.
 template <int kMode, bool kCount>
 __device__ __forceinline__ bool process_vec(uint32_t mw, const float4& l, const float4& o,
                                             const float4& r, bool has_ref, const FastCtx& f,
@@ -419,18 +468,25 @@ __device__ __forceinline__ bool process_vec(uint32_t mw, const float4& l, const 
   if (mw == 0u) return true;
   float vq, vk;
   int nclip;
+  int ncl2[2];
   unsigned nc[3];
   if (mode_packed(kMode) && all_active(mw) &&
       vec_fast<kCount, mode_kl(kMode)>(l, o, r, has_ref, f, w, vq, vk, nclip)) {
     if (kCount) acc.count(f.clip_kind, (unsigned)nclip);
   } else if (kMode == kModeGspo && all_active(mw) && vec_fast_gspo(l, r, has_ref, gs, w, vq, vk)) {
     if (gs.clip) acc.count(gs.clip, 4u);
+  } else if (kMode == kModeCispo && all_active(mw) &&
+             vec_cispo<kCount>(l, o, r, has_ref, f, w, vq, vk, ncl2)) {
+    if (kCount) {
+      acc.nc[0] += (unsigned)ncl2[0];
+      acc.nc[1] += (unsigned)ncl2[1];
+    }
   } else if (kMode == kModeVariant && all_active(mw) &&
              vec_fast_variant(l, o, r, has_ref, x, a, w, vq, vk, nc)) {
     acc.nc[0] += nc[0];
     acc.nc[1] += nc[1];
     acc.nc[2] += nc[2];
-  } else if (kMode != kModeVariant) {
+  } else if (mode_defers(kMode)) {
     return false;
   } else {
     vec_general(mw, l, o, r, x, a, w, vq, vk, acc);
@@ -565,9 +621,9 @@ __device__ __forceinline__ bool grid_wait(const unsigned long long* c, unsigned 
 
 // kMode: the call's loss is the default variant (clipped surrogate, k3:
 // kModeDefault), the clipped surrogate with k1 or k2 (kModeK1, kModeK2: the
-// same packed path with the other KL term), GSPO with the clipped surrogate
-// and k3 (kModeGspo), or any other variant (kModeVariant); kCount: the call
-// wants the clip counters.
+// same packed path with the other KL term), CISPO with k3 (kModeCispo), GSPO
+// with the clipped surrogate and k3 (kModeGspo), or any other variant
+// (kModeVariant); kCount: the call wants the clip counters.
 // Each form is its own instantiation, so that another's fast path does not
 // cost it registers or instructions.
 template <int kMode, bool kCount>
@@ -827,6 +883,8 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
     f.neg_beta2 = f2(-a.beta);
     f.beta2 = f2(a.beta);
     f.lim = x.A > 0.f ? a.eps_hi : a.eps_lo;
+    f.lo = -a.eps_lo;
+    f.hi = a.eps_hi;
     {
       const float gm = x.gc > 0.f ? __fdiv_rn(kWPrecise, x.gc) : INFINITY;
       f.g2_max = __fmul_rn(gm, gm);
@@ -1047,7 +1105,8 @@ static cudaError_t prepare_device(int dev, int64_t* cap) {
                    logps_kernel<kModeVariant, false>, logps_kernel<kModeVariant, true>,
                    logps_kernel<kModeGspo, false>, logps_kernel<kModeGspo, true>,
                    logps_kernel<kModeK1, false>, logps_kernel<kModeK1, true>,
-                   logps_kernel<kModeK2, false>, logps_kernel<kModeK2, true>})
+                   logps_kernel<kModeK2, false>, logps_kernel<kModeK2, true>,
+                   logps_kernel<kModeCispo, false>, logps_kernel<kModeCispo, true>})
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
@@ -1122,6 +1181,10 @@ cudaError_t launch_logps(const LogpsArgs& a, const grpo_profile_t* prof, cudaStr
   else if (plain_clip && a.var.kl_type == GRPO_KL_K2)
     e = count ? cudaLaunchKernelEx(&cfg, logps_kernel<kModeK2, true>, a)
               : cudaLaunchKernelEx(&cfg, logps_kernel<kModeK2, false>, a);
+  else if (a.var.surrogate == GRPO_SURROGATE_CISPO && a.var.kl_type == GRPO_KL_K3 &&
+           !a.var.seq_ratio)
+    e = count ? cudaLaunchKernelEx(&cfg, logps_kernel<kModeCispo, true>, a)
+              : cudaLaunchKernelEx(&cfg, logps_kernel<kModeCispo, false>, a);
   else if (gspo)
     e = count ? cudaLaunchKernelEx(&cfg, logps_kernel<kModeGspo, true>, a)
               : cudaLaunchKernelEx(&cfg, logps_kernel<kModeGspo, false>, a);

@@ -79,3 +79,14 @@ def test_committed_profiles_name_their_own_key():
     assert bench.profile_key(w, tp=2) not in bench.PROFILES
     assert bench.profile_key(w, "k2") == "large_vocab"
     assert bench.profile_key(synth.WORKLOADS["logps"], "k2") not in bench.PROFILES
+
+
+def test_source_hash_ignores_comments_only():
+    # a profile's traffic figure outlives a comment edit but not a code edit
+    import bench
+    code = 'int f(int x) {  // doubles\n  /* a\n block */ return 2 * x;\n}\n\nconst char* s = "a//b";\n'
+    same = 'int f(int x) {\n  return 2 * x;  // twice x\n}\nconst char* s = "a//b";\n'
+    assert bench._code_only(code) == bench._code_only(same)
+    for changed in (code.replace("2 * x", "3 * x"), code.replace('"a//b"', '"a/b"'),
+                    code.replace('"a//b"', '"a  //b"')):
+        assert bench._code_only(changed) != bench._code_only(code)

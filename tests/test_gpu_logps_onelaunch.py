@@ -69,6 +69,7 @@ OPTIONS = {
     "fixed-k2-dual": dict(reduction="fixed_constant", norm_constant=50.0, kl="k2",
                           dual_clip_c=1.4),
     "cispo-k1": dict(surrogate="cispo", kl="k1"),
+    "cispo": dict(surrogate="cispo"),
     "k1": dict(kl="k1"),
     "k2-sequence-mean": dict(kl="k2", reduction="sequence_mean"),
     "gspo": dict(reduction="sequence_mean", ratio_level="sequence"),

@@ -217,6 +217,38 @@ def test_logps_variants_on_the_fast_path(name):
     assert np.all(ok | near), np.argwhere(~(ok | near))[:5]
 
 
+@pytest.mark.parametrize("name", ["k1", "k2", "cispo", "gspo"])
+def test_logps_variants_with_every_vector_deferred(name):
+    # log ratios ~N(0, 2): nearly every vector fails the fast path's range
+    # check, so the variants with a packed path of their own (the clipped
+    # surrogate with k1 or k2, CISPO with k3, GSPO with k3) leave each thread's
+    # whole share of the row to the general path after the token loop
+    v = VARIANTS[name]
+    w = LOGPS_WIDE.with_(B=8, T=4096, len_range=(3000, 4096), old_sigma=2.0,
+                         ref_logp_sigma=1.0)
+    lp, old, ref, mask, R = _logps_inputs(w)
+    A = oracle.group_advantages(R, w.group_boundaries())
+    exp = oracle.loss_from_logps(lp, ref, old, mask, A, w.eps_lo, w.eps_hi, w.beta,
+                                 **_oracle_kw(v, w))
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    for flags in (0, g.GRPO_FLAG_SEPARATE_PREP):
+        args = dict(samples_per_prompt=w.samples_per_prompt, clip_eps=w.eps_lo,
+                    clip_eps_hi=w.eps_hi, beta=w.beta, reduction=w.reduction,
+                    want_per_seq=True, want_clip_counts=True, extra_flags=flags)
+        args.update(v)
+        res = g.grpo_loss_from_logps(t(lp), t(old), t(ref), t(mask), t(R), **args)
+        torch.cuda.synchronize()
+        out = res["out3"].cpu().numpy().astype(np.float64)
+        for i, k in enumerate(("loss", "policy_loss", "kl")):
+            assert_scalar(out[i], exp[k], f"{name} {k}")
+        near = _band(exp, w.eps_lo, w.eps_hi, v.get("dual_clip_c"))
+        _check_counts(res["clip_counts"], exp, near)
+        want = exp["w"].astype(np.float32)
+        got = res["grad"].cpu().numpy()
+        ok = np.abs(got.astype(np.float64) - want) <= np.spacing(np.abs(want)) + 1e-9
+        assert np.all(ok | near), np.argwhere(~(ok | near))[:5]
+
+
 def test_variant_parameters_are_checked_on_the_host():
     x = torch.zeros((2, 1, 4), device="cuda")
     a = torch.zeros((2, 1), dtype=torch.int64, device="cuda")
