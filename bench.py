@@ -443,7 +443,87 @@ def logits_side_bytes(w, active: int, s_in: int, skip_masked: bool) -> dict:
                                                       float(w.V * s_in * masked))}
 
 
-class LogitsCase:
+class ReadBack:
+    """The end-to-end steps' read-back on a second stream: step i's outputs go
+    to the host while step i+1's inputs come in (the two directions of the
+    host link at once), and the call of step i+1 waits for that read-back
+    before it overwrites the outputs.  With two device input sets
+    (`pipe_init`), the copies in run on a third stream too, into the set the
+    previous call did not read, so that they also overlap the calls."""
+
+    READBACK = ("; step i's read-back runs on a second stream, overlapping step i+1's "
+                "copies in (step i+1's call waits for it before it overwrites the outputs)")
+    PIPELINE = ("; three streams: step i+1's inputs are copied into a second device input set "
+                "while step i's call runs, and step i's read-back overlaps step i+1's copies in "
+                "(a call waits for its inputs and for the previous read-back; the copies into an "
+                "input set wait for the call that last read it)")
+
+    def rb_init(self):
+        import torch
+        self.side = torch.cuda.Stream(device=self.device)
+        self.rb_done = None
+        self.cin = None
+
+    def pipe_init(self, make_set):
+        """Two device input sets and the copy-in stream."""
+        import torch
+        self.rb_init()
+        self.cin = torch.cuda.Stream(device=self.device)
+        self.sets = [make_set(), make_set()]
+        self.used = [None, None]
+        self.k_set = 0
+
+    def pipe_next(self) -> int:
+        """The input set of the next step, once the call that last read it is done."""
+        j = self.k_set % 2
+        self.k_set += 1
+        if self.used[j] is not None:
+            self.cin.wait_event(self.used[j])
+        return j
+
+    def pipe_ready(self):
+        """The current stream waits for the copies in queued so far."""
+        import torch
+        ev = torch.cuda.Event()
+        ev.record(self.cin)
+        torch.cuda.current_stream().wait_event(ev)
+
+    def pipe_called(self, j: int):
+        import torch
+        self.used[j] = torch.cuda.Event()
+        self.used[j].record(torch.cuda.current_stream())
+
+    def e2e_begin(self):
+        """The side streams start after the work queued so far (the start event)."""
+        import torch
+        for st in (self.side, self.cin):
+            if st is not None:
+                st.wait_stream(torch.cuda.current_stream())
+
+    def rb_before_call(self):
+        import torch
+        if self.rb_done is not None:
+            torch.cuda.current_stream().wait_event(self.rb_done)
+
+    def rb_stream(self):
+        """The side stream, made to wait for the work queued so far."""
+        import torch
+        self.side.wait_stream(torch.cuda.current_stream())
+        return torch.cuda.stream(self.side)
+
+    def rb_end(self):
+        import torch
+        self.rb_done = torch.cuda.Event()
+        self.rb_done.record(self.side)
+
+    def e2e_join(self):
+        import torch
+        for st in (self.side, self.cin):
+            if st is not None:
+                torch.cuda.current_stream().wait_stream(st)
+
+
+class LogitsCase(ReadBack):
     """grpo_loss_fwd_bwd on a logits workload (inputs larger than L2)."""
 
     launches_per_step = 3  # prep, rows, reduce
@@ -480,7 +560,7 @@ class LogitsCase:
                 "host mask inside each step: masked rows are never read), the other inputs "
                 "whole; out: the loss outputs and the gradient rows of the active tokens into a "
                 "pinned host gradient buffer (the masked rows' gradient is zero by contract: "
-                "the host buffer is zeroed once before the timed steps)")
+                "the host buffer is zeroed once before the timed steps)" + ReadBack.PIPELINE)
 
     def e2e_setup(self):
         import torch
@@ -488,12 +568,10 @@ class LogitsCase:
         for k, v in self.inp.items():
             self.host[k] = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
             self.host[k].copy_(v)
-        self.dev_in = {k: torch.empty_like(v) for k, v in self.inp.items()}
-        self.dev_in["bounds"] = self.inp["bounds"]
-        # the same call as the resident steps (variant, masked-row mode), on the copied inputs
+        self.pipe_init(lambda: {k: torch.empty_like(v) for k, v in self.inp.items()})
+        # the same call as the resident steps (variant, masked-row mode), on the copied
+        # inputs; the group boundaries are configuration, not a step's data
         self.kw_e = dict(self.kw)
-        if "group_boundaries" in self.kw_e:
-            self.kw_e["group_boundaries"] = self.dev_in["bounds"]
         self.loss_host = torch.empty(3, dtype=torch.float32).pin_memory()
         self.mask_host = self.host["mask"].numpy()
         self.runs = active_runs(self.mask_host)
@@ -521,24 +599,32 @@ class LogitsCase:
             raise RuntimeError("masked rows of the host gradient are not zero")
 
     def e2e_step(self):
-        d, h, V = self.dev_in, self.host, self.w.V
+        import torch
+        j = self.pipe_next()
+        d, h, V = self.sets[j], self.host, self.w.V
         xd, yd = d["X"].view(-1, V), d["Y"].view(-1, V)
         xh, yh = h["X"].view(-1, V), h["Y"].view(-1, V)
         runs = active_runs(self.mask_host)
-        for b, e in runs:
-            xd[b:e].copy_(xh[b:e], non_blocking=True)
-            yd[b:e].copy_(yh[b:e], non_blocking=True)
-        for k in ("acts", "old", "mask", "R"):
-            d[k].copy_(h[k], non_blocking=True)
+        with torch.cuda.stream(self.cin):
+            for b, e in runs:
+                xd[b:e].copy_(xh[b:e], non_blocking=True)
+                yd[b:e].copy_(yh[b:e], non_blocking=True)
+            for k in ("acts", "old", "mask", "R"):
+                d[k].copy_(h[k], non_blocking=True)
+        self.pipe_ready()
+        self.rb_before_call()
         self.g.grpo_loss_fwd_bwd(d["X"], d["Y"], d["acts"], d["old"], d["mask"], d["R"],
                                  grad=self.grad, out3=self.out3, workspace=self.wsp, **self.kw_e)
-        self.loss_host.copy_(self.out3, non_blocking=True)
-        gd, gh = self.grad.view(-1, V), self.grad_host.view(-1, V)
-        for b, e in runs:
-            gh[b:e].copy_(gd[b:e], non_blocking=True)
+        self.pipe_called(j)
+        with self.rb_stream():
+            self.loss_host.copy_(self.out3, non_blocking=True)
+            gd, gh = self.grad.view(-1, V), self.grad_host.view(-1, V)
+            for b, e in runs:
+                gh[b:e].copy_(gd[b:e], non_blocking=True)
+        self.rb_end()
 
 
-class VocabCase:
+class VocabCase(ReadBack):
     """The vocabulary-parallel path on a logits workload, emulated with `tp`
     slices on one GPU: every slice's partials, the rank-order exchange
     (a concatenation and a sum, as the collectives would leave them), the
@@ -594,7 +680,8 @@ class VocabCase:
 
     e2e_copy = ("in: every slice's logits rows the calls read (runs of active tokens), the "
                 "other inputs whole; out: the loss outputs and every slice's gradient rows of the "
-                "active tokens into pinned host buffers (masked rows are zero by contract)")
+                "active tokens into pinned host buffers (masked rows are zero by contract)"
+                + ReadBack.READBACK)
 
     def e2e_setup(self):
         import torch
@@ -610,6 +697,7 @@ class VocabCase:
         self.mask_host = self.host_small["mask"].numpy()
         self.grads_host = [torch.zeros(t.shape, dtype=t.dtype, pin_memory=True)
                            for t in self.grads]
+        self.rb_init()
         rows = sum(e - b for b, e in active_runs(self.mask_host))
         h2d = (rows * sum(t.shape[-1] * t.element_size() for t in self.host)
                + sum(t.numel() * t.element_size() for t in self.host_small.values()))
@@ -634,15 +722,19 @@ class VocabCase:
             self.dev_small[k].copy_(self.host_small[k], non_blocking=True)
         self.Xs, self.Ys = self.dev_in[:n], self.dev_in[n:]
         self.inp = dict(self.inp, **self.dev_small)
+        self.rb_before_call()
         self.step()
-        self.loss_host.copy_(self.out3, non_blocking=True)
-        for gd, gh in zip(self.grads, self.grads_host):  # every slice's active gradient rows
-            dv, hv = gd.view(-1, gd.shape[-1]), gh.view(-1, gh.shape[-1])
-            for b, e in runs:
-                hv[b:e].copy_(dv[b:e], non_blocking=True)
+        self.out3.record_stream(self.side)  # allocated by this step, read on the side stream
+        with self.rb_stream():
+            self.loss_host.copy_(self.out3, non_blocking=True)
+            for gd, gh in zip(self.grads, self.grads_host):  # every slice's active gradient rows
+                dv, hv = gd.view(-1, gd.shape[-1]), gh.view(-1, gh.shape[-1])
+                for b, e in runs:
+                    hv[b:e].copy_(dv[b:e], non_blocking=True)
+        self.rb_end()
 
 
-class LogpsCase:
+class LogpsCase(ReadBack):
     """grpo_loss_from_logps on the logps-only workload.  One copy of its
     inputs (54 MB) fits in L2, so the timed steps rotate over COPIES copies
     (with their own gradient buffers): a step's inputs were last touched
@@ -708,21 +800,30 @@ class LogpsCase:
                 continue
             self.host[k] = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
             self.host[k].copy_(v)
-        self.dev_in = {k: torch.empty_like(v) for k, v in self.inp.items()}
+        self.pipe_init(lambda: {k: torch.empty_like(v) for k, v in self.inp.items()})
         self.loss_host = torch.empty(3, dtype=torch.float32).pin_memory()
         self.grad_host = torch.empty(self.grad.shape, dtype=torch.float32, pin_memory=True)
         return (sum(v.numel() * v.element_size() for v in self.host.values()),
                 self.grad_host.numel() * 4 + 12)
 
     e2e_copy = ("in: every input whole; out: the loss outputs and dL/dlogp of every slot "
-                "into pinned host memory")
+                "into pinned host memory" + ReadBack.PIPELINE)
 
     def e2e_step(self):
-        for k in self.host:
-            self.dev_in[k].copy_(self.host[k], non_blocking=True)
-        self._call(self.dev_in)
-        self.loss_host.copy_(self.out3, non_blocking=True)
-        self.grad_host.copy_(self.dev_in["grad"], non_blocking=True)
+        import torch
+        j = self.pipe_next()
+        d = self.sets[j]
+        with torch.cuda.stream(self.cin):
+            for k in self.host:
+                d[k].copy_(self.host[k], non_blocking=True)
+        self.pipe_ready()
+        self.rb_before_call()
+        self._call(d)
+        self.pipe_called(j)
+        with self.rb_stream():
+            self.loss_host.copy_(self.out3, non_blocking=True)
+            self.grad_host.copy_(d["grad"], non_blocking=True)
+        self.rb_end()
 
     def e2e_check(self):
         import torch
@@ -823,8 +924,10 @@ def run_gpu(args, w, ws, rank, local):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    case.e2e_begin()
     for _ in range(e2e_steps):
         case.e2e_step()
+    case.e2e_join()  # the last step's read-back
     e1.record(stream)
     torch.cuda.synchronize(device)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, device)
