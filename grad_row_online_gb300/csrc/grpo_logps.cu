@@ -174,6 +174,7 @@ struct FastCtx {
   float2 s2, neg_absA2, negA2, gc2, neg_beta2, beta2;
   float lim;
   float lo, hi;  // CISPO: the bounds on r - 1, -eps_lo and eps_hi
+  float dlo;     // the dual clip's floor on s(r - 1): -(c - 1) when A < 0, else -inf
   float g2_max;  // (kWPrecise / gc)^2: a vector whose sum of g^2 stays below
                  // it has every |w| <= kWPrecise
 };
@@ -196,11 +197,15 @@ __device__ __forceinline__ float2 Q_poly2(float2 d) {
 // kKL: the KL estimator, 0 k3 (the default; k = e^d - d - 1 from the
 // polynomial, its gradient -(e^d - 1)), 1 k1 (k = -d, gradient 1), 2 k2
 // (k = d^2 / 2, gradient -d); d = ref_logp - logp, and only k3 puts d under
-// the polynomial's range check.
-template <bool kCount, int kKL>
+// the polynomial's range check.  kDual: the dual clip on negative-advantage
+// tokens, min(s(r-1), lim) held at or above dlo = -(c-1) (A < 0; -inf
+// otherwise), so that q = -|A| max(min(s(r-1), lim), dlo), and the policy
+// gradient is 0 where s(r-1) < dlo too (counted apart, in ndual).
+template <bool kCount, int kKL, bool kDual>
 __device__ __forceinline__ float2 pair_fast(float2 lp, float2 od, float2 rf, bool has_ref,
                                             const FastCtx& f, float2& vq, float2& vk,
-                                            float2& d2sum, float2& g2sum, int& nclip) {
+                                            float2& d2sum, float2& g2sum, int& nclip,
+                                            int& ndual) {
   const float2 dp = __ffma2_rn(od, f2(-1.f), lp);  // logp - old
   const float2 Qp = Q_poly2(dp), ddp = __fmul2_rn(dp, dp);
   const float2 em = __ffma2_rn(ddp, Qp, dp);       // r - 1
@@ -217,13 +222,18 @@ __device__ __forceinline__ float2 pair_fast(float2 lp, float2 od, float2 rf, boo
     k = __fmul2_rn(__fmul2_rn(dr, dr), f2(0.5f));  // k2 = d^2 / 2
   }
   const float2 se = __fmul2_rn(f.s2, em);
-  const float2 mn = make_float2(fminf(se.x, f.lim), fminf(se.y, f.lim));
+  float2 mn = make_float2(fminf(se.x, f.lim), fminf(se.y, f.lim));
+  if (kDual) mn = make_float2(fmaxf(mn.x, f.dlo), fmaxf(mn.y, f.dlo));
   const float2 q = __fmul2_rn(f.neg_absA2, mn);
   float2 gp = __fmul2_rn(f.negA2, __fadd2_rn(em, f2(1.f)));  // -A r
   const bool cx = se.x > f.lim, cy = se.y > f.lim;
-  gp.x = cx ? 0.f : gp.x;
-  gp.y = cy ? 0.f : gp.y;
-  if (kCount) nclip += (int)cx + (int)cy;
+  const bool dx = kDual && se.x < f.dlo, dy = kDual && se.y < f.dlo;
+  gp.x = (cx || dx) ? 0.f : gp.x;
+  gp.y = (cy || dy) ? 0.f : gp.y;
+  if (kCount) {
+    nclip += (int)cx + (int)cy;
+    if (kDual) ndual += (int)dx + (int)dy;
+  }
   const float2 g = kKL == 0 ? __ffma2_rn(f.neg_beta2, emr, gp)
                  : kKL == 1 ? __fadd2_rn(gp, f.beta2)
                             : __ffma2_rn(f.neg_beta2, dr, gp);
@@ -282,16 +292,19 @@ __device__ __forceinline__ bool vec_cispo(const float4& l4, const float4& o4, co
 // token needs the general path: a log ratio outside |d| < 1/2 (caught by
 // the vector's sum of d^2 reaching 1/4), or a gradient above kWPrecise
 // (caught by its sum of g^2); NaNs fail the check too.
-template <bool kCount, int kKL>
+template <bool kCount, int kKL, bool kDual>
 __device__ __forceinline__ bool vec_fast(const float4& l4, const float4& o4, const float4& r4,
                                          bool has_ref, const FastCtx& f, float4& w,
-                                         float& vq, float& vk, int& nclip) {
+                                         float& vq, float& vk, int& nclip, int& ndual) {
   float2 sq = f2(0.f), sk = f2(0.f), d2 = f2(0.f), g2 = f2(0.f);
   nclip = 0;
-  const float2 w01 = pair_fast<kCount, kKL>(make_float2(l4.x, l4.y), make_float2(o4.x, o4.y),
-                                       make_float2(r4.x, r4.y), has_ref, f, sq, sk, d2, g2, nclip);
-  const float2 w23 = pair_fast<kCount, kKL>(make_float2(l4.z, l4.w), make_float2(o4.z, o4.w),
-                                       make_float2(r4.z, r4.w), has_ref, f, sq, sk, d2, g2, nclip);
+  ndual = 0;
+  const float2 w01 = pair_fast<kCount, kKL, kDual>(
+      make_float2(l4.x, l4.y), make_float2(o4.x, o4.y), make_float2(r4.x, r4.y), has_ref, f, sq,
+      sk, d2, g2, nclip, ndual);
+  const float2 w23 = pair_fast<kCount, kKL, kDual>(
+      make_float2(l4.z, l4.w), make_float2(o4.z, o4.w), make_float2(r4.z, r4.w), has_ref, f, sq,
+      sk, d2, g2, nclip, ndual);
   w = make_float4(w01.x, w01.y, w23.x, w23.y);
   vq = __fadd_rn(sq.x, sq.y);
   vk = __fadd_rn(sk.x, sk.y);
@@ -364,14 +377,14 @@ __device__ __forceinline__ bool vec_fast_variant(const float4& l4, const float4&
 }
 
 enum : int { kModeDefault = 0, kModeVariant = 1, kModeGspo = 2, kModeK1 = 3, kModeK2 = 4,
-             kModeCispo = 5 };
+             kModeCispo = 5, kModeDual = 6 };
 // The clipped surrogate without the dual clip or sequence ratios, with the KL
 // estimator of the mode: the packed fast path of vec_fast.
 __host__ __device__ constexpr int mode_kl(int mode) {
   return mode == kModeK1 ? 1 : (mode == kModeK2 ? 2 : 0);
 }
 __host__ __device__ constexpr bool mode_packed(int mode) {
-  return mode == kModeDefault || mode == kModeK1 || mode == kModeK2;
+  return mode == kModeDefault || mode == kModeK1 || mode == kModeK2 || mode == kModeDual;
 }
 // Modes whose general-path vectors wait for the end of the token loop.
 __host__ __device__ constexpr bool mode_defers(int mode) { return mode != kModeVariant; }
@@ -467,12 +480,16 @@ __device__ __forceinline__ bool process_vec(uint32_t mw, const float4& l, const 
   w = make_float4(0.f, 0.f, 0.f, 0.f);
   if (mw == 0u) return true;
   float vq, vk;
-  int nclip;
+  int nclip, ndual;
   int ncl2[2];
   unsigned nc[3];
   if (mode_packed(kMode) && all_active(mw) &&
-      vec_fast<kCount, mode_kl(kMode)>(l, o, r, has_ref, f, w, vq, vk, nclip)) {
-    if (kCount) acc.count(f.clip_kind, (unsigned)nclip);
+      vec_fast<kCount, mode_kl(kMode), kMode == kModeDual>(l, o, r, has_ref, f, w, vq, vk, nclip,
+                                                           ndual)) {
+    if (kCount) {
+      acc.count(f.clip_kind, (unsigned)nclip);
+      if (kMode == kModeDual) acc.nc[2] += (unsigned)ndual;
+    }
   } else if (kMode == kModeGspo && all_active(mw) && vec_fast_gspo(l, r, has_ref, gs, w, vq, vk)) {
     if (gs.clip) acc.count(gs.clip, 4u);
   } else if (kMode == kModeCispo && all_active(mw) &&
@@ -621,7 +638,8 @@ __device__ __forceinline__ bool grid_wait(const unsigned long long* c, unsigned 
 
 // kMode: the call's loss is the default variant (clipped surrogate, k3:
 // kModeDefault), the clipped surrogate with k1 or k2 (kModeK1, kModeK2: the
-// same packed path with the other KL term), CISPO with k3 (kModeCispo), GSPO
+// same packed path with the other KL term), the clipped surrogate with the
+// dual clip and k3 (kModeDual), CISPO with k3 (kModeCispo), GSPO
 // with the clipped surrogate and k3 (kModeGspo), or any other variant
 // (kModeVariant); kCount: the call wants the clip counters.
 // Each form is its own instantiation, so that another's fast path does not
@@ -885,6 +903,7 @@ __global__ void __launch_bounds__(kLogpsThreads, 7) logps_kernel(const LogpsArgs
     f.lim = x.A > 0.f ? a.eps_hi : a.eps_lo;
     f.lo = -a.eps_lo;
     f.hi = a.eps_hi;
+    f.dlo = a.var.dual_c > 0.f && x.A < 0.f ? -__fsub_rn(a.var.dual_c, 1.f) : -INFINITY;
     {
       const float gm = x.gc > 0.f ? __fdiv_rn(kWPrecise, x.gc) : INFINITY;
       f.g2_max = __fmul_rn(gm, gm);
@@ -1106,7 +1125,8 @@ static cudaError_t prepare_device(int dev, int64_t* cap) {
                    logps_kernel<kModeGspo, false>, logps_kernel<kModeGspo, true>,
                    logps_kernel<kModeK1, false>, logps_kernel<kModeK1, true>,
                    logps_kernel<kModeK2, false>, logps_kernel<kModeK2, true>,
-                   logps_kernel<kModeCispo, false>, logps_kernel<kModeCispo, true>})
+                   logps_kernel<kModeCispo, false>, logps_kernel<kModeCispo, true>,
+                   logps_kernel<kModeDual, false>, logps_kernel<kModeDual, true>})
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
@@ -1181,6 +1201,10 @@ cudaError_t launch_logps(const LogpsArgs& a, const grpo_profile_t* prof, cudaStr
   else if (plain_clip && a.var.kl_type == GRPO_KL_K2)
     e = count ? cudaLaunchKernelEx(&cfg, logps_kernel<kModeK2, true>, a)
               : cudaLaunchKernelEx(&cfg, logps_kernel<kModeK2, false>, a);
+  else if (a.var.surrogate == GRPO_SURROGATE_CLIP && a.var.dual_c > 0.f && !a.var.seq_ratio &&
+           a.var.kl_type == GRPO_KL_K3)
+    e = count ? cudaLaunchKernelEx(&cfg, logps_kernel<kModeDual, true>, a)
+              : cudaLaunchKernelEx(&cfg, logps_kernel<kModeDual, false>, a);
   else if (a.var.surrogate == GRPO_SURROGATE_CISPO && a.var.kl_type == GRPO_KL_K3 &&
            !a.var.seq_ratio)
     e = count ? cudaLaunchKernelEx(&cfg, logps_kernel<kModeCispo, true>, a)

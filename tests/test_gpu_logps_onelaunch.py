@@ -70,6 +70,7 @@ OPTIONS = {
                           dual_clip_c=1.4),
     "cispo-k1": dict(surrogate="cispo", kl="k1"),
     "cispo": dict(surrogate="cispo"),
+    "dual": dict(dual_clip_c=1.4),
     "k1": dict(kl="k1"),
     "k2-sequence-mean": dict(kl="k2", reduction="sequence_mean"),
     "gspo": dict(reduction="sequence_mean", ratio_level="sequence"),

@@ -200,6 +200,8 @@ def test_logps_variants_on_the_fast_path(name):
     A = oracle.group_advantages(R, w.group_boundaries())
     exp = oracle.loss_from_logps(lp, ref, old, mask, A, w.eps_lo, w.eps_hi, w.beta,
                                  **_oracle_kw(v, w))
+    if v.get("dual_clip_c") and not v.get("ratio_level"):  # the dual clip binds on
+        assert exp["clip_counts"][2] > 0                     # the fast path too
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     args = dict(samples_per_prompt=w.samples_per_prompt, clip_eps=w.eps_lo, clip_eps_hi=w.eps_hi,
                 beta=w.beta, reduction=w.reduction, want_per_seq=True, want_clip_counts=True)
@@ -217,11 +219,11 @@ def test_logps_variants_on_the_fast_path(name):
     assert np.all(ok | near), np.argwhere(~(ok | near))[:5]
 
 
-@pytest.mark.parametrize("name", ["k1", "k2", "cispo", "gspo"])
+@pytest.mark.parametrize("name", ["k1", "k2", "dual", "cispo", "gspo"])
 def test_logps_variants_with_every_vector_deferred(name):
     # log ratios ~N(0, 2): nearly every vector fails the fast path's range
     # check, so the variants with a packed path of their own (the clipped
-    # surrogate with k1 or k2, CISPO with k3, GSPO with k3) leave each thread's
+    # surrogate with k1, k2 or the dual clip, CISPO with k3, GSPO with k3) leave each thread's
     # whole share of the row to the general path after the token loop
     v = VARIANTS[name]
     w = LOGPS_WIDE.with_(B=8, T=4096, len_range=(3000, 4096), old_sigma=2.0,
