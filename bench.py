@@ -451,8 +451,6 @@ class ReadBack:
     (`pipe_init`), the copies in run on a third stream too, into the set the
     previous call did not read, so that they also overlap the calls."""
 
-    READBACK = ("; step i's read-back runs on a second stream, overlapping step i+1's "
-                "copies in (step i+1's call waits for it before it overwrites the outputs)")
     PIPELINE = ("; three streams: step i+1's inputs are copied into a second device input set "
                 "while step i's call runs, and step i's read-back overlaps step i+1's copies in "
                 "(a call waits for its inputs and for the previous read-back; the copies into an "
@@ -681,7 +679,7 @@ class VocabCase(ReadBack):
     e2e_copy = ("in: every slice's logits rows the calls read (runs of active tokens), the "
                 "other inputs whole; out: the loss outputs and every slice's gradient rows of the "
                 "active tokens into pinned host buffers (masked rows are zero by contract)"
-                + ReadBack.READBACK)
+                + ReadBack.PIPELINE)
 
     def e2e_setup(self):
         import torch
@@ -691,13 +689,12 @@ class VocabCase(ReadBack):
         self.host_small = {k: torch.empty(self.inp[k].shape, dtype=self.inp[k].dtype,
                                           pin_memory=True).copy_(self.inp[k])
                            for k in self.small}
-        self.dev_in = [torch.empty_like(t) for t in self.Xs + self.Ys]
-        self.dev_small = {k: torch.empty_like(self.inp[k]) for k in self.small}
+        self.pipe_init(lambda: ([torch.empty_like(t) for t in self.Xs + self.Ys],
+                                {k: torch.empty_like(self.inp[k]) for k in self.small}))
         self.loss_host = torch.empty(3, dtype=torch.float32).pin_memory()
         self.mask_host = self.host_small["mask"].numpy()
         self.grads_host = [torch.zeros(t.shape, dtype=t.dtype, pin_memory=True)
                            for t in self.grads]
-        self.rb_init()
         rows = sum(e - b for b, e in active_runs(self.mask_host))
         h2d = (rows * sum(t.shape[-1] * t.element_size() for t in self.host)
                + sum(t.numel() * t.element_size() for t in self.host_small.values()))
@@ -712,18 +709,24 @@ class VocabCase(ReadBack):
                 raise RuntimeError("the end-to-end gradient rows differ from the device's")
 
     def e2e_step(self):
+        import torch
         n = len(self.Xs)
         runs = active_runs(self.mask_host)
-        for d, h in zip(self.dev_in, self.host):  # every slice: the rows the calls read
-            dv, hv = d.view(-1, d.shape[-1]), h.view(-1, h.shape[-1])
-            for b, e in runs:
-                dv[b:e].copy_(hv[b:e], non_blocking=True)
-        for k in self.small:
-            self.dev_small[k].copy_(self.host_small[k], non_blocking=True)
-        self.Xs, self.Ys = self.dev_in[:n], self.dev_in[n:]
-        self.inp = dict(self.inp, **self.dev_small)
+        j = self.pipe_next()
+        dev_in, dev_small = self.sets[j]
+        with torch.cuda.stream(self.cin):
+            for d, h in zip(dev_in, self.host):  # every slice: the rows the calls read
+                dv, hv = d.view(-1, d.shape[-1]), h.view(-1, h.shape[-1])
+                for b, e in runs:
+                    dv[b:e].copy_(hv[b:e], non_blocking=True)
+            for k in self.small:
+                dev_small[k].copy_(self.host_small[k], non_blocking=True)
+        self.Xs, self.Ys = dev_in[:n], dev_in[n:]
+        self.inp = dict(self.inp, **dev_small)
+        self.pipe_ready()
         self.rb_before_call()
         self.step()
+        self.pipe_called(j)
         self.out3.record_stream(self.side)  # allocated by this step, read on the side stream
         with self.rb_stream():
             self.loss_host.copy_(self.out3, non_blocking=True)
