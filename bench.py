@@ -48,6 +48,11 @@ PROFILES = {
     "large_vocab/gspo": ("gspo_kernels_large_vocab.md",
                          ("grpo_rows.cu", "grpo_rows_common.cuh", "grpo_internal.cuh",
                           "grpo_reduce.cu")),
+    "large_vocab/skip_masked": ("rows_kernel_large_vocab_skip_masked.md",
+                                ("grpo_rows.cu", "grpo_rows_common.cuh", "grpo_internal.cuh")),
+    "large_vocab/tp2": ("vocab_kernels_large_vocab_tp2.md",
+                        ("grpo_vocab.cu", "grpo_rows.cu", "grpo_rows_common.cuh",
+                         "grpo_internal.cuh", "grpo_reduce.cu", "grpo_prep.cu")),
 }
 
 

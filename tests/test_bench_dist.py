@@ -75,8 +75,11 @@ def test_committed_profiles_name_their_own_key():
         assert re.search(r"^traffic_bytes_per_launch:\s*[0-9.eE+]+", text, re.M)
         assert re.search(r"^kernel_source_sha:\s*\w+", text, re.M)
     w = synth.WORKLOADS["large_vocab"]
-    assert bench.profile_key(w, skip_masked=True) not in bench.PROFILES
-    assert bench.profile_key(w, tp=2) not in bench.PROFILES
+    default = bench.PROFILES[bench.profile_key(w)][0]
+    for key in (bench.profile_key(w, skip_masked=True), bench.profile_key(w, tp=2),
+                bench.profile_key(w, tp=4)):
+        assert key != "large_vocab"
+        assert key not in bench.PROFILES or bench.PROFILES[key][0] != default
     assert bench.profile_key(w, "k2") == "large_vocab"
     assert bench.profile_key(synth.WORKLOADS["logps"], "k2") not in bench.PROFILES
 
