@@ -45,6 +45,7 @@ PROFILES = {
     "fused": ("rows_kernel_fused.md",
               ("grpo_rows.cu", "grpo_rows_common.cuh", "grpo_internal.cuh")),
     "logps": ("logps_kernel_logps.md", ("grpo_logps.cu", "grpo_internal.cuh")),
+    "logps_full": ("logps_kernel_logps_full.md", ("grpo_logps.cu", "grpo_internal.cuh")),
     "large_vocab/gspo": ("gspo_kernels_large_vocab.md",
                          ("grpo_rows.cu", "grpo_rows_common.cuh", "grpo_internal.cuh",
                           "grpo_reduce.cu")),
