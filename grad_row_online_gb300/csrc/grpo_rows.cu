@@ -804,27 +804,20 @@ static cudaError_t launch_rows_kernel(const RowArgs& a, int tmem_cols, const grp
   // together, or an allocation would wait for another CTA to exit
   RowArgs ka = a;
   ka.tmem_cols = (kTmem && per_sm * tmem_cols <= 512) ? tmem_cols : 0;
-  // Claim order.  Sweep 2 re-reads the part of each active row not kept on
-  // chip; prefix masks put a sequence's active rows together, so row-major
-  // claims keep up to `grid` active rows in flight.  When their re-reads
-  // would hold between one half and one and a half of L2's capacity, the
-  // claims go token-major: masked rows (zero fills) then sit among the active
-  // ones and the active rows' re-reads fit L2 better.  Measured: the
-  // large-vocabulary rows (bf16, 193 KB re-read per row, 118 MB in flight)
-  // 2.863 -> 2.827 ms; the 64 KB fused rows (12 MB) and the 513 KB fp32 rows
-  // (245 MB), re-reading well within or far beyond L2 either way, 0.4-0.7 %
-  // slower token-major.
-  {
-    int l2 = 0;
-    if ((e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev)) != cudaSuccess) return e;
-    const int64_t kept = a.grad ? (int64_t)kPolicySmemBytes +
-                                      (ka.tmem_cols ? (int64_t)16 * kRowThreads * kTmemVecs : 0)
-                                : 0;
-    const int64_t reread = a.grad ? a.V * (int64_t)sizeof(T) - kept : 0;
-    const int64_t in_flight = reread > 0 ? grid * reread : 0;
-    if (2 * in_flight > (int64_t)l2 && 2 * in_flight < 3 * (int64_t)l2)
-      ka.flags |= kClaimTokenMajor;
-  }
+  // Claim order.  Prefix masks put a sequence's active rows together, so
+  // row-major claims alternate between stretches of active rows (both rows
+  // read, the gradient written) and stretches of masked rows (zero fills
+  // only); token-major claims (slot t of every sequence, then t + 1) change
+  // that mix gradually over the launch.  Measured per launch, token-major
+  // against row-major: the large-vocabulary rows (16-bit, tensor-memory
+  // slice, masked rows zero-filled) 2.827 against 2.861 ms, with the same
+  // DRAM traffic; the 64 KB fused rows 1.393 against 1.384 ms, the 513 KB
+  // fp32 rows 5.605 against 5.584 ms, and the masked-row mode (no zero
+  // fills) 2.024 against 1.995 ms.  So only the first kind claims
+  // token-major.
+  if (kTmem && sizeof(T) == 2 && ka.tmem_cols && a.grad &&
+      !(a.flags & GRPO_SKIP_MASKED_GRAD_ROWS))
+    ka.flags |= kClaimTokenMajor;
   if (prof && prof->start) cudaEventRecord((cudaEvent_t)prof->start, s);
   rows_kernel<T, kTmem><<<(unsigned)grid, kRowThreads, kPolicySmemBytes, s>>>(ka);
   e = cudaGetLastError();
