@@ -111,6 +111,25 @@ def test_logits_variants(name, which, dtype):
     assert_grad_rows(got[keep], exp["grad"][keep], dtype, what=f"{name} grad")
 
 
+@pytest.mark.parametrize("name", ["gspo", "default"])
+def test_long_16bit_rows_claimed_token_major(name):
+    # bf16 rows long enough for the tensor-memory slice: the row kernel and
+    # GSPO's second sweep claim their rows token-major (slot t of every
+    # sequence before slot t + 1), which must change no result
+    v = VARIANTS[name]
+    w = WIDE.with_(name="wide_long", V=90000, T=6, len_range=(1, 6))
+    case = make_case(w, "bf16")
+    exp = oracle.fused(case["X"], case["Y"], "bf16", case["acts"], case["old"], case["mask"],
+                       case["R"], case["bounds"], w.eps_lo, w.eps_hi, w.beta, **_oracle_kw(v, w))
+    res = _run_logits(case, to_device(case), v)
+    out = res["out3"].cpu().numpy().astype(np.float64)
+    for i, k in enumerate(("loss", "policy_loss", "kl")):
+        assert_scalar(out[i], exp[k], f"{name} {k}")
+    near = _band(exp, w.eps_lo, w.eps_hi, v.get("dual_clip_c"))
+    assert_grad_rows(torch_storage(res["grad"])[~near], exp["grad"][~near], "bf16",
+                     what=f"{name} grad")
+
+
 def test_wide_case_reaches_every_clip():
     case = make_case(WIDE, "f32")
     w = WIDE
