@@ -146,6 +146,25 @@ def test_full_mask_cancellation(dtype, V):
     check(case, run(case, to_device(case)), exp, f"full mask {dtype} V={V}")
 
 
+def test_a_gradient_step_lowers_the_loss():
+    # the gradient the library writes is the derivative of the loss it reports:
+    # a small step s of the policy logits against it changes the loss by
+    # grad . s to first order (the second-order term is ~1e-5 of it here)
+    case = make_case(MEDIUM, "f32")
+    dev = to_device(case)
+    res = run(case, dev)
+    loss0 = float(res["out3"][0])
+    grad = res["grad"].clone()
+    eta = 1e-5 / float((grad.double() ** 2).sum())  # a predicted decrease of ~1e-5
+    x1 = dev["X"] - eta * grad
+    step = (x1.double() - dev["X"].double())        # the step as rounded to fp32
+    predicted = float((grad.double() * step).sum())
+    res1 = run(case, dict(dev, X=x1))
+    change = float(res1["out3"][0]) - loss0
+    assert predicted < -5e-6
+    assert abs(change - predicted) <= 0.02 * abs(predicted), (change, predicted)
+
+
 def test_token_mean_and_options():
     case = make_case(MEDIUM.with_(reduction=0), "f32")
     dev = to_device(case)
