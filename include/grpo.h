@@ -65,7 +65,8 @@ typedef enum {
   GRPO_ERR_ALIGN = 4,      /* a pointer is not aligned to its element size, or
                               the workspace is not 256-byte aligned */
   GRPO_ERR_GROUP_SPEC = 5, /* not exactly one of samples_per_prompt / boundaries */
-  GRPO_ERR_PARAM = 6,      /* eps / beta / adv_eps / grad_scale / reduction / variant invalid */
+  GRPO_ERR_PARAM = 6,      /* eps / beta / adv_eps / grad_scale / reduction / variant invalid,
+                              or a flag bit this header does not define */
   GRPO_ERR_WORKSPACE = 7,  /* ws_bytes < grpo_workspace_size(...) */
   GRPO_ERR_CUDA = 8,       /* a CUDA launch failed */
   /* device-detected; bits of the status word (grpo_read_device_status) */

@@ -113,6 +113,7 @@ def test_fwd_rejects_bad_arguments(lib):
     assert _fwd(lib, p=_params(grad_scale=float("inf"))) == 6
     assert _fwd(lib, p=_params(reduction=3)) == 6
     assert _fwd(lib, p=_params(flags=64)) == 6
+    assert _fwd(lib, p=_params(flags=0x20000000)) == 6  # a bit the header does not define
     # loss variants
     assert _fwd(lib, p=_params(reduction=2)) == 6  # fixed constant without a constant
     assert _fwd(lib, p=_params(reduction=2, norm_constant=-1.0)) == 6
