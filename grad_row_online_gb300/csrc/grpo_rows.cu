@@ -2,7 +2,8 @@
 //
 // Persistent CTAs (kRowThreads threads, kRowBlocksPerSM per SM) claim token
 // rows from a device counter, one row per CTA at a time (the next row is
-// claimed while the current one is processed).  For an active row
+// claimed while the current one is processed), in row-major or, where that
+// measured faster, token-major order (see the launcher).  For an active row
 // (completion_mask != 0):
 //   sweep 1   one streaming read of the policy and reference rows, both in
 //             flight together, each reduced to (max, sum exp) by a per-thread
